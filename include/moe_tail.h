@@ -1,0 +1,163 @@
+/*
+ * moe_tail.h -- C ABI of the GB300 MoE decode tail.
+ *
+ * The MoE decode tail is the per-token finalize that turns the routed
+ * experts' output rows into the layer's BF16 output row, plus the dense
+ * latent up-projection and the fused shared expert that add into it.  One
+ * process drives one GPU: the "ranks" (partitions) of the multi-GPU method
+ * are the leading [tp, ...] dimension of a partial-slot tensor in device
+ * memory, so there are no mailboxes, peer stores or collectives.
+ *
+ * Sources (vLLM API pages, cited by page and section):
+ *   [MS] vllm.models.muse_spark.nvidia.specialized_decode.cutedsl.moe.tail --
+ *        module docstring, BoundTail.run, _check_tail_args, _TpTailKernel.
+ *   [KT] vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.tail_runtime --
+ *        module docstring, MoeTailBox, MoeTailWeights.
+ *   [KS] vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.moe.shared --
+ *        module docstring, SharedUmma (load_tile, owned_h), SharedBase.push.
+ *
+ * Conventions of every call
+ *   - Pointers are DEVICE pointers owned by the caller; nothing is allocated,
+ *     freed or retained.  `stream` is a cudaStream_t (NULL: legacy default
+ *     stream); the call only enqueues work and returns.
+ *   - BF16 is IEEE bfloat16 in uint16 storage; FP32 is IEEE binary32.
+ *     Tensors are dense, row-major, with the shapes given below.
+ *   - Arguments are checked on the host before anything is launched ([MS]
+ *     _check_tail_args: a refused call launches nothing).  b = 0 succeeds and
+ *     launches nothing ([MS] BoundTail.run).  Refusal reasons: a negative or
+ *     out-of-range size, a null pointer with b > 0, a vector pointer not
+ *     16-byte aligned (BF16 rows, gamma, out, workspace; the index 4-byte,
+ *     route weights 4- or 2-byte), a width not a multiple of 8, an unknown
+ *     dtype, a workspace smaller than moe_tail_workspace_bytes(), or `out`
+ *     overlapping any input or the workspace.
+ *   - Every BF16 result is rounded to nearest-even with -0 written as +0.
+ *   - Errors are returned synchronously; a launch failure returns
+ *     MOE_TAIL_ECUDA (the CUDA error is cleared).  Faults inside a kernel
+ *     surface through the stream like any CUDA error; a bounded internal wait
+ *     that expires sets a bit read by moe_tail_take_device_error().
+ */
+#ifndef MOE_TAIL_H
+#define MOE_TAIL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_TAIL_OK = 0,
+  MOE_TAIL_EINVAL = 1,  /* arguments refused before any launch */
+  MOE_TAIL_ECUDA = 2,   /* a CUDA call failed */
+  MOE_TAIL_ENOTSUP = 3  /* valid arguments this build does not support */
+} moe_tail_status;
+
+enum { MOE_TAIL_W_FP32 = 0, MOE_TAIL_W_BF16 = 1 };
+
+/*
+ * EP finalize ([MS] module docstring, expert parallelism).  Per token t:
+ *   g[c]       = fp32(gamma[c]) + gain_center
+ *   for slot s in 0..tp-1 (rank order), over the routes k (in order) with
+ *   j = permuted_idx[s][t][k] in [0, rows_per_slot)  ("local to s"):
+ *     x = rows[s][j][:];  v = weight_before_norm ? x*g : x
+ *     inv = 1 / sqrt(sum_squares(v) * (1/P) + eps)
+ *     n = weight_before_norm ? v*inv : (x*inv)*g
+ *     part_s += n * w[t][k]                     (FP32 from +0, each product rounded)
+ *   out[t] = bf16( sum over s of fp32(bf16(part_s)) )   (FP32 from +0)
+ * sum_squares: per 256-column chunk, lane l squares and adds columns
+ * 8l..8l+7 in order, 32 lanes combine by xor butterfly (1,2,4,8,16), chunk
+ * sums are added in chunk order.  Routes with no local row contribute nothing.
+ *
+ *   rows          BF16 [tp][rows_per_slot][P]  slot s's GEMM2 output rows
+ *   rows_per_slot rows per slot (>= 0)
+ *   permuted_idx  int32 [tp][b][K]
+ *   route_weights [b][K], FP32 or BF16 per weight_dtype (MOE_TAIL_W_*)
+ *   gamma         BF16 [P] norm weight (ones when the norm has none)
+ *   out           BF16 [b][P]
+ * Limits: 1 <= tp <= 32, 1 <= K <= 32, 8 <= P <= 32768, P % 8 == 0, b <= 65535.
+ */
+int moe_tail_ep_finalize(const void* rows, int64_t rows_per_slot, const int32_t* permuted_idx,
+                         const void* route_weights, int weight_dtype, const void* gamma,
+                         float gain_center, float eps, int weight_before_norm, int b, int tp, int K,
+                         int P, void* out, void* stream);
+
+/*
+ * Expert-TP finalize ([MS] module docstring, expert TP; _TpTailKernel).
+ * Every slot holds a K-partial of every route row.  Per token t, routes k in
+ * order with j = permuted_idx[t][k] in [0, num_rows):
+ *   x_k = bf16( sum over s in slot order of fp32(partials[s][j][:]) )
+ *   out[t] = bf16( sum over k from +0 of fp32(w[t][k] * norm(x_k)) )
+ * with norm() the EP finalize's normalisation.  A route whose index is out
+ * of range contributes nothing.
+ *
+ *   partials      BF16 [tp][num_rows][P]
+ *   permuted_idx  int32 [b][K] (shared by all slots)
+ *   route_weights, gamma, out, limits: as moe_tail_ep_finalize.
+ */
+int moe_tail_tp_finalize(const void* partials, int64_t num_rows, const int32_t* permuted_idx,
+                         const void* route_weights, int weight_dtype, const void* gamma,
+                         float gain_center, float eps, int weight_before_norm, int b, int tp, int K,
+                         int P, void* out, void* stream);
+
+/*
+ * Latent tail ([KT] module docstring): the latent partials of the tp slots
+ * are summed, RMS-normalised per row, up-projected and the shared expert's
+ * partials are added:
+ *   x    = bf16( sum over s in slot order of fp32(latent[s][t][:]) )
+ *   y    = bf16( (x * inv) * fp32(gamma) ),  inv as above with 1/L, eps
+ *   out  = bf16( y . w_up^T  (FP32 accumulate)  + sum over s of fp32(shared[s][t][:]) )
+ *
+ *   latent     BF16 [tp][b][L]
+ *   gamma      BF16 [L]
+ *   w_up       BF16 [H][L] row-major (output feature n is row n)
+ *   shared     BF16 [tp_s][b][H] or NULL when tp_s == 0
+ *   out        BF16 [b][H]
+ *   workspace  >= moe_tail_workspace_bytes(0, b, L) bytes, 16-byte aligned;
+ *              holds y (BF16 [b][L]) after the call
+ * Limits: 1 <= tp <= 32, 0 <= tp_s <= 32, 8 <= L <= 32768, 8 <= H, L % 8 == 0,
+ * H % 8 == 0, b <= 65535.
+ */
+int moe_tail_latent_up(const void* latent, const void* gamma, float eps, const void* w_up,
+                       const void* shared, int tp_s, int b, int tp, int L, int H, void* out,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Fused shared expert ([KS] module docstring, SharedUmma.owned_h,
+ * SharedBase.push): gate/up projection, gated activation, down projection,
+ * added into the tail's output:
+ *   gate = bf16(x . w_gate^T), up = bf16(x . w_up^T)     (FP32 accumulate)
+ *   h    = bf16( silu(gate) * up ),  silu(g) = g / (1 + exp(-g))
+ *   d    = h . w_down^T                                   (FP32 accumulate)
+ *   out  = accumulate ? bf16( fp32(out) + fp32(bf16(d)) ) : bf16(d)
+ *
+ *   x          BF16 [b][H]
+ *   w_gate     BF16 [I][H];  w_up BF16 [I][H];  w_down BF16 [H][I]
+ *   out        BF16 [b][H] (read as well when accumulate != 0)
+ *   workspace  >= moe_tail_workspace_bytes(1, b, I) bytes, 16-byte aligned;
+ *              holds h (BF16 [b][I]) after the call
+ * Limits: 8 <= H, 8 <= I, H % 8 == 0, I % 8 == 0.
+ */
+int moe_shared_expert(const void* x, const void* w_gate, const void* w_up, const void* w_down,
+                      int b, int H, int I, void* out, int accumulate, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of moe_tail_latent_up (which = 0, dim = L) or
+ * moe_shared_expert (which = 1, dim = I) at b tokens; 0 for bad arguments. */
+size_t moe_tail_workspace_bytes(int which, int b, int dim);
+
+/* Static text for a moe_tail_status value. */
+const char* moe_tail_status_str(int status);
+
+/* Reads and clears the device error word of the calling thread's current
+ * device (synchronises with it).  *bits receives the bits raised since the
+ * last read: 1 operand stage never arrived, 2 stage never released,
+ * 4 accumulator never completed, 8 drain after abort failed.  Returns
+ * MOE_TAIL_OK or MOE_TAIL_ECUDA. */
+int moe_tail_take_device_error(unsigned int* bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_TAIL_H */

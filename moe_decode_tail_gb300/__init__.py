@@ -1,0 +1,158 @@
+"""GB300-native MoE decode tail: thin Python binding of libmoetail.so.
+
+Every function here only marshals torch CUDA tensors into the C ABI of
+``include/moe_tail.h`` (same names, sizes read from tensor shapes); all of the
+tail's arithmetic runs in the library's CUDA kernels.  There is no CPU path:
+if the library is missing or a call is refused, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB
+
+__all__ = [
+    "MoeTailError", "lib", "moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up",
+    "moe_shared_expert", "moe_tail_workspace_bytes", "moe_tail_status_str", "moe_tail_take_device_error",
+]
+
+OK, EINVAL, ECUDA, ENOTSUP = 0, 1, 2, 3
+W_FP32, W_BF16 = 0, 1
+
+
+class MoeTailError(RuntimeError):
+    def __init__(self, name: str, status: int):
+        super().__init__(f"{name}: {status_string(status)} ({status})")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"{LIB} is missing: build it with moe_decode_tail_gb300.build.build()")
+        L = ctypes.CDLL(LIB)
+        P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        fin = [P, i64, P, P, i32, P, f32, f32, i32, i32, i32, i32, i32, P, P]
+        L.moe_tail_ep_finalize.argtypes = fin
+        L.moe_tail_tp_finalize.argtypes = fin
+        L.moe_tail_latent_up.argtypes = [P, P, f32, P, P, i32, i32, i32, i32, i32, P, P, sz, P]
+        L.moe_shared_expert.argtypes = [P, P, P, P, i32, i32, i32, P, i32, P, sz, P]
+        L.moe_tail_workspace_bytes.argtypes = [i32, i32, i32]
+        L.moe_tail_workspace_bytes.restype = sz
+        L.moe_tail_status_str.argtypes = [i32]
+        L.moe_tail_status_str.restype = ctypes.c_char_p
+        L.moe_tail_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        for name in ("moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up", "moe_shared_expert",
+                     "moe_tail_take_device_error"):
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().moe_tail_status_str(status).decode()
+
+
+def _check(name: str, status: int) -> None:
+    if status != OK:
+        raise MoeTailError(name, status)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def _weights(w: torch.Tensor) -> int:
+    if w.dtype == torch.float32:
+        return W_FP32
+    if w.dtype == torch.bfloat16:
+        return W_BF16
+    raise ValueError("route weights must be FP32 or BF16")
+
+
+def moe_tail_ep_finalize(rows, permuted_idx, route_weights, gamma, out, *, gain_center=1.0, eps=1e-6,
+                         weight_before_norm=True, stream=None) -> torch.Tensor:
+    """EP finalize into out (BF16 [b, P]); rows BF16 [tp, rows_per_slot, P],
+    permuted_idx int32 [tp, b, K], route_weights [b, K], gamma BF16 [P]."""
+    _cuda(rows, permuted_idx, route_weights, gamma, out)
+    tp, rows_per_slot, P = rows.shape
+    b, K = route_weights.shape
+    _check("moe_tail_ep_finalize", lib().moe_tail_ep_finalize(
+        _p(rows), rows_per_slot, _p(permuted_idx), _p(route_weights), _weights(route_weights), _p(gamma),
+        gain_center, eps, int(bool(weight_before_norm)), b, tp, K, P, _p(out), _stream(stream)))
+    return out
+
+
+def moe_tail_tp_finalize(partials, permuted_idx, route_weights, gamma, out, *, gain_center=1.0, eps=1e-6,
+                         weight_before_norm=True, stream=None) -> torch.Tensor:
+    """Expert-TP finalize into out (BF16 [b, P]); partials BF16 [tp, num_rows, P],
+    permuted_idx int32 [b, K], route_weights [b, K], gamma BF16 [P]."""
+    _cuda(partials, permuted_idx, route_weights, gamma, out)
+    tp, num_rows, P = partials.shape
+    b, K = route_weights.shape
+    _check("moe_tail_tp_finalize", lib().moe_tail_tp_finalize(
+        _p(partials), num_rows, _p(permuted_idx), _p(route_weights), _weights(route_weights), _p(gamma),
+        gain_center, eps, int(bool(weight_before_norm)), b, tp, K, P, _p(out), _stream(stream)))
+    return out
+
+
+def moe_tail_workspace_bytes(which: int, b: int, dim: int) -> int:
+    return int(lib().moe_tail_workspace_bytes(which, b, dim))
+
+
+def moe_tail_latent_up(latent, gamma, w_up, shared, out, workspace, *, eps=1e-6, stream=None) -> torch.Tensor:
+    """Latent tail into out (BF16 [b, H]): latent BF16 [tp, b, L], gamma BF16 [L],
+    w_up BF16 [H, L], shared BF16 [tp_s, b, H] or None, workspace uint8 CUDA
+    tensor of at least moe_tail_workspace_bytes(0, b, L) bytes (y after the call)."""
+    _cuda(latent, gamma, w_up, shared, out, workspace)
+    tp, b, L = latent.shape
+    H = w_up.shape[0]
+    tp_s = 0 if shared is None else shared.shape[0]
+    _check("moe_tail_latent_up", lib().moe_tail_latent_up(
+        _p(latent), _p(gamma), eps, _p(w_up), _p(shared), tp_s, b, tp, L, H, _p(out), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def moe_shared_expert(x, w_gate, w_up, w_down, out, workspace, *, accumulate=True, stream=None) -> torch.Tensor:
+    """Fused shared expert into out (BF16 [b, H]): x BF16 [b, H], w_gate/w_up BF16
+    [I, H], w_down BF16 [H, I], workspace of at least moe_tail_workspace_bytes(1, b, I)
+    bytes (h after the call); out += down(...) when accumulate."""
+    _cuda(x, w_gate, w_up, w_down, out, workspace)
+    b, H = x.shape
+    I = w_gate.shape[0]
+    _check("moe_shared_expert", lib().moe_shared_expert(
+        _p(x), _p(w_gate), _p(w_up), _p(w_down), b, H, I, _p(out), int(bool(accumulate)), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def moe_tail_status_str(status: int) -> str:
+    return status_string(status)
+
+
+def moe_tail_take_device_error() -> int:
+    """Bits raised by bounded waits inside the kernels since the last read (0: none)."""
+    bits = ctypes.c_uint(0)
+    _check("moe_tail_take_device_error", lib().moe_tail_take_device_error(ctypes.byref(bits)))
+    return int(bits.value)

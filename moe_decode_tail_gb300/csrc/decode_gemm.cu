@@ -1,0 +1,481 @@
+// Small-batch decode GEMM on the 5th-generation tensor cores (sm_103a).
+//
+//   D[m, t] = sum_k W[m, k] * X[t, k]       (W: weights [M, K], X: tokens [b, K])
+//
+// The weights are the MMA's M=128 operand and the tokens its N operand
+// ("swap AB"), so a decode batch of b <= 128 tokens is one N tile and the
+// kernel is a stream of weight tiles: its roofline is the weight bytes over
+// HBM bandwidth.  Per CTA: warp 4 (one thread) streams 128x64 BF16 weight
+// tiles and Nx64 token tiles with TMA (128-byte swizzle) into a ring of
+// shared-memory stages guarded by mbarriers; warp 5 (one thread) issues four
+// K=16 tcgen05.mma per stage into an FP32 accumulator in tensor memory and
+// releases the stage with tcgen05.commit; warps 0-3 read the accumulator
+// (tcgen05.ld, one TMEM lane = one weight row per thread).  The K range is
+// split over the CTAs of a thread-block cluster; their FP32 partial tiles are
+// added in cluster-rank order over distributed shared memory, so the result
+// is deterministic, and the fused epilogue writes BF16:
+//
+//   kGemmUpShared   out = bf16(acc + sum_s shared[s])   (latent tail up-projection
+//                   plus the shared-expert partials, Kimi-K3 tail runtime page,
+//                   module docstring)
+//   kGemmGateUpSilu rows 0..63 of the tile are gate rows, 64..127 the matching
+//                   up rows; h = bf16(silu(bf16(gate)) * bf16(up))  (Kimi-K3
+//                   shared expert page: SharedUmma.load_tile pairs gate and up
+//                   rows in one M tile; owned_h rounds gate and up to BF16)
+//   kGemmDown       out = bf16(out + bf16(d)) or bf16(d)  (the down projection
+//                   pushed as BF16, -0 made +0, added into the tail's output)
+//
+// Every wait is bounded in time; on expiry the kernel raises a bit in the
+// device error word, drains what it started, frees its tensor memory and
+// returns.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moetail {
+
+constexpr int kBlockK = 64;                        // BF16 per K block: one 128-byte swizzle row
+constexpr int kTileM = 128;                        // MMA M: weight rows per CTA
+constexpr int kATileBytes = kTileM * kBlockK * 2;  // 16 KiB
+constexpr int kThreads = 192;                      // warps 0-3 epilogue, 4 TMA, 5 MMA
+constexpr int kMaxStages = 12;
+
+// The device error word of this library (see the enum in common.cuh).
+__device__ unsigned int g_device_error = 0;
+__device__ __forceinline__ void raise_error(unsigned bit) { atomicOr(&g_device_error, bit); }
+
+cudaError_t take_device_error(unsigned* bits) {
+  unsigned v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+  *bits = v;
+  return e;
+}
+
+// ---- PTX wrappers --------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of the given parity to complete; false if the time limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 2-D tiled TMA load of box (x = inner coordinate, y = row) into shared memory.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// 16 consecutive FP32 accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile whose rows are
+// 128 bytes, written by TMA with 128-byte swizzle: 8-row groups 1024 bytes
+// apart (stride byte offset), the leading byte offset unused by this layout,
+// descriptor version 1 (bit 46), swizzle mode 2 = 128B (bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)(16 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: FP32 accumulate (bits 4-5 = 1), BF16 A
+// and B (bits 7-9, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+struct GemmSmem {  // offsets from the 1024-aligned base of dynamic shared memory
+  uint32_t ring, full, empty, accum, tmem_slot, abort_flag;
+};
+
+template <int MODE, int N>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_gemm_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
+                       const __grid_constant__ CUtensorMap map_x, const GemmArgs a, const int stages) {
+  extern __shared__ uint8_t smem_raw[];
+  constexpr int kBTileBytes = N * kBlockK * 2;
+  constexpr int kStageBytes = kATileBytes + kBTileBytes;
+  constexpr uint32_t kTmemCols = N < 32 ? 32 : N;
+  constexpr uint32_t kIdesc = idesc_bf16(kTileM, N);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank(), ksplit = cluster_size();
+  const int m_tile = blockIdx.y;
+  const int tok0 = blockIdx.z * N;
+
+  // K blocks of this CTA: an even split of the tile's K range over the cluster.
+  const int kb_per = a.kblocks / (int)ksplit, kb_rem = a.kblocks % (int)ksplit;
+  const int kb0 = (int)rank * kb_per + min((int)rank, kb_rem);
+  const int nk = kb_per + ((int)rank < kb_rem ? 1 : 0);
+
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  GemmSmem L;
+  L.ring = base;
+  L.full = base + stages * kStageBytes;
+  L.empty = L.full + 8 * stages;
+  L.accum = L.empty + 8 * stages;
+  L.tmem_slot = L.accum + 8;
+  L.abort_flag = L.tmem_slot + 4;
+  volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (L.tmem_slot - base));
+  volatile uint32_t* abort_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (L.abort_flag - base));
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(L.full + 8 * s, 1);
+      mbar_init(L.empty + 8 * s, 1);
+    }
+    mbar_init(L.accum, 1);
+    *abort_ptr = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_map(&map_w0);
+    if (MODE == kGemmGateUpSilu) prefetch_map(&map_w1);
+    prefetch_map(&map_x);
+  }
+  if (warp == 5) tmem_alloc(L.tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot_ptr;
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();   // token tiles: re-read by every M tile
+      const uint64_t stream = policy_evict_first();  // weights: read once
+      int issued = 0;
+      bool ok = true;
+      // Weights do not depend on the preceding kernel: the first ring's worth is
+      // requested before waiting for it.
+      const int pre = min(nk, stages);
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t st = L.ring + i * kStageBytes;
+        const uint32_t bar = L.full + 8 * i;
+        mbar_expect_tx(bar, kStageBytes);
+        const int kx = (kb0 + i) * kBlockK;
+        if (MODE == kGemmGateUpSilu) {
+          tma_load_2d(st, &map_w0, bar, kx, m_tile * 64, stream);
+          tma_load_2d(st + kATileBytes / 2, &map_w1, bar, kx, m_tile * 64, stream);
+        } else {
+          tma_load_2d(st, &map_w0, bar, kx, m_tile * kTileM, stream);
+        }
+      }
+      grid_dependency_wait();
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d(L.ring + i * kStageBytes + kATileBytes, &map_x, L.full + 8 * i, (kb0 + i) * kBlockK, tok0, keep);
+      issued = pre;
+      for (int i = pre; i < nk; ++i) {
+        const int s = i % stages;
+        const uint32_t round = (uint32_t)(i / stages);
+        if (!mbar_wait(L.empty + 8 * s, (round - 1u) & 1u)) {
+          raise_error(kErrWaitEmpty);
+          *abort_ptr = 1;
+          ok = false;
+          break;
+        }
+        const uint32_t st = L.ring + s * kStageBytes;
+        const uint32_t bar = L.full + 8 * s;
+        mbar_expect_tx(bar, kStageBytes);
+        const int kx = (kb0 + i) * kBlockK;
+        if (MODE == kGemmGateUpSilu) {
+          tma_load_2d(st, &map_w0, bar, kx, m_tile * 64, stream);
+          tma_load_2d(st + kATileBytes / 2, &map_w1, bar, kx, m_tile * 64, stream);
+        } else {
+          tma_load_2d(st, &map_w0, bar, kx, m_tile * kTileM, stream);
+        }
+        tma_load_2d(st + kATileBytes, &map_x, bar, kx, tok0, keep);
+        ++issued;
+      }
+      if (!ok) {  // let the copies already in flight land before the CTA's memory goes away
+        for (int i = max(0, issued - stages); i < issued; ++i)
+          if (!mbar_wait(L.full + 8 * (i % stages), (uint32_t)(i / stages) & 1u)) raise_error(kErrWaitDrain);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    grid_dependency_wait();
+    if (lane == 0) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % stages;
+        if (!mbar_wait(L.full + 8 * s, (uint32_t)(i / stages) & 1u)) {
+          raise_error(kErrWaitFull);
+          *abort_ptr = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = L.ring + s * kStageBytes;
+        const uint64_t adesc = smem_desc_sw128(st);
+        const uint64_t bdesc = smem_desc_sw128(st + kATileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBlockK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
+          mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(L.empty + 8 * s);
+      }
+      mma_commit(L.accum);  // also on abort: completes once the issued MMAs are done
+    }
+    __syncwarp();
+  } else {
+    // ---------------- accumulator -> FP32 staging tile [N tokens][128 rows] ----------------
+    grid_dependency_wait();
+    const bool got = mbar_wait(L.accum, 0);
+    if (!got) {
+      if (lane == 0) raise_error(kErrWaitAccum);
+      *abort_ptr = 1;
+    }
+    tc_fence_after();
+    if (got && nk > 0) {
+      float* stage = reinterpret_cast<float*>(base_ptr);
+      const int row = warp * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < N; c += 16) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) stage[(c + i) * kTileM + row] = v[i];
+      }
+    } else if (got) {  // an empty K range contributes zeros
+      float* stage = reinterpret_cast<float*>(base_ptr);
+      const int row = warp * 32 + lane;
+      for (int c = 0; c < N; ++c) stage[c * kTileM + row] = 0.0f;
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  const bool aborted = *abort_ptr != 0;
+  cluster_sync_all();  // every CTA's partial tile is staged
+
+  // ---------------- rank-order reduction over the cluster + fused epilogue ----------------
+  const int n_valid = min(N, a.n_tok - tok0);
+  const int t_per = n_valid / (int)ksplit, t_rem = n_valid % (int)ksplit;
+  const int t_begin = (int)rank * t_per + min((int)rank, t_rem);
+  const int t_count = t_per + ((int)rank < t_rem ? 1 : 0);
+  constexpr int kQuads = (MODE == kGemmGateUpSilu) ? 16 : 32;  // 4-column groups per token
+  if (!aborted) {
+    for (int item = threadIdx.x; item < t_count * kQuads; item += kThreads) {
+      const int t = t_begin + item / kQuads;
+      const int q = item % kQuads;
+      const int tg = tok0 + t;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 acc2 = make_float4(0.f, 0.f, 0.f, 0.f);
+      const uint32_t off = base + (uint32_t)((t * kTileM + 4 * q) * 4);
+      for (uint32_t p = 0; p < ksplit; ++p) {
+        const float4 v = ld_cluster_v4(map_to_rank(off, p));
+        acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
+        acc.z = __fadd_rn(acc.z, v.z); acc.w = __fadd_rn(acc.w, v.w);
+        if (MODE == kGemmGateUpSilu) {
+          const float4 u = ld_cluster_v4(map_to_rank(off + 64 * 4, p));
+          acc2.x = __fadd_rn(acc2.x, u.x); acc2.y = __fadd_rn(acc2.y, u.y);
+          acc2.z = __fadd_rn(acc2.z, u.z); acc2.w = __fadd_rn(acc2.w, u.w);
+        }
+      }
+      float r[4] = {acc.x, acc.y, acc.z, acc.w};
+      if (MODE == kGemmGateUpSilu) {
+        const int j = m_tile * 64 + 4 * q;
+        if (j >= a.M) continue;
+        const float u[4] = {acc2.x, acc2.y, acc2.z, acc2.w};
+        uint32_t hb[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hb[e] = bf16_bits_pz(silu(bf16_round(r[e])) * bf16_round(u[e]));
+        uint2 pk = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+        *reinterpret_cast<uint2*>(a.out + (int64_t)tg * a.M + j) = pk;
+      } else {
+        const int n = m_tile * kTileM + 4 * q;
+        if (n >= a.M) continue;
+        uint16_t* dst = a.out + (int64_t)tg * a.M + n;
+        if (MODE == kGemmUpShared) {
+          if (a.shared) {
+            for (int s = 0; s < a.tp_s; ++s) {
+              const uint2 sv = *reinterpret_cast<const uint2*>(a.shared + ((int64_t)s * a.n_tok + tg) * a.M + n);
+              r[0] = __fadd_rn(r[0], bf16_lo(sv.x)); r[1] = __fadd_rn(r[1], bf16_hi(sv.x));
+              r[2] = __fadd_rn(r[2], bf16_lo(sv.y)); r[3] = __fadd_rn(r[3], bf16_hi(sv.y));
+            }
+          }
+        } else {  // down projection: BF16 d, optionally added into out
+          if (a.accumulate) {
+            const uint2 ov = *reinterpret_cast<const uint2*>(dst);
+            const float o[4] = {bf16_lo(ov.x), bf16_hi(ov.x), bf16_lo(ov.y), bf16_hi(ov.y)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) r[e] = __fadd_rn(o[e], __uint_as_float(bf16_bits_pz(r[e]) << 16));
+          }
+        }
+        uint2 pk = make_uint2(pack_bf16x2_pz(r[0], r[1]), pack_bf16x2_pz(r[2], r[3]));
+        *reinterpret_cast<uint2*>(dst) = pk;
+      }
+    }
+  }
+  launch_dependents();
+  cluster_sync_all();  // peers are done reading this CTA's staging tile
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---- host side ---------------------------------------------------------------------
+
+static int stage_bytes(int n_tile) { return kATileBytes + n_tile * kBlockK * 2; }
+
+GemmPlan plan_gemm(int mode, int M, int K, int b, int sms) {
+  GemmPlan p;
+  p.n_tile = b <= 16 ? 16 : b <= 32 ? 32 : b <= 64 ? 64 : 128;
+  const int tok_tiles = (b + p.n_tile - 1) / p.n_tile;
+  p.m_tiles = mode == kGemmGateUpSilu ? (M + 63) / 64 : (M + kTileM - 1) / kTileM;
+  const int kblocks = (K + kBlockK - 1) / kBlockK;
+  const int target = 2 * sms;  // two CTAs per SM
+  int ks = target / std::max(1, p.m_tiles * tok_tiles);
+  ks = std::max(1, std::min(ks, 8));
+  ks = std::min(ks, kblocks);
+  p.ksplit = ks;
+  const int per_cta = (kblocks + ks - 1) / ks;
+  const int budget = 110 * 1024;  // two CTAs per SM
+  const int sb = stage_bytes(p.n_tile);
+  int st = budget / sb;
+  st = std::max(2, std::min(st, kMaxStages));
+  st = std::min(st, std::max(2, per_cta));
+  // the FP32 staging tile reuses the ring
+  while (st * sb < p.n_tile * kTileM * 4) ++st;
+  p.stages = st;
+  return p;
+}
+
+static size_t smem_bytes(const GemmPlan& p) {
+  return 1024 + (size_t)p.stages * stage_bytes(p.n_tile) + 16 * (size_t)p.stages + 8 + 8 + 64;
+}
+
+template <int MODE, int N>
+static cudaError_t launch_t(const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& x,
+                            const GemmArgs& a, bool pdl, cudaStream_t stream) {
+  auto kernel = decode_gemm_kernel<MODE, N>;
+  const size_t smem = smem_bytes(p);
+  // Raise the kernel's shared-memory limit once per device to the largest
+  // plan (not per call, so that a captured stream sees only launches).
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured[dev] < (int)smem) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 200 * 1024;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.ksplit, p.m_tiles, (a.n_tok + N - 1) / N);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.ksplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, w0, w1, x, a, p.stages);
+}
+
+template <int MODE>
+static cudaError_t launch_mode(const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1,
+                               const CUtensorMap& x, const GemmArgs& a, bool pdl, cudaStream_t stream) {
+  switch (p.n_tile) {
+    case 16: return launch_t<MODE, 16>(p, w0, w1, x, a, pdl, stream);
+    case 32: return launch_t<MODE, 32>(p, w0, w1, x, a, pdl, stream);
+    case 64: return launch_t<MODE, 64>(p, w0, w1, x, a, pdl, stream);
+    case 128: return launch_t<MODE, 128>(p, w0, w1, x, a, pdl, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode_gemm(int mode, const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1,
+                               const CUtensorMap& x, const GemmArgs& a, bool pdl, cudaStream_t stream) {
+  switch (mode) {
+    case kGemmUpShared: return launch_mode<kGemmUpShared>(p, w0, w1, x, a, pdl, stream);
+    case kGemmGateUpSilu: return launch_mode<kGemmGateUpSilu>(p, w0, w1, x, a, pdl, stream);
+    case kGemmDown: return launch_mode<kGemmDown>(p, w0, w1, x, a, pdl, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moetail

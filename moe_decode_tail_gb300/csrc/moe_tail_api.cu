@@ -1,0 +1,314 @@
+// C ABI of the MoE decode tail: argument checks, TMA descriptors, launches.
+// Every check runs before the first CUDA call, so a refused call touches no
+// device state ([MS] _check_tail_args: refuse before anything launches).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/moe_tail.h"
+#include "kernels.h"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using moetail::EpArgs;
+using moetail::GemmArgs;
+using moetail::GemmPlan;
+using moetail::TpArgs;
+
+constexpr int kMaxTp = 32, kMaxK = 32, kMaxP = 32768;
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+Range span(const void* p, size_t bytes) { return Range{(uintptr_t)p, (uintptr_t)p + bytes}; }
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+int device_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cache[dev]) return cache[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+  if (dev < 64) cache[dev] = sms;
+  return sms;
+}
+
+int finish(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_TAIL_OK;
+  (void)cudaGetLastError();
+  return MOE_TAIL_ECUDA;
+}
+
+// ---- TMA descriptors --------------------------------------------------------
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+// Row-major BF16 matrix [rows][cols] read in boxes of box_rows x 64 columns
+// (128 bytes: the swizzle span), 128-byte swizzle; out-of-range boxes read zeros.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows,
+                    CUtensorMapL2promotion promo) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+int check_finalize_common(const void* w, int weight_dtype, const void* gamma, int b, int tp, int K, int P,
+                          void* out) {
+  if (b < 0 || tp < 1 || tp > kMaxTp || K < 1 || K > kMaxK || P < 8 || P > kMaxP || P % 8) return MOE_TAIL_EINVAL;
+  if (b > 65535) return MOE_TAIL_EINVAL;
+  if (weight_dtype != MOE_TAIL_W_FP32 && weight_dtype != MOE_TAIL_W_BF16) return MOE_TAIL_EINVAL;
+  if (b == 0) return MOE_TAIL_OK;
+  if (!w || !gamma || !out) return MOE_TAIL_EINVAL;
+  if (!aligned(gamma, 16) || !aligned(out, 16)) return MOE_TAIL_EINVAL;
+  if (!aligned(w, weight_dtype == MOE_TAIL_W_FP32 ? 4 : 2)) return MOE_TAIL_EINVAL;
+  return MOE_TAIL_OK;
+}
+
+}  // namespace
+
+// ============================================================================ EP finalize
+
+MOE_API int moe_tail_ep_finalize(const void* rows, int64_t rows_per_slot, const int32_t* permuted_idx,
+                                 const void* route_weights, int weight_dtype, const void* gamma,
+                                 float gain_center, float eps, int weight_before_norm, int b, int tp, int K,
+                                 int P, void* out, void* stream) {
+  int rc = check_finalize_common(route_weights, weight_dtype, gamma, b, tp, K, P, out);
+  if (rc != MOE_TAIL_OK || b == 0) return rc;
+  if (rows_per_slot < 0 || rows_per_slot > ((int64_t)1 << 31) - 1) return MOE_TAIL_EINVAL;
+  if (!permuted_idx || !aligned(permuted_idx, 4)) return MOE_TAIL_EINVAL;
+  if (rows_per_slot > 0 && (!rows || !aligned(rows, 16))) return MOE_TAIL_EINVAL;
+  const Range o = span(out, (size_t)b * P * 2);
+  const size_t wsz = weight_dtype == MOE_TAIL_W_FP32 ? 4 : 2;
+  if (overlaps(o, span(rows, (size_t)tp * rows_per_slot * P * 2)) ||
+      overlaps(o, span(permuted_idx, (size_t)tp * b * K * 4)) || overlaps(o, span(route_weights, (size_t)b * K * wsz)) ||
+      overlaps(o, span(gamma, (size_t)P * 2)))
+    return MOE_TAIL_EINVAL;
+  EpArgs a;
+  a.rows = static_cast<const uint16_t*>(rows);
+  a.rows_per_slot = rows_per_slot;
+  a.idx = permuted_idx;
+  a.w = route_weights;
+  a.gamma = static_cast<const uint16_t*>(gamma);
+  a.gain_center = gain_center;
+  a.eps = eps;
+  a.rcpP = (float)(1.0 / (double)P);
+  a.b = b;
+  a.tp = tp;
+  a.K = K;
+  a.P = P;
+  a.chunks = (P + 255) / 256;
+  a.out = static_cast<uint16_t*>(out);
+  return finish(moetail::launch_ep_finalize(a, weight_before_norm != 0, weight_dtype, device_sms(), 0,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+// ============================================================================ expert-TP finalize
+
+MOE_API int moe_tail_tp_finalize(const void* partials, int64_t num_rows, const int32_t* permuted_idx,
+                                 const void* route_weights, int weight_dtype, const void* gamma,
+                                 float gain_center, float eps, int weight_before_norm, int b, int tp, int K,
+                                 int P, void* out, void* stream) {
+  int rc = check_finalize_common(route_weights, weight_dtype, gamma, b, tp, K, P, out);
+  if (rc != MOE_TAIL_OK || b == 0) return rc;
+  if (num_rows < 0 || num_rows > ((int64_t)1 << 31) - 1) return MOE_TAIL_EINVAL;
+  if (!permuted_idx || !aligned(permuted_idx, 4)) return MOE_TAIL_EINVAL;
+  if (num_rows > 0 && (!partials || !aligned(partials, 16))) return MOE_TAIL_EINVAL;
+  const Range o = span(out, (size_t)b * P * 2);
+  const size_t wsz = weight_dtype == MOE_TAIL_W_FP32 ? 4 : 2;
+  if (overlaps(o, span(partials, (size_t)tp * num_rows * P * 2)) ||
+      overlaps(o, span(permuted_idx, (size_t)b * K * 4)) || overlaps(o, span(route_weights, (size_t)b * K * wsz)) ||
+      overlaps(o, span(gamma, (size_t)P * 2)))
+    return MOE_TAIL_EINVAL;
+  TpArgs a;
+  a.partials = static_cast<const uint16_t*>(partials);
+  a.num_rows = num_rows;
+  a.slot_stride = num_rows * P;
+  a.idx = permuted_idx;
+  a.w = route_weights;
+  a.gamma = static_cast<const uint16_t*>(gamma);
+  a.gain_center = gain_center;
+  a.eps = eps;
+  a.rcpP = (float)(1.0 / (double)P);
+  a.b = b;
+  a.tp = tp;
+  a.K = K;
+  a.P = P;
+  a.chunks = (P + 255) / 256;
+  a.out = static_cast<uint16_t*>(out);
+  return finish(moetail::launch_tp_finalize(a, weight_before_norm != 0, weight_dtype, device_sms(), 0,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+// ============================================================================ latent tail
+
+MOE_API size_t moe_tail_workspace_bytes(int which, int b, int dim) {
+  if (b < 0 || dim < 1 || (which != 0 && which != 1)) return 0;
+  return round256((size_t)b * dim * 2);
+}
+
+MOE_API int moe_tail_latent_up(const void* latent, const void* gamma, float eps, const void* w_up,
+                               const void* shared, int tp_s, int b, int tp, int L, int H, void* out,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (b < 0 || b > 65535 || tp < 1 || tp > kMaxTp || tp_s < 0 || tp_s > kMaxTp) return MOE_TAIL_EINVAL;
+  if (L < 8 || L > kMaxP || L % 8 || H < 8 || H % 8 || H > (1 << 24)) return MOE_TAIL_EINVAL;
+  if (b == 0) return MOE_TAIL_OK;
+  if (!latent || !gamma || !w_up || !out || !workspace) return MOE_TAIL_EINVAL;
+  if ((tp_s > 0) != (shared != nullptr)) return MOE_TAIL_EINVAL;
+  if (!aligned(latent, 16) || !aligned(gamma, 16) || !aligned(w_up, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 16) || (shared && !aligned(shared, 16)))
+    return MOE_TAIL_EINVAL;
+  if (workspace_bytes < moe_tail_workspace_bytes(0, b, L)) return MOE_TAIL_EINVAL;
+  const Range o = span(out, (size_t)b * H * 2);
+  const Range ws = span(workspace, (size_t)b * L * 2);
+  if (overlaps(o, span(latent, (size_t)tp * b * L * 2)) || overlaps(o, span(gamma, (size_t)L * 2)) ||
+      overlaps(o, span(w_up, (size_t)H * L * 2)) || overlaps(o, span(shared, (size_t)tp_s * b * H * 2)) ||
+      overlaps(o, ws) || overlaps(ws, span(latent, (size_t)tp * b * L * 2)) || overlaps(ws, span(w_up, (size_t)H * L * 2)) ||
+      overlaps(ws, span(shared, (size_t)tp_s * b * H * 2)) || overlaps(ws, span(gamma, (size_t)L * 2)))
+    return MOE_TAIL_EINVAL;
+
+  const GemmPlan plan = moetail::plan_gemm(moetail::kGemmUpShared, H, L, b, device_sms());
+  CUtensorMap mw, mx;
+  if (!encode_bf16_2d(&mw, w_up, H, L, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&mx, workspace, b, L, plan.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+    return MOE_TAIL_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // 1. y = RMS norm of the slot-summed latent (an expert-TP finalize with one
+  //    "route" per token: row = token, unit weight, gain center 0).
+  TpArgs n;
+  n.partials = static_cast<const uint16_t*>(latent);
+  n.num_rows = b;
+  n.slot_stride = (int64_t)b * L;
+  n.idx = nullptr;
+  n.w = nullptr;
+  n.gamma = static_cast<const uint16_t*>(gamma);
+  n.gain_center = 0.0f;
+  n.eps = eps;
+  n.rcpP = (float)(1.0 / (double)L);
+  n.b = b;
+  n.tp = tp;
+  n.K = 1;
+  n.P = L;
+  n.chunks = (L + 255) / 256;
+  n.out = static_cast<uint16_t*>(workspace);
+  cudaError_t e = moetail::launch_tp_finalize(n, false, moetail::kWeightUnit, device_sms(), 0, st);
+  if (e != cudaSuccess) return finish(e);
+
+  // 2. out = y . w_up^T + sum_s shared[s]
+  GemmArgs g;
+  g.M = H;
+  g.K = L;
+  g.n_tok = b;
+  g.kblocks = (L + 63) / 64;
+  g.shared = static_cast<const uint16_t*>(shared);
+  g.tp_s = tp_s;
+  g.out = static_cast<uint16_t*>(out);
+  g.accumulate = 0;
+  return finish(moetail::launch_decode_gemm(moetail::kGemmUpShared, plan, mw, mw, mx, g, true, st));
+}
+
+// ============================================================================ shared expert
+
+MOE_API int moe_shared_expert(const void* x, const void* w_gate, const void* w_up, const void* w_down, int b,
+                              int H, int I, void* out, int accumulate, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (b < 0 || b > 65535 || H < 8 || H % 8 || I < 8 || I % 8 || H > (1 << 24) || I > (1 << 24))
+    return MOE_TAIL_EINVAL;
+  if (b == 0) return MOE_TAIL_OK;
+  if (!x || !w_gate || !w_up || !w_down || !out || !workspace) return MOE_TAIL_EINVAL;
+  if (!aligned(x, 16) || !aligned(w_gate, 16) || !aligned(w_up, 16) || !aligned(w_down, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 16))
+    return MOE_TAIL_EINVAL;
+  if (workspace_bytes < moe_tail_workspace_bytes(1, b, I)) return MOE_TAIL_EINVAL;
+  const Range o = span(out, (size_t)b * H * 2);
+  const Range ws = span(workspace, (size_t)b * I * 2);
+  const Range rx = span(x, (size_t)b * H * 2), rg = span(w_gate, (size_t)I * H * 2),
+              ru = span(w_up, (size_t)I * H * 2), rd = span(w_down, (size_t)H * I * 2);
+  if (overlaps(o, rx) || overlaps(o, rg) || overlaps(o, ru) || overlaps(o, rd) || overlaps(o, ws) ||
+      overlaps(ws, rx) || overlaps(ws, rg) || overlaps(ws, ru) || overlaps(ws, rd))
+    return MOE_TAIL_EINVAL;
+
+  const int sms = device_sms();
+  const GemmPlan p1 = moetail::plan_gemm(moetail::kGemmGateUpSilu, I, H, b, sms);
+  const GemmPlan p2 = moetail::plan_gemm(moetail::kGemmDown, H, I, b, sms);
+  CUtensorMap mg, mu, mx, md, mh;
+  if (!encode_bf16_2d(&mg, w_gate, I, H, 64, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&mu, w_up, I, H, 64, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&mx, x, b, H, p1.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
+      !encode_bf16_2d(&md, w_down, H, I, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&mh, workspace, b, I, p2.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+    return MOE_TAIL_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  GemmArgs g;
+  g.M = I;
+  g.K = H;
+  g.n_tok = b;
+  g.kblocks = (H + 63) / 64;
+  g.shared = nullptr;
+  g.tp_s = 0;
+  g.out = static_cast<uint16_t*>(workspace);
+  g.accumulate = 0;
+  cudaError_t e = moetail::launch_decode_gemm(moetail::kGemmGateUpSilu, p1, mg, mu, mx, g, false, st);
+  if (e != cudaSuccess) return finish(e);
+
+  GemmArgs d;
+  d.M = H;
+  d.K = I;
+  d.n_tok = b;
+  d.kblocks = (I + 63) / 64;
+  d.shared = nullptr;
+  d.tp_s = 0;
+  d.out = static_cast<uint16_t*>(out);
+  d.accumulate = accumulate != 0;
+  return finish(moetail::launch_decode_gemm(moetail::kGemmDown, p2, md, md, mh, d, true, st));
+}
+
+// ============================================================================ misc
+
+MOE_API const char* moe_tail_status_str(int status) {
+  switch (status) {
+    case MOE_TAIL_OK: return "ok";
+    case MOE_TAIL_EINVAL: return "invalid argument";
+    case MOE_TAIL_ECUDA: return "CUDA error";
+    case MOE_TAIL_ENOTSUP: return "not supported";
+    default: return "unknown status";
+  }
+}
+
+MOE_API int moe_tail_take_device_error(unsigned int* bits) {
+  if (!bits) return MOE_TAIL_EINVAL;
+  return finish(moetail::take_device_error(bits));
+}

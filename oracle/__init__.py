@@ -47,6 +47,7 @@ def lib():
         L.oracle_latent_norm.argtypes = [P, P, f32, i32, i32, i32, P]
         L.oracle_latent_up.argtypes = [P, P, P, i32, i32, i32, i32, P]
         L.oracle_shared_expert.argtypes = [P, P, P, P, i32, i32, i32, P, P, i32]
+        L.oracle_shared_down.argtypes = [P, P, i32, i32, i32, P, i32]
         L.oracle_sum_of_squares.argtypes = [P, i32]
         L.oracle_sum_of_squares.restype = f32
         L.oracle_bf16_from_f32.argtypes = [f32]
@@ -56,7 +57,7 @@ def lib():
         L.oracle_f32_from_bf16.argtypes = [ctypes.c_uint16]
         L.oracle_f32_from_bf16.restype = f32
         for name in ("oracle_ep_finalize", "oracle_tp_finalize", "oracle_latent_norm",
-                     "oracle_latent_up", "oracle_shared_expert"):
+                     "oracle_latent_up", "oracle_shared_expert", "oracle_shared_down"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -143,6 +144,15 @@ def shared_expert(x, w_gate, w_up, w_down, b, H, I, out_in=None, accumulate=True
     _check(lib().oracle_shared_expert(_ptr(x), _ptr(w_gate), _ptr(w_up), _ptr(w_down), b, H, I,
                                       _ptr(h), _ptr(out), int(accumulate)), "shared_expert")
     return h, out
+
+
+def shared_down(h, w_down, b, H, I, out_in=None, accumulate=True):
+    """BF16 [b, H]: the shared expert's down projection of h [b, I] (double),
+    added into out_in (accumulate) or alone."""
+    h, w_down = _c(h), _c(w_down)
+    out = _c(out_in).clone() if accumulate else torch.empty((b, H), dtype=torch.bfloat16)
+    _check(lib().oracle_shared_down(_ptr(h), _ptr(w_down), b, H, I, _ptr(out), int(accumulate)), "shared_down")
+    return out
 
 
 def sum_of_squares(v: np.ndarray) -> float:

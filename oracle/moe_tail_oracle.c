@@ -186,7 +186,9 @@ int oracle_ep_finalize(const uint16_t* rows, int64_t rows_per_slot, const int32_
  * partials : BF16 [tp][num_rows][P]  slot s's K-partial of every route row
  * idx      : int32 [b][K]            route (t,k)'s row, the same in every slot
  * x_r = bf16(sum over s in order of partial_s[row]); out = bf16(sum over routes
- * in order of w * norm(x_r)), from +0.  A row outside [0, num_rows) loads as 0. */
+ * in order of w * norm(x_r)), from +0.  A route whose row is outside [0, num_rows)
+ * contributes nothing (the page predicates its loads off; a zero row would add
+ * w * 0, the same bits for any finite w). */
 int oracle_tp_finalize(const uint16_t* partials, int64_t num_rows, const int32_t* idx,
                        const void* w, int w_is_bf16, const uint16_t* gamma, float gain_center,
                        float eps, int wbn, int b, int tp, int K, int P, uint16_t* out) {
@@ -200,14 +202,11 @@ int oracle_tp_finalize(const uint16_t* partials, int64_t num_rows, const int32_t
         for (int c = 0; c < P; ++c) acc[c] = 0.0f;
         for (int k = 0; k < K; ++k) {
             int32_t j = idx[(int64_t)t * K + k];
-            int local = j >= 0 && (int64_t)j < num_rows;
+            if (j < 0 || (int64_t)j >= num_rows) continue; /* no row: contributes nothing */
             for (int c = 0; c < P; ++c) {
                 float sum = 0.0f;
-                for (int s = 0; s < tp; ++s) {
-                    float q = local ? oracle_f32_from_bf16(partials[((int64_t)s * num_rows + j) * P + c])
-                                    : 0.0f;
-                    sum = sum + q;
-                }
+                for (int s = 0; s < tp; ++s)
+                    sum = sum + oracle_f32_from_bf16(partials[((int64_t)s * num_rows + j) * P + c]);
                 x[c] = bf16_round(sum);
             }
             add_normalised_route(x, g, wbn, eps, route_weight(w, w_is_bf16, (int64_t)t * K + k), P,
@@ -266,34 +265,15 @@ int oracle_latent_up(const uint16_t* y, const uint16_t* w_up, const uint16_t* sh
     return 0;
 }
 
-/* ---- fused shared expert ([KS]) --------------------------------------------
- * x : BF16 [b][H]; w_gate, w_up : BF16 [I][H]; w_down : BF16 [H][I]
- * h (optional out) : BF16 [b][I]; out : BF16 [b][H] (read too if accumulate)
- * gate = bf16(x . w_gate), up = bf16(x . w_up), h = bf16(silu(gate) * up),
- * d = h . w_down; out = bf16(out + bf16(d)) (accumulate) or bf16(d). */
-int oracle_shared_expert(const uint16_t* x, const uint16_t* w_gate, const uint16_t* w_up,
-                         const uint16_t* w_down, int b, int H, int I, uint16_t* h_out,
-                         uint16_t* out, int accumulate) {
+/* ---- shared expert down projection ([KS] SharedBase.push) ------------------
+ * h : BF16 [b][I]; w_down : BF16 [H][I]; out : BF16 [b][H] (read too if accumulate)
+ * d = h . w_down (double); out = bf16(out + bf16(d)) (accumulate) or bf16(d). */
+int oracle_shared_down(const uint16_t* h, const uint16_t* w_down, int b, int H, int I, uint16_t* out,
+                       int accumulate) {
     if (b < 0 || H < 1 || I < 1) return -1;
-    double* xd = malloc(sizeof(double) * H);
     double* hd = malloc(sizeof(double) * I);
     for (int t = 0; t < b; ++t) {
-        for (int c = 0; c < H; ++c) xd[c] = oracle_f32_from_bf16(x[(int64_t)t * H + c]);
-        for (int i = 0; i < I; ++i) {
-            const uint16_t* gr = w_gate + (int64_t)i * H;
-            const uint16_t* ur = w_up + (int64_t)i * H;
-            double ga = 0.0, ua = 0.0;
-            for (int c = 0; c < H; ++c) {
-                ga += xd[c] * (double)oracle_f32_from_bf16(gr[c]);
-                ua += xd[c] * (double)oracle_f32_from_bf16(ur[c]);
-            }
-            double gate = oracle_f32_from_bf16(oracle_bf16_from_f64(ga));
-            double up = oracle_f32_from_bf16(oracle_bf16_from_f64(ua));
-            double silu = gate / (1.0 + exp(-gate));
-            uint16_t hb = pz(oracle_bf16_from_f64(silu * up));
-            if (h_out) h_out[(int64_t)t * I + i] = hb;
-            hd[i] = oracle_f32_from_bf16(hb);
-        }
+        for (int i = 0; i < I; ++i) hd[i] = oracle_f32_from_bf16(h[(int64_t)t * I + i]);
         for (int n = 0; n < H; ++n) {
             const uint16_t* dr = w_down + (int64_t)n * I;
             double acc = 0.0;
@@ -308,6 +288,36 @@ int oracle_shared_expert(const uint16_t* x, const uint16_t* w_gate, const uint16
             }
         }
     }
-    free(xd); free(hd);
+    free(hd);
     return 0;
+}
+
+/* ---- fused shared expert ([KS]) --------------------------------------------
+ * x : BF16 [b][H]; w_gate, w_up : BF16 [I][H]; w_down : BF16 [H][I]
+ * h (out) : BF16 [b][I]; out : BF16 [b][H] (read too if accumulate)
+ * gate = bf16(x . w_gate), up = bf16(x . w_up), h = bf16(silu(gate) * up),
+ * then the down projection above. */
+int oracle_shared_expert(const uint16_t* x, const uint16_t* w_gate, const uint16_t* w_up,
+                         const uint16_t* w_down, int b, int H, int I, uint16_t* h_out,
+                         uint16_t* out, int accumulate) {
+    if (b < 0 || H < 1 || I < 1 || !h_out) return -1;
+    double* xd = malloc(sizeof(double) * H);
+    for (int t = 0; t < b; ++t) {
+        for (int c = 0; c < H; ++c) xd[c] = oracle_f32_from_bf16(x[(int64_t)t * H + c]);
+        for (int i = 0; i < I; ++i) {
+            const uint16_t* gr = w_gate + (int64_t)i * H;
+            const uint16_t* ur = w_up + (int64_t)i * H;
+            double ga = 0.0, ua = 0.0;
+            for (int c = 0; c < H; ++c) {
+                ga += xd[c] * (double)oracle_f32_from_bf16(gr[c]);
+                ua += xd[c] * (double)oracle_f32_from_bf16(ur[c]);
+            }
+            double gate = oracle_f32_from_bf16(oracle_bf16_from_f64(ga));
+            double up = oracle_f32_from_bf16(oracle_bf16_from_f64(ua));
+            double silu = gate / (1.0 + exp(-gate));
+            h_out[(int64_t)t * I + i] = pz(oracle_bf16_from_f64(silu * up));
+        }
+    }
+    free(xd);
+    return oracle_shared_down(h_out, w_down, b, H, I, out, accumulate);
 }

@@ -1,0 +1,158 @@
+"""The C ABI library: it builds, loads, exports exactly what include/moe_tail.h
+declares, and refuses bad arguments on the host before any CUDA call (these
+tests pass fake device addresses and never launch anything)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from moe_decode_tail_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_tail.h")
+EINVAL, OK = 1, 0
+FAKE = 0x7F0000000000  # a 4 KiB-aligned address no call may dereference
+
+# The refusal tests hand the library fake device addresses: run them only where
+# no GPU is visible, so a regression in the checks can never launch on them.
+host_only = pytest.mark.skipif(torch.cuda.is_available(), reason="fake device addresses: host-only")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    import moe_decode_tail_gb300 as mt
+
+    return mt.lib()
+
+
+def declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(moe_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_four_calls_and_helpers():
+    names = declared()
+    for n in ("moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up", "moe_shared_expert",
+              "moe_tail_workspace_bytes", "moe_tail_status_str", "moe_tail_take_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared():
+        assert hasattr(lib, n), n
+
+
+def test_library_exports_nothing_else():
+    out = subprocess.run(["nm", "-D", "--defined-only", cuda_build.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.split() and line.split()[-2] in "TtDdBbRr"}
+    exported = {e for e in exported if not e.startswith("_")}
+    assert exported == set(declared())
+
+
+def a(x=0):
+    return ctypes.c_void_p(FAKE + x)
+
+
+def ep(lib, **kw):
+    args = dict(rows=a(), rps=16, idx=a(), w=a(), wd=0, gamma=a(), gc=1.0, eps=1e-6, wbn=1, b=4, tp=2, K=4, P=512,
+                out=a(1 << 20), stream=None)
+    args.update(kw)
+    return lib.moe_tail_ep_finalize(args["rows"], args["rps"], args["idx"], args["w"], args["wd"], args["gamma"],
+                                    args["gc"], args["eps"], args["wbn"], args["b"], args["tp"], args["K"], args["P"],
+                                    args["out"], args["stream"])
+
+
+def tp(lib, **kw):
+    args = dict(q=a(), rows=16, idx=a(), w=a(), wd=0, gamma=a(), gc=1.0, eps=1e-6, wbn=1, b=4, tp=2, K=4, P=512,
+                out=a(1 << 20), stream=None)
+    args.update(kw)
+    return lib.moe_tail_tp_finalize(args["q"], args["rows"], args["idx"], args["w"], args["wd"], args["gamma"],
+                                    args["gc"], args["eps"], args["wbn"], args["b"], args["tp"], args["K"], args["P"],
+                                    args["out"], args["stream"])
+
+
+@host_only
+@pytest.mark.parametrize("fn", [ep, tp])
+@pytest.mark.parametrize("bad", [
+    dict(tp=0), dict(tp=33), dict(K=0), dict(K=33), dict(P=7), dict(P=4), dict(P=516 + 2), dict(P=32776),
+    dict(b=-1), dict(b=65536), dict(wd=2), dict(gamma=None), dict(out=None), dict(w=None), dict(idx=None),
+    dict(out=a(8)), dict(gamma=a(4)), dict(idx=a(2)), dict(w=a(2)),
+    dict(out=a(0)),  # out overlaps the rows / partials
+])
+def test_finalize_refuses_bad_arguments(lib, fn, bad):
+    assert fn(lib, **bad) == EINVAL
+
+
+@host_only
+@pytest.mark.parametrize("fn", [ep, tp])
+def test_finalize_b_zero_does_nothing(lib, fn):
+    # b = 0 succeeds without touching memory, even with null pointers
+    assert fn(lib, b=0, rows=None, idx=None, w=None, gamma=None, out=None) == OK if fn is ep else \
+        fn(lib, b=0, q=None, idx=None, w=None, gamma=None, out=None) == OK
+
+
+@host_only
+def test_bf16_weights_need_only_2_byte_alignment_but_fp32_need_4(lib):
+    assert ep(lib, w=a(2), wd=0) == EINVAL
+    # with BF16 weights a 2-byte aligned pointer passes the checks; moving out
+    # to overlap the gamma vector is refused instead, so nothing launches
+    assert ep(lib, w=a(2), wd=1, out=a(0), rps=0, rows=None) == EINVAL
+
+
+def latent(lib, **kw):
+    args = dict(lat=a(), gamma=a(1 << 24), eps=1e-6, w=a(2 << 24), sh=a(3 << 24), tp_s=8, b=16, tp=8, L=3584, H=7168,
+                out=a(4 << 24), ws=a(5 << 24), wsb=16 * 3584 * 2, stream=None)
+    args.update(kw)
+    return lib.moe_tail_latent_up(args["lat"], args["gamma"], args["eps"], args["w"], args["sh"], args["tp_s"],
+                                  args["b"], args["tp"], args["L"], args["H"], args["out"], args["ws"], args["wsb"],
+                                  args["stream"])
+
+
+@host_only
+@pytest.mark.parametrize("bad", [
+    dict(tp=0), dict(tp_s=-1), dict(tp_s=33), dict(L=3583), dict(H=7170), dict(L=4), dict(b=-2),
+    dict(sh=None), dict(tp_s=0), dict(ws=None), dict(wsb=16 * 3584 * 2 - 1), dict(out=a(5 << 24)),
+    dict(ws=a(4 << 24)), dict(lat=a(3)), dict(w=a(8)), dict(L=40000),
+])
+def test_latent_up_refuses_bad_arguments(lib, bad):
+    assert latent(lib, **bad) == EINVAL
+
+
+@host_only
+def test_latent_up_b_zero(lib):
+    assert latent(lib, b=0, lat=None, w=None, out=None, ws=None) == OK
+
+
+def shared(lib, **kw):
+    args = dict(x=a(), wg=a(1 << 28), wu=a(2 << 28), wd=a(3 << 28), b=64, H=7168, I=6144, out=a(4 << 28), acc=1,
+                ws=a(5 << 28), wsb=64 * 6144 * 2, stream=None)
+    args.update(kw)
+    return lib.moe_shared_expert(args["x"], args["wg"], args["wu"], args["wd"], args["b"], args["H"], args["I"],
+                                 args["out"], args["acc"], args["ws"], args["wsb"], args["stream"])
+
+
+@host_only
+@pytest.mark.parametrize("bad", [
+    dict(H=7169), dict(I=6140 + 2), dict(H=0), dict(b=-1), dict(x=None), dict(wd=None), dict(ws=None),
+    dict(wsb=64 * 6144 * 2 - 2), dict(out=a(0)), dict(ws=a(4 << 28)), dict(x=a(8)), dict(out=a(4 << 28 | 8)),
+])
+def test_shared_expert_refuses_bad_arguments(lib, bad):
+    assert shared(lib, **bad) == EINVAL
+
+
+def test_workspace_bytes(lib):
+    assert lib.moe_tail_workspace_bytes(0, 16, 3584) == 16 * 3584 * 2
+    assert lib.moe_tail_workspace_bytes(1, 3, 100) == 768  # rounded up to 256 bytes
+    assert lib.moe_tail_workspace_bytes(2, 3, 100) == 0
+    assert lib.moe_tail_workspace_bytes(0, -1, 100) == 0
+
+
+def test_status_strings(lib):
+    assert lib.moe_tail_status_str(0) == b"ok"
+    assert lib.moe_tail_status_str(1) == b"invalid argument"
+    assert lib.moe_tail_status_str(99) == b"unknown status"

@@ -1,0 +1,404 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Finalize outputs and the latent norm's y must be bit-exact BF16; the GEMM
+paths (latent up-projection, shared expert h and output) must satisfy
+|gpu - oracle| <= 2 ulp_bf16(|oracle|) + 1e-3 element by element.  Inputs are
+the seeded decode workloads (full sizes where the oracle finishes in seconds,
+sampled tokens otherwise) plus ragged, degenerate and crafted-rounding cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_decode_tail_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def mt():
+    from moe_decode_tail_gb300 import build as cuda_build
+
+    cuda_build.build()
+    oracle.build()
+    import moe_decode_tail_gb300
+
+    moe_decode_tail_gb300.lib()
+    yield moe_decode_tail_gb300
+    assert moe_decode_tail_gb300.moe_tail_take_device_error() == 0
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy()
+
+
+def assert_bitexact(got, ref, what=""):
+    g, r = bits(got), bits(ref)
+    if not np.array_equal(g, r):
+        bad = np.argwhere(g != r)
+        i = tuple(bad[0])
+        raise AssertionError(f"{what}: {len(bad)} of {g.size} differ; first at {i}: "
+                             f"gpu {got.float().cpu()[i].item()!r} oracle {ref.float()[i].item()!r}")
+
+
+def assert_gemm_close(got, ref, what=""):
+    g = got.detach().float().cpu()
+    r = ref.float()
+    ulp = torch.exp2(torch.floor(torch.log2(r.abs().clamp_min(2.0 ** -126))) - 7)
+    err = (g - r).abs()
+    ok = err <= 2 * ulp + 1e-3
+    if not bool(ok.all()):
+        i = tuple(torch.nonzero(~ok)[0].tolist())
+        raise AssertionError(f"{what}: {int((~ok).sum())} of {ok.numel()} out of tolerance; first at {i}: "
+                             f"gpu {g[i].item()!r} oracle {r[i].item()!r}")
+
+
+def assert_accumulated_close(got, ref, d_ref, what=""):
+    """out = bf16(out_in + bf16(d)): a 1-ulp difference in the pushed bf16(d)
+    (allowed by the GEMM tolerance) carries into out whole, so the bound is
+    2 ulp(|out|) + ulp(|d|) + 1e-3."""
+    g = got.detach().float().cpu()
+    r, dr = ref.float(), d_ref.float()
+    ulp = lambda v: torch.exp2(torch.floor(torch.log2(v.abs().clamp_min(2.0 ** -126))) - 7)
+    ok = (g - r).abs() <= 2 * ulp(r) + ulp(dr) + 1e-3
+    if not bool(ok.all()):
+        i = tuple(torch.nonzero(~ok)[0].tolist())
+        raise AssertionError(f"{what}: {int((~ok).sum())} of {ok.numel()} out of tolerance; first at {i}: "
+                             f"gpu {g[i].item()!r} oracle {r[i].item()!r} d {dr[i].item()!r}")
+
+
+# ------------------------------------------------------------------ EP finalize
+
+def run_ep(mt, d, out=None, **kw):
+    a = dict(d)
+    a.update(kw)
+    if out is None:
+        out = torch.full((a["b"], a["P"]), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mt.moe_tail_ep_finalize(a["rows"].to(DEV), a["idx"].to(DEV), a["w"].to(DEV), a["gamma"].to(DEV), out,
+                            gain_center=a["gain_center"], eps=a["eps"], weight_before_norm=a["weight_before_norm"])
+    torch.cuda.synchronize()
+    return out
+
+
+def ref_ep(d, **kw):
+    a = dict(d)
+    a.update(kw)
+    return oracle.ep_finalize(a["rows"], a["rows_per_slot"], a["idx"], a["w"], a["gamma"], a["gain_center"],
+                              a["eps"], a["weight_before_norm"], a["b"], a["tp"], a["K"], a["P"])
+
+
+@pytest.mark.parametrize("wbn", [True, False])
+def test_ep_tiny(mt, wbn):
+    d = synth.config(1, weight_before_norm=wbn)
+    assert_bitexact(run_ep(mt, d), ref_ep(d), "EP b=4 tp=2 P=512")
+
+
+@pytest.mark.parametrize("wbn", [True, False])
+def test_ep_decode_full(mt, wbn):
+    d = synth.config(2, weight_before_norm=wbn)
+    assert_bitexact(run_ep(mt, d), ref_ep(d), "EP b=64 tp=8 P=4096 K=8")
+
+
+def test_ep_bf16_route_weights(mt):
+    d = synth.config(2)
+    d["w"] = d["w"].to(torch.bfloat16)
+    assert_bitexact(run_ep(mt, d), ref_ep(d), "EP bf16 weights")
+
+
+@pytest.mark.parametrize("kw", [
+    dict(b=1, tp=1, P=8, K=1, num_experts=1),             # smallest
+    dict(b=5, tp=3, P=264, K=3, num_experts=9),           # ragged last chunk
+    dict(b=7, tp=4, P=1000, K=5, num_experts=16),         # P not a multiple of 256
+    dict(b=3, tp=32, P=512, K=32, num_experts=64),        # widest slots and routes
+    dict(b=2, tp=8, P=32768, K=8, num_experts=64),        # widest row
+    dict(b=130, tp=2, P=2048, K=8, num_experts=32),       # many tokens
+])
+def test_ep_shapes(mt, kw):
+    d = synth.ep_finalize_inputs(0xE9 + kw["P"], **kw)
+    assert_bitexact(run_ep(mt, d), ref_ep(d), f"EP {kw}")
+
+
+def test_ep_non_local_and_out_of_range_indices(mt):
+    d = synth.config(2, b=16)
+    idx = d["idx"].clone()
+    idx[:, 3, :] = -1                       # token 3: nothing local anywhere
+    idx[2, 5, :] = d["rows_per_slot"] + 3    # out of range on the high side
+    idx[0, 6, :] = -100
+    d["idx"] = idx
+    out = run_ep(mt, d)
+    assert_bitexact(out, ref_ep(d), "EP non-local")
+    assert np.all(bits(out)[3] == 0)
+
+
+def test_ep_many_local_routes_per_slot(mt):
+    # every route of every token local to every slot: tp * K = 64 rows per token
+    b, tp, K, P, R = 4, 8, 8, 1024, 16
+    rows = synth.bf16(synth.normal(77, 1, tp * R * P), (tp, R, P))
+    idx = torch.from_numpy((synth.u64(77, 2, tp * b * K) % R).astype(np.int32).reshape(tp, b, K))
+    d = dict(rows=rows, rows_per_slot=R, idx=idx, w=synth.softmax_weights(77, 3, b, K),
+             gamma=synth.bf16(synth.normal(77, 4, P, std=0.1), (P,)), gain_center=1.0, eps=1e-6,
+             weight_before_norm=True, b=b, tp=tp, K=K, P=P)
+    assert_bitexact(run_ep(mt, d), ref_ep(d), "EP 64 local rows")
+
+
+def test_ep_b_zero_leaves_out_untouched(mt):
+    d = synth.config(1)
+    out = torch.full((4, 512), 3.0, dtype=torch.bfloat16, device=DEV)
+    mt.moe_tail_ep_finalize(d["rows"].to(DEV), d["idx"][:, :0].contiguous().to(DEV), d["w"][:0].contiguous().to(DEV),
+                            d["gamma"].to(DEV), out[:0])
+    torch.cuda.synchronize()
+    assert bool((out.float() == 3.0).all())
+
+
+def _const_ep(weights_per_slot, P=256, row_value=1.0, gamma=0.0, gc=1.0, eps=0.0, wbn=True):
+    tp = len(weights_per_slot)
+    K = sum(len(ws) for ws in weights_per_slot)
+    R = max(1, max(len(ws) for ws in weights_per_slot))
+    idx = np.full((tp, 1, K), -1, dtype=np.int32)
+    w = np.zeros((1, K), dtype=np.float32)
+    k = 0
+    for s, ws in enumerate(weights_per_slot):
+        for r, wv in enumerate(ws):
+            idx[s, 0, k] = r
+            w[0, k] = wv
+            k += 1
+    return dict(rows=torch.full((tp, R, P), row_value).to(torch.bfloat16), rows_per_slot=R,
+                idx=torch.from_numpy(idx), w=torch.from_numpy(w), gamma=torch.full((P,), gamma).to(torch.bfloat16),
+                gain_center=gc, eps=eps, weight_before_norm=wbn, b=1, tp=tp, K=K, P=P)
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(weights_per_slot=[[1.0 + 2.0 ** -8 + 2.0 ** -20], [2.0 ** -8]]), 1.015625),   # per-slot rounding
+    (dict(weights_per_slot=[[1.0], [2.0 ** -8], [2.0 ** -24], [2.0 ** -24]]), 1.0),       # slot order
+    (dict(weights_per_slot=[[1.0 + 2.0 ** -8, 2.0 ** -24, 2.0 ** -24]]), 1.0),            # route order
+    (dict(weights_per_slot=[[1.0]], row_value=1.75 * 2.0 ** -75, gamma=1.625 * 2.0 ** -73, gc=0.0,
+          eps=2.0 ** -100, wbn=True), 1.5 * 2.0 ** -97),                                  # subnormals kept,
+    (dict(weights_per_slot=[[1.0]], row_value=1.75 * 2.0 ** -75, gamma=1.625 * 2.0 ** -73, gc=0.0,
+          eps=2.0 ** -100, wbn=False), 1.421875 * 2.0 ** -97),                            # product order
+])
+def test_ep_crafted_rounding_cases(mt, case, expect):
+    # the oracle pins' hand-derived cases, on the GPU
+    d = _const_ep(**case)
+    out = run_ep(mt, d)
+    assert bool((out.float().cpu() == expect).all()), out.float().cpu()[0, :4]
+
+
+@pytest.mark.parametrize("pattern", ["lane", "butterfly", "chunks"])
+def test_ep_sum_of_squares_tree(mt, pattern):
+    # one route, w = 1, gains 1, eps 0: out = bf16(x / sqrt(ss / P)).  The rows
+    # are the oracle pins' tree cases, whose ss differ by tree shape; the GPU
+    # must give the oracle's bits for P = 4096 split over a cluster.
+    P = 4096
+    v = torch.zeros(P)
+    if pattern == "lane":
+        v[0], v[1:8] = 4096.0, 1.0
+    elif pattern == "butterfly":
+        v[0], v[8:256:8] = 4096.0, 1.0
+    else:
+        v[0], v[256::256] = 4096.0, 1.0
+    d = _const_ep([[1.0]], P=P)
+    d["rows"] = v.to(torch.bfloat16).reshape(1, 1, P)
+    assert_bitexact(run_ep(mt, d), ref_ep(d), f"SS tree {pattern}")
+
+
+# ------------------------------------------------------------------ expert-TP finalize
+
+def run_tp(mt, d, **kw):
+    a = dict(d)
+    a.update(kw)
+    out = torch.full((a["b"], a["P"]), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mt.moe_tail_tp_finalize(a["partials"].to(DEV), a["idx"].to(DEV), a["w"].to(DEV), a["gamma"].to(DEV), out,
+                            gain_center=a["gain_center"], eps=a["eps"], weight_before_norm=a["weight_before_norm"])
+    torch.cuda.synchronize()
+    return out
+
+
+def ref_tp(d, **kw):
+    a = dict(d)
+    a.update(kw)
+    return oracle.tp_finalize(a["partials"], a["num_rows"], a["idx"], a["w"], a["gamma"], a["gain_center"],
+                              a["eps"], a["weight_before_norm"], a["b"], a["tp"], a["K"], a["P"])
+
+
+@pytest.mark.parametrize("wbn", [True, False])
+def test_tp_decode_full(mt, wbn):
+    d = synth.config(3, weight_before_norm=wbn)
+    assert_bitexact(run_tp(mt, d), ref_tp(d), "TP b=128 tp=8 P=4096 K=8")
+
+
+def test_tp_bf16_weights_and_bad_indices(mt):
+    d = synth.config(3, b=32)
+    d["w"] = d["w"].to(torch.bfloat16)
+    idx = d["idx"].clone()
+    idx[4, 2] = -1
+    idx[9, :] = d["num_rows"]
+    d["idx"] = idx
+    out = run_tp(mt, d)
+    assert_bitexact(out, ref_tp(d), "TP bf16 weights, bad indices")
+    assert np.all(bits(out)[9] == 0)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(b=1, tp=1, P=8, K=1), dict(b=9, tp=3, P=264, K=5), dict(b=4, tp=32, P=512, K=32),
+    dict(b=3, tp=2, P=32768, K=2), dict(b=300, tp=2, P=768, K=3),
+])
+def test_tp_shapes(mt, kw):
+    d = synth.tp_finalize_inputs(0x7B + kw["P"], num_experts=64, **kw)
+    assert_bitexact(run_tp(mt, d), ref_tp(d), f"TP {kw}")
+
+
+# ------------------------------------------------------------------ latent tail
+
+def run_latent(mt, d):
+    b, L, H = d["b"], d["L"], d["H"]
+    ws = torch.full((mt.moe_tail_workspace_bytes(0, b, L),), 0xFF, dtype=torch.uint8, device=DEV)
+    out = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    sh = None if d["shared"] is None else d["shared"].to(DEV)
+    mt.moe_tail_latent_up(d["latent"].to(DEV), d["gamma"].to(DEV), d["w_up"].to(DEV), sh, out, ws, eps=d["eps"])
+    torch.cuda.synchronize()
+    y = ws[: b * L * 2].view(torch.bfloat16).view(b, L)
+    return y, out
+
+
+def test_latent_up_full(mt):
+    d = synth.config(4)
+    y_ref, out_ref = oracle.latent_tail(d["latent"], d["gamma"], d["eps"], d["w_up"], d["shared"], d["tp_s"],
+                                        d["b"], d["tp"], d["L"], d["H"])
+    y, out = run_latent(mt, d)
+    assert_bitexact(y, y_ref, "latent y b=16")
+    assert_gemm_close(out, out_ref, "latent out b=16 [7168]")
+
+
+@pytest.mark.parametrize("kw", [
+    dict(b=1, tp=1, tp_s=0, L=3584, H=7168),
+    dict(b=5, tp=3, tp_s=2, L=264, H=200),        # ragged K tail and M tail
+    dict(b=33, tp=8, tp_s=8, L=1024, H=384),       # N tile 64
+    dict(b=64, tp=8, tp_s=8, L=3584, H=1024),      # the shared-expert batch
+    dict(b=100, tp=2, tp_s=1, L=512, H=256),       # N tile 128
+    dict(b=130, tp=2, tp_s=1, L=512, H=256),       # two token tiles
+])
+def test_latent_up_shapes(mt, kw):
+    d = synth.latent_up_inputs(0x1A7 + kw["b"], **kw)
+    y_ref, out_ref = oracle.latent_tail(d["latent"], d["gamma"], d["eps"], d["w_up"], d["shared"], d["tp_s"],
+                                        d["b"], d["tp"], d["L"], d["H"])
+    y, out = run_latent(mt, d)
+    assert_bitexact(y, y_ref, f"latent y {kw}")
+    assert_gemm_close(out, out_ref, f"latent out {kw}")
+
+
+def test_latent_up_identity_weight(mt):
+    # W_up = [I; 0]: out[:, :L] = bf16(y + sum shared) exactly equals the oracle
+    b, tp, L, H = 4, 2, 256, 512
+    d = synth.latent_up_inputs(0x1D, b=b, tp=tp, L=L, H=H, tp_s=0)
+    w = torch.zeros((H, L))
+    w[:L, :L] = torch.eye(L)
+    d["w_up"] = w.to(torch.bfloat16)
+    y, out = run_latent(mt, d)
+    assert_bitexact(out[:, :L], y, "identity up-projection")
+    assert np.all(bits(out)[:, L:] == 0)
+
+
+# ------------------------------------------------------------------ shared expert
+#
+# gate and up are FP32 sums whose order the pages leave open, so bf16(gate),
+# bf16(up) and h may differ from the double oracle by an ulp in a few elements
+# per token: several h are correct.  The unique parts are compared with the
+# oracle on oracle-only inputs -- h itself, and the down stage on an h both
+# sides compute exactly -- and the GPU's d is checked to be a valid down
+# projection of the GPU's own h.
+
+def run_shared(mt, s, out_in, accumulate=True):
+    b, H, I = s["b"], s["H"], s["I"]
+    ws = torch.full((mt.moe_tail_workspace_bytes(1, b, I),), 0xFF, dtype=torch.uint8, device=DEV)
+    out = out_in.to(DEV).clone()
+    mt.moe_shared_expert(s["x"].to(DEV), s["w_gate"].to(DEV), s["w_up"].to(DEV), s["w_down"].to(DEV), out, ws,
+                         accumulate=accumulate)
+    torch.cuda.synchronize()
+    return ws[: b * I * 2].view(torch.bfloat16).view(b, I).cpu(), out.cpu()
+
+
+def check_shared(mt, s, out_in, tokens=None, what=""):
+    b, H, I = s["b"], s["H"], s["I"]
+    h, out = run_shared(mt, s, out_in, accumulate=True)
+    h2, d = run_shared(mt, s, torch.zeros((b, H), dtype=torch.bfloat16), accumulate=False)
+    assert_bitexact(h2, h, f"{what} h is deterministic")
+    for t in (range(b) if tokens is None else tokens):
+        sl = slice(t, t + 1)
+        h_ref, _ = oracle.shared_expert(s["x"][sl], s["w_gate"], s["w_up"], s["w_down"], 1, H, I, accumulate=False)
+        assert_gemm_close(h[sl], h_ref, f"{what} h token {t}")
+        d_valid = oracle.shared_down(h[sl], s["w_down"], 1, H, I, accumulate=False)
+        assert_gemm_close(d[sl], d_valid, f"{what} d token {t} (down projection of the GPU's h)")
+        out_valid = oracle.shared_down(h[sl], s["w_down"], 1, H, I, out_in=out_in[sl], accumulate=True)
+        assert_accumulated_close(out[sl], out_valid, d_valid, f"{what} out token {t}")
+
+
+@pytest.mark.parametrize("kw", [
+    dict(b=1, H=512, I=256), dict(b=3, H=520, I=200), dict(b=17, H=1024, I=768), dict(b=64, H=768, I=512),
+    dict(b=100, H=256, I=384), dict(b=129, H=256, I=128),
+])
+def test_shared_expert_shapes(mt, kw):
+    s = synth.shared_expert_inputs(0x5E + kw["b"], **kw)
+    out_in = synth.bf16(synth.normal(0x5E, 99, kw["b"] * kw["H"]), (kw["b"], kw["H"]))
+    check_shared(mt, s, out_in, what=str(kw))
+
+
+def test_shared_expert_full_size_sampled_tokens(mt):
+    # the full decode layer: latent tail at b = 64, then the shared expert
+    # added into its output; the oracle recomputes 6 sampled tokens
+    b = 64
+    lat = synth.latent_up_inputs(0x5EED0004, b=b)
+    s = synth.config(5)
+    _, out = run_latent(mt, lat)
+    latent_out = out.cpu().clone()
+    for t in (0, 1, 17, 31, 50, 63):
+        _, lat_ref = oracle.latent_tail(lat["latent"][:, t:t + 1].contiguous(), lat["gamma"], lat["eps"],
+                                        lat["w_up"], lat["shared"][:, t:t + 1].contiguous(), 8, 1, 8, 3584, 7168)
+        assert_gemm_close(latent_out[t:t + 1], lat_ref, f"latent out token {t}")
+    check_shared(mt, s, latent_out, tokens=(0, 1, 17, 31, 50, 63), what="b=64 H=7168 I=6144")
+
+
+def test_shared_expert_down_stage_full_size_exact_h(mt):
+    # x is one-hot (column c_t for token t) and W_gate is 32 on those columns,
+    # so gate = 32 and up = W_up[:, c_t] exactly in FP32 and in double, and
+    # silu(32) * up = 32 * up on both sides (exp(-32) vanishes next to 1 in
+    # FP32 and moves the double product by far less than half a BF16 ulp):
+    # h is one exact value.  The down projection is then compared with the
+    # oracle's at the GEMM tolerance, at full size.
+    b, H, I = 64, 7168, 6144
+    s = synth.config(5, with_weights=False)
+    cols = [(t * 97 + 5) % H for t in range(b)]
+    x = torch.zeros((b, H))
+    wg = torch.zeros((I, H))
+    for t, c in enumerate(cols):
+        x[t, c] = 1.0
+        wg[:, c] = 32.0
+    s["x"], s["w_gate"] = x.to(torch.bfloat16), wg.to(torch.bfloat16)
+    s["w_up"] = synth.bf16(synth.normal(0x5EED0005, 22, I * H, std=0.02), (I, H))
+    s["w_down"] = synth.bf16(synth.normal(0x5EED0005, 23, H * I, std=0.02), (H, I))
+    out_in = synth.bf16(synth.normal(0x5EED0005, 30, b * H), (b, H))
+    h, out = run_shared(mt, s, out_in, accumulate=True)
+    _, d = run_shared(mt, s, torch.zeros((b, H), dtype=torch.bfloat16), accumulate=False)
+    for t in (0, 9, 33, 63):
+        sl = slice(t, t + 1)
+        h_ref, d_ref = oracle.shared_expert(s["x"][sl], s["w_gate"], s["w_up"], s["w_down"], 1, H, I,
+                                            accumulate=False)
+        assert_bitexact(h[sl], h_ref, f"exact h token {t}")
+        assert_gemm_close(d[sl], d_ref, f"down projection token {t}")
+        _, out_ref = oracle.shared_expert(s["x"][sl], s["w_gate"], s["w_up"], s["w_down"], 1, H, I,
+                                          out_in=out_in[sl])
+        assert_accumulated_close(out[sl], out_ref, d_ref, f"accumulated token {t}")
+
+
+def test_shared_expert_zero_input_leaves_out(mt):
+    s = synth.shared_expert_inputs(3, b=5, H=256, I=128)
+    s["x"] = torch.zeros_like(s["x"])
+    out_in = synth.bf16(synth.normal(3, 9, 5 * 256), (5, 256))
+    _, out = run_shared(mt, s, out_in)
+    assert_bitexact(out, out_in, "x = 0")
+
+
+def test_no_device_error_raised(mt):
+    assert mt.moe_tail_take_device_error() == 0

@@ -502,3 +502,12 @@ def test_shared_matches_library_matmul():
     assert np.array_equal(bits(out), bits(ref))
     _, plain = oracle.shared_expert(d["x"], d["w_gate"], d["w_up"], d["w_down"], 3, 64, 96, accumulate=False)
     assert np.array_equal(bits(plain), bits(dd))
+
+
+def test_shared_down_matches_library_matmul_and_composes():
+    d = synth.shared_expert_inputs(12, b=2, H=64, I=96)
+    h, out = oracle.shared_expert(d["x"], d["w_gate"], d["w_up"], d["w_down"], 2, 64, 96, accumulate=False)
+    ref = torch.from_numpy(h.double().numpy() @ d["w_down"].double().numpy().T).float().to(torch.bfloat16)
+    got = oracle.shared_down(h, d["w_down"], 2, 64, 96, accumulate=False)
+    assert np.array_equal(bits(got), bits(ref))
+    assert np.array_equal(bits(got), bits(out))
