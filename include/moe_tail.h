@@ -142,6 +142,33 @@ int moe_shared_expert(const void* x, const void* w_gate, const void* w_up, const
                       int b, int H, int I, void* out, int accumulate, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/*
+ * Latent tail without a workspace (no counterpart on the pages: an addition
+ * of this library).  Same computation and arguments as moe_tail_latent_up,
+ * minus the workspace: for callers that cannot allocate device memory -- a
+ * plugin that its host runtime hands only input and output buffers, a
+ * process whose device memory is all reserved by its own pool, or a hot path
+ * that must not call cudaMalloc because it can synchronise the device.
+ *
+ * The intermediate y rows live in a fixed array of
+ * MOE_TAIL_NOALLOC_SCRATCH_BYTES bytes inside the library's device code,
+ * which every GPU that loads the library keeps until the process exits.  The
+ * call allocates and frees nothing.  Limits and refusals are those of
+ * moe_tail_latent_up, plus: b * L * 2 > MOE_TAIL_NOALLOC_SCRATCH_BYTES
+ * returns MOE_TAIL_EINVAL before anything runs.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array and each overwrites all of the y rows it
+ *     uses, so nothing has to start at zero; calls that may run at the same
+ *     time on the GPU (different streams, or different host threads) race on
+ *     it and must be serialised by the caller.
+ */
+#define MOE_TAIL_NOALLOC_SCRATCH_BYTES (1u << 20)
+int moe_tail_latent_up_noalloc(const void* latent, const void* gamma, float eps, const void* w_up,
+                               const void* shared, int tp_s, int b, int tp, int L, int H, void* out,
+                               void* stream);
+
 /* Workspace bytes of moe_tail_latent_up (which = 0, dim = L) or
  * moe_shared_expert (which = 1, dim = I) at b tokens; 0 for bad arguments. */
 size_t moe_tail_workspace_bytes(int which, int b, int dim);

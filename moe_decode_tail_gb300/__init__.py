@@ -17,9 +17,11 @@ from .build import LIB
 __all__ = [
     "MoeTailError", "lib", "moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up",
     "moe_shared_expert", "moe_tail_workspace_bytes", "moe_tail_status_str", "moe_tail_take_device_error",
+    "moe_tail_latent_up_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 OK, EINVAL, ECUDA, ENOTSUP = 0, 1, 2, 3
+NOALLOC_SCRATCH_BYTES = 1 << 20  # MOE_TAIL_NOALLOC_SCRATCH_BYTES
 W_FP32, W_BF16 = 0, 1
 
 
@@ -45,13 +47,14 @@ def lib() -> ctypes.CDLL:
         L.moe_tail_tp_finalize.argtypes = fin
         L.moe_tail_latent_up.argtypes = [P, P, f32, P, P, i32, i32, i32, i32, i32, P, P, sz, P]
         L.moe_shared_expert.argtypes = [P, P, P, P, i32, i32, i32, P, i32, P, sz, P]
+        L.moe_tail_latent_up_noalloc.argtypes = [P, P, f32, P, P, i32, i32, i32, i32, i32, P, P]
         L.moe_tail_workspace_bytes.argtypes = [i32, i32, i32]
         L.moe_tail_workspace_bytes.restype = sz
         L.moe_tail_status_str.argtypes = [i32]
         L.moe_tail_status_str.restype = ctypes.c_char_p
         L.moe_tail_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         for name in ("moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up", "moe_shared_expert",
-                     "moe_tail_take_device_error"):
+                     "moe_tail_take_device_error", "moe_tail_latent_up_noalloc"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -131,6 +134,26 @@ def moe_tail_latent_up(latent, gamma, w_up, shared, out, workspace, *, eps=1e-6,
     _check("moe_tail_latent_up", lib().moe_tail_latent_up(
         _p(latent), _p(gamma), eps, _p(w_up), _p(shared), tp_s, b, tp, L, H, _p(out), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def moe_tail_latent_up_noalloc(latent, gamma, w_up, shared, out, *, eps=1e-6, stream=None) -> torch.Tensor:
+    """The latent tail without a workspace, for callers that cannot allocate
+    device memory (a plugin given only its input and output buffers, a host
+    whose device memory is all held by its own pool, a path that must not
+    call cudaMalloc): y lives in a fixed array of NOALLOC_SCRATCH_BYTES inside
+    the library, shared by every call.  Same arguments as moe_tail_latent_up
+    minus the workspace; b * L * 2 must not exceed NOALLOC_SCRATCH_BYTES.
+    Calls that may overlap on the GPU race on the shared array."""
+    _cuda(latent, gamma, w_up, shared, out)
+    tp, b, L = latent.shape
+    H = w_up.shape[0]
+    if b * L * 2 > NOALLOC_SCRATCH_BYTES:
+        raise ValueError(f"moe_tail_latent_up_noalloc: y needs {b * L * 2} bytes, more than the library's "
+                         f"built-in {NOALLOC_SCRATCH_BYTES}-byte scratch; use moe_tail_latent_up with a workspace")
+    tp_s = 0 if shared is None else shared.shape[0]
+    _check("moe_tail_latent_up_noalloc", lib().moe_tail_latent_up_noalloc(
+        _p(latent), _p(gamma), eps, _p(w_up), _p(shared), tp_s, b, tp, L, H, _p(out), _stream(stream)))
     return out
 
 

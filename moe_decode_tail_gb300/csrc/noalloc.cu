@@ -1,0 +1,161 @@
+// moe_tail_latent_up_noalloc: the latent tail for callers that cannot
+// allocate device memory.
+//
+// Some callers have no way to hand this library a workspace: a plugin that an
+// inference runtime gives only its input and output buffers, or a host
+// process whose device memory is entirely reserved by its own pool allocator.
+// Others must not call cudaMalloc on their hot path because it can
+// synchronise the device.  This entry point runs the same two kernels as
+// moe_tail_latent_up, but keeps the intermediate y rows in a fixed array in
+// device memory that is part of the library itself, so the caller passes only
+// inputs and outputs and nothing is allocated per call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/moe_tail.h"
+#include "kernels.h"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+// The y rows (BF16 [b][L]) of a no-alloc latent tail call.  Every GPU that
+// loads the library holds this array until the process exits; all calls share
+// it.  Host code must not use this name as a device address: the device
+// address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) uint8_t g_noalloc_y[MOE_TAIL_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch[kMaxDevices] = {nullptr};
+std::mutex g_scratch_mutex;
+
+// The device address of g_noalloc_y on the current device, looked up once
+// per device (the first call on a device does this).
+cudaError_t scratch_on_current_device(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_y);
+    if (e != cudaSuccess) return e;
+    g_scratch[dev] = p;
+  }
+  *out = g_scratch[dev];
+  return cudaSuccess;
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows,
+                 CUtensorMapL2promotion promo) {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return an && bn && a0 < b0 + bn && b0 < a0 + an;
+}
+
+}  // namespace
+
+MOE_API int moe_tail_latent_up_noalloc(const void* latent, const void* gamma, float eps, const void* w_up,
+                                       const void* shared, int tp_s, int b, int tp, int L, int H, void* out,
+                                       void* stream) {
+  if (b < 0 || b > 65535 || tp < 1 || tp > 32 || tp_s < 0 || tp_s > 32) return MOE_TAIL_EINVAL;
+  if (L < 8 || L > 32768 || L % 8 || H < 8 || H % 8 || H > (1 << 24)) return MOE_TAIL_EINVAL;
+  if (b == 0) return MOE_TAIL_OK;
+  // y must fit the library's fixed scratch array
+  if ((size_t)b * (size_t)L * 2 > (size_t)MOE_TAIL_NOALLOC_SCRATCH_BYTES) return MOE_TAIL_EINVAL;
+  if (!latent || !gamma || !w_up || !out) return MOE_TAIL_EINVAL;
+  if ((tp_s > 0) != (shared != nullptr)) return MOE_TAIL_EINVAL;
+  if (!aligned16(latent) || !aligned16(gamma) || !aligned16(w_up) || !aligned16(out) ||
+      (shared && !aligned16(shared)))
+    return MOE_TAIL_EINVAL;
+  const size_t out_n = (size_t)b * H * 2;
+  if (overlaps(out, out_n, latent, (size_t)tp * b * L * 2) || overlaps(out, out_n, gamma, (size_t)L * 2) ||
+      overlaps(out, out_n, w_up, (size_t)H * L * 2) || overlaps(out, out_n, shared, (size_t)tp_s * b * H * 2))
+    return MOE_TAIL_EINVAL;
+
+  void* y = nullptr;
+  cudaError_t e = scratch_on_current_device(&y);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_TAIL_ECUDA;
+  }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_TAIL_ECUDA;
+  }
+  const moetail::GemmPlan plan = moetail::plan_gemm(moetail::kGemmUpShared, H, L, b, sms);
+  CUtensorMap mw, mx;
+  if (!encode_rows(&mw, w_up, H, L, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_rows(&mx, y, b, L, plan.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+    return MOE_TAIL_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // 1. y (every element written, so nothing has to start at zero)
+  moetail::TpArgs n;
+  n.partials = static_cast<const uint16_t*>(latent);
+  n.num_rows = b;
+  n.slot_stride = (int64_t)b * L;
+  n.idx = nullptr;
+  n.w = nullptr;
+  n.gamma = static_cast<const uint16_t*>(gamma);
+  n.gain_center = 0.0f;
+  n.eps = eps;
+  n.rcpP = (float)(1.0 / (double)L);
+  n.b = b;
+  n.tp = tp;
+  n.K = 1;
+  n.P = L;
+  n.chunks = (L + 255) / 256;
+  n.out = static_cast<uint16_t*>(y);
+  e = moetail::launch_tp_finalize(n, false, moetail::kWeightUnit, sms, 0, st);
+  if (e == cudaSuccess) {
+    // 2. out = y . w_up^T + sum_s shared[s]
+    moetail::GemmArgs g;
+    g.M = H;
+    g.K = L;
+    g.n_tok = b;
+    g.kblocks = (L + 63) / 64;
+    g.shared = static_cast<const uint16_t*>(shared);
+    g.tp_s = tp_s;
+    g.out = static_cast<uint16_t*>(out);
+    g.accumulate = 0;
+    e = moetail::launch_decode_gemm(moetail::kGemmUpShared, plan, mw, mw, mx, g, true, st);
+  }
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_TAIL_ECUDA;
+  }
+  return MOE_TAIL_OK;
+}
