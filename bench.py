@@ -391,9 +391,10 @@ def cuda_arm(args, world, rank, local):
     rest = K % G
     rest_g = capture(rest, False)[0] if rest else None
     torch.cuda.synchronize()
-    # warm-up: W steps from the same graph
-    for _ in range(max(1, -(-W // G))):
-        main_g.replay()
+    # warm-up: W steps from the same graph (replay() launches on the current stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, -(-W // G))):
+            main_g.replay()
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
@@ -402,12 +403,13 @@ def cuda_arm(args, world, rank, local):
     barrier(dist, dev)
     torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(K // G):
-        main_g.replay()
-    if rest_g is not None:
-        rest_g.replay()
-    stop.record(stream)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(K // G):
+            main_g.replay()
+        if rest_g is not None:
+            rest_g.replay()
+        stop.record(stream)
     torch.cuda.synchronize()
     barrier(dist, dev)
     clocks = sampler.stop() if rank == 0 else None

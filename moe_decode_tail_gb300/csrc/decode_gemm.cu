@@ -2,24 +2,24 @@
 //
 //   D[m, t] = sum_k W[m, k] * X[t, k]       (W: weights [M, K], X: tokens [b, K])
 //
-// The weights are the MMA's M=128 operand and the tokens its N operand
-// ("swap AB"), so a decode batch of b <= 128 tokens is one N tile and the
-// kernel is a stream of weight tiles: its roofline is the weight bytes over
-// HBM bandwidth.  Per CTA: warp 4 (one thread) streams 128x64 BF16 weight
-// tiles and Nx64 token tiles with TMA (128-byte swizzle) into a ring of
+// The weights are the MMA's M operand (64 or 128 rows per CTA) and the tokens
+// its N operand ("swap AB"), so a decode batch of b <= 128 tokens is one N
+// tile and the kernel is a stream of weight tiles: its roofline is the weight
+// bytes over HBM bandwidth.  Per CTA: warp 4 (one thread) streams Mx64 BF16
+// weight tiles and Nx64 token tiles with TMA (128-byte swizzle) into a ring of
 // shared-memory stages guarded by mbarriers; warp 5 (one thread) issues four
 // K=16 tcgen05.mma per stage into an FP32 accumulator in tensor memory and
 // releases the stage with tcgen05.commit; warps 0-3 read the accumulator
-// (tcgen05.ld, one TMEM lane = one weight row per thread).  The K range is
-// split over the CTAs of a thread-block cluster; their FP32 partial tiles are
-// added in cluster-rank order over distributed shared memory, so the result
-// is deterministic, and the fused epilogue writes BF16:
+// (tcgen05.ld, one TMEM lane = one weight row per thread).  The K range may
+// be split over the CTAs of a thread-block cluster; their FP32 partial tiles
+// are then added in cluster-rank order over distributed shared memory, so the
+// result is deterministic, and the fused epilogue writes BF16:
 //
 //   kGemmUpShared   out = bf16(acc + sum_s shared[s])   (latent tail up-projection
 //                   plus the shared-expert partials, Kimi-K3 tail runtime page,
 //                   module docstring)
-//   kGemmGateUpSilu rows 0..63 of the tile are gate rows, 64..127 the matching
-//                   up rows; h = bf16(silu(bf16(gate)) * bf16(up))  (Kimi-K3
+//   kGemmGateUpSilu the first half of the tile's rows are gate rows, the second
+//                   half the matching up rows; h = bf16(silu(bf16(gate)) * bf16(up))  (Kimi-K3
 //                   shared expert page: SharedUmma.load_tile pairs gate and up
 //                   rows in one M tile; owned_h rounds gate and up to BF16)
 //   kGemmDown       out = bf16(out + bf16(d)) or bf16(d)  (the down projection
@@ -28,6 +28,9 @@
 // Every wait is bounded in time; on expiry the kernel raises a bit in the
 // device error word, drains what it started, frees its tensor memory and
 // returns.
+#include <stdio.h>
+#include <stdlib.h>
+
 #include <algorithm>
 
 #include "common.cuh"
@@ -36,8 +39,6 @@
 namespace moetail {
 
 constexpr int kBlockK = 64;                        // BF16 per K block: one 128-byte swizzle row
-constexpr int kTileM = 128;                        // MMA M: weight rows per CTA
-constexpr int kATileBytes = kTileM * kBlockK * 2;  // 16 KiB
 constexpr int kThreads = 192;                      // warps 0-3 epilogue, 4 TMA, 5 MMA
 constexpr int kMaxStages = 12;
 
@@ -166,15 +167,21 @@ struct GemmSmem {  // offsets from the 1024-aligned base of dynamic shared memor
   uint32_t ring, full, empty, accum, tmem_slot, abort_flag;
 };
 
-template <int MODE, int N>
-__global__ void __launch_bounds__(kThreads, 2)
+// TM = weight rows per CTA (the MMA's M: 64 or 128).  With TM = 128 the
+// accumulator row r sits in TMEM lane r; with TM = 64 it sits in lane
+// 32 * (r / 16) + r % 16 (lanes 16..31 of each warp's quarter stay unused).
+// Gate/up tiles hold TM/2 gate rows then the TM/2 matching up rows.
+template <int MODE, int N, int TM>
+__global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
                        const __grid_constant__ CUtensorMap map_x, const GemmArgs a, const int stages) {
   extern __shared__ uint8_t smem_raw[];
+  constexpr int kATile = TM * kBlockK * 2;
   constexpr int kBTileBytes = N * kBlockK * 2;
-  constexpr int kStageBytes = kATileBytes + kBTileBytes;
+  constexpr int kStageBytes = kATile + kBTileBytes;
   constexpr uint32_t kTmemCols = N < 32 ? 32 : N;
-  constexpr uint32_t kIdesc = idesc_bf16(kTileM, N);
+  constexpr uint32_t kIdesc = idesc_bf16(TM, N);
+  constexpr int kOutRows = (MODE == kGemmGateUpSilu) ? TM / 2 : TM;  // output features per tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank(), ksplit = cluster_size();
@@ -217,10 +224,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot_ptr;
 
+  // Weight box of K block kb into stage st (two half-height boxes for gate/up).
+  auto load_weights = [&](uint32_t st, uint32_t bar, int kb, uint64_t policy) {
+    const int kx = kb * kBlockK;
+    if (MODE == kGemmGateUpSilu) {
+      tma_load_2d(st, &map_w0, bar, kx, m_tile * (TM / 2), policy);
+      tma_load_2d(st + kATile / 2, &map_w1, bar, kx, m_tile * (TM / 2), policy);
+    } else {
+      tma_load_2d(st, &map_w0, bar, kx, m_tile * TM, policy);
+    }
+  };
+
   if (warp == 4) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint64_t keep = policy_evict_last();   // token tiles: re-read by every M tile
+      const uint64_t keep = policy_evict_last();     // token tiles: re-read by every M tile
       const uint64_t stream = policy_evict_first();  // weights: read once
       int issued = 0;
       bool ok = true;
@@ -228,20 +246,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       // requested before waiting for it.
       const int pre = min(nk, stages);
       for (int i = 0; i < pre; ++i) {
-        const uint32_t st = L.ring + i * kStageBytes;
-        const uint32_t bar = L.full + 8 * i;
-        mbar_expect_tx(bar, kStageBytes);
-        const int kx = (kb0 + i) * kBlockK;
-        if (MODE == kGemmGateUpSilu) {
-          tma_load_2d(st, &map_w0, bar, kx, m_tile * 64, stream);
-          tma_load_2d(st + kATileBytes / 2, &map_w1, bar, kx, m_tile * 64, stream);
-        } else {
-          tma_load_2d(st, &map_w0, bar, kx, m_tile * kTileM, stream);
-        }
+        mbar_expect_tx(L.full + 8 * i, kStageBytes);
+        load_weights(L.ring + i * kStageBytes, L.full + 8 * i, kb0 + i, stream);
       }
       grid_dependency_wait();
       for (int i = 0; i < pre; ++i)
-        tma_load_2d(L.ring + i * kStageBytes + kATileBytes, &map_x, L.full + 8 * i, (kb0 + i) * kBlockK, tok0, keep);
+        tma_load_2d(L.ring + i * kStageBytes + kATile, &map_x, L.full + 8 * i, (kb0 + i) * kBlockK, tok0, keep);
       issued = pre;
       for (int i = pre; i < nk; ++i) {
         const int s = i % stages;
@@ -255,14 +265,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t st = L.ring + s * kStageBytes;
         const uint32_t bar = L.full + 8 * s;
         mbar_expect_tx(bar, kStageBytes);
-        const int kx = (kb0 + i) * kBlockK;
-        if (MODE == kGemmGateUpSilu) {
-          tma_load_2d(st, &map_w0, bar, kx, m_tile * 64, stream);
-          tma_load_2d(st + kATileBytes / 2, &map_w1, bar, kx, m_tile * 64, stream);
-        } else {
-          tma_load_2d(st, &map_w0, bar, kx, m_tile * kTileM, stream);
-        }
-        tma_load_2d(st + kATileBytes, &map_x, bar, kx, tok0, keep);
+        load_weights(st, bar, kb0 + i, stream);
+        tma_load_2d(st + kATile, &map_x, bar, (kb0 + i) * kBlockK, tok0, keep);
         ++issued;
       }
       if (!ok) {  // let the copies already in flight land before the CTA's memory goes away
@@ -285,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after();
         const uint32_t st = L.ring + s * kStageBytes;
         const uint64_t adesc = smem_desc_sw128(st);
-        const uint64_t bdesc = smem_desc_sw128(st + kATileBytes);
+        const uint64_t bdesc = smem_desc_sw128(st + kATile);
 #pragma unroll
         for (int kk = 0; kk < kBlockK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
           mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     __syncwarp();
   } else {
-    // ---------------- accumulator -> FP32 staging tile [N tokens][128 rows] ----------------
+    // ---------------- accumulator -> FP32 staging tile [N tokens][TM rows] ----------------
     grid_dependency_wait();
     const bool got = mbar_wait(L.accum, 0);
     if (!got) {
@@ -303,33 +307,34 @@ __global__ void __launch_bounds__(kThreads, 2)
       *abort_ptr = 1;
     }
     tc_fence_after();
+    float* stage = reinterpret_cast<float*>(base_ptr);
+    const bool holds_row = TM == 128 || lane < 16;
+    const int row = TM == 128 ? warp * 32 + lane : warp * 16 + lane;
     if (got && nk > 0) {
-      float* stage = reinterpret_cast<float*>(base_ptr);
-      const int row = warp * 32 + lane;
 #pragma unroll 1
       for (int c = 0; c < N; c += 16) {
         float v[16];
         tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+        if (holds_row) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) stage[(c + i) * kTileM + row] = v[i];
+          for (int i = 0; i < 16; ++i) stage[(c + i) * TM + row] = v[i];
+        }
       }
-    } else if (got) {  // an empty K range contributes zeros
-      float* stage = reinterpret_cast<float*>(base_ptr);
-      const int row = warp * 32 + lane;
-      for (int c = 0; c < N; ++c) stage[c * kTileM + row] = 0.0f;
+    } else if (got && holds_row) {  // an empty K range contributes zeros
+      for (int c = 0; c < N; ++c) stage[c * TM + row] = 0.0f;
     }
     tc_fence_before();
   }
   __syncthreads();
   const bool aborted = *abort_ptr != 0;
-  cluster_sync_all();  // every CTA's partial tile is staged
+  if (ksplit > 1) cluster_sync_all();  // every CTA's partial tile is staged
 
   // ---------------- rank-order reduction over the cluster + fused epilogue ----------------
   const int n_valid = min(N, a.n_tok - tok0);
   const int t_per = n_valid / (int)ksplit, t_rem = n_valid % (int)ksplit;
   const int t_begin = (int)rank * t_per + min((int)rank, t_rem);
   const int t_count = t_per + ((int)rank < t_rem ? 1 : 0);
-  constexpr int kQuads = (MODE == kGemmGateUpSilu) ? 16 : 32;  // 4-column groups per token
+  constexpr int kQuads = kOutRows / 4;  // 4-column groups per token
   if (!aborted) {
     for (int item = threadIdx.x; item < t_count * kQuads; item += kThreads) {
       const int t = t_begin + item / kQuads;
@@ -337,20 +342,20 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int tg = tok0 + t;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       float4 acc2 = make_float4(0.f, 0.f, 0.f, 0.f);
-      const uint32_t off = base + (uint32_t)((t * kTileM + 4 * q) * 4);
+      const uint32_t off = base + (uint32_t)((t * TM + 4 * q) * 4);
       for (uint32_t p = 0; p < ksplit; ++p) {
         const float4 v = ld_cluster_v4(map_to_rank(off, p));
         acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
         acc.z = __fadd_rn(acc.z, v.z); acc.w = __fadd_rn(acc.w, v.w);
         if (MODE == kGemmGateUpSilu) {
-          const float4 u = ld_cluster_v4(map_to_rank(off + 64 * 4, p));
+          const float4 u = ld_cluster_v4(map_to_rank(off + (TM / 2) * 4, p));
           acc2.x = __fadd_rn(acc2.x, u.x); acc2.y = __fadd_rn(acc2.y, u.y);
           acc2.z = __fadd_rn(acc2.z, u.z); acc2.w = __fadd_rn(acc2.w, u.w);
         }
       }
       float r[4] = {acc.x, acc.y, acc.z, acc.w};
       if (MODE == kGemmGateUpSilu) {
-        const int j = m_tile * 64 + 4 * q;
+        const int j = m_tile * kOutRows + 4 * q;
         if (j >= a.M) continue;
         const float u[4] = {acc2.x, acc2.y, acc2.z, acc2.w};
         uint32_t hb[4];
@@ -359,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint2 pk = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
         *reinterpret_cast<uint2*>(a.out + (int64_t)tg * a.M + j) = pk;
       } else {
-        const int n = m_tile * kTileM + 4 * q;
+        const int n = m_tile * kOutRows + 4 * q;
         if (n >= a.M) continue;
         uint16_t* dst = a.out + (int64_t)tg * a.M + n;
         if (MODE == kGemmUpShared) {
@@ -384,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
   launch_dependents();
-  cluster_sync_all();  // peers are done reading this CTA's staging tile
+  if (ksplit > 1) cluster_sync_all();  // peers are done reading this CTA's staging tile
+  __syncthreads();
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -393,79 +399,106 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // ---- host side ---------------------------------------------------------------------
 
-static int stage_bytes(int n_tile) { return kATileBytes + n_tile * kBlockK * 2; }
+static int stage_bytes(int tm, int n_tile) { return tm * kBlockK * 2 + n_tile * kBlockK * 2; }
+
+// Plan override for tuning: MOE_TAIL_GEMM_PLAN_<UP|GATEUP|DOWN>="tm,ksplit,stages".
+static bool plan_override(int mode, GemmPlan& p) {
+  const char* names[3] = {"MOE_TAIL_GEMM_PLAN_UP", "MOE_TAIL_GEMM_PLAN_GATEUP", "MOE_TAIL_GEMM_PLAN_DOWN"};
+  const char* v = getenv(names[mode]);
+  int tm = 0, ks = 0, st = 0;
+  if (!v || sscanf(v, "%d,%d,%d", &tm, &ks, &st) != 3) return false;
+  if ((tm != 64 && tm != 128) || ks < 1 || ks > 8 || st < 2 || st > kMaxStages) return false;
+  p.tm = tm;
+  p.ksplit = ks;
+  p.stages = st;
+  return true;
+}
 
 GemmPlan plan_gemm(int mode, int M, int K, int b, int sms) {
   GemmPlan p;
   p.n_tile = b <= 16 ? 16 : b <= 32 ? 32 : b <= 64 ? 64 : 128;
   const int tok_tiles = (b + p.n_tile - 1) / p.n_tile;
-  p.m_tiles = mode == kGemmGateUpSilu ? (M + 63) / 64 : (M + kTileM - 1) / kTileM;
   const int kblocks = (K + kBlockK - 1) / kBlockK;
-  const int target = 2 * sms;  // two CTAs per SM
-  int ks = target / std::max(1, p.m_tiles * tok_tiles);
-  ks = std::max(1, std::min(ks, 8));
-  ks = std::min(ks, kblocks);
-  p.ksplit = ks;
-  const int per_cta = (kblocks + ks - 1) / ks;
-  const int budget = 110 * 1024;  // two CTAs per SM
-  const int sb = stage_bytes(p.n_tile);
-  int st = budget / sb;
-  st = std::max(2, std::min(st, kMaxStages));
-  st = std::min(st, std::max(2, per_cta));
+  p.tm = 128;
+  p.stages = 0;
+  const bool forced = plan_override(mode, p);
+  const int rows_per_tile = mode == kGemmGateUpSilu ? p.tm / 2 : p.tm;
+  p.m_tiles = (M + rows_per_tile - 1) / rows_per_tile;
+  if (!forced) {  // two CTAs per SM, K split over a cluster
+    int ks = 2 * sms / std::max(1, p.m_tiles * tok_tiles);
+    p.ksplit = std::max(1, std::min(ks, 8));
+  }
+  p.ksplit = std::min(p.ksplit, kblocks);
+  const int sb = stage_bytes(p.tm, p.n_tile);
+  if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, (110 * 1024) / sb));
+  const int per_cta = (kblocks + p.ksplit - 1) / p.ksplit;
+  p.stages = std::min(p.stages, std::max(2, per_cta));
   // the FP32 staging tile reuses the ring
-  while (st * sb < p.n_tile * kTileM * 4) ++st;
-  p.stages = st;
+  while (p.stages * sb < p.n_tile * p.tm * 4) ++p.stages;
   return p;
 }
 
 static size_t smem_bytes(const GemmPlan& p) {
-  return 1024 + (size_t)p.stages * stage_bytes(p.n_tile) + 16 * (size_t)p.stages + 8 + 8 + 64;
+  return 1024 + (size_t)p.stages * stage_bytes(p.tm, p.n_tile) + 16 * (size_t)p.stages + 8 + 8 + 64;
 }
 
-template <int MODE, int N>
+template <int MODE, int N, int TM>
 static cudaError_t launch_t(const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& x,
                             const GemmArgs& a, bool pdl, cudaStream_t stream) {
-  auto kernel = decode_gemm_kernel<MODE, N>;
+  auto kernel = decode_gemm_kernel<MODE, N, TM>;
   const size_t smem = smem_bytes(p);
-  // Raise the kernel's shared-memory limit once per device to the largest
-  // plan (not per call, so that a captured stream sees only launches).
+  // Raise the kernel's shared-memory limit once per device (not per call, so
+  // that a captured stream sees only launches).
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (configured[dev] < (int)smem) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     if (e != cudaSuccess) return e;
-    configured[dev] = 200 * 1024;
+    configured[dev] = 1;
   }
+  if (smem > 220 * 1024) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.ksplit, p.m_tiles, (a.n_tok + N - 1) / N);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.ksplit;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  ++n;
+  if (p.ksplit > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = p.ksplit;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, w0, w1, x, a, p.stages);
+}
+
+template <int MODE, int TM>
+static cudaError_t launch_n(const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1,
+                            const CUtensorMap& x, const GemmArgs& a, bool pdl, cudaStream_t stream) {
+  switch (p.n_tile) {
+    case 16: return launch_t<MODE, 16, TM>(p, w0, w1, x, a, pdl, stream);
+    case 32: return launch_t<MODE, 32, TM>(p, w0, w1, x, a, pdl, stream);
+    case 64: return launch_t<MODE, 64, TM>(p, w0, w1, x, a, pdl, stream);
+    case 128: return launch_t<MODE, 128, TM>(p, w0, w1, x, a, pdl, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int MODE>
 static cudaError_t launch_mode(const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1,
                                const CUtensorMap& x, const GemmArgs& a, bool pdl, cudaStream_t stream) {
-  switch (p.n_tile) {
-    case 16: return launch_t<MODE, 16>(p, w0, w1, x, a, pdl, stream);
-    case 32: return launch_t<MODE, 32>(p, w0, w1, x, a, pdl, stream);
-    case 64: return launch_t<MODE, 64>(p, w0, w1, x, a, pdl, stream);
-    case 128: return launch_t<MODE, 128>(p, w0, w1, x, a, pdl, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return p.tm == 128 ? launch_n<MODE, 128>(p, w0, w1, x, a, pdl, stream)
+                     : launch_n<MODE, 64>(p, w0, w1, x, a, pdl, stream);
 }
 
 cudaError_t launch_decode_gemm(int mode, const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1,

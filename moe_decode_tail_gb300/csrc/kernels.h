@@ -9,33 +9,23 @@ namespace moetail {
 
 enum { kWeightF32 = 0, kWeightBF16 = 1, kWeightUnit = 2 };
 
-struct EpArgs {
-  const uint16_t* rows;  // BF16 [tp][rows_per_slot][P]
-  int64_t rows_per_slot;
-  const int32_t* idx;    // [tp][b][K]
-  const void* w;         // [b][K] FP32 or BF16
-  const uint16_t* gamma; // BF16 [P]
+// Rows of one finalize call: slot s's row j starts at rows + s * slot_stride + j * P.
+struct FinalizeArgs {
+  const uint16_t* rows;   // EP: GEMM2 rows [tp][num_rows][P]; TP: K-partials; latent: [tp][b][L]
+  int64_t num_rows;       // rows per slot (EP rows_per_slot, TP num_rows, latent b)
+  int64_t slot_stride;    // elements between slots
+  const int32_t* idx;     // EP [tp][b][K]; TP [b][K]; latent unused
+  const void* w;          // [b][K] FP32 or BF16; latent unused (unit weight)
+  const uint16_t* gamma;  // BF16 [P]
   float gain_center, eps, rcpP;
-  int b, tp, K, P, chunks;
-  uint16_t* out;         // BF16 [b][P]
+  int b, tp, K, P;
+  int chunks, band_vectors, routes_per_pass;  // set by the launcher
+  uint16_t* out;          // BF16 [b][P]
 };
 
-struct TpArgs {
-  const uint16_t* partials;  // BF16 [tp][num_rows][P]
-  int64_t num_rows;
-  int64_t slot_stride;       // elements between slots (num_rows * P)
-  const int32_t* idx;        // [b][K], or null: row = token (K = 1)
-  const void* w;             // [b][K] FP32 or BF16, or null with unit weights
-  const uint16_t* gamma;     // BF16 [P]
-  float gain_center, eps, rcpP;
-  int b, tp, K, P, chunks;
-  uint16_t* out;             // BF16 [b][P]
-};
+enum { kFinalizeEP = 0, kFinalizeTP = 1, kFinalizeLatent = 2 };
 
-cudaError_t launch_ep_finalize(const EpArgs& a, bool wbn, int wmode, int sms, int force_split,
-                               cudaStream_t stream);
-cudaError_t launch_tp_finalize(const TpArgs& a, bool wbn, int wmode, int sms, int force_split,
-                               cudaStream_t stream);
+cudaError_t launch_finalize(int mode, const FinalizeArgs& a, bool wbn, int wmode, int sms, cudaStream_t stream);
 
 // ---- decode GEMM (tcgen05) ---------------------------------------------------
 
@@ -53,6 +43,7 @@ struct GemmArgs {
 };
 
 struct GemmPlan {
+  int tm;       // MMA M: weight rows per CTA (64 or 128)
   int n_tile;   // MMA N (tokens, padded)
   int ksplit;   // cluster size (K split)
   int stages;   // shared-memory ring depth

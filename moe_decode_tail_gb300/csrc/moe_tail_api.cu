@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -15,10 +16,9 @@
 
 namespace {
 
-using moetail::EpArgs;
+using moetail::FinalizeArgs;
 using moetail::GemmArgs;
 using moetail::GemmPlan;
-using moetail::TpArgs;
 
 constexpr int kMaxTp = 32, kMaxK = 32, kMaxP = 32768;
 
@@ -115,9 +115,10 @@ MOE_API int moe_tail_ep_finalize(const void* rows, int64_t rows_per_slot, const 
       overlaps(o, span(permuted_idx, (size_t)tp * b * K * 4)) || overlaps(o, span(route_weights, (size_t)b * K * wsz)) ||
       overlaps(o, span(gamma, (size_t)P * 2)))
     return MOE_TAIL_EINVAL;
-  EpArgs a;
+  FinalizeArgs a;
   a.rows = static_cast<const uint16_t*>(rows);
-  a.rows_per_slot = rows_per_slot;
+  a.num_rows = rows_per_slot;
+  a.slot_stride = rows_per_slot * P;
   a.idx = permuted_idx;
   a.w = route_weights;
   a.gamma = static_cast<const uint16_t*>(gamma);
@@ -128,10 +129,9 @@ MOE_API int moe_tail_ep_finalize(const void* rows, int64_t rows_per_slot, const 
   a.tp = tp;
   a.K = K;
   a.P = P;
-  a.chunks = (P + 255) / 256;
   a.out = static_cast<uint16_t*>(out);
-  return finish(moetail::launch_ep_finalize(a, weight_before_norm != 0, weight_dtype, device_sms(), 0,
-                                            static_cast<cudaStream_t>(stream)));
+  return finish(moetail::launch_finalize(moetail::kFinalizeEP, a, weight_before_norm != 0, weight_dtype,
+                                         device_sms(), static_cast<cudaStream_t>(stream)));
 }
 
 // ============================================================================ expert-TP finalize
@@ -151,8 +151,8 @@ MOE_API int moe_tail_tp_finalize(const void* partials, int64_t num_rows, const i
       overlaps(o, span(permuted_idx, (size_t)b * K * 4)) || overlaps(o, span(route_weights, (size_t)b * K * wsz)) ||
       overlaps(o, span(gamma, (size_t)P * 2)))
     return MOE_TAIL_EINVAL;
-  TpArgs a;
-  a.partials = static_cast<const uint16_t*>(partials);
+  FinalizeArgs a;
+  a.rows = static_cast<const uint16_t*>(partials);
   a.num_rows = num_rows;
   a.slot_stride = num_rows * P;
   a.idx = permuted_idx;
@@ -165,10 +165,9 @@ MOE_API int moe_tail_tp_finalize(const void* partials, int64_t num_rows, const i
   a.tp = tp;
   a.K = K;
   a.P = P;
-  a.chunks = (P + 255) / 256;
   a.out = static_cast<uint16_t*>(out);
-  return finish(moetail::launch_tp_finalize(a, weight_before_norm != 0, weight_dtype, device_sms(), 0,
-                                            static_cast<cudaStream_t>(stream)));
+  return finish(moetail::launch_finalize(moetail::kFinalizeTP, a, weight_before_norm != 0, weight_dtype,
+                                         device_sms(), static_cast<cudaStream_t>(stream)));
 }
 
 // ============================================================================ latent tail
@@ -200,15 +199,15 @@ MOE_API int moe_tail_latent_up(const void* latent, const void* gamma, float eps,
 
   const GemmPlan plan = moetail::plan_gemm(moetail::kGemmUpShared, H, L, b, device_sms());
   CUtensorMap mw, mx;
-  if (!encode_bf16_2d(&mw, w_up, H, L, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+  if (!encode_bf16_2d(&mw, w_up, H, L, plan.tm, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !encode_bf16_2d(&mx, workspace, b, L, plan.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
     return MOE_TAIL_ECUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   // 1. y = RMS norm of the slot-summed latent (an expert-TP finalize with one
   //    "route" per token: row = token, unit weight, gain center 0).
-  TpArgs n;
-  n.partials = static_cast<const uint16_t*>(latent);
+  FinalizeArgs n;
+  n.rows = static_cast<const uint16_t*>(latent);
   n.num_rows = b;
   n.slot_stride = (int64_t)b * L;
   n.idx = nullptr;
@@ -221,9 +220,8 @@ MOE_API int moe_tail_latent_up(const void* latent, const void* gamma, float eps,
   n.tp = tp;
   n.K = 1;
   n.P = L;
-  n.chunks = (L + 255) / 256;
   n.out = static_cast<uint16_t*>(workspace);
-  cudaError_t e = moetail::launch_tp_finalize(n, false, moetail::kWeightUnit, device_sms(), 0, st);
+  cudaError_t e = moetail::launch_finalize(moetail::kFinalizeLatent, n, false, moetail::kWeightUnit, device_sms(), st);
   if (e != cudaSuccess) return finish(e);
 
   // 2. out = y . w_up^T + sum_s shared[s]
@@ -264,10 +262,10 @@ MOE_API int moe_shared_expert(const void* x, const void* w_gate, const void* w_u
   const GemmPlan p1 = moetail::plan_gemm(moetail::kGemmGateUpSilu, I, H, b, sms);
   const GemmPlan p2 = moetail::plan_gemm(moetail::kGemmDown, H, I, b, sms);
   CUtensorMap mg, mu, mx, md, mh;
-  if (!encode_bf16_2d(&mg, w_gate, I, H, 64, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
-      !encode_bf16_2d(&mu, w_up, I, H, 64, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+  if (!encode_bf16_2d(&mg, w_gate, I, H, p1.tm / 2, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&mu, w_up, I, H, p1.tm / 2, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !encode_bf16_2d(&mx, x, b, H, p1.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
-      !encode_bf16_2d(&md, w_down, H, I, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&md, w_down, H, I, p2.tm, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !encode_bf16_2d(&mh, workspace, b, I, p2.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
     return MOE_TAIL_ECUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

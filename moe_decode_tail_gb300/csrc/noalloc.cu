@@ -117,14 +117,14 @@ MOE_API int moe_tail_latent_up_noalloc(const void* latent, const void* gamma, fl
   }
   const moetail::GemmPlan plan = moetail::plan_gemm(moetail::kGemmUpShared, H, L, b, sms);
   CUtensorMap mw, mx;
-  if (!encode_rows(&mw, w_up, H, L, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+  if (!encode_rows(&mw, w_up, H, L, plan.tm, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !encode_rows(&mx, y, b, L, plan.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
     return MOE_TAIL_ECUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   // 1. y (every element written, so nothing has to start at zero)
-  moetail::TpArgs n;
-  n.partials = static_cast<const uint16_t*>(latent);
+  moetail::FinalizeArgs n;
+  n.rows = static_cast<const uint16_t*>(latent);
   n.num_rows = b;
   n.slot_stride = (int64_t)b * L;
   n.idx = nullptr;
@@ -137,9 +137,8 @@ MOE_API int moe_tail_latent_up_noalloc(const void* latent, const void* gamma, fl
   n.tp = tp;
   n.K = 1;
   n.P = L;
-  n.chunks = (L + 255) / 256;
   n.out = static_cast<uint16_t*>(y);
-  e = moetail::launch_tp_finalize(n, false, moetail::kWeightUnit, sms, 0, st);
+  e = moetail::launch_finalize(moetail::kFinalizeLatent, n, false, moetail::kWeightUnit, sms, st);
   if (e == cudaSuccess) {
     // 2. out = y . w_up^T + sum_s shared[s]
     moetail::GemmArgs g;
