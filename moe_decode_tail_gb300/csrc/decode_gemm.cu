@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot_ptr;
+  launch_dependents();  // the next kernel may be scheduled as this one's CTAs retire
 
   // Weight box of K block kb into stage st (two half-height boxes for gate/up).
   auto load_weights = [&](uint32_t st, uint32_t bar, int kb, uint64_t policy) {
@@ -242,14 +243,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t stream = policy_evict_first();  // weights: read once
       int issued = 0;
       bool ok = true;
-      // Weights do not depend on the preceding kernel: the first ring's worth is
-      // requested before waiting for it.
+      // Inside the library's own kernel chains the weights never depend on the
+      // preceding kernel, so the first ring's worth is requested before waiting
+      // for it; the first kernel of a call waits first.
       const int pre = min(nk, stages);
+      if (!a.weights_before_wait) grid_dependency_wait();
       for (int i = 0; i < pre; ++i) {
         mbar_expect_tx(L.full + 8 * i, kStageBytes);
         load_weights(L.ring + i * kStageBytes, L.full + 8 * i, kb0 + i, stream);
       }
-      grid_dependency_wait();
+      if (a.weights_before_wait) grid_dependency_wait();
       for (int i = 0; i < pre; ++i)
         tma_load_2d(L.ring + i * kStageBytes + kATile, &map_x, L.full + 8 * i, (kb0 + i) * kBlockK, tok0, keep);
       issued = pre;
@@ -388,7 +391,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  launch_dependents();
   if (ksplit > 1) cluster_sync_all();  // peers are done reading this CTA's staging tile
   __syncthreads();
   if (warp == 5) {

@@ -40,6 +40,7 @@ struct GemmArgs {
   int tp_s;
   uint16_t* out;     // mode 0, 2: BF16 [b][M]; mode 1: h BF16 [b][M]
   int accumulate;    // mode 2: out = bf16(out + bf16(d))
+  int weights_before_wait;  // 1 only when the preceding kernel is this library's own
 };
 
 struct GemmPlan {

@@ -234,6 +234,7 @@ MOE_API int moe_tail_latent_up(const void* latent, const void* gamma, float eps,
   g.tp_s = tp_s;
   g.out = static_cast<uint16_t*>(out);
   g.accumulate = 0;
+  g.weights_before_wait = 1;  // follows this call's own norm kernel
   return finish(moetail::launch_decode_gemm(moetail::kGemmUpShared, plan, mw, mw, mx, g, true, st));
 }
 
@@ -279,7 +280,8 @@ MOE_API int moe_shared_expert(const void* x, const void* w_gate, const void* w_u
   g.tp_s = 0;
   g.out = static_cast<uint16_t*>(workspace);
   g.accumulate = 0;
-  cudaError_t e = moetail::launch_decode_gemm(moetail::kGemmGateUpSilu, p1, mg, mu, mx, g, false, st);
+  g.weights_before_wait = 0;  // first kernel of the call: the caller may just have written the weights
+  cudaError_t e = moetail::launch_decode_gemm(moetail::kGemmGateUpSilu, p1, mg, mu, mx, g, true, st);
   if (e != cudaSuccess) return finish(e);
 
   GemmArgs d;
@@ -291,6 +293,7 @@ MOE_API int moe_shared_expert(const void* x, const void* w_gate, const void* w_u
   d.tp_s = 0;
   d.out = static_cast<uint16_t*>(out);
   d.accumulate = accumulate != 0;
+  d.weights_before_wait = 1;  // follows this call's own gate/up kernel
   return finish(moetail::launch_decode_gemm(moetail::kGemmDown, p2, md, md, mh, d, true, st));
 }
 

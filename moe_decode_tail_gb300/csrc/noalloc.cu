@@ -150,6 +150,7 @@ MOE_API int moe_tail_latent_up_noalloc(const void* latent, const void* gamma, fl
     g.tp_s = tp_s;
     g.out = static_cast<uint16_t*>(out);
     g.accumulate = 0;
+    g.weights_before_wait = 1;
     e = moetail::launch_decode_gemm(moetail::kGemmUpShared, plan, mw, mw, mx, g, true, st);
   }
   if (e != cudaSuccess) {
