@@ -167,10 +167,12 @@ struct GemmSmem {  // offsets from the 1024-aligned base of dynamic shared memor
   uint32_t ring, full, empty, accum, tmem_slot, abort_flag;
 };
 
-// TM = weight rows per CTA (the MMA's M: 64 or 128).  With TM = 128 the
-// accumulator row r sits in TMEM lane r; with TM = 64 it sits in lane
-// 32 * (r / 16) + r % 16 (lanes 16..31 of each warp's quarter stay unused).
-// Gate/up tiles hold TM/2 gate rows then the TM/2 matching up rows.
+// TM = weight rows per CTA: 64 (one M=64 MMA), 128 (one M=128 MMA) or 256
+// (two M=128 MMAs per K step sharing the token tile, into two accumulators
+// at TMEM columns [0, N) and [N, 2N)).  With M = 128 accumulator row r sits
+// in TMEM lane r; with M = 64 it sits in lane 32 * (r / 16) + r % 16 (lanes
+// 16..31 of each warp's quarter stay unused).  Gate/up tiles hold TM/2 gate
+// rows then the TM/2 matching up rows.
 template <int MODE, int N, int TM>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
@@ -179,8 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kATile = TM * kBlockK * 2;
   constexpr int kBTileBytes = N * kBlockK * 2;
   constexpr int kStageBytes = kATile + kBTileBytes;
-  constexpr uint32_t kTmemCols = N < 32 ? 32 : N;
-  constexpr uint32_t kIdesc = idesc_bf16(TM, N);
+  constexpr int kMmaM = TM == 64 ? 64 : 128;
+  constexpr int kNumAcc = TM / kMmaM;
+  constexpr uint32_t kTmemCols = N * kNumAcc < 32 ? 32 : N * kNumAcc;
+  constexpr uint32_t kIdesc = idesc_bf16(kMmaM, N);
   constexpr int kOutRows = (MODE == kGemmGateUpSilu) ? TM / 2 : TM;  // output features per tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -295,7 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bdesc = smem_desc_sw128(st + kATile);
 #pragma unroll
         for (int kk = 0; kk < kBlockK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
-          mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int acc = 0; acc < kNumAcc; ++acc)  // accumulator acc: weight rows acc*128 .. +127
+            mma_bf16(tmem + (uint32_t)(acc * N), adesc + (uint64_t)(acc * (kMmaM * 128 >> 4)) + 2 * kk,
+                     bdesc + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(L.empty + 8 * s);
       }
       mma_commit(L.accum);  // also on abort: completes once the issued MMAs are done
@@ -311,20 +318,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_after();
     float* stage = reinterpret_cast<float*>(base_ptr);
-    const bool holds_row = TM == 128 || lane < 16;
-    const int row = TM == 128 ? warp * 32 + lane : warp * 16 + lane;
-    if (got && nk > 0) {
+    const bool holds_row = kMmaM == 128 || lane < 16;
+    const int row = kMmaM == 128 ? warp * 32 + lane : warp * 16 + lane;
+    for (int acc = 0; acc < kNumAcc; ++acc) {
+      const int r = acc * kMmaM + row;
+      if (got && nk > 0) {
 #pragma unroll 1
-      for (int c = 0; c < N; c += 16) {
-        float v[16];
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
-        if (holds_row) {
+        for (int c = 0; c < N; c += 16) {
+          float v[16];
+          tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * N + c), v);
+          if (holds_row) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) stage[(c + i) * TM + row] = v[i];
+            for (int i = 0; i < 16; ++i) stage[(c + i) * TM + r] = v[i];
+          }
         }
+      } else if (got && holds_row) {  // an empty K range contributes zeros
+        for (int c = 0; c < N; ++c) stage[c * TM + r] = 0.0f;
       }
-    } else if (got && holds_row) {  // an empty K range contributes zeros
-      for (int c = 0; c < N; ++c) stage[c * TM + row] = 0.0f;
     }
     tc_fence_before();
   }
@@ -409,7 +419,7 @@ static bool plan_override(int mode, GemmPlan& p) {
   const char* v = getenv(names[mode]);
   int tm = 0, ks = 0, st = 0;
   if (!v || sscanf(v, "%d,%d,%d", &tm, &ks, &st) != 3) return false;
-  if ((tm != 64 && tm != 128) || ks < 1 || ks > 8 || st < 2 || st > kMaxStages) return false;
+  if ((tm != 64 && tm != 128 && tm != 256) || ks < 1 || ks > 8 || st < 2 || st > kMaxStages) return false;
   p.tm = tm;
   p.ksplit = ks;
   p.stages = st;
@@ -432,7 +442,7 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms) {
   }
   p.ksplit = std::min(p.ksplit, kblocks);
   const int sb = stage_bytes(p.tm, p.n_tile);
-  if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, (110 * 1024) / sb));
+  if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, (p.tm == 256 ? 200 * 1024 : 110 * 1024) / sb));
   const int per_cta = (kblocks + p.ksplit - 1) / p.ksplit;
   p.stages = std::min(p.stages, std::max(2, per_cta));
   // the FP32 staging tile reuses the ring
@@ -499,6 +509,7 @@ static cudaError_t launch_n(const GemmPlan& p, const CUtensorMap& w0, const CUte
 template <int MODE>
 static cudaError_t launch_mode(const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1,
                                const CUtensorMap& x, const GemmArgs& a, bool pdl, cudaStream_t stream) {
+  if (p.tm == 256) return launch_n<MODE, 256>(p, w0, w1, x, a, pdl, stream);
   return p.tm == 128 ? launch_n<MODE, 128>(p, w0, w1, x, a, pdl, stream)
                      : launch_n<MODE, 64>(p, w0, w1, x, a, pdl, stream);
 }

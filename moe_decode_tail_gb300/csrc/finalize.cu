@@ -250,6 +250,261 @@ __global__ void __launch_bounds__(kMaxThreads) finalize_kernel(const FinalizeArg
   }
 }
 
+// ------------------------------------------- expert-TP / latent: staged rows
+//
+// The same arithmetic as finalize_kernel for expert-TP and the latent norm,
+// with the rows staged in shared memory: warp 0 of the CTA is a producer that
+// streams, for each route of each token the CTA owns (in route order), the
+// route's rows of this column band in every slot with 1-D bulk asynchronous
+// copies into a ring of stages (one route = one stage = tp band rows),
+// tracked by mbarriers.  Consumer thread v owns 16-byte vector v of the band.
+// A CTA finalizes tokens blockIdx.y, + gridDim.y, ... so the ring keeps
+// streaming across tokens.  Every wait is bounded; once a wait gives up, all
+// later waits return at once, so the kernel ends without skipping a barrier.
+
+constexpr int kStagedMaxStages = 16;
+
+__device__ unsigned int g_finalize_error = 0;
+
+struct __align__(16) StagedSmem {
+  float ss[2][kMaxRoutesPerPass][kMaxChunks];
+  unsigned long long full[kStagedMaxStages], empty[kStagedMaxStages];
+  uint32_t abort_flag;
+};
+
+__device__ __forceinline__ void sb_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void sb_expect(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void sb_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool sb_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool sb_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
+  if (sb_try(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!sb_try(bar, parity)) {
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(&g_finalize_error, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Route cursor of the staged kernel's copy issuer: the next (token, route)
+// with a row, in the order the consumers take them.
+struct RouteCursor {
+  int t, k;
+};
+
+template <bool LATENT>
+__device__ __forceinline__ bool next_route(const FinalizeArgs& a, RouteCursor& c, int64_t& row) {
+  while (c.t < a.b) {
+    if (c.k >= a.K) {
+      c.t += gridDim.y;
+      c.k = 0;
+      continue;
+    }
+    const int64_t j = LATENT ? (int64_t)c.t : (int64_t)a.idx[(int64_t)c.t * a.K + c.k];
+    ++c.k;
+    if (j >= 0 && j < a.num_rows) {
+      row = j;
+      return true;
+    }
+  }
+  return false;
+}
+
+template <bool WBN, int WMODE, bool LATENT>
+__global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs a) {
+  extern __shared__ __align__(128) uint8_t ring_raw[];
+  __shared__ StagedSmem sm;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int VB = a.band_vectors;  // one 16-byte vector of the band per thread
+  const int S = a.stages;
+  const uint32_t split = cluster_size();
+  const int band = (int)cluster_rank();
+  const int col0 = band * VB * 8;
+  const uint32_t band_bytes = (uint32_t)VB * 16;
+  const uint32_t copy_bytes = col0 < a.P ? (uint32_t)min(VB * 8, a.P - col0) * 2 : 0u;
+  const uint32_t stage_bytes = band_bytes * (uint32_t)a.tp;
+  const uint32_t ring = smem_addr(ring_raw);
+  volatile uint32_t* abort_flag = &sm.abort_flag;
+  const bool issuer = tid == 0;  // lane 0 of warp 0 also issues the copies
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      sb_init(smem_addr(&sm.full[i]), 1);
+      sb_init(smem_addr(&sm.empty[i]), (uint32_t)(VB / 32));
+    }
+    sm.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  grid_dependency_wait();
+  launch_dependents();
+
+  // The issuer copies route number n (counting the routes with a row, in the
+  // consumers' order) into stage n % S.  Stage reuse waits until every warp
+  // has released the stage; the issuer's own warp releases it first, and no
+  // warp waits on the issuer before releasing, so this cannot deadlock.
+  RouteCursor cur = {(int)blockIdx.y, 0};
+  uint32_t issued = 0;
+  auto issue_next = [&]() {
+    int64_t j;
+    if (!next_route<LATENT>(a, cur, j)) return;
+    const int st = (int)(issued % (uint32_t)S);
+    if (issued >= (uint32_t)S) sb_wait(smem_addr(&sm.empty[st]), ((issued / S) - 1) & 1, abort_flag);
+    ++issued;
+    const uint32_t bar = smem_addr(&sm.full[st]);
+    if (*abort_flag) {  // still complete the stage so that nobody waits for it
+      sb_arrive(bar);
+      return;
+    }
+    sb_expect(bar, copy_bytes * (uint32_t)a.tp);
+    if (copy_bytes) {
+      const uint16_t* src = a.rows + j * a.P + col0;
+      const uint32_t dst = ring + (uint32_t)st * stage_bytes;
+      for (int s = 0; s < a.tp; ++s) bulk_copy(dst + (uint32_t)s * band_bytes, src + (int64_t)s * a.slot_stride, copy_bytes, bar);
+    }
+  };
+  if (issuer)
+    for (int i = 0; i < S; ++i) issue_next();
+
+  const int vb = tid;
+  const int vec = band * VB + vb;
+  const bool valid = vec * 8 < a.P;
+  const int chunk = vec >> 5;
+  float g8[8];
+  {
+    const uint4 gv = valid ? ld_v4(a.gamma + vec * 8) : make_uint4(0, 0, 0, 0);
+    unpack8(gv, g8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g8[i] = __fadd_rn(g8[i], a.gain_center);
+  }
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // peers started: DSMEM is live
+
+  uint32_t g = 0;  // stages consumed
+  int pass = 0;
+  for (int t = blockIdx.y; t < a.b; t += gridDim.y) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int base = 0; base < a.K; base += kMaxRoutesPerPass, ++pass) {
+      float xr[kMaxRoutesPerPass][8];
+      bool has[kMaxRoutesPerPass];
+      float wr[kMaxRoutesPerPass];
+      float* ss = &sm.ss[pass & 1][0][0];
+#pragma unroll
+      for (int rr = 0; rr < kMaxRoutesPerPass; ++rr) {
+        const int k = base + rr;
+        int64_t j = -1;
+        if (k < a.K) j = LATENT ? (int64_t)t : (int64_t)a.idx[(int64_t)t * a.K + k];
+        has[rr] = k < a.K && j >= 0 && j < a.num_rows;
+        wr[rr] = has[rr] ? route_weight<WMODE>(a.w, (int64_t)t * a.K + k) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xr[rr][i] = 0.0f;
+        if (has[rr]) {
+          const int st = (int)(g % (uint32_t)S);
+          sb_wait(smem_addr(&sm.full[st]), (g / S) & 1, abort_flag);
+          ++g;
+          if (valid) {
+            const uint8_t* src = ring_raw + (size_t)st * stage_bytes + (size_t)vb * 16;
+            for (int s = 0; s < a.tp; ++s, src += band_bytes) {  // slot order, FP32 from +0
+              float f[8];
+              unpack8(*reinterpret_cast<const uint4*>(src), f);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) xr[rr][i] = __fadd_rn(xr[rr][i], f[i]);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) sb_arrive(smem_addr(&sm.empty[st]));
+          if (issuer) issue_next();  // refill the stage just consumed
+#pragma unroll
+          for (int i = 0; i < 8; ++i) xr[rr][i] = bf16_round(xr[rr][i]);
+          float sq = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float v = WBN ? __fmul_rn(xr[rr][i], g8[i]) : xr[rr][i];
+            sq = __fadd_rn(sq, __fmul_rn(v, v));
+          }
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, off));
+          if (chunk < a.chunks && lane < (int)split)
+            st_cluster_f32(map_to_rank(smem_addr(&ss[rr * kMaxChunks + chunk]), (uint32_t)lane), sq);
+        }
+      }
+      cluster_sync_all();
+      // fold the chunk sums of the pass's routes (independent chains side by side)
+      float tot[kMaxRoutesPerPass];
+#pragma unroll
+      for (int rr = 0; rr < kMaxRoutesPerPass; ++rr) tot[rr] = 0.0f;
+      for (int c = 0; c < a.chunks; ++c) {
+#pragma unroll
+        for (int rr = 0; rr < kMaxRoutesPerPass; ++rr)
+          if (has[rr]) tot[rr] = __fadd_rn(tot[rr], ss[rr * kMaxChunks + c]);
+      }
+#pragma unroll
+      for (int rr = 0; rr < kMaxRoutesPerPass; ++rr) {
+        if (has[rr]) {  // a route with no row contributes nothing
+          const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(tot[rr], a.rcpP), a.eps)));
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float x = xr[rr][i];
+            const float nv = WBN ? __fmul_rn(__fmul_rn(x, g8[i]), inv) : __fmul_rn(__fmul_rn(x, inv), g8[i]);
+            acc[i] = __fadd_rn(acc[i], __fmul_rn(nv, wr[rr]));
+          }
+        }
+      }
+    }
+    if (valid) {
+      uint4 r;
+      r.x = pack_bf16x2_pz(acc[0], acc[1]);
+      r.y = pack_bf16x2_pz(acc[2], acc[3]);
+      r.z = pack_bf16x2_pz(acc[4], acc[5]);
+      r.w = pack_bf16x2_pz(acc[6], acc[7]);
+      st_v4(a.out + (int64_t)t * a.P + vec * 8, r);
+    }
+  }
+  // on abort, let copies in flight land before the CTA's memory goes away
+  if (issuer && *abort_flag) {
+    for (uint32_t i = issued > (uint32_t)S ? issued - S : 0; i < issued; ++i) {
+      const unsigned long long t0 = global_ns();
+      while (!sb_try(smem_addr(&sm.full[i % S]), (i / S) & 1))
+        if (global_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+}
+
+cudaError_t take_finalize_error(unsigned* bits) {
+  unsigned v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_finalize_error, sizeof v);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_finalize_error, &zero, sizeof zero);
+  *bits = v;
+  return e;
+}
+
 // ---------------------------------------------------------------- launcher
 
 // Tuning override of the column split: MOE_TAIL_FIN_SPLIT=<1|2|4|8>.
@@ -292,16 +547,91 @@ static cudaError_t launch_t(const FinalizeArgs& a, int split, cudaStream_t strea
   return cudaLaunchKernelEx(&cfg, k, a);
 }
 
-cudaError_t launch_finalize(int mode, const FinalizeArgs& args, bool wbn, int wmode, int sms, cudaStream_t stream) {
+template <bool WBN, int WMODE, bool LATENT>
+static cudaError_t launch_staged_t(const FinalizeArgs& a, int split, int groups, size_t smem, cudaStream_t stream) {
+  auto k = staged_finalize_kernel<WBN, WMODE, LATENT>;
+  static int configured[64] = {0};  // raise the limit once per device, not per call
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 192 * 1024);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(split, groups, 1);
+  cfg.blockDim = dim3(a.band_vectors, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k, a);
+}
+
+static int env_int(const char* name, int fallback) {
+  const char* v = getenv(name);
+  return v ? atoi(v) : fallback;
+}
+
+// Expert-TP and latent with the rows staged in shared memory; returns
+// cudaErrorNotSupported when a stage (one route's rows of a band in every
+// slot) does not fit, so the caller can fall back to finalize_kernel.
+static cudaError_t launch_staged(int mode, const FinalizeArgs& args, bool wbn, int wmode, int sms, cudaStream_t stream) {
   FinalizeArgs a = args;
   a.chunks = (a.P + 255) / 256;
-  const int routes = mode == kModeLatent ? 1 : (mode == kModeEP ? a.tp * a.K : a.K);
-  // Bands per token: enough CTAs to cover the SMs about twice, at most 8
-  // (portable cluster size), one band per chunk at most.
+  // Bands per token: the fewest that keep a stage (one route's band rows in
+  // every slot) within 32 KB, then more while the batch leaves over half of
+  // the SMs idle (measured on GB300: tp = 8, P = 4096 is best at 2 bands for
+  // b = 64 and b = 128).
   int split = split_override();
   if (split == 0) {
     split = 1;
-    while (split < 8 && split < a.chunks && (int64_t)a.b * split < 2 * sms) split *= 2;
+    while (split < 8 && split < a.chunks && (size_t)a.tp * ((a.P + split - 1) / split) * 2 > 32 * 1024) split *= 2;
+    while (split < 8 && split < a.chunks && (int64_t)a.b * split < sms / 2) split *= 2;
+  }
+  while (split < 8 && (a.chunks + split - 1) / split > 16) split *= 2;
+  a.band_vectors = 32 * ((a.chunks + split - 1) / split);
+  if (a.band_vectors > 512) return cudaErrorNotSupported;
+  const size_t stage_bytes = (size_t)a.tp * a.band_vectors * 16;
+  const size_t budget = (size_t)env_int("MOE_TAIL_FIN_RING_KB", 64) * 1024;
+  a.stages = (int)std::min<size_t>(16, budget / stage_bytes);
+  if (a.stages < 2) return cudaErrorNotSupported;
+  const int groups = (int)std::min<int64_t>(a.b, std::max<int64_t>(1, 2 * (int64_t)sms / split));
+  const size_t smem = (size_t)a.stages * stage_bytes;
+  if (mode == kModeLatent) return launch_staged_t<false, kWeightUnit, true>(a, split, groups, smem, stream);
+  if (wbn) return wmode == kWeightBF16 ? launch_staged_t<true, kWeightBF16, false>(a, split, groups, smem, stream)
+                                       : launch_staged_t<true, kWeightF32, false>(a, split, groups, smem, stream);
+  return wmode == kWeightBF16 ? launch_staged_t<false, kWeightBF16, false>(a, split, groups, smem, stream)
+                              : launch_staged_t<false, kWeightF32, false>(a, split, groups, smem, stream);
+}
+
+cudaError_t launch_finalize(int mode, const FinalizeArgs& args, bool wbn, int wmode, int sms, cudaStream_t stream) {
+  // Staged rows pay off for expert-TP (tp rows per route); the latent norm
+  // (one route per token) is faster on the route-parallel kernel.
+  if (mode == kModeTP && env_int("MOE_TAIL_FIN_STAGED", 1)) {
+    const cudaError_t e = launch_staged(mode, args, wbn, wmode, sms, stream);
+    if (e != cudaErrorNotSupported) return e;
+  }
+  FinalizeArgs a = args;
+  a.chunks = (a.P + 255) / 256;
+  const int routes = mode == kModeLatent ? 1 : (mode == kModeEP ? a.tp * a.K : a.K);
+  // Bands per token: EP moves little data per token, so about one wave of
+  // CTAs (b * split >= 3/4 of the SMs); expert-TP and latent about two.  At
+  // most 8 bands (portable cluster size), one band per chunk at most.
+  int split = split_override();
+  if (split == 0) {
+    const int64_t target = mode == kModeEP ? (3 * (int64_t)sms) / 4 : 2 * (int64_t)sms;
+    split = 1;
+    while (split < 8 && split < a.chunks && (int64_t)a.b * split < target) split *= 2;
   }
   while (split < 8 && (a.chunks + split - 1) / split > 32) split *= 2;
   a.band_vectors = 32 * ((a.chunks + split - 1) / split);

@@ -19,13 +19,15 @@ struct FinalizeArgs {
   const uint16_t* gamma;  // BF16 [P]
   float gain_center, eps, rcpP;
   int b, tp, K, P;
-  int chunks, band_vectors, routes_per_pass;  // set by the launcher
+  int chunks, band_vectors, routes_per_pass, stages;  // set by the launcher
   uint16_t* out;          // BF16 [b][P]
 };
 
 enum { kFinalizeEP = 0, kFinalizeTP = 1, kFinalizeLatent = 2 };
 
 cudaError_t launch_finalize(int mode, const FinalizeArgs& a, bool wbn, int wmode, int sms, cudaStream_t stream);
+// Read and clear the finalize kernels' device error word (synchronises).
+cudaError_t take_finalize_error(unsigned* bits);
 
 // ---- decode GEMM (tcgen05) ---------------------------------------------------
 

@@ -311,5 +311,9 @@ MOE_API const char* moe_tail_status_str(int status) {
 
 MOE_API int moe_tail_take_device_error(unsigned int* bits) {
   if (!bits) return MOE_TAIL_EINVAL;
-  return finish(moetail::take_device_error(bits));
+  unsigned g = 0, f = 0;
+  cudaError_t e = moetail::take_device_error(&g);
+  if (e == cudaSuccess) e = moetail::take_finalize_error(&f);
+  *bits = g | f;
+  return finish(e);
 }
