@@ -64,6 +64,8 @@ def parse_args():
     ap.add_argument("--graph-steps", type=int, default=50, help="steps captured per CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sequential", action="store_true",
+                    help="run the four calls in order on one stream (shared expert accumulating into out)")
     return ap.parse_args()
 
 
@@ -185,26 +187,69 @@ def make_workload(dev):
     w["out"] = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
     w["ws_lat"] = torch.empty(mt.moe_tail_workspace_bytes(0, B, L), dtype=torch.uint8, device=dev)
     w["ws_sh"] = torch.empty(mt.moe_tail_workspace_bytes(1, B, I), dtype=torch.uint8, device=dev)
+    # the latent tail's shared partials plus one slot that receives the shared expert's output
+    w["shared9"] = torch.empty((TP + 1, B, H), dtype=torch.bfloat16, device=dev)
+    w["shared9"][:TP].copy_(w["shared"])
+    w["d_slot"] = w["shared9"][TP]
+    w["fork"], w["join"] = torch.cuda.Event(), torch.cuda.Event()
     return cpu, w
 
 
-def run_step(mt, w, stream, events=None):
-    """The four calls of one step; events: optional list of 5 events."""
-    ev = events or [None] * 5
-    rec = lambda i: ev[i].record(stream) if ev[i] is not None else None
-    rec(0)
-    mt.moe_tail_ep_finalize(w["ep_rows"], w["ep_idx"], w["ep_w"], w["ep_gamma"], w["out_ep"], gain_center=1.0,
-                            eps=1e-6, weight_before_norm=True, stream=stream)
-    rec(1)
-    mt.moe_tail_tp_finalize(w["tp_part"], w["tp_idx"], w["tp_w"], w["tp_gamma"], w["out_tp"], gain_center=1.0,
-                            eps=1e-6, weight_before_norm=True, stream=stream)
-    rec(2)
-    mt.moe_tail_latent_up(w["latent"], w["lat_gamma"], w["w_up"], w["shared"], w["out"], w["ws_lat"], eps=1e-6,
-                          stream=stream)
-    rec(3)
-    mt.moe_shared_expert(w["x"], w["w_gate"], w["w_up_s"], w["w_down"], w["out"], w["ws_sh"], accumulate=True,
-                         stream=stream)
-    rec(4)
+def run_step(mt, w, stream, events=None, side=None):
+    """The four calls of one step.  events: optional list of 8 events, a
+    (start, end) pair per call in CALLS order, recorded on the call's stream.
+
+    With a side stream the shared expert runs beside the routed path, as the
+    Kimi-K3 tail does (its output is pushed into the tail's reduce-scatter
+    partials): moe_shared_expert writes d = bf16(down(h)) into the last of the
+    latent tail's shared-partial slots, and moe_tail_latent_up adds it with
+    the other slots in its epilogue once the side branch is done.  Without
+    one, the calls run in order and the shared expert accumulates into the
+    latent tail's output."""
+    ev = events or [None] * 8
+
+    def rec(i, st):
+        if ev[i] is not None:
+            ev[i].record(st)
+
+    def ep(st):
+        rec(0, st)
+        mt.moe_tail_ep_finalize(w["ep_rows"], w["ep_idx"], w["ep_w"], w["ep_gamma"], w["out_ep"], gain_center=1.0,
+                                eps=1e-6, weight_before_norm=True, stream=st)
+        rec(1, st)
+
+    def tp(st):
+        rec(2, st)
+        mt.moe_tail_tp_finalize(w["tp_part"], w["tp_idx"], w["tp_w"], w["tp_gamma"], w["out_tp"], gain_center=1.0,
+                                eps=1e-6, weight_before_norm=True, stream=st)
+        rec(3, st)
+
+    def latent(st, shared):
+        rec(4, st)
+        mt.moe_tail_latent_up(w["latent"], w["lat_gamma"], w["w_up"], shared, w["out"], w["ws_lat"], eps=1e-6,
+                              stream=st)
+        rec(5, st)
+
+    def shared_expert(st, out, accumulate):
+        rec(6, st)
+        mt.moe_shared_expert(w["x"], w["w_gate"], w["w_up_s"], w["w_down"], out, w["ws_sh"], accumulate=accumulate,
+                             stream=st)
+        rec(7, st)
+
+    if side is None:
+        ep(stream)
+        tp(stream)
+        latent(stream, w["shared"])
+        shared_expert(stream, w["out"], True)
+        return
+    w["fork"].record(stream)
+    side.wait_event(w["fork"])
+    shared_expert(side, w["d_slot"], False)
+    w["join"].record(side)
+    ep(stream)
+    tp(stream)
+    stream.wait_event(w["join"])
+    latent(stream, w["shared9"])
 
 
 CALLS = ["ep_finalize", "tp_finalize", "latent_up", "shared_expert"]
@@ -368,25 +413,28 @@ def cuda_arm(args, world, rank, local):
 
     mt.lib()
     cpu, w = make_workload(dev)
-    stream = torch.cuda.Stream(dev)
+    # the routed path (latency-bound finalize kernels) on a high-priority stream,
+    # the shared expert (a weight stream) beside it
+    stream = torch.cuda.Stream(dev, priority=-1)
+    side = None if args.sequential else torch.cuda.Stream(dev, priority=0)
     K, W = args.steps, args.warmup
     G = max(1, min(args.graph_steps, K))
 
     with torch.cuda.stream(stream):
         for _ in range(3):  # eager warm-up: loads the kernels
-            run_step(mt, w, stream)
-    stream.synchronize()
+            run_step(mt, w, stream, side=side)
+    torch.cuda.synchronize()
 
     def capture(n, with_events):
         # Per-call events (external: recorded as event nodes of the graph, replayed
         # with it) in every tenth step only: an event between two calls keeps the
         # second from being scheduled while the first drains.
-        evs = ([[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)] if i % 10 == 0 else None
+        evs = ([[torch.cuda.Event(enable_timing=True, external=True) for _ in range(8)] if i % 10 == 0 else None
                 for i in range(n)] if with_events else None)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                run_step(mt, w, stream, evs[i] if evs else None)
+                run_step(mt, w, stream, evs[i] if evs else None, side=side)
         return g, [e for e in evs if e is not None] if evs else None
 
     main_g, main_ev = capture(G, True)
@@ -422,19 +470,23 @@ def cuda_arm(args, world, rank, local):
     per_call = {c: [] for c in CALLS}
     for evs in main_ev:
         for i, c in enumerate(CALLS):
-            per_call[c].append(evs[i].elapsed_time(evs[i + 1]) * 1e3)  # us
+            per_call[c].append(evs[2 * i].elapsed_time(evs[2 * i + 1]) * 1e3)  # us
     calls = {}
     hbm, bf16_tf, peak_kind = peaks()
+    nbytes = dict(BYTES)
+    if side is not None:  # d written once and read once as a partial slot, instead of out read + written
+        nbytes["shared_expert"] = 3 * I * H * 2 + B * H * 2 + B * H * 2
+        nbytes["latent_up"] = BYTES["latent_up"] + B * H * 2
     for c in CALLS:
         us = statistics.mean(per_call[c])
-        gbs = BYTES[c] / (us * 1e-6) / 1e9
-        calls[c] = {"us": round(us, 3), "tokens_per_s": B / (us * 1e-6), "algorithmic_bytes": BYTES[c],
+        gbs = nbytes[c] / (us * 1e-6) / 1e9
+        calls[c] = {"us": round(us, 3), "tokens_per_s": B / (us * 1e-6), "algorithmic_bytes": nbytes[c],
                     "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)}
         if c in FLOPS:
             calls[c]["tflops"] = round(FLOPS[c] / (us * 1e-6) / 1e12, 2)
 
     # end to end through the public API from pinned host buffers
-    e2e = e2e_leg(mt, w, stream, min(args.e2e_steps, K), dist, dev)
+    e2e = e2e_leg(mt, w, stream, min(args.e2e_steps, K), dist, dev, side)
 
     if rank != 0:
         return 0
@@ -445,7 +497,7 @@ def cuda_arm(args, world, rank, local):
         "launches": 2 if dom in ("shared_expert", "latent_up") else 1,
         "achieved": calls[dom]["achieved_gbs"], "peak": hbm, "unit": "GB/s",
         "frac": round(calls[dom]["achieved_gbs"] / hbm, 4), "traffic": traffic,
-        "algorithmic_bytes_per_call": BYTES[dom], "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+        "algorithmic_bytes_per_call": nbytes[dom], "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
         "note": "per-call CUDA events on the launch stream, recorded as graph nodes in every tenth step of the "
                 "timed graph replays (those steps lose the overlap between calls, so the per-call figures are "
                 "conservative)",
@@ -455,7 +507,11 @@ def cuda_arm(args, world, rank, local):
         "metric": METRIC, "value": units / max_s, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms, "us_per_layer": ms * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64 + Box-Muller; random-init weights)",
-        "config": workload_config(), "roofline": roof, "calls": calls, "e2e": e2e,
+        "config": dict(workload_config(), composition=(
+            "sequential: EP, TP, latent tail, then the shared expert accumulating into out" if side is None else
+            "two branches: the shared expert on a side stream writes d into an extra shared-partial slot; EP and "
+            "TP on a high-priority stream; the latent tail adds all slots once both are done")),
+        "roofline": roof, "calls": calls, "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * K, "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -464,7 +520,7 @@ def cuda_arm(args, world, rank, local):
     return 0
 
 
-def e2e_leg(mt, w, stream, steps, dist, dev):
+def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
     """The same step through the public API with host buffers: every step
     copies its activations from pinned host memory and reads its outputs back
     (weights stay resident, as in serving)."""
@@ -478,7 +534,7 @@ def e2e_leg(mt, w, stream, steps, dist, dev):
     def one():
         for k in inputs:
             w[k].copy_(host_in[k], non_blocking=True)
-        run_step(mt, w, stream)
+        run_step(mt, w, stream, side=side)
         for k in outputs:
             host_out[k].copy_(w[k], non_blocking=True)
 
