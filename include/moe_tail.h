@@ -183,6 +183,18 @@ const char* moe_tail_status_str(int status);
  * MOE_TAIL_OK or MOE_TAIL_ECUDA. */
 int moe_tail_take_device_error(unsigned int* bits);
 
+/* Failure-detection self-test (no counterpart on the pages).  Every wait
+ * inside these kernels is bounded in time: when one expires the kernel sets a
+ * bit in the device error word, finishes what it started and returns, instead
+ * of hanging or trapping.  This call exercises that path: it launches one
+ * thread that waits, with the same bounded wait, on a barrier nothing arrives
+ * at, for limit_us microseconds (1..1000000).  Afterwards
+ * moe_tail_take_device_error() reports 1 (an operand stage never arrived)
+ * and the device stays usable.
+ * Returns MOE_TAIL_EINVAL for a limit out of range, MOE_TAIL_ECUDA if the
+ * launch fails. */
+int moe_tail_selftest_wait_timeout(unsigned int limit_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,7 +17,7 @@ from .build import LIB
 __all__ = [
     "MoeTailError", "lib", "moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up",
     "moe_shared_expert", "moe_tail_workspace_bytes", "moe_tail_status_str", "moe_tail_take_device_error",
-    "moe_tail_latent_up_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "moe_tail_latent_up_noalloc", "NOALLOC_SCRATCH_BYTES", "moe_tail_selftest_wait_timeout",
 ]
 
 OK, EINVAL, ECUDA, ENOTSUP = 0, 1, 2, 3
@@ -48,13 +48,14 @@ def lib() -> ctypes.CDLL:
         L.moe_tail_latent_up.argtypes = [P, P, f32, P, P, i32, i32, i32, i32, i32, P, P, sz, P]
         L.moe_shared_expert.argtypes = [P, P, P, P, i32, i32, i32, P, i32, P, sz, P]
         L.moe_tail_latent_up_noalloc.argtypes = [P, P, f32, P, P, i32, i32, i32, i32, i32, P, P]
+        L.moe_tail_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
         L.moe_tail_workspace_bytes.argtypes = [i32, i32, i32]
         L.moe_tail_workspace_bytes.restype = sz
         L.moe_tail_status_str.argtypes = [i32]
         L.moe_tail_status_str.restype = ctypes.c_char_p
         L.moe_tail_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         for name in ("moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up", "moe_shared_expert",
-                     "moe_tail_take_device_error", "moe_tail_latent_up_noalloc"):
+                     "moe_tail_take_device_error", "moe_tail_latent_up_noalloc", "moe_tail_selftest_wait_timeout"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -179,3 +180,9 @@ def moe_tail_take_device_error() -> int:
     bits = ctypes.c_uint(0)
     _check("moe_tail_take_device_error", lib().moe_tail_take_device_error(ctypes.byref(bits)))
     return int(bits.value)
+
+
+def moe_tail_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch the failure-detection self-test: a bounded wait that expires after
+    limit_us and reports it through moe_tail_take_device_error()."""
+    _check("moe_tail_selftest_wait_timeout", lib().moe_tail_selftest_wait_timeout(limit_us, _stream(stream)))

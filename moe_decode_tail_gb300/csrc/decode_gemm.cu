@@ -74,11 +74,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase of the given parity to complete; false if the time limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   return true;
 }
 
@@ -407,6 +408,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// Failure-detection self-test: one thread waits, with the kernels' bounded
+// wait, on an mbarrier that nothing arrives at; after limit_ns it gives up,
+// raises kErrWaitFull and returns, so the host sees the error and the context
+// stays usable.
+__global__ void selftest_wait_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_addr(&bar);
+  mbar_init(b, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (!mbar_wait(b, 0, limit_ns)) raise_error(kErrWaitFull);
+}
+
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cudaGetLastError();
 }
 
 // ---- host side ---------------------------------------------------------------------

@@ -59,5 +59,7 @@ cudaError_t launch_decode_gemm(int mode, const GemmPlan& plan, const CUtensorMap
 
 // Read and clear the device error word (synchronises with the device).
 cudaError_t take_device_error(unsigned* bits);
+// A one-thread kernel whose bounded wait expires after limit_ns.
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
 
 }  // namespace moetail

@@ -317,3 +317,8 @@ MOE_API int moe_tail_take_device_error(unsigned int* bits) {
   *bits = g | f;
   return finish(e);
 }
+
+MOE_API int moe_tail_selftest_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return MOE_TAIL_EINVAL;
+  return finish(moetail::launch_selftest_wait((unsigned long long)limit_us * 1000ull, static_cast<cudaStream_t>(stream)));
+}
