@@ -199,13 +199,15 @@ def run_step(mt, w, stream, events=None, side=None):
     """The four calls of one step.  events: optional list of 8 events, a
     (start, end) pair per call in CALLS order, recorded on the call's stream.
 
-    With a side stream the shared expert runs beside the routed path, as the
-    Kimi-K3 tail does (its output is pushed into the tail's reduce-scatter
-    partials): moe_shared_expert writes d = bf16(down(h)) into the last of the
-    latent tail's shared-partial slots, and moe_tail_latent_up adds it with
-    the other slots in its epilogue once the side branch is done.  Without
-    one, the calls run in order and the shared expert accumulates into the
-    latent tail's output."""
+    With a side stream the weight-streaming calls run beside the routed
+    finalize calls, as the Kimi-K3 tail runs its shared expert (its output is
+    pushed into the tail's reduce-scatter partials): on the side stream
+    moe_shared_expert writes d = bf16(down(h)) into the last of the latent
+    tail's shared-partial slots and moe_tail_latent_up follows it, adding d
+    with the other slots in its epilogue; EP and expert-TP finalize run on
+    the main stream, which joins the side stream at the end of the step.
+    Without one, the calls run in order and the shared expert accumulates
+    into the latent tail's output."""
     ev = events or [None] * 8
 
     def rec(i, st):
@@ -245,11 +247,11 @@ def run_step(mt, w, stream, events=None, side=None):
     w["fork"].record(stream)
     side.wait_event(w["fork"])
     shared_expert(side, w["d_slot"], False)
+    latent(side, w["shared9"])
     w["join"].record(side)
     ep(stream)
     tp(stream)
     stream.wait_event(w["join"])
-    latent(stream, w["shared9"])
 
 
 CALLS = ["ep_finalize", "tp_finalize", "latent_up", "shared_expert"]
@@ -413,8 +415,8 @@ def cuda_arm(args, world, rank, local):
 
     mt.lib()
     cpu, w = make_workload(dev)
-    # the routed path (latency-bound finalize kernels) on a high-priority stream,
-    # the shared expert (a weight stream) beside it
+    # the routed finalize calls (latency-bound) on a high-priority stream, the
+    # weight-streaming calls (shared expert, then latent tail) beside them
     stream = torch.cuda.Stream(dev, priority=-1)
     side = None if args.sequential else torch.cuda.Stream(dev, priority=0)
     K, W = args.steps, args.warmup
@@ -509,8 +511,8 @@ def cuda_arm(args, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64 + Box-Muller; random-init weights)",
         "config": dict(workload_config(), composition=(
             "sequential: EP, TP, latent tail, then the shared expert accumulating into out" if side is None else
-            "two branches: the shared expert on a side stream writes d into an extra shared-partial slot; EP and "
-            "TP on a high-priority stream; the latent tail adds all slots once both are done")),
+            "two branches: on a side stream the shared expert writes d into an extra shared-partial slot and the "
+            "latent tail follows, adding all slots; EP and TP on a high-priority stream beside them")),
         "roofline": roof, "calls": calls, "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * K, "clocks": clocks,
     }
