@@ -461,7 +461,11 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms) {
   }
   p.ksplit = std::min(p.ksplit, kblocks);
   const int sb = stage_bytes(p.tm, p.n_tile);
-  if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, (p.tm == 256 ? 200 * 1024 : 110 * 1024) / sb));
+  // Ring budget 72 KB at TM <= 128 (3 stages at b = 64): two GEMM CTAs then
+  // leave room on their SM for one finalize CTA of a concurrent stream (up to
+  // ~80 KB of shared memory), which measured faster in the composed decode
+  // step than deeper rings that keep the finalize kernels waiting for an SM.
+  if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, (p.tm == 256 ? 200 * 1024 : 72 * 1024) / sb));
   const int per_cta = (kblocks + p.ksplit - 1) / p.ksplit;
   p.stages = std::min(p.stages, std::max(2, per_cta));
   // the FP32 staging tile reuses the ring

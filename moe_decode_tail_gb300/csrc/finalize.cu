@@ -40,7 +40,10 @@ enum { kModeEP = kFinalizeEP, kModeTP = kFinalizeTP, kModeLatent = kFinalizeLate
 constexpr int kMaxRoutesPerPass = 8;
 constexpr int kMaxChunks = 128;  // P <= 32768
 constexpr int kMaxList = 1024;   // tp * K <= 32 * 32
-constexpr int kMaxThreads = 1024;
+// At most 512 threads of at most 64 registers (half an SM's register file), so
+// that a finalize CTA fits on an SM beside the GEMM CTAs of a concurrent
+// weight stream; a 1024-thread CTA at 64 registers would need a whole SM.
+constexpr int kMaxThreads = 512;
 
 struct __align__(16) FinalizeSmem {
   float ss[2][kMaxRoutesPerPass][kMaxChunks];  // chunk sums of squares, per pass parity
@@ -61,7 +64,7 @@ __device__ __forceinline__ float route_weight(const void* w, int64_t i) {
 }
 
 template <int MODE, bool WBN, int WMODE>
-__global__ void __launch_bounds__(kMaxThreads) finalize_kernel(const FinalizeArgs a) {
+__global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const FinalizeArgs a) {
   extern __shared__ __align__(16) float prod[];  // [R][VB][8] products of a pass
   __shared__ FinalizeSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -633,13 +636,15 @@ cudaError_t launch_finalize(int mode, const FinalizeArgs& args, bool wbn, int wm
     split = 1;
     while (split < 8 && split < a.chunks && (int64_t)a.b * split < target) split *= 2;
   }
-  while (split < 8 && (a.chunks + split - 1) / split > 32) split *= 2;
+  while (split < 8 && (a.chunks + split - 1) / split > kMaxThreads / 32) split *= 2;
   a.band_vectors = 32 * ((a.chunks + split - 1) / split);
   if (a.band_vectors > kMaxThreads) return cudaErrorInvalidValue;
   a.routes_per_pass = std::min(std::min(kMaxRoutesPerPass, std::max(1, routes)), kMaxThreads / a.band_vectors);
   if (mode == kModeEP) {  // a token has about K local rows in all: more groups would idle
     a.routes_per_pass = std::max(1, std::min(a.routes_per_pass, a.K));
   }
+  const int routes_cap = env_int("MOE_TAIL_FIN_ROUTES", 0);  // tuning override
+  if (routes_cap >= 1 && routes_cap <= kMaxRoutesPerPass) a.routes_per_pass = std::min(a.routes_per_pass, routes_cap);
   if (mode == kModeEP) {
     if (wbn) return wmode == kWeightBF16 ? launch_t<kModeEP, true, kWeightBF16>(a, split, stream)
                                          : launch_t<kModeEP, true, kWeightF32>(a, split, stream);
