@@ -186,18 +186,24 @@ def make_workload(dev):
     w["out_tp"] = torch.empty((B, P), dtype=torch.bfloat16, device=dev)
     w["out"] = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
     w["ws_lat"] = torch.empty(mt.moe_tail_workspace_bytes(0, B, L), dtype=torch.uint8, device=dev)
+    w["y"] = w["ws_lat"][: B * L * 2].view(torch.bfloat16).view(B, L)
     w["ws_sh"] = torch.empty(mt.moe_tail_workspace_bytes(1, B, I), dtype=torch.uint8, device=dev)
     # the latent tail's shared partials plus one slot that receives the shared expert's output
     w["shared9"] = torch.empty((TP + 1, B, H), dtype=torch.bfloat16, device=dev)
     w["shared9"][:TP].copy_(w["shared"])
     w["d_slot"] = w["shared9"][TP]
-    w["fork"], w["join"] = torch.cuda.Event(), torch.cuda.Event()
+    w["fork"], w["join"], w["normed"] = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
     return cpu, w
 
 
+EVENTS_PER_STEP = 10  # (start, end) of EP, TP, latent norm, up-projection, shared expert
+
+
 def run_step(mt, w, stream, events=None, side=None):
-    """The four calls of one step.  events: optional list of 8 events, a
-    (start, end) pair per call in CALLS order, recorded on the call's stream.
+    """The four calls of one step.  events: optional list of EVENTS_PER_STEP
+    events, a (start, end) pair per call recorded on the call's stream (the
+    latent tail has two pairs, for when its norm and up-projection run as
+    separate calls; in one call the second pair is empty).
 
     With a side stream the weight-streaming calls run beside the routed
     finalize calls, as the Kimi-K3 tail runs its shared expert (its output is
@@ -206,9 +212,9 @@ def run_step(mt, w, stream, events=None, side=None):
     tail's shared-partial slots and moe_tail_latent_up follows it, adding d
     with the other slots in its epilogue; EP and expert-TP finalize run on
     the main stream, which joins the side stream at the end of the step.
-    Without one, the calls run in order and the shared expert accumulates
-    into the latent tail's output."""
-    ev = events or [None] * 8
+    Without a side stream the calls run in order and the shared expert
+    accumulates into the latent tail's output."""
+    ev = events or [None] * EVENTS_PER_STEP
 
     def rec(i, st):
         if ev[i] is not None:
@@ -226,28 +232,32 @@ def run_step(mt, w, stream, events=None, side=None):
                                 eps=1e-6, weight_before_norm=True, stream=st)
         rec(3, st)
 
-    def latent(st, shared):
-        rec(4, st)
-        mt.moe_tail_latent_up(w["latent"], w["lat_gamma"], w["w_up"], shared, w["out"], w["ws_lat"], eps=1e-6,
-                              stream=st)
-        rec(5, st)
-
     def shared_expert(st, out, accumulate):
-        rec(6, st)
+        rec(8, st)
         mt.moe_shared_expert(w["x"], w["w_gate"], w["w_up_s"], w["w_down"], out, w["ws_sh"], accumulate=accumulate,
                              stream=st)
-        rec(7, st)
+        rec(9, st)
 
     if side is None:
         ep(stream)
         tp(stream)
-        latent(stream, w["shared"])
+        rec(4, stream)
+        mt.moe_tail_latent_up(w["latent"], w["lat_gamma"], w["w_up"], w["shared"], w["out"], w["ws_lat"], eps=1e-6,
+                              stream=stream)
+        rec(5, stream)
+        rec(6, stream)
+        rec(7, stream)
         shared_expert(stream, w["out"], True)
         return
     w["fork"].record(stream)
     side.wait_event(w["fork"])
     shared_expert(side, w["d_slot"], False)
-    latent(side, w["shared9"])
+    rec(4, side)
+    mt.moe_tail_latent_up(w["latent"], w["lat_gamma"], w["w_up"], w["shared9"], w["out"], w["ws_lat"], eps=1e-6,
+                          stream=side)
+    rec(5, side)
+    rec(6, side)
+    rec(7, side)
     w["join"].record(side)
     ep(stream)
     tp(stream)
@@ -431,7 +441,7 @@ def cuda_arm(args, world, rank, local):
         # Per-call events (external: recorded as event nodes of the graph, replayed
         # with it) in every tenth step only: an event between two calls keeps the
         # second from being scheduled while the first drains.
-        evs = ([[torch.cuda.Event(enable_timing=True, external=True) for _ in range(8)] if i % 10 == 0 else None
+        evs = ([[torch.cuda.Event(enable_timing=True, external=True) for _ in range(EVENTS_PER_STEP)] if i % 10 == 0 else None
                 for i in range(n)] if with_events else None)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
@@ -470,9 +480,11 @@ def cuda_arm(args, world, rank, local):
 
     # per-call durations over the G steps of the last replay of the main graph
     per_call = {c: [] for c in CALLS}
+    pairs = {"ep_finalize": [(0, 1)], "tp_finalize": [(2, 3)], "latent_up": [(4, 5), (6, 7)],
+             "shared_expert": [(8, 9)]}
     for evs in main_ev:
-        for i, c in enumerate(CALLS):
-            per_call[c].append(evs[2 * i].elapsed_time(evs[2 * i + 1]) * 1e3)  # us
+        for c in CALLS:
+            per_call[c].append(sum(evs[i].elapsed_time(evs[j]) for i, j in pairs[c]) * 1e3)  # us
     calls = {}
     hbm, bf16_tf, peak_kind = peaks()
     nbytes = dict(BYTES)

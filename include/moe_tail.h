@@ -123,6 +123,37 @@ int moe_tail_latent_up(const void* latent, const void* gamma, float eps, const v
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The latent tail's two steps as separate calls ([KT] module docstring), for
+ * callers that schedule them apart: the norm needs only the latent partials,
+ * the up-projection only y, the weights and the shared partials, so the norm
+ * can run early (beside other work) and the up-projection right after the
+ * last shared partial is written.  moe_tail_latent_up is these two calls in
+ * a row, and each gives bit for bit the same result as that step there.
+ *
+ * moe_tail_latent_norm:  y = the x and y lines of moe_tail_latent_up.
+ *   latent BF16 [tp][b][L];  gamma BF16 [L];  y BF16 [b][L] (written)
+ *   Limits: 1 <= tp <= 32, 8 <= L <= 32768, L % 8 == 0, b <= 65535; y must
+ *   not overlap latent or gamma.
+ *
+ * moe_tail_up_project:  out = the out line of moe_tail_latent_up, from y.
+ *   y BF16 [b][L];  w_up BF16 [H][L];  shared BF16 [tp_s][b][H] or NULL when
+ *   tp_s == 0;  out BF16 [b][H] (written; must not overlap an input).
+ *   flags: 0, or MOE_TAIL_WEIGHTS_STATIC -- a promise that w_up is not being
+ *   written by work still in flight on the stream when the call is enqueued
+ *   (model weights loaded before serving).  The kernel then requests its
+ *   first weight tiles before it waits for the stream's preceding kernel, so
+ *   with programmatic dependent launch the weight stream starts while that
+ *   kernel drains; y and shared are always read after the wait.
+ *   Limits: 0 <= tp_s <= 32, 8 <= L <= 32768, 8 <= H, L % 8 == 0,
+ *   H % 8 == 0, b <= 65535.
+ */
+#define MOE_TAIL_WEIGHTS_STATIC 1
+int moe_tail_latent_norm(const void* latent, const void* gamma, float eps, int b, int tp, int L, void* y,
+                         void* stream);
+int moe_tail_up_project(const void* y, const void* w_up, const void* shared, int tp_s, int b, int L, int H,
+                        void* out, int flags, void* stream);
+
+/*
  * Fused shared expert ([KS] module docstring, SharedUmma.owned_h,
  * SharedBase.push): gate/up projection, gated activation, down projection,
  * added into the tail's output:

@@ -18,11 +18,13 @@ __all__ = [
     "MoeTailError", "lib", "moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up",
     "moe_shared_expert", "moe_tail_workspace_bytes", "moe_tail_status_str", "moe_tail_take_device_error",
     "moe_tail_latent_up_noalloc", "NOALLOC_SCRATCH_BYTES", "moe_tail_selftest_wait_timeout",
+    "moe_tail_latent_norm", "moe_tail_up_project", "WEIGHTS_STATIC",
 ]
 
 OK, EINVAL, ECUDA, ENOTSUP = 0, 1, 2, 3
 NOALLOC_SCRATCH_BYTES = 1 << 20  # MOE_TAIL_NOALLOC_SCRATCH_BYTES
 W_FP32, W_BF16 = 0, 1
+WEIGHTS_STATIC = 1  # MOE_TAIL_WEIGHTS_STATIC
 
 
 class MoeTailError(RuntimeError):
@@ -49,13 +51,16 @@ def lib() -> ctypes.CDLL:
         L.moe_shared_expert.argtypes = [P, P, P, P, i32, i32, i32, P, i32, P, sz, P]
         L.moe_tail_latent_up_noalloc.argtypes = [P, P, f32, P, P, i32, i32, i32, i32, i32, P, P]
         L.moe_tail_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
+        L.moe_tail_latent_norm.argtypes = [P, P, f32, i32, i32, i32, P, P]
+        L.moe_tail_up_project.argtypes = [P, P, P, i32, i32, i32, i32, P, i32, P]
         L.moe_tail_workspace_bytes.argtypes = [i32, i32, i32]
         L.moe_tail_workspace_bytes.restype = sz
         L.moe_tail_status_str.argtypes = [i32]
         L.moe_tail_status_str.restype = ctypes.c_char_p
         L.moe_tail_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         for name in ("moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up", "moe_shared_expert",
-                     "moe_tail_take_device_error", "moe_tail_latent_up_noalloc", "moe_tail_selftest_wait_timeout"):
+                     "moe_tail_take_device_error", "moe_tail_latent_up_noalloc", "moe_tail_selftest_wait_timeout",
+                     "moe_tail_latent_norm", "moe_tail_up_project"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -135,6 +140,31 @@ def moe_tail_latent_up(latent, gamma, w_up, shared, out, workspace, *, eps=1e-6,
     _check("moe_tail_latent_up", lib().moe_tail_latent_up(
         _p(latent), _p(gamma), eps, _p(w_up), _p(shared), tp_s, b, tp, L, H, _p(out), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def moe_tail_latent_norm(latent, gamma, y, *, eps=1e-6, stream=None) -> torch.Tensor:
+    """The latent tail's first step into y (BF16 [b, L]): the slot-summed latent
+    BF16 [tp, b, L], RMS-normalised and scaled by gamma BF16 [L]."""
+    _cuda(latent, gamma, y)
+    tp, b, L = latent.shape
+    _check("moe_tail_latent_norm", lib().moe_tail_latent_norm(_p(latent), _p(gamma), eps, b, tp, L, _p(y),
+                                                              _stream(stream)))
+    return y
+
+
+def moe_tail_up_project(y, w_up, shared, out, *, weights_static=False, stream=None) -> torch.Tensor:
+    """The latent tail's second step into out (BF16 [b, H]): y BF16 [b, L] times
+    w_up BF16 [H, L] transposed, plus shared BF16 [tp_s, b, H] (or None).
+    weights_static: w_up is not written by work still in flight on the stream,
+    so the kernel may request weight tiles before the preceding kernel ends."""
+    _cuda(y, w_up, shared, out)
+    b, L = y.shape
+    H = w_up.shape[0]
+    tp_s = 0 if shared is None else shared.shape[0]
+    _check("moe_tail_up_project", lib().moe_tail_up_project(
+        _p(y), _p(w_up), _p(shared), tp_s, b, L, H, _p(out), WEIGHTS_STATIC if weights_static else 0,
+        _stream(stream)))
     return out
 
 

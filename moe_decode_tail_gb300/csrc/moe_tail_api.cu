@@ -177,35 +177,13 @@ MOE_API size_t moe_tail_workspace_bytes(int which, int b, int dim) {
   return round256((size_t)b * dim * 2);
 }
 
-MOE_API int moe_tail_latent_up(const void* latent, const void* gamma, float eps, const void* w_up,
-                               const void* shared, int tp_s, int b, int tp, int L, int H, void* out,
-                               void* workspace, size_t workspace_bytes, void* stream) {
-  if (b < 0 || b > 65535 || tp < 1 || tp > kMaxTp || tp_s < 0 || tp_s > kMaxTp) return MOE_TAIL_EINVAL;
-  if (L < 8 || L > kMaxP || L % 8 || H < 8 || H % 8 || H > (1 << 24)) return MOE_TAIL_EINVAL;
-  if (b == 0) return MOE_TAIL_OK;
-  if (!latent || !gamma || !w_up || !out || !workspace) return MOE_TAIL_EINVAL;
-  if ((tp_s > 0) != (shared != nullptr)) return MOE_TAIL_EINVAL;
-  if (!aligned(latent, 16) || !aligned(gamma, 16) || !aligned(w_up, 16) || !aligned(out, 16) ||
-      !aligned(workspace, 16) || (shared && !aligned(shared, 16)))
-    return MOE_TAIL_EINVAL;
-  if (workspace_bytes < moe_tail_workspace_bytes(0, b, L)) return MOE_TAIL_EINVAL;
-  const Range o = span(out, (size_t)b * H * 2);
-  const Range ws = span(workspace, (size_t)b * L * 2);
-  if (overlaps(o, span(latent, (size_t)tp * b * L * 2)) || overlaps(o, span(gamma, (size_t)L * 2)) ||
-      overlaps(o, span(w_up, (size_t)H * L * 2)) || overlaps(o, span(shared, (size_t)tp_s * b * H * 2)) ||
-      overlaps(o, ws) || overlaps(ws, span(latent, (size_t)tp * b * L * 2)) || overlaps(ws, span(w_up, (size_t)H * L * 2)) ||
-      overlaps(ws, span(shared, (size_t)tp_s * b * H * 2)) || overlaps(ws, span(gamma, (size_t)L * 2)))
-    return MOE_TAIL_EINVAL;
+namespace {
 
-  const GemmPlan plan = moetail::plan_gemm(moetail::kGemmUpShared, H, L, b, device_sms());
-  CUtensorMap mw, mx;
-  if (!encode_bf16_2d(&mw, w_up, H, L, plan.tm, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
-      !encode_bf16_2d(&mx, workspace, b, L, plan.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
-    return MOE_TAIL_ECUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-  // 1. y = RMS norm of the slot-summed latent (an expert-TP finalize with one
-  //    "route" per token: row = token, unit weight, gain center 0).
+// Step 1 of the latent tail: y = RMS norm of the slot-summed latent (an
+// expert-TP finalize with one "route" per token: row = token, unit weight,
+// gain center 0).  Arguments already checked.
+cudaError_t launch_latent_norm(const void* latent, const void* gamma, float eps, int b, int tp, int L, void* y,
+                               cudaStream_t st) {
   FinalizeArgs n;
   n.rows = static_cast<const uint16_t*>(latent);
   n.num_rows = b;
@@ -220,11 +198,18 @@ MOE_API int moe_tail_latent_up(const void* latent, const void* gamma, float eps,
   n.tp = tp;
   n.K = 1;
   n.P = L;
-  n.out = static_cast<uint16_t*>(workspace);
-  cudaError_t e = moetail::launch_finalize(moetail::kFinalizeLatent, n, false, moetail::kWeightUnit, device_sms(), st);
-  if (e != cudaSuccess) return finish(e);
+  n.out = static_cast<uint16_t*>(y);
+  return moetail::launch_finalize(moetail::kFinalizeLatent, n, false, moetail::kWeightUnit, device_sms(), st);
+}
 
-  // 2. out = y . w_up^T + sum_s shared[s]
+// Step 2: out = y . w_up^T + sum_s shared[s].  Arguments already checked.
+int launch_up_project(const void* y, const void* w_up, const void* shared, int tp_s, int b, int L, int H, void* out,
+                      bool weights_before_wait, cudaStream_t st) {
+  const GemmPlan plan = moetail::plan_gemm(moetail::kGemmUpShared, H, L, b, device_sms());
+  CUtensorMap mw, mx;
+  if (!encode_bf16_2d(&mw, w_up, H, L, plan.tm, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&mx, y, b, L, plan.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+    return MOE_TAIL_ECUDA;
   GemmArgs g;
   g.M = H;
   g.K = L;
@@ -234,8 +219,72 @@ MOE_API int moe_tail_latent_up(const void* latent, const void* gamma, float eps,
   g.tp_s = tp_s;
   g.out = static_cast<uint16_t*>(out);
   g.accumulate = 0;
-  g.weights_before_wait = 1;  // follows this call's own norm kernel
+  g.weights_before_wait = weights_before_wait ? 1 : 0;
   return finish(moetail::launch_decode_gemm(moetail::kGemmUpShared, plan, mw, mw, mx, g, true, st));
+}
+
+bool latent_sizes_ok(int b, int tp, int L) {
+  return b >= 0 && b <= 65535 && tp >= 1 && tp <= kMaxTp && L >= 8 && L <= kMaxP && L % 8 == 0;
+}
+bool up_sizes_ok(int b, int tp_s, int L, int H) {
+  return b >= 0 && b <= 65535 && tp_s >= 0 && tp_s <= kMaxTp && L >= 8 && L <= kMaxP && L % 8 == 0 && H >= 8 &&
+         H % 8 == 0 && H <= (1 << 24);
+}
+
+}  // namespace
+
+MOE_API int moe_tail_latent_up(const void* latent, const void* gamma, float eps, const void* w_up,
+                               const void* shared, int tp_s, int b, int tp, int L, int H, void* out,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (!latent_sizes_ok(b, tp, L) || !up_sizes_ok(b, tp_s, L, H)) return MOE_TAIL_EINVAL;
+  if (b == 0) return MOE_TAIL_OK;
+  if (!latent || !gamma || !w_up || !out || !workspace) return MOE_TAIL_EINVAL;
+  if ((tp_s > 0) != (shared != nullptr)) return MOE_TAIL_EINVAL;
+  if (!aligned(latent, 16) || !aligned(gamma, 16) || !aligned(w_up, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 16) || (shared && !aligned(shared, 16)))
+    return MOE_TAIL_EINVAL;
+  if (workspace_bytes < moe_tail_workspace_bytes(0, b, L)) return MOE_TAIL_EINVAL;
+  const Range o = span(out, (size_t)b * H * 2);
+  const Range ws = span(workspace, (size_t)b * L * 2);
+  if (overlaps(o, span(latent, (size_t)tp * b * L * 2)) || overlaps(o, span(gamma, (size_t)L * 2)) ||
+      overlaps(o, span(w_up, (size_t)H * L * 2)) || overlaps(o, span(shared, (size_t)tp_s * b * H * 2)) ||
+      overlaps(o, ws) || overlaps(ws, span(latent, (size_t)tp * b * L * 2)) || overlaps(ws, span(w_up, (size_t)H * L * 2)) ||
+      overlaps(ws, span(shared, (size_t)tp_s * b * H * 2)) || overlaps(ws, span(gamma, (size_t)L * 2)))
+    return MOE_TAIL_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // 1. y (in the workspace), 2. the up-projection; the GEMM follows this
+  // call's own norm kernel, which never writes w_up.
+  const cudaError_t e = launch_latent_norm(latent, gamma, eps, b, tp, L, workspace, st);
+  if (e != cudaSuccess) return finish(e);
+  return launch_up_project(workspace, w_up, shared, tp_s, b, L, H, out, true, st);
+}
+
+MOE_API int moe_tail_latent_norm(const void* latent, const void* gamma, float eps, int b, int tp, int L, void* y,
+                                 void* stream) {
+  if (!latent_sizes_ok(b, tp, L)) return MOE_TAIL_EINVAL;
+  if (b == 0) return MOE_TAIL_OK;
+  if (!latent || !gamma || !y) return MOE_TAIL_EINVAL;
+  if (!aligned(latent, 16) || !aligned(gamma, 16) || !aligned(y, 16)) return MOE_TAIL_EINVAL;
+  const Range yr = span(y, (size_t)b * L * 2);
+  if (overlaps(yr, span(latent, (size_t)tp * b * L * 2)) || overlaps(yr, span(gamma, (size_t)L * 2)))
+    return MOE_TAIL_EINVAL;
+  return finish(launch_latent_norm(latent, gamma, eps, b, tp, L, y, static_cast<cudaStream_t>(stream)));
+}
+
+MOE_API int moe_tail_up_project(const void* y, const void* w_up, const void* shared, int tp_s, int b, int L, int H,
+                                void* out, int flags, void* stream) {
+  if (!up_sizes_ok(b, tp_s, L, H) || (flags & ~MOE_TAIL_WEIGHTS_STATIC)) return MOE_TAIL_EINVAL;
+  if (b == 0) return MOE_TAIL_OK;
+  if (!y || !w_up || !out) return MOE_TAIL_EINVAL;
+  if ((tp_s > 0) != (shared != nullptr)) return MOE_TAIL_EINVAL;
+  if (!aligned(y, 16) || !aligned(w_up, 16) || !aligned(out, 16) || (shared && !aligned(shared, 16)))
+    return MOE_TAIL_EINVAL;
+  const Range o = span(out, (size_t)b * H * 2);
+  if (overlaps(o, span(y, (size_t)b * L * 2)) || overlaps(o, span(w_up, (size_t)H * L * 2)) ||
+      overlaps(o, span(shared, (size_t)tp_s * b * H * 2)))
+    return MOE_TAIL_EINVAL;
+  return launch_up_project(y, w_up, shared, tp_s, b, L, H, out, (flags & MOE_TAIL_WEIGHTS_STATIC) != 0,
+                           static_cast<cudaStream_t>(stream));
 }
 
 // ============================================================================ shared expert

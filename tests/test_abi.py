@@ -128,6 +128,46 @@ def test_latent_up_b_zero(lib):
     assert latent(lib, b=0, lat=None, w=None, out=None, ws=None) == OK
 
 
+def norm(lib, **kw):
+    args = dict(lat=a(), gamma=a(1 << 24), eps=1e-6, b=16, tp=8, L=3584, y=a(2 << 24), stream=None)
+    args.update(kw)
+    return lib.moe_tail_latent_norm(args["lat"], args["gamma"], args["eps"], args["b"], args["tp"], args["L"],
+                                    args["y"], args["stream"])
+
+
+@host_only
+@pytest.mark.parametrize("bad", [
+    dict(tp=0), dict(tp=33), dict(L=3583), dict(L=4), dict(L=40000), dict(b=-1), dict(b=65536), dict(lat=None),
+    dict(gamma=None), dict(y=None), dict(y=a(8)), dict(lat=a(4)), dict(y=a(16)),  # y over the latent partials
+])
+def test_latent_norm_refuses_bad_arguments(lib, bad):
+    assert norm(lib, **bad) == EINVAL
+
+
+def up(lib, **kw):
+    args = dict(y=a(), w=a(1 << 24), sh=a(2 << 24), tp_s=8, b=16, L=3584, H=7168, out=a(3 << 24), flags=0,
+                stream=None)
+    args.update(kw)
+    return lib.moe_tail_up_project(args["y"], args["w"], args["sh"], args["tp_s"], args["b"], args["L"], args["H"],
+                                   args["out"], args["flags"], args["stream"])
+
+
+@host_only
+@pytest.mark.parametrize("bad", [
+    dict(tp_s=-1), dict(tp_s=33), dict(L=3583), dict(H=7170), dict(H=4), dict(b=-2), dict(sh=None), dict(tp_s=0),
+    dict(y=None), dict(w=None), dict(out=None), dict(flags=2), dict(flags=-1), dict(out=a(8)),
+    dict(out=a(2 << 24)), dict(out=a(16)),  # out over shared, over y
+])
+def test_up_project_refuses_bad_arguments(lib, bad):
+    assert up(lib, **bad) == EINVAL
+
+
+@host_only
+def test_latent_steps_b_zero(lib):
+    assert norm(lib, b=0, lat=None, gamma=None, y=None) == OK
+    assert up(lib, b=0, y=None, w=None, out=None, flags=1) == OK
+
+
 def shared(lib, **kw):
     args = dict(x=a(), wg=a(1 << 28), wu=a(2 << 28), wd=a(3 << 28), b=64, H=7168, I=6144, out=a(4 << 28), acc=1,
                 ws=a(5 << 28), wsb=64 * 6144 * 2, stream=None)

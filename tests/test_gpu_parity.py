@@ -301,6 +301,41 @@ def test_latent_up_identity_weight(mt):
     assert np.all(bits(out)[:, L:] == 0)
 
 
+@pytest.mark.parametrize("kw", [
+    dict(b=16, tp=8, tp_s=8, L=3584, H=7168),
+    dict(b=5, tp=3, tp_s=2, L=264, H=200),
+    dict(b=64, tp=8, tp_s=9, L=3584, H=1024),
+    dict(b=3, tp=1, tp_s=0, L=512, H=256),
+])
+@pytest.mark.parametrize("static", [False, True])
+def test_latent_steps_as_separate_calls(mt, kw, static):
+    # moe_tail_latent_norm then moe_tail_up_project, on two streams joined by an
+    # event as a scheduler would run them: y bit-exact against the oracle's
+    # norm, out within the GEMM bound of the oracle's up-projection of that y,
+    # and both bit-identical to the one-call latent tail
+    d = synth.latent_up_inputs(0x5E9 + kw["b"] + kw["tp_s"], **kw)
+    b, L, H = d["b"], d["L"], d["H"]
+    y_ref, out_ref = oracle.latent_tail(d["latent"], d["gamma"], d["eps"], d["w_up"], d["shared"], d["tp_s"],
+                                        b, d["tp"], L, H)
+    y = torch.full((b, L), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    sh = None if d["shared"] is None else d["shared"].to(DEV)
+    lat, gam, w = d["latent"].to(DEV), d["gamma"].to(DEV), d["w_up"].to(DEV)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    ready = torch.cuda.Event()
+    mt.moe_tail_latent_norm(lat, gam, y, eps=d["eps"], stream=s1)
+    ready.record(s1)
+    s2.wait_event(ready)
+    mt.moe_tail_up_project(y, w, sh, out, weights_static=static, stream=s2)
+    torch.cuda.synchronize()
+    assert_bitexact(y, y_ref, f"latent norm {kw}")
+    assert_gemm_close(out, out_ref, f"up-projection {kw}")
+    y1, out1 = run_latent(mt, d)
+    assert np.array_equal(bits(y1), bits(y)) and np.array_equal(bits(out1), bits(out))
+    assert mt.moe_tail_take_device_error() == 0
+
+
 # ------------------------------------------------------------------ shared expert
 #
 # gate and up are FP32 sums whose order the pages leave open, so bf16(gate),
