@@ -209,11 +209,14 @@ def run_step(mt, w, stream, events=None, side=None):
     finalize calls, as the Kimi-K3 tail runs its shared expert (its output is
     pushed into the tail's reduce-scatter partials): on the side stream
     moe_shared_expert writes d = bf16(down(h)) into the last of the latent
-    tail's shared-partial slots and moe_tail_latent_up follows it, adding d
-    with the other slots in its epilogue; EP and expert-TP finalize run on
-    the main stream, which joins the side stream at the end of the step.
-    Without a side stream the calls run in order and the shared expert
-    accumulates into the latent tail's output."""
+    tail's shared-partial slots, then the latent tail follows as its two calls
+    -- moe_tail_latent_norm (inputs ready: it reads the latent partials while
+    the down projection drains) and moe_tail_up_project (static weights: its
+    first weight tiles are requested during the norm), which adds d with the
+    other slots in its epilogue; EP and expert-TP finalize run on the main
+    stream, which joins the side stream at the end of the step.  Without a
+    side stream the calls run in order (moe_tail_latent_up in one call) and
+    the shared expert accumulates into the latent tail's output."""
     ev = events or [None] * EVENTS_PER_STEP
 
     def rec(i, st):
@@ -253,10 +256,10 @@ def run_step(mt, w, stream, events=None, side=None):
     side.wait_event(w["fork"])
     shared_expert(side, w["d_slot"], False)
     rec(4, side)
-    mt.moe_tail_latent_up(w["latent"], w["lat_gamma"], w["w_up"], w["shared9"], w["out"], w["ws_lat"], eps=1e-6,
-                          stream=side)
+    mt.moe_tail_latent_norm(w["latent"], w["lat_gamma"], w["y"], eps=1e-6, inputs_ready=True, stream=side)
     rec(5, side)
     rec(6, side)
+    mt.moe_tail_up_project(w["y"], w["w_up"], w["shared9"], w["out"], weights_static=True, stream=side)
     rec(7, side)
     w["join"].record(side)
     ep(stream)
@@ -523,8 +526,8 @@ def cuda_arm(args, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64 + Box-Muller; random-init weights)",
         "config": dict(workload_config(), composition=(
             "sequential: EP, TP, latent tail, then the shared expert accumulating into out" if side is None else
-            "two branches: on a side stream the shared expert writes d into an extra shared-partial slot and the "
-            "latent tail follows, adding all slots; EP and TP on a high-priority stream beside them")),
+            "two branches: on a side stream the shared expert writes d into an extra shared-partial slot, then the "
+            "latent norm and up-projection follow, adding all slots; EP and TP on a high-priority stream beside them")),
         "roofline": roof, "calls": calls, "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * K, "clocks": clocks,
     }

@@ -132,6 +132,11 @@ int moe_tail_latent_up(const void* latent, const void* gamma, float eps, const v
  *
  * moe_tail_latent_norm:  y = the x and y lines of moe_tail_latent_up.
  *   latent BF16 [tp][b][L];  gamma BF16 [L];  y BF16 [b][L] (written)
+ *   flags: 0, or MOE_TAIL_INPUTS_READY -- a promise that latent and gamma are
+ *   not being written by work still in flight on the stream when the call is
+ *   enqueued.  The kernel then reads and normalises them while the stream's
+ *   preceding kernel still runs and waits for that kernel only before it
+ *   writes y (which in-flight work may still be reading).
  *   Limits: 1 <= tp <= 32, 8 <= L <= 32768, L % 8 == 0, b <= 65535; y must
  *   not overlap latent or gamma.
  *
@@ -148,8 +153,9 @@ int moe_tail_latent_up(const void* latent, const void* gamma, float eps, const v
  *   H % 8 == 0, b <= 65535.
  */
 #define MOE_TAIL_WEIGHTS_STATIC 1
+#define MOE_TAIL_INPUTS_READY 2
 int moe_tail_latent_norm(const void* latent, const void* gamma, float eps, int b, int tp, int L, void* y,
-                         void* stream);
+                         int flags, void* stream);
 int moe_tail_up_project(const void* y, const void* w_up, const void* shared, int tp_s, int b, int L, int H,
                         void* out, int flags, void* stream);
 

@@ -18,13 +18,14 @@ __all__ = [
     "MoeTailError", "lib", "moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up",
     "moe_shared_expert", "moe_tail_workspace_bytes", "moe_tail_status_str", "moe_tail_take_device_error",
     "moe_tail_latent_up_noalloc", "NOALLOC_SCRATCH_BYTES", "moe_tail_selftest_wait_timeout",
-    "moe_tail_latent_norm", "moe_tail_up_project", "WEIGHTS_STATIC",
+    "moe_tail_latent_norm", "moe_tail_up_project", "WEIGHTS_STATIC", "INPUTS_READY",
 ]
 
 OK, EINVAL, ECUDA, ENOTSUP = 0, 1, 2, 3
 NOALLOC_SCRATCH_BYTES = 1 << 20  # MOE_TAIL_NOALLOC_SCRATCH_BYTES
 W_FP32, W_BF16 = 0, 1
 WEIGHTS_STATIC = 1  # MOE_TAIL_WEIGHTS_STATIC
+INPUTS_READY = 2  # MOE_TAIL_INPUTS_READY
 
 
 class MoeTailError(RuntimeError):
@@ -51,7 +52,7 @@ def lib() -> ctypes.CDLL:
         L.moe_shared_expert.argtypes = [P, P, P, P, i32, i32, i32, P, i32, P, sz, P]
         L.moe_tail_latent_up_noalloc.argtypes = [P, P, f32, P, P, i32, i32, i32, i32, i32, P, P]
         L.moe_tail_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
-        L.moe_tail_latent_norm.argtypes = [P, P, f32, i32, i32, i32, P, P]
+        L.moe_tail_latent_norm.argtypes = [P, P, f32, i32, i32, i32, P, i32, P]
         L.moe_tail_up_project.argtypes = [P, P, P, i32, i32, i32, i32, P, i32, P]
         L.moe_tail_workspace_bytes.argtypes = [i32, i32, i32]
         L.moe_tail_workspace_bytes.restype = sz
@@ -143,13 +144,15 @@ def moe_tail_latent_up(latent, gamma, w_up, shared, out, workspace, *, eps=1e-6,
     return out
 
 
-def moe_tail_latent_norm(latent, gamma, y, *, eps=1e-6, stream=None) -> torch.Tensor:
+def moe_tail_latent_norm(latent, gamma, y, *, eps=1e-6, inputs_ready=False, stream=None) -> torch.Tensor:
     """The latent tail's first step into y (BF16 [b, L]): the slot-summed latent
-    BF16 [tp, b, L], RMS-normalised and scaled by gamma BF16 [L]."""
+    BF16 [tp, b, L], RMS-normalised and scaled by gamma BF16 [L].
+    inputs_ready: latent and gamma are not written by work still in flight on
+    the stream, so the kernel may read them before the preceding kernel ends."""
     _cuda(latent, gamma, y)
     tp, b, L = latent.shape
-    _check("moe_tail_latent_norm", lib().moe_tail_latent_norm(_p(latent), _p(gamma), eps, b, tp, L, _p(y),
-                                                              _stream(stream)))
+    _check("moe_tail_latent_norm", lib().moe_tail_latent_norm(
+        _p(latent), _p(gamma), eps, b, tp, L, _p(y), INPUTS_READY if inputs_ready else 0, _stream(stream)))
     return y
 
 

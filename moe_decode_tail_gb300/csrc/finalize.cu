@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
   const int nthreads = blockDim.x;
 
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  grid_dependency_wait();
+  if (!a.inputs_before_wait) grid_dependency_wait();
   launch_dependents();  // a kernel chained behind this one may start its own prologue
 
   // One trip for the gains, the route weights and the route indices.
@@ -249,6 +249,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
     r.y = pack_bf16x2_pz(o[2], o[3]);
     r.z = pack_bf16x2_pz(o[4], o[5]);
     r.w = pack_bf16x2_pz(o[6], o[7]);
+    if (a.inputs_before_wait) grid_dependency_wait();  // the preceding kernel may still read out
     st_v4(a.out + (int64_t)t * a.P + col, r);
   }
 }
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
   }
   __syncthreads();
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  grid_dependency_wait();
+  if (!a.inputs_before_wait) grid_dependency_wait();
   launch_dependents();
 
   // The issuer copies route number n (counting the routes with a row, in the
@@ -487,6 +488,7 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
       r.y = pack_bf16x2_pz(acc[2], acc[3]);
       r.z = pack_bf16x2_pz(acc[4], acc[5]);
       r.w = pack_bf16x2_pz(acc[6], acc[7]);
+      if (a.inputs_before_wait) grid_dependency_wait();  // the preceding kernel may still read out
       st_v4(a.out + (int64_t)t * a.P + vec * 8, r);
     }
   }

@@ -21,6 +21,9 @@ struct FinalizeArgs {
   int b, tp, K, P;
   int chunks, band_vectors, routes_per_pass, stages;  // set by the launcher
   uint16_t* out;          // BF16 [b][P]
+  // 1: the inputs are complete before the preceding kernel of the stream ends,
+  // so they are read before the grid dependency wait (out is written after it)
+  int inputs_before_wait = 0;
 };
 
 enum { kFinalizeEP = 0, kFinalizeTP = 1, kFinalizeLatent = 2 };

@@ -183,8 +183,9 @@ namespace {
 // expert-TP finalize with one "route" per token: row = token, unit weight,
 // gain center 0).  Arguments already checked.
 cudaError_t launch_latent_norm(const void* latent, const void* gamma, float eps, int b, int tp, int L, void* y,
-                               cudaStream_t st) {
+                               bool inputs_ready, cudaStream_t st) {
   FinalizeArgs n;
+  n.inputs_before_wait = inputs_ready ? 1 : 0;
   n.rows = static_cast<const uint16_t*>(latent);
   n.num_rows = b;
   n.slot_stride = (int64_t)b * L;
@@ -254,21 +255,22 @@ MOE_API int moe_tail_latent_up(const void* latent, const void* gamma, float eps,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // 1. y (in the workspace), 2. the up-projection; the GEMM follows this
   // call's own norm kernel, which never writes w_up.
-  const cudaError_t e = launch_latent_norm(latent, gamma, eps, b, tp, L, workspace, st);
+  const cudaError_t e = launch_latent_norm(latent, gamma, eps, b, tp, L, workspace, false, st);
   if (e != cudaSuccess) return finish(e);
   return launch_up_project(workspace, w_up, shared, tp_s, b, L, H, out, true, st);
 }
 
 MOE_API int moe_tail_latent_norm(const void* latent, const void* gamma, float eps, int b, int tp, int L, void* y,
-                                 void* stream) {
-  if (!latent_sizes_ok(b, tp, L)) return MOE_TAIL_EINVAL;
+                                 int flags, void* stream) {
+  if (!latent_sizes_ok(b, tp, L) || (flags & ~MOE_TAIL_INPUTS_READY)) return MOE_TAIL_EINVAL;
   if (b == 0) return MOE_TAIL_OK;
   if (!latent || !gamma || !y) return MOE_TAIL_EINVAL;
   if (!aligned(latent, 16) || !aligned(gamma, 16) || !aligned(y, 16)) return MOE_TAIL_EINVAL;
   const Range yr = span(y, (size_t)b * L * 2);
   if (overlaps(yr, span(latent, (size_t)tp * b * L * 2)) || overlaps(yr, span(gamma, (size_t)L * 2)))
     return MOE_TAIL_EINVAL;
-  return finish(launch_latent_norm(latent, gamma, eps, b, tp, L, y, static_cast<cudaStream_t>(stream)));
+  return finish(launch_latent_norm(latent, gamma, eps, b, tp, L, y, (flags & MOE_TAIL_INPUTS_READY) != 0,
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 MOE_API int moe_tail_up_project(const void* y, const void* w_up, const void* shared, int tp_s, int b, int L, int H,

@@ -129,16 +129,17 @@ def test_latent_up_b_zero(lib):
 
 
 def norm(lib, **kw):
-    args = dict(lat=a(), gamma=a(1 << 24), eps=1e-6, b=16, tp=8, L=3584, y=a(2 << 24), stream=None)
+    args = dict(lat=a(), gamma=a(1 << 24), eps=1e-6, b=16, tp=8, L=3584, y=a(2 << 24), flags=0, stream=None)
     args.update(kw)
     return lib.moe_tail_latent_norm(args["lat"], args["gamma"], args["eps"], args["b"], args["tp"], args["L"],
-                                    args["y"], args["stream"])
+                                    args["y"], args["flags"], args["stream"])
 
 
 @host_only
 @pytest.mark.parametrize("bad", [
     dict(tp=0), dict(tp=33), dict(L=3583), dict(L=4), dict(L=40000), dict(b=-1), dict(b=65536), dict(lat=None),
     dict(gamma=None), dict(y=None), dict(y=a(8)), dict(lat=a(4)), dict(y=a(16)),  # y over the latent partials
+    dict(flags=1), dict(flags=4), dict(flags=-1),
 ])
 def test_latent_norm_refuses_bad_arguments(lib, bad):
     assert norm(lib, **bad) == EINVAL
@@ -164,7 +165,7 @@ def test_up_project_refuses_bad_arguments(lib, bad):
 
 @host_only
 def test_latent_steps_b_zero(lib):
-    assert norm(lib, b=0, lat=None, gamma=None, y=None) == OK
+    assert norm(lib, b=0, lat=None, gamma=None, y=None, flags=2) == OK
     assert up(lib, b=0, y=None, w=None, out=None, flags=1) == OK
 
 

@@ -324,7 +324,7 @@ def test_latent_steps_as_separate_calls(mt, kw, static):
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
     torch.cuda.synchronize()
     ready = torch.cuda.Event()
-    mt.moe_tail_latent_norm(lat, gam, y, eps=d["eps"], stream=s1)
+    mt.moe_tail_latent_norm(lat, gam, y, eps=d["eps"], inputs_ready=static, stream=s1)
     ready.record(s1)
     s2.wait_event(ready)
     mt.moe_tail_up_project(y, w, sh, out, weights_static=static, stream=s2)
@@ -333,6 +333,31 @@ def test_latent_steps_as_separate_calls(mt, kw, static):
     assert_gemm_close(out, out_ref, f"up-projection {kw}")
     y1, out1 = run_latent(mt, d)
     assert np.array_equal(bits(y1), bits(y)) and np.array_equal(bits(out1), bits(out))
+    assert mt.moe_tail_take_device_error() == 0
+
+
+def test_latent_norm_inputs_ready_waits_before_writing_y(mt):
+    # norm(A) -> up-projection reading y -> norm(B) with inputs_ready on one
+    # stream: the second norm may start while the GEMM still reads y, so it
+    # must not write y before the GEMM is done; outA must be A's up-projection
+    kw = dict(b=64, tp=8, tp_s=8, L=3584, H=7168)
+    A = synth.latent_up_inputs(0xA11, **kw)
+    B = synth.latent_up_inputs(0xB22, **kw)
+    _, out_ref = oracle.latent_tail(A["latent"], A["gamma"], A["eps"], A["w_up"], A["shared"], A["tp_s"],
+                                    64, 8, 3584, 7168)
+    yB_ref = oracle.latent_norm(B["latent"], B["gamma"], B["eps"], 64, 8, 3584)
+    y = torch.empty((64, 3584), dtype=torch.bfloat16, device=DEV)
+    out = torch.full((64, 7168), float("nan"), dtype=torch.bfloat16, device=DEV)
+    latA, latB, gam = A["latent"].to(DEV), B["latent"].to(DEV), A["gamma"].to(DEV)
+    gamB, w, sh = B["gamma"].to(DEV), A["w_up"].to(DEV), A["shared"].to(DEV)
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    mt.moe_tail_latent_norm(latA, gam, y, eps=A["eps"], stream=st)
+    mt.moe_tail_up_project(y, w, sh, out, weights_static=True, stream=st)
+    mt.moe_tail_latent_norm(latB, gamB, y, eps=B["eps"], inputs_ready=True, stream=st)
+    torch.cuda.synchronize()
+    assert_gemm_close(out, out_ref, "up-projection of the first y")
+    assert_bitexact(y, yB_ref, "second y")
     assert mt.moe_tail_take_device_error() == 0
 
 
