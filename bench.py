@@ -64,6 +64,7 @@ def parse_args():
     ap.add_argument("--graph-steps", type=int, default=50, help="steps captured per CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload isolated timings")
     ap.add_argument("--sequential", action="store_true",
                     help="run the four calls in order on one stream (shared expert accumulating into out)")
     return ap.parse_args()
@@ -533,8 +534,122 @@ def cuda_arm(args, world, rank, local):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cpu)
+    if not args.no_configs:
+        line["configs_isolated"] = isolated_configs(mt, cpu, w, dev, stream)
     print(json.dumps(line), flush=True)
     return 0
+
+
+def config_bytes(name: str, d: dict) -> int:
+    """Algorithmic bytes (read + write) of one call at a workload's sizes: every
+    route row, weight and partial read once, the output written once."""
+    if name == "ep":
+        b, tp, K, P = d["b"], d["tp"], d["K"], d["P"]
+        return b * K * P * 2 + tp * b * K * 4 + b * K * 4 + P * 2 + b * P * 2
+    if name == "tp":
+        b, tp, K, P = d["b"], d["tp"], d["K"], d["P"]
+        return tp * b * K * P * 2 + 2 * b * K * 4 + P * 2 + b * P * 2
+    if name == "latent":
+        b, tp, tp_s, L_, H_ = d["b"], d["tp"], d["tp_s"], d["L"], d["H"]
+        return H_ * L_ * 2 + tp * b * L_ * 2 + tp_s * b * H_ * 2 + L_ * 2 + b * H_ * 2
+    b, H_, I_ = d["b"], d["H"], d["I"]  # shared expert added into out: h written + read, out read + written
+    return 3 * H_ * I_ * 2 + b * H_ * 2 + 2 * b * I_ * 2 + 2 * b * H_ * 2
+
+
+def isolated_configs(mt, cpu, w, dev, stream) -> dict:
+    """Each workload timed alone: one call per graph node, CUDA events around
+    graph replays of 20 calls that rotate over copies of the call's large
+    inputs (together more than twice the L2), median of 7 replays."""
+    from moe_decode_tail_gb300 import synth
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    hbm, _, kind = peaks()
+
+    def timed(fn, copies, reps=20, replays=7):
+        with torch.cuda.stream(stream):
+            for i in range(copies):
+                fn(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(reps):
+                fn(r % copies)
+        ts = []
+        with torch.cuda.stream(stream):
+            g.replay()
+            for _ in range(replays):
+                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                e.record(stream)
+                e.synchronize()
+                ts.append(a.elapsed_time(e) * 1e3 / reps)
+        return statistics.median(ts)
+
+    def copies_for(nbytes):
+        return max(1, -(-2 * l2 // max(1, nbytes)) + 1)
+
+    res = {}
+
+    def report(key, us, nbytes, copies, target):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[key] = {"us": round(us, 3), "algorithmic_bytes": nbytes, "achieved_gbs": round(gbs, 1),
+                    "hbm_frac": round(gbs / hbm, 4), "input_copies": copies, "target": target}
+
+    def ep_like(key, d, target, n=None):
+        nb = config_bytes("ep", d)
+        n = n or copies_for(nb)
+        rows = [d["rows"].to(dev)] + [None] * (n - 1)
+        for i in range(1, n):
+            rows[i] = rows[0].clone()
+        idx, wt, gam = d["idx"].to(dev), d["w"].to(dev), d["gamma"].to(dev)
+        out = torch.empty((d["b"], d["P"]), dtype=torch.bfloat16, device=dev)
+        us = timed(lambda i: mt.moe_tail_ep_finalize(rows[i], idx, wt, gam, out, gain_center=d["gain_center"],
+                                                     eps=d["eps"], weight_before_norm=d["weight_before_norm"],
+                                                     stream=stream), n)
+        report(key, us, nb, n, target)
+
+    ep_like("1_ep_tiny_b4_P512", synth.config(1), "parity; latency-bound (report us; inputs L2-resident)", n=1)
+    ep_like("2_ep_b64_P4096", cpu["ep"], ">= 0.70 of HBM (hard at 4.7 MB)")
+
+    d = synth.config(3)
+    nb = config_bytes("tp", d)
+    n = copies_for(nb)
+    parts = [d["partials"].to(dev)]
+    parts += [parts[0].clone() for _ in range(n - 1)]
+    idx, wt, gam = d["idx"].to(dev), d["w"].to(dev), d["gamma"].to(dev)
+    out = torch.empty((d["b"], d["P"]), dtype=torch.bfloat16, device=dev)
+    us = timed(lambda i: mt.moe_tail_tp_finalize(parts[i], idx, wt, gam, out, gain_center=d["gain_center"],
+                                                 eps=d["eps"], weight_before_norm=d["weight_before_norm"],
+                                                 stream=stream), n)
+    report("3_tp_b128_P4096", us, nb, n, ">= 0.70 of HBM")
+    del parts
+
+    d = synth.config(4)
+    nb = config_bytes("latent", d)
+    n = copies_for(nb)
+    wu = [d["w_up"].to(dev)]
+    wu += [wu[0].clone() for _ in range(n - 1)]
+    lat, gam, sh = d["latent"].to(dev), d["gamma"].to(dev), d["shared"].to(dev)
+    out = torch.empty((d["b"], d["H"]), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mt.moe_tail_workspace_bytes(0, d["b"], d["L"]), dtype=torch.uint8, device=dev)
+    us = timed(lambda i: mt.moe_tail_latent_up(lat, gam, wu[i], sh, out, ws, eps=d["eps"], stream=stream), n)
+    report("4_latent_up_b16", us, nb, n, ">= 0.60 of the weight-stream roofline")
+    del wu
+
+    d = dict(b=B, H=H, I=I)
+    nb = config_bytes("shared", d)
+    n = 2
+    ws_ = [(w["w_gate"], w["w_up_s"], w["w_down"])]
+    ws_.append(tuple(t.clone() for t in ws_[0]))
+    out = torch.zeros((B, H), dtype=torch.bfloat16, device=dev)
+    us = timed(lambda i: mt.moe_shared_expert(w["x"], *ws_[i], out, w["ws_sh"], accumulate=True, stream=stream), n)
+    report("5_shared_expert_b64", us, nb, n, ">= 0.60 of the weight-stream roofline")
+    del ws_
+    torch.cuda.synchronize()
+    return {"peak_gbs": hbm, "peak_source": f"{kind} hbm_gbs (MEASURED_PEAKS.json)", "l2_bytes": l2,
+            "method": "each call alone: graph of 20 calls rotating over input copies > 2x L2, median of 7 replays",
+            "results": res}
 
 
 def e2e_leg(mt, w, stream, steps, dist, dev, side=None):

@@ -230,6 +230,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot_ptr;
   launch_dependents();  // the next kernel may be scheduled as this one's CTAs retire
 
+  // Tokens whose outputs this CTA finishes (the tile's tokens split over the cluster).
+  const int n_valid = min(N, a.n_tok - tok0);
+  const int t_per = n_valid / (int)ksplit, t_rem = n_valid % (int)ksplit;
+  const int t_begin = (int)rank * t_per + min((int)rank, t_rem);
+  const int t_count = t_per + ((int)rank < t_rem ? 1 : 0);
+  constexpr int kQuads = kOutRows / 4;  // an epilogue item: 4 output features of one token
+  const int n_items = t_count * kQuads;
+  // The epilogue's addend of an item -- the slot sum of the shared partials
+  // (up-projection) or the old out (accumulating down projection) -- does not
+  // depend on the accumulator, so the four epilogue warps gather it while the
+  // K loop runs when each holds at most kPre items.
+  constexpr int kPre = 4;
+  const bool has_addend = MODE == kGemmUpShared ? a.shared != nullptr : (MODE == kGemmDown && a.accumulate != 0);
+  const bool pre = has_addend && n_items <= 128 * kPre;
+  float4 pre_add[kPre];
+  auto addend = [&](int item) -> float4 {
+    const int tg = tok0 + t_begin + item / kQuads;
+    const int n = m_tile * kOutRows + 4 * (item % kQuads);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (n >= a.M) return v;
+    if (MODE == kGemmUpShared) {  // slot order, from +0
+      for (int s = 0; s < a.tp_s; ++s) {
+        const uint2 sv = *reinterpret_cast<const uint2*>(a.shared + ((int64_t)s * a.n_tok + tg) * a.M + n);
+        v.x = __fadd_rn(v.x, bf16_lo(sv.x)); v.y = __fadd_rn(v.y, bf16_hi(sv.x));
+        v.z = __fadd_rn(v.z, bf16_lo(sv.y)); v.w = __fadd_rn(v.w, bf16_hi(sv.y));
+      }
+    } else {
+      const uint2 ov = *reinterpret_cast<const uint2*>(a.out + (int64_t)tg * a.M + n);
+      v = make_float4(bf16_lo(ov.x), bf16_hi(ov.x), bf16_lo(ov.y), bf16_hi(ov.y));
+    }
+    return v;
+  };
+
   // Weight box of K block kb into stage st (two half-height boxes for gate/up).
   auto load_weights = [&](uint32_t st, uint32_t bar, int kb, uint64_t policy) {
     const int kx = kb * kBlockK;
@@ -312,6 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- accumulator -> FP32 staging tile [N tokens][TM rows] ----------------
     grid_dependency_wait();
+    if (pre) {
+#pragma unroll
+      for (int j = 0; j < kPre; ++j) {
+        const int item = threadIdx.x + 128 * j;
+        if (item < n_items) pre_add[j] = addend(item);
+      }
+    }
     const bool got = mbar_wait(L.accum, 0);
     if (!got) {
       if (lane == 0) raise_error(kErrWaitAccum);
@@ -344,62 +384,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (ksplit > 1) cluster_sync_all();  // every CTA's partial tile is staged
 
   // ---------------- rank-order reduction over the cluster + fused epilogue ----------------
-  const int n_valid = min(N, a.n_tok - tok0);
-  const int t_per = n_valid / (int)ksplit, t_rem = n_valid % (int)ksplit;
-  const int t_begin = (int)rank * t_per + min((int)rank, t_rem);
-  const int t_count = t_per + ((int)rank < t_rem ? 1 : 0);
-  constexpr int kQuads = kOutRows / 4;  // 4-column groups per token
-  if (!aborted) {
-    for (int item = threadIdx.x; item < t_count * kQuads; item += kThreads) {
-      const int t = t_begin + item / kQuads;
-      const int q = item % kQuads;
-      const int tg = tok0 + t;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      float4 acc2 = make_float4(0.f, 0.f, 0.f, 0.f);
-      const uint32_t off = base + (uint32_t)((t * TM + 4 * q) * 4);
-      for (uint32_t p = 0; p < ksplit; ++p) {
-        const float4 v = ld_cluster_v4(map_to_rank(off, p));
-        acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
-        acc.z = __fadd_rn(acc.z, v.z); acc.w = __fadd_rn(acc.w, v.w);
-        if (MODE == kGemmGateUpSilu) {
-          const float4 u = ld_cluster_v4(map_to_rank(off + (TM / 2) * 4, p));
-          acc2.x = __fadd_rn(acc2.x, u.x); acc2.y = __fadd_rn(acc2.y, u.y);
-          acc2.z = __fadd_rn(acc2.z, u.z); acc2.w = __fadd_rn(acc2.w, u.w);
-        }
-      }
-      float r[4] = {acc.x, acc.y, acc.z, acc.w};
+  auto finish_item = [&](int item, float4 add) {
+    const int t = t_begin + item / kQuads;
+    const int q = item % kQuads;
+    const int tg = tok0 + t;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc2 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint32_t off = base + (uint32_t)((t * TM + 4 * q) * 4);
+    for (uint32_t p = 0; p < ksplit; ++p) {
+      const float4 v = ld_cluster_v4(map_to_rank(off, p));
+      acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
+      acc.z = __fadd_rn(acc.z, v.z); acc.w = __fadd_rn(acc.w, v.w);
       if (MODE == kGemmGateUpSilu) {
-        const int j = m_tile * kOutRows + 4 * q;
-        if (j >= a.M) continue;
-        const float u[4] = {acc2.x, acc2.y, acc2.z, acc2.w};
-        uint32_t hb[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) hb[e] = bf16_bits_pz(silu(bf16_round(r[e])) * bf16_round(u[e]));
-        uint2 pk = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
-        *reinterpret_cast<uint2*>(a.out + (int64_t)tg * a.M + j) = pk;
-      } else {
-        const int n = m_tile * kOutRows + 4 * q;
-        if (n >= a.M) continue;
-        uint16_t* dst = a.out + (int64_t)tg * a.M + n;
-        if (MODE == kGemmUpShared) {
-          if (a.shared) {
-            for (int s = 0; s < a.tp_s; ++s) {
-              const uint2 sv = *reinterpret_cast<const uint2*>(a.shared + ((int64_t)s * a.n_tok + tg) * a.M + n);
-              r[0] = __fadd_rn(r[0], bf16_lo(sv.x)); r[1] = __fadd_rn(r[1], bf16_hi(sv.x));
-              r[2] = __fadd_rn(r[2], bf16_lo(sv.y)); r[3] = __fadd_rn(r[3], bf16_hi(sv.y));
-            }
-          }
-        } else {  // down projection: BF16 d, optionally added into out
-          if (a.accumulate) {
-            const uint2 ov = *reinterpret_cast<const uint2*>(dst);
-            const float o[4] = {bf16_lo(ov.x), bf16_hi(ov.x), bf16_lo(ov.y), bf16_hi(ov.y)};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) r[e] = __fadd_rn(o[e], __uint_as_float(bf16_bits_pz(r[e]) << 16));
-          }
-        }
-        uint2 pk = make_uint2(pack_bf16x2_pz(r[0], r[1]), pack_bf16x2_pz(r[2], r[3]));
-        *reinterpret_cast<uint2*>(dst) = pk;
+        const float4 u = ld_cluster_v4(map_to_rank(off + (TM / 2) * 4, p));
+        acc2.x = __fadd_rn(acc2.x, u.x); acc2.y = __fadd_rn(acc2.y, u.y);
+        acc2.z = __fadd_rn(acc2.z, u.z); acc2.w = __fadd_rn(acc2.w, u.w);
       }
+    }
+    float r[4] = {acc.x, acc.y, acc.z, acc.w};
+    if (MODE == kGemmGateUpSilu) {
+      const int j = m_tile * kOutRows + 4 * q;
+      if (j >= a.M) return;
+      const float u[4] = {acc2.x, acc2.y, acc2.z, acc2.w};
+      uint32_t hb[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) hb[e] = bf16_bits_pz(silu(bf16_round(r[e])) * bf16_round(u[e]));
+      uint2 pk = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+      *reinterpret_cast<uint2*>(a.out + (int64_t)tg * a.M + j) = pk;
+    } else {
+      const int n = m_tile * kOutRows + 4 * q;
+      if (n >= a.M) return;
+      const float ad[4] = {add.x, add.y, add.z, add.w};
+      if (MODE == kGemmUpShared) {  // out = bf16(acc + slot sum of the shared partials)
+        if (has_addend) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) r[e] = __fadd_rn(r[e], ad[e]);
+        }
+      } else if (has_addend) {  // down projection added into out: bf16(out + bf16(d))
+#pragma unroll
+        for (int e = 0; e < 4; ++e) r[e] = __fadd_rn(ad[e], __uint_as_float(bf16_bits_pz(r[e]) << 16));
+      }
+      uint2 pk = make_uint2(pack_bf16x2_pz(r[0], r[1]), pack_bf16x2_pz(r[2], r[3]));
+      *reinterpret_cast<uint2*>(a.out + (int64_t)tg * a.M + n) = pk;
+    }
+  };
+  if (!aborted) {
+    if (pre) {  // the items whose addends the epilogue warps gathered
+      if (threadIdx.x < 128) {
+#pragma unroll
+        for (int j = 0; j < kPre; ++j) {
+          const int item = threadIdx.x + 128 * j;
+          if (item < n_items) finish_item(item, pre_add[j]);
+        }
+      }
+    } else {
+      for (int item = threadIdx.x; item < n_items; item += kThreads)
+        finish_item(item, has_addend ? addend(item) : make_float4(0.f, 0.f, 0.f, 0.f));
     }
   }
   if (ksplit > 1) cluster_sync_all();  // peers are done reading this CTA's staging tile

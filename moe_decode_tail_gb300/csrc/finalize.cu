@@ -63,6 +63,64 @@ __device__ __forceinline__ float route_weight(const void* w, int64_t i) {
   return ((const float*)w)[i];
 }
 
+// The token's route weights into sm.w and its routes that have a row into
+// sm.list_* (EP in (slot, route) order over the slots' local routes, expert-TP
+// in route order; the latent norm has one "route", the token's own row);
+// returns their count.  Called by every thread of the CTA.
+template <int MODE, int WMODE>
+__device__ int load_route_list(const FinalizeArgs& a, FinalizeSmem& sm, int t) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x;
+  if (MODE != kModeLatent && tid < a.K) sm.w[tid] = route_weight<WMODE>(a.w, (int64_t)t * a.K + tid);
+  if (MODE == kModeLatent) {
+    if (tid == 0) {
+      sm.list_row[0] = t;
+      sm.list_slot[0] = 0;
+      sm.list_route[0] = 0;
+      sm.w[0] = 1.0f;
+    }
+    __syncthreads();
+    return 1;
+  }
+  const int n = MODE == kModeEP ? a.tp * a.K : a.K;
+  int running = 0;
+  for (int base = 0; base < n; base += nthreads) {
+    const int i = base + tid;
+    int j = -1, s = 0, k = i;
+    if (i < n) {
+      if (MODE == kModeEP) {
+        s = i / a.K;
+        k = i - s * a.K;
+        j = a.idx[((int64_t)s * a.b + t) * a.K + k];
+      } else {
+        j = a.idx[(int64_t)t * a.K + i];
+      }
+    }
+    const bool has_row = i < n && j >= 0 && (int64_t)j < a.num_rows;
+    const unsigned ballot = __ballot_sync(0xffffffffu, has_row);
+    if (lane == 0) sm.warp_count[warp] = __popc(ballot);
+    __syncthreads();
+    if (tid == 0) {
+      int acc = 0;
+      for (int w = 0; w < (nthreads >> 5); ++w) {
+        sm.warp_base[w] = acc;
+        acc += sm.warp_count[w];
+      }
+      sm.count = acc;
+    }
+    __syncthreads();
+    if (has_row) {
+      const int pos = running + sm.warp_base[warp] + __popc(ballot & ((1u << lane) - 1u));
+      sm.list_row[pos] = j;
+      sm.list_slot[pos] = (int16_t)s;
+      sm.list_route[pos] = (int16_t)k;
+    }
+    running += sm.count;
+    __syncthreads();
+  }
+  return running;
+}
+
 template <int MODE, bool WBN, int WMODE>
 __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const FinalizeArgs a) {
   extern __shared__ __align__(16) float prod[];  // [R][VB][8] products of a pass
@@ -85,57 +143,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
 
   // One trip for the gains, the route weights and the route indices.
   const uint4 gv = valid ? ld_v4(a.gamma + col) : make_uint4(0, 0, 0, 0);
-  if (MODE != kModeLatent && tid < a.K) sm.w[tid] = route_weight<WMODE>(a.w, (int64_t)t * a.K + tid);
-  int count = 1;
-  if (MODE == kModeLatent) {
-    if (tid == 0) {
-      sm.list_row[0] = t;
-      sm.list_slot[0] = 0;
-      sm.list_route[0] = 0;
-      sm.w[0] = 1.0f;
-    }
-    __syncthreads();
-  } else {
-    // The token's routes with a row, in the order their sums run: EP in
-    // (slot, route) order over the slots' local routes, expert-TP in route order.
-    const int n = MODE == kModeEP ? a.tp * a.K : a.K;
-    int running = 0;
-    for (int base = 0; base < n; base += nthreads) {
-      const int i = base + tid;
-      int j = -1, s = 0, k = i;
-      if (i < n) {
-        if (MODE == kModeEP) {
-          s = i / a.K;
-          k = i - s * a.K;
-          j = a.idx[((int64_t)s * a.b + t) * a.K + k];
-        } else {
-          j = a.idx[(int64_t)t * a.K + i];
-        }
-      }
-      const bool has_row = i < n && j >= 0 && (int64_t)j < a.num_rows;
-      const unsigned ballot = __ballot_sync(0xffffffffu, has_row);
-      if (lane == 0) sm.warp_count[warp] = __popc(ballot);
-      __syncthreads();
-      if (tid == 0) {
-        int acc = 0;
-        for (int w = 0; w < (nthreads >> 5); ++w) {
-          sm.warp_base[w] = acc;
-          acc += sm.warp_count[w];
-        }
-        sm.count = acc;
-      }
-      __syncthreads();
-      if (has_row) {
-        const int pos = running + sm.warp_base[warp] + __popc(ballot & ((1u << lane) - 1u));
-        sm.list_row[pos] = j;
-        sm.list_slot[pos] = (int16_t)s;
-        sm.list_route[pos] = (int16_t)k;
-      }
-      running += sm.count;
-      __syncthreads();
-    }
-    count = running;
-  }
+  const int count = load_route_list<MODE, WMODE>(a, sm, t);
 
   float g[8];
   unpack8(gv, g);
@@ -250,6 +258,121 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
     r.z = pack_bf16x2_pz(o[4], o[5]);
     r.w = pack_bf16x2_pz(o[6], o[7]);
     if (a.inputs_before_wait) grid_dependency_wait();  // the preceding kernel may still read out
+    st_v4(a.out + (int64_t)t * a.P + col, r);
+  }
+}
+
+// ------------------------------------------- EP: a token's routes in registers
+//
+// The same arithmetic as finalize_kernel in EP mode, with one thread per
+// 16-byte vector of the band holding up to kEpRoutes of the token's routes at
+// once: their rows are loaded together, their chunk sums of squares are
+// published together, and one cluster barrier serves them all, so a token
+// whose local routes number at most kEpRoutes (the usual top-K) costs one trip
+// to memory and one barrier.  The products never leave registers: each thread
+// adds its columns' products in (slot, route) order itself, rounding each
+// slot's partial to BF16 at the slot boundary.
+constexpr int kEpRoutes = 8;
+constexpr int kEpMaxThreads = 512;
+
+template <bool WBN, int WMODE>
+__global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const FinalizeArgs a) {
+  __shared__ FinalizeSmem sm;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int t = blockIdx.y;
+  const uint32_t split = cluster_size();
+  const int vec = (int)cluster_rank() * a.band_vectors + tid;
+  const int col = vec * 8;
+  const int chunk = vec >> 5;  // a warp is one 256-column chunk
+  const bool valid = col < a.P;
+
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  if (!a.inputs_before_wait) grid_dependency_wait();
+  launch_dependents();
+
+  const uint4 gv = valid ? ld_v4(a.gamma + col) : make_uint4(0, 0, 0, 0);
+  const int count = load_route_list<kModeEP, WMODE>(a, sm, t);
+  float g[8];
+  unpack8(gv, g);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) g[i] = __fadd_rn(g[i], a.gain_center);
+  float o[8], part[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = part[i] = 0.0f;
+  int cur_slot = -1;
+
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // peers started: DSMEM is live
+
+  for (int base = 0, pass = 0; base < count; base += kEpRoutes, ++pass) {
+    const int n_pass = min(kEpRoutes, count - base);  // the same in every thread of the cluster
+    uint4 raw[kEpRoutes];
+#pragma unroll
+    for (int q = 0; q < kEpRoutes; ++q) {
+      raw[q] = make_uint4(0, 0, 0, 0);
+      if (q < n_pass && valid) {
+        const int e = base + q;
+        raw[q] = ld_stream_v4(a.rows + (int64_t)sm.list_slot[e] * a.slot_stride + (int64_t)sm.list_row[e] * a.P + col);
+      }
+    }
+    float* ssp = &sm.ss[pass & 1][0][0];  // [route of the pass][chunk]
+#pragma unroll
+    for (int q = 0; q < kEpRoutes; ++q) {
+      if (q < n_pass) {
+        float x[8];
+        unpack8(raw[q], x);
+        float acc = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float v = WBN ? __fmul_rn(x[i], g[i]) : x[i];
+          acc = __fadd_rn(acc, __fmul_rn(v, v));
+        }
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+        if (chunk < a.chunks && lane < (int)split)
+          st_cluster_f32(map_to_rank(smem_addr(&ssp[q * kMaxChunks + chunk]), (uint32_t)lane), acc);
+      }
+    }
+    cluster_sync_all();
+#pragma unroll
+    for (int q = 0; q < kEpRoutes; ++q) {
+      if (q < n_pass) {
+        const int e = base + q;
+        float ss = 0.0f;
+        for (int c = 0; c < a.chunks; ++c) ss = __fadd_rn(ss, ssp[q * kMaxChunks + c]);
+        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, a.rcpP), a.eps)));
+        const float w = sm.w[sm.list_route[e]];
+        const int s = sm.list_slot[e];
+        if (s != cur_slot) {  // slot boundary: its BF16 partial joins the slot sum
+          if (cur_slot >= 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              o[i] = __fadd_rn(o[i], bf16_round(part[i]));
+              part[i] = 0.0f;
+            }
+          }
+          cur_slot = s;
+        }
+        float x[8];
+        unpack8(raw[q], x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float nv = WBN ? __fmul_rn(__fmul_rn(x[i], g[i]), inv) : __fmul_rn(__fmul_rn(x[i], inv), g[i]);
+          part[i] = __fadd_rn(part[i], __fmul_rn(nv, w));  // each product rounded alone
+        }
+      }
+    }
+  }
+  if (cur_slot >= 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = __fadd_rn(o[i], bf16_round(part[i]));
+  }
+  if (valid) {
+    uint4 r;
+    r.x = pack_bf16x2_pz(o[0], o[1]);
+    r.y = pack_bf16x2_pz(o[2], o[3]);
+    r.z = pack_bf16x2_pz(o[4], o[5]);
+    r.w = pack_bf16x2_pz(o[6], o[7]);
+    if (a.inputs_before_wait) grid_dependency_wait();
     st_v4(a.out + (int64_t)t * a.P + col, r);
   }
 }
@@ -552,6 +675,25 @@ static cudaError_t launch_t(const FinalizeArgs& a, int split, cudaStream_t strea
   return cudaLaunchKernelEx(&cfg, k, a);
 }
 
+template <bool WBN, int WMODE>
+static cudaError_t launch_ep_t(const FinalizeArgs& a, int split, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(split, a.b, 1);
+  cfg.blockDim = dim3(a.band_vectors, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, ep_finalize_kernel<WBN, WMODE>, a);
+}
+
 template <bool WBN, int WMODE, bool LATENT>
 static cudaError_t launch_staged_t(const FinalizeArgs& a, int split, int groups, size_t smem, cudaStream_t stream) {
   auto k = staged_finalize_kernel<WBN, WMODE, LATENT>;
@@ -647,6 +789,12 @@ cudaError_t launch_finalize(int mode, const FinalizeArgs& args, bool wbn, int wm
   }
   const int routes_cap = env_int("MOE_TAIL_FIN_ROUTES", 0);  // tuning override
   if (routes_cap >= 1 && routes_cap <= kMaxRoutesPerPass) a.routes_per_pass = std::min(a.routes_per_pass, routes_cap);
+  if (mode == kModeEP && a.band_vectors <= kEpMaxThreads && env_int("MOE_TAIL_FIN_EP_REGS", 1)) {
+    if (wbn) return wmode == kWeightBF16 ? launch_ep_t<true, kWeightBF16>(a, split, stream)
+                                         : launch_ep_t<true, kWeightF32>(a, split, stream);
+    return wmode == kWeightBF16 ? launch_ep_t<false, kWeightBF16>(a, split, stream)
+                                : launch_ep_t<false, kWeightF32>(a, split, stream);
+  }
   if (mode == kModeEP) {
     if (wbn) return wmode == kWeightBF16 ? launch_t<kModeEP, true, kWeightBF16>(a, split, stream)
                                          : launch_t<kModeEP, true, kWeightF32>(a, split, stream);

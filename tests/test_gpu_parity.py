@@ -144,6 +144,18 @@ def test_ep_many_local_routes_per_slot(mt):
     assert_bitexact(run_ep(mt, d), ref_ep(d), "EP 64 local rows")
 
 
+@pytest.mark.parametrize("regs", ["0", "1"])
+def test_ep_both_kernels(mt, monkeypatch, regs):
+    # the register-resident EP kernel (default) and the route-parallel one
+    # (MOE_TAIL_FIN_EP_REGS=0) on the decode shape and on one token with more
+    # local routes than a pass holds
+    monkeypatch.setenv("MOE_TAIL_FIN_EP_REGS", regs)
+    d = synth.config(2, weight_before_norm=False)
+    assert_bitexact(run_ep(mt, d), ref_ep(d), f"EP b=64 kernel regs={regs}")
+    d = synth.ep_finalize_inputs(0xE11, b=9, tp=4, P=2048, K=24, num_experts=24)
+    assert_bitexact(run_ep(mt, d), ref_ep(d), f"EP K=24 kernel regs={regs}")
+
+
 def test_ep_b_zero_leaves_out_untouched(mt):
     d = synth.config(1)
     out = torch.full((4, 512), 3.0, dtype=torch.bfloat16, device=DEV)
