@@ -125,7 +125,7 @@ template <int MODE, bool WBN, int WMODE>
 __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const FinalizeArgs a) {
   extern __shared__ __align__(16) float prod[];  // [R][VB][8] products of a pass
   __shared__ FinalizeSmem sm;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int VB = a.band_vectors, R = a.routes_per_pass;
   const int r_local = tid / VB, vb = tid - r_local * VB;
   const int t = blockIdx.y;
@@ -135,7 +135,6 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
   const int col = vec * 8;
   const int chunk = vec >> 5;  // VB is a multiple of 32: a warp is one chunk of one route
   const bool valid = col < a.P;
-  const int nthreads = blockDim.x;
 
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   if (!a.inputs_before_wait) grid_dependency_wait();
@@ -466,7 +465,7 @@ template <bool WBN, int WMODE, bool LATENT>
 __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs a) {
   extern __shared__ __align__(128) uint8_t ring_raw[];
   __shared__ StagedSmem sm;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int VB = a.band_vectors;  // one 16-byte vector of the band per thread
   const int S = a.stages;
   const uint32_t split = cluster_size();
