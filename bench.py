@@ -290,12 +290,16 @@ def traffic_record():
         return None
 
 
+# The sources that define the shared-expert call's kernels and their launch
+# (plans, tensor maps): a change to any of them invalidates its ncu traffic.
+GEMM_SOURCES = ("common.cuh", "decode_gemm.cu", "kernels.h", "moe_tail_api.cu")
+
+
 def kernel_sources_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_decode_tail_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in GEMM_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()
 
 
@@ -558,14 +562,17 @@ def config_bytes(name: str, d: dict) -> int:
 
 def isolated_configs(mt, cpu, w, dev, stream) -> dict:
     """Each workload timed alone: one call per graph node, CUDA events around
-    graph replays of 20 calls that rotate over copies of the call's large
-    inputs (together more than twice the L2), median of 7 replays."""
+    replays of a graph of max(20, copies) calls that cycles over copies of the
+    call's large inputs (together more than twice the L2; at most 256 copies,
+    so the smallest calls stay L2-resident), median of 7 replays.  Also each
+    call at b = 1 and b = 8 (the small-batch decode regime)."""
     from moe_decode_tail_gb300 import synth
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     hbm, _, kind = peaks()
 
     def timed(fn, copies, reps=20, replays=7):
+        reps = max(reps, copies)  # every replay cycles through all the copies
         with torch.cuda.stream(stream):
             for i in range(copies):
                 fn(i)
@@ -586,8 +593,8 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
                 ts.append(a.elapsed_time(e) * 1e3 / reps)
         return statistics.median(ts)
 
-    def copies_for(nbytes):
-        return max(1, -(-2 * l2 // max(1, nbytes)) + 1)
+    def copies_for(nbytes):  # enough copies to exceed twice the L2, at most 256 (tiny calls stay L2-resident)
+        return min(256, max(1, -(-2 * l2 // max(1, nbytes)) + 1))
 
     res = {}
 
@@ -647,9 +654,53 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
     report("5_shared_expert_b64", us, nb, n, ">= 0.60 of the weight-stream roofline")
     del ws_
     torch.cuda.synchronize()
+
+    # the small-batch decode regime: each call at b = 1 and b = 8 (decode shapes of
+    # configs 2, 3, 4 and 5; weights rotate over copies, activations are tiny)
+    small = {}
+    for bs in (1, 8):
+        row = {}
+        d = synth.config(2, b=bs)
+        nb = config_bytes("ep", d)
+        n = copies_for(nb)
+        rows = [d["rows"].to(dev)]
+        rows += [rows[0].clone() for _ in range(n - 1)]
+        idx, wt, gam = d["idx"].to(dev), d["w"].to(dev), d["gamma"].to(dev)
+        out = torch.empty((bs, d["P"]), dtype=torch.bfloat16, device=dev)
+        row["ep_finalize"] = timed(lambda i: mt.moe_tail_ep_finalize(rows[i], idx, wt, gam, out, stream=stream), n)
+        del rows
+        d = synth.config(3, b=bs)
+        nb = config_bytes("tp", d)
+        n = copies_for(nb)
+        parts = [d["partials"].to(dev)]
+        parts += [parts[0].clone() for _ in range(n - 1)]
+        idx, wt, gam = d["idx"].to(dev), d["w"].to(dev), d["gamma"].to(dev)
+        out = torch.empty((bs, d["P"]), dtype=torch.bfloat16, device=dev)
+        row["tp_finalize"] = timed(lambda i: mt.moe_tail_tp_finalize(parts[i], idx, wt, gam, out, stream=stream), n)
+        del parts
+        lat = w["latent"][:, :bs].contiguous()
+        sh = w["shared"][:, :bs].contiguous()
+        wu = [w["w_up"], w["w_up"].clone(), w["w_up"].clone(), w["w_up"].clone(), w["w_up"].clone(),
+              w["w_up"].clone()]
+        out = torch.empty((bs, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(mt.moe_tail_workspace_bytes(0, bs, L), dtype=torch.uint8, device=dev)
+        row["latent_up"] = timed(lambda i: mt.moe_tail_latent_up(lat, w["lat_gamma"], wu[i], sh, out, ws,
+                                                                 stream=stream), len(wu))
+        del wu
+        x = w["x"][:bs].contiguous()
+        sw = [(w["w_gate"], w["w_up_s"], w["w_down"])]
+        sw.append(tuple(t.clone() for t in sw[0]))
+        wss = torch.empty(mt.moe_tail_workspace_bytes(1, bs, I), dtype=torch.uint8, device=dev)
+        out = torch.zeros((bs, H), dtype=torch.bfloat16, device=dev)
+        row["shared_expert"] = timed(lambda i: mt.moe_shared_expert(x, *sw[i], out, wss, accumulate=True,
+                                                                    stream=stream), 2)
+        del sw
+        small[f"b{bs}"] = {k: round(v, 3) for k, v in row.items()}
+    torch.cuda.synchronize()
     return {"peak_gbs": hbm, "peak_source": f"{kind} hbm_gbs (MEASURED_PEAKS.json)", "l2_bytes": l2,
-            "method": "each call alone: graph of 20 calls rotating over input copies > 2x L2, median of 7 replays",
-            "results": res}
+            "method": ("each call alone: a graph of max(20, copies) calls cycling over copies of the call's large "
+                       "inputs (together > 2x L2, at most 256 copies), median of 7 replays"),
+            "results": res, "small_batch_us": small}
 
 
 def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
