@@ -761,9 +761,14 @@ static cudaError_t launch_staged(int mode, const FinalizeArgs& args, bool wbn, i
 }
 
 cudaError_t launch_finalize(int mode, const FinalizeArgs& args, bool wbn, int wmode, int sms, cudaStream_t stream) {
-  // Staged rows pay off for expert-TP (tp rows per route); the latent norm
-  // (one route per token) is faster on the route-parallel kernel.
-  if (mode == kModeTP && env_int("MOE_TAIL_FIN_STAGED", 1)) {
+  // Staged rows pay off for expert-TP (tp rows per route) once a call has
+  // enough routes to keep the ring streaming (measured: b * K >= 512, i.e.
+  // b >= 64 at top-8); fewer routes finish sooner on the route-parallel
+  // kernel's single trip (b = 1: 4.6 vs 13.5 us).  The latent norm (one route
+  // per token) is faster on the route-parallel kernel.  MOE_TAIL_FIN_STAGED
+  // = 1 / 0 forces either kernel.
+  const int staged = env_int("MOE_TAIL_FIN_STAGED", -1);
+  if (mode == kModeTP && (staged == 1 || (staged != 0 && (int64_t)args.b * args.K >= 512))) {
     const cudaError_t e = launch_staged(mode, args, wbn, wmode, sms, stream);
     if (e != cudaErrorNotSupported) return e;
   }

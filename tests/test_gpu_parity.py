@@ -262,6 +262,16 @@ def test_tp_shapes(mt, kw):
     assert_bitexact(run_tp(mt, d), ref_tp(d), f"TP {kw}")
 
 
+@pytest.mark.parametrize("staged", ["0", "1"])
+@pytest.mark.parametrize("b", [3, 64])
+def test_tp_both_kernels(mt, monkeypatch, staged, b):
+    # the staged kernel (chosen from b * K >= 512) and the route-parallel one
+    # (chosen below), each forced on a batch the other would take
+    monkeypatch.setenv("MOE_TAIL_FIN_STAGED", staged)
+    d = synth.config(3, b=b, weight_before_norm=(b == 3))
+    assert_bitexact(run_tp(mt, d), ref_tp(d), f"TP b={b} staged={staged}")
+
+
 # ------------------------------------------------------------------ latent tail
 
 def run_latent(mt, d):
