@@ -689,6 +689,17 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
     ws = torch.empty(mt.moe_tail_workspace_bytes(0, d["b"], d["L"]), dtype=torch.uint8, device=dev)
     us = timed(lambda i: mt.moe_tail_latent_up(lat, gam, wu[i], sh, out, ws, eps=d["eps"], stream=stream), n)
     report("4_latent_up_b16", us, nb, n, ">= 0.60 of the weight-stream roofline")
+    # the same tail as its two calls with the promises a serving loop can make
+    # here (inputs ready, weights static): the norm of call i+1 reads its inputs
+    # while the up-projection of call i streams
+    y = ws[: d["b"] * d["L"] * 2].view(torch.bfloat16).view(d["b"], d["L"])
+
+    def split_call(i):
+        mt.moe_tail_latent_norm(lat, gam, y, eps=d["eps"], inputs_ready=True, stream=stream)
+        mt.moe_tail_up_project(y, wu[i], sh, out, weights_static=True, stream=stream)
+
+    us = timed(split_call, n)
+    report("4_latent_up_b16_two_calls", us, nb, n, ">= 0.60 of the weight-stream roofline")
     del wu
 
     d = dict(b=B, H=H, I=I)

@@ -751,7 +751,9 @@ static cudaError_t launch_staged(int mode, const FinalizeArgs& args, bool wbn, i
   const size_t budget = (size_t)env_int("MOE_TAIL_FIN_RING_KB", 64) * 1024;
   a.stages = (int)std::min<size_t>(16, budget / stage_bytes);
   if (a.stages < 2) return cudaErrorNotSupported;
-  const int groups = (int)std::min<int64_t>(a.b, std::max<int64_t>(1, 2 * (int64_t)sms / split));
+  const int group_cap = env_int("MOE_TAIL_FIN_GROUPS", 0);  // tuning override: CTAs along the tokens
+  const int groups = (int)std::min<int64_t>(
+      a.b, group_cap > 0 ? group_cap : std::max<int64_t>(1, 2 * (int64_t)sms / split));
   const size_t smem = (size_t)a.stages * stage_bytes;
   if (mode == kModeLatent) return launch_staged_t<false, kWeightUnit, true>(a, split, groups, smem, stream);
   if (wbn) return wmode == kWeightBF16 ? launch_staged_t<true, kWeightBF16, false>(a, split, groups, smem, stream)
@@ -775,12 +777,15 @@ cudaError_t launch_finalize(int mode, const FinalizeArgs& args, bool wbn, int wm
   FinalizeArgs a = args;
   a.chunks = (a.P + 255) / 256;
   const int routes = mode == kModeLatent ? 1 : (mode == kModeEP ? a.tp * a.K : a.K);
-  // Bands per token: EP moves little data per token, so about one wave of
-  // CTAs (b * split >= 3/4 of the SMs); expert-TP and latent about two.  At
-  // most 8 bands (portable cluster size), one band per chunk at most.
+  // Bands per token: EP and the latent norm move little data per token, so
+  // about one wave of CTAs (b * split >= 3/4 of the SMs; fewer, smaller
+  // clusters also find room beside a running weight stream: the latent norm
+  // at b = 64 with 2 bands instead of 8 shortened the composed step by 1.3 us);
+  // expert-TP about two waves.  At most 8 bands (portable cluster size), one
+  // band per chunk at most.
   int split = split_override();
   if (split == 0) {
-    const int64_t target = mode == kModeEP ? (3 * (int64_t)sms) / 4 : 2 * (int64_t)sms;
+    const int64_t target = mode == kModeTP ? 2 * (int64_t)sms : (3 * (int64_t)sms) / 4;
     split = 1;
     while (split < 8 && split < a.chunks && (int64_t)a.b * split < target) split *= 2;
   }
