@@ -189,9 +189,11 @@ def make_workload(dev):
     w["ws_lat"] = torch.empty(mt.moe_tail_workspace_bytes(0, B, L), dtype=torch.uint8, device=dev)
     w["y"] = w["ws_lat"][: B * L * 2].view(torch.bfloat16).view(B, L)
     w["ws_sh"] = torch.empty(mt.moe_tail_workspace_bytes(1, B, I), dtype=torch.uint8, device=dev)
-    # the latent tail's shared partials plus one slot that receives the shared expert's output
+    # the latent tail's shared partials plus one slot that receives the shared expert's output;
+    # "shared" is a view of the first TP slots, so data copied into it reaches both compositions
     w["shared9"] = torch.empty((TP + 1, B, H), dtype=torch.bfloat16, device=dev)
     w["shared9"][:TP].copy_(w["shared"])
+    w["shared"] = w["shared9"][:TP]
     w["d_slot"] = w["shared9"][TP]
     w["fork"], w["join"], w["normed"] = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
     return cpu, w
@@ -764,20 +766,49 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
 def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
     """The same step through the public API with host buffers: every step
     copies its activations from pinned host memory and reads its outputs back
-    (weights stay resident, as in serving)."""
+    (weights stay resident, as in serving).  Two sets of activation and output
+    buffers alternate, so step i+1's host-to-device copies (on their own
+    stream) run while step i computes, and step i's outputs are read back on a
+    third stream; every step still moves all of its inputs and outputs."""
     inputs = ["ep_rows", "ep_idx", "ep_w", "tp_part", "tp_idx", "tp_w", "latent", "shared", "x"]
     outputs = ["out_ep", "out_tp", "out"]
     host_in = {k: w[k].cpu().pin_memory() for k in inputs}
-    host_out = {k: torch.empty(w[k].shape, dtype=w[k].dtype).pin_memory() for k in outputs}
+    host_out = [{k: torch.empty(w[k].shape, dtype=w[k].dtype).pin_memory() for k in outputs} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+    sets = [w, dict(w)]
+    second = sets[1]
+    for k in inputs + outputs:
+        if k != "shared":
+            second[k] = torch.empty_like(w[k])
+    second["shared9"] = torch.empty_like(w["shared9"])
+    second["shared"], second["d_slot"] = second["shared9"][:TP], second["shared9"][TP]
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    computed, read_back = [ev(), ev()], [ev(), ev()]
+    issued = [0]
 
     def one():
-        for k in inputs:
-            w[k].copy_(host_in[k], non_blocking=True)
-        run_step(mt, w, stream, side=side)
-        for k in outputs:
-            host_out[k].copy_(w[k], non_blocking=True)
+        i = issued[0]
+        s, buf = sets[i % 2], i % 2
+        ready = ev()
+        if i >= 2:
+            h2d_stream.wait_event(computed[buf])  # step i-2 is done with these inputs
+        with torch.cuda.stream(h2d_stream):
+            for k in inputs:
+                s[k].copy_(host_in[k], non_blocking=True)
+            ready.record(h2d_stream)
+        stream.wait_event(ready)
+        if i >= 2:
+            stream.wait_event(read_back[buf])  # step i-2's outputs have been read back
+        run_step(mt, s, stream, side=side)
+        computed[buf].record(stream)
+        d2h_stream.wait_event(computed[buf])
+        with torch.cuda.stream(d2h_stream):
+            for k in outputs:
+                host_out[buf][k].copy_(s[k], non_blocking=True)
+            read_back[buf].record(d2h_stream)
+        issued[0] += 1
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -786,13 +817,17 @@ def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
         barrier(dist, dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
+        h2d_stream.wait_event(a)
         for _ in range(steps):
             one()
+        for e in read_back:
+            stream.wait_event(e)
         b.record(stream)
         torch.cuda.synchronize()
     s, units = aggregate(a.elapsed_time(b) / 1e3, float(B * steps), dist, dev)
     return {"value": units / s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "ms_per_step": s * 1e3 / steps}
+            "steps": steps, "ms_per_step": s * 1e3 / steps,
+            "pipelining": "double-buffered activations: step i+1's H2D copies overlap step i's compute"}
 
 
 def main():

@@ -495,8 +495,13 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms) {
   const bool forced = plan_override(mode, p);
   const int rows_per_tile = mode == kGemmGateUpSilu ? p.tm / 2 : p.tm;
   p.m_tiles = (M + rows_per_tile - 1) / rows_per_tile;
-  if (!forced) {  // two CTAs per SM, K split over a cluster
-    int ks = 2 * sms / std::max(1, p.m_tiles * tok_tiles);
+  if (!forced) {  // K split over a cluster: about two CTAs per SM
+    // Above 32 tokens the down projection takes about 1.5 per SM: in a decode
+    // step it runs beside the expert-TP finalize, which then finds SMs sooner
+    // (b = 64: K split 4 instead of 5, 72.7 -> 71.4 us per step).  Small
+    // batches keep two (b = 1 alone: 45.9 vs 48.5 us for the shared expert).
+    const int slots = (mode == kGemmDown && b > 32) ? 3 * sms / 2 : 2 * sms;
+    int ks = slots / std::max(1, p.m_tiles * tok_tiles);
     p.ksplit = std::max(1, std::min(ks, 8));
   }
   p.ksplit = std::min(p.ksplit, kblocks);
@@ -505,7 +510,11 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms) {
   // leave room on their SM for one finalize CTA of a concurrent stream (up to
   // ~80 KB of shared memory), which measured faster in the composed decode
   // step than deeper rings that keep the finalize kernels waiting for an SM.
-  if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, (p.tm == 256 ? 200 * 1024 : 72 * 1024) / sb));
+  // The up-projection ends the step, after the finalize kernels, and takes a
+  // 96 KB ring (4 stages at b = 64: 71.4 -> 70.3 us per step with the down
+  // projection's split above).
+  const int budget = p.tm == 256 ? 200 * 1024 : (mode == kGemmUpShared ? 96 * 1024 : 72 * 1024);
+  if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, budget / sb));
   const int per_cta = (kblocks + p.ksplit - 1) / p.ksplit;
   p.stages = std::min(p.stages, std::max(2, per_cta));
   // the FP32 staging tile reuses the ring

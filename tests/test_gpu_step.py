@@ -1,0 +1,82 @@
+"""The composed decode step exactly as bench.py times it (two branches: the
+shared expert then the latent tail on a side stream, EP and expert-TP
+finalize beside them), checked against the oracle on sampled tokens:
+EP and expert-TP outputs and the latent norm's y bit for bit; the step's
+output against the oracle's up-projection of the GPU's y with the shared
+expert's BF16 output d as one more shared partial (GEMM bound); and d against
+the oracle's down projection of the GPU's h (GEMM bound)."""
+import importlib.util
+import os
+
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+TOKENS = (0, 1, 29, 63)
+
+
+def close(got, ref, what):
+    g, r = got.float(), ref.float()
+    ulp = torch.exp2(torch.floor(torch.log2(r.abs().clamp_min(2.0 ** -126))) - 7)
+    bad = (g - r).abs() > 2 * ulp + 1e-3
+    assert not bool(bad.any()), f"{what}: {int(bad.sum())} of {bad.numel()} out of tolerance"
+
+
+@pytest.fixture(scope="module")
+def step():
+    from moe_decode_tail_gb300 import build as cuda_build
+
+    cuda_build.build()
+    import moe_decode_tail_gb300 as mt
+
+    mt.lib()
+    spec = importlib.util.spec_from_file_location("bench_step", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    dev = torch.device("cuda", 0)
+    cpu, w = bench.make_workload(dev)
+    stream = torch.cuda.Stream(dev, priority=-1)
+    side = torch.cuda.Stream(dev, priority=0)
+    for k in ("out_ep", "out_tp", "out", "y"):
+        w[k].fill_(float("nan"))
+    w["d_slot"].fill_(float("nan"))
+    with torch.cuda.stream(stream):
+        bench.run_step(mt, w, stream, side=side)
+    torch.cuda.synchronize()
+    assert mt.moe_tail_take_device_error() == 0
+    return bench, cpu, {k: w[k].cpu() for k in ("out_ep", "out_tp", "out", "y", "shared9")}, w["ws_sh"].cpu()
+
+
+def test_step_finalize_outputs(step):
+    bench, cpu, got, _ = step
+    ep, tp = cpu["ep"], cpu["tp"]
+    for t in TOKENS:
+        ref = oracle.ep_finalize(ep["rows"], ep["rows_per_slot"], ep["idx"][:, t:t + 1].contiguous(),
+                                 ep["w"][t:t + 1].contiguous(), ep["gamma"], 1.0, 1e-6, True, 1, bench.TP,
+                                 bench.K_ROUTES, bench.P)
+        assert torch.equal(got["out_ep"][t:t + 1].view(torch.int16), ref.view(torch.int16)), f"EP token {t}"
+        ref = oracle.tp_finalize(tp["partials"], tp["num_rows"], tp["idx"][t:t + 1].contiguous(),
+                                 tp["w"][t:t + 1].contiguous(), tp["gamma"], 1.0, 1e-6, True, 1, bench.TP,
+                                 bench.K_ROUTES, bench.P)
+        assert torch.equal(got["out_tp"][t:t + 1].view(torch.int16), ref.view(torch.int16)), f"TP token {t}"
+
+
+def test_step_latent_tail_and_shared_expert(step):
+    bench, cpu, got, ws_sh = step
+    lat, sh = cpu["lat"], cpu["sh"]
+    B, L, H, I, TP = bench.B, bench.L, bench.H, bench.I, bench.TP
+    h_gpu = ws_sh[: B * I * 2].view(torch.bfloat16).view(B, I)
+    d_gpu = got["shared9"][TP]
+    for t in TOKENS:
+        y_ref = oracle.latent_norm(lat["latent"][:, t:t + 1].contiguous(), lat["gamma"], 1e-6, 1, TP, L)
+        assert torch.equal(got["y"][t:t + 1].view(torch.int16), y_ref.view(torch.int16)), f"y token {t}"
+        # the shared expert's d: a valid down projection of the GPU's h
+        d_ref = oracle.shared_down(h_gpu[t:t + 1].contiguous(), sh["w_down"], 1, H, I, accumulate=False)
+        close(d_gpu[t:t + 1], d_ref, f"d token {t}")
+        # the step's output: the up-projection of y plus all nine partials (d included)
+        out_ref = oracle.latent_up(got["y"][t:t + 1].contiguous(), lat["w_up"],
+                                   got["shared9"][:, t:t + 1].contiguous(), TP + 1, 1, L, H)
+        close(got["out"][t:t + 1], out_ref, f"out token {t}")
