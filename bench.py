@@ -583,6 +583,13 @@ def cuda_arm(args, world, rank, local):
             "two branches: on a side stream the shared expert writes d into an extra shared-partial slot, then the "
             "latent norm and up-projection follow, adding all slots; EP and TP on a high-priority stream beside them")),
         "roofline": roof, "calls": calls, "e2e": e2e,
+        "step_roofline": {
+            "algorithmic_bytes": sum(nbytes.values()),
+            "achieved_gbs": round(sum(nbytes.values()) / (max_s / K) / 1e9, 1),
+            "peak": hbm, "unit": "GB/s",
+            "frac": round(sum(nbytes.values()) / (max_s / K) / 1e9 / hbm, 4),
+            "note": "every call's algorithmic bytes per step over the step time: the whole step is an HBM stream",
+        },
         "gpu_launches": LAUNCHES_PER_STEP * K, "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -1,6 +1,8 @@
 """The composed decode step exactly as bench.py times it (two branches: the
 shared expert then the latent tail on a side stream, EP and expert-TP
-finalize beside them), checked against the oracle on sampled tokens:
+finalize beside them; and the sequential composition, where the shared
+expert accumulates into the latent tail's output), checked against the
+oracle on sampled tokens:
 EP and expert-TP outputs and the latent norm's y bit for bit; the step's
 output against the oracle's up-projection of the GPU's y with the shared
 expert's BF16 output d as one more shared partial (GEMM bound); and d against
@@ -25,8 +27,8 @@ def close(got, ref, what):
     assert not bool(bad.any()), f"{what}: {int(bad.sum())} of {bad.numel()} out of tolerance"
 
 
-@pytest.fixture(scope="module")
-def step():
+@pytest.fixture(scope="module", params=["two_branch", "sequential"])
+def step(request):
     from moe_decode_tail_gb300 import build as cuda_build
 
     cuda_build.build()
@@ -39,19 +41,23 @@ def step():
     dev = torch.device("cuda", 0)
     cpu, w = bench.make_workload(dev)
     stream = torch.cuda.Stream(dev, priority=-1)
-    side = torch.cuda.Stream(dev, priority=0)
+    side = torch.cuda.Stream(dev, priority=0) if request.param == "two_branch" else None
     for k in ("out_ep", "out_tp", "out", "y"):
         w[k].fill_(float("nan"))
     w["d_slot"].fill_(float("nan"))
+    if request.param == "sequential":  # the shared expert adds into the latent tail's output
+        w["out"].zero_()
     with torch.cuda.stream(stream):
         bench.run_step(mt, w, stream, side=side)
     torch.cuda.synchronize()
     assert mt.moe_tail_take_device_error() == 0
-    return bench, cpu, {k: w[k].cpu() for k in ("out_ep", "out_tp", "out", "y", "shared9")}, w["ws_sh"].cpu()
+    got = {k: w[k].cpu() for k in ("out_ep", "out_tp", "out", "shared9")}
+    got["y"] = w["ws_lat"][: bench.B * bench.L * 2].view(torch.bfloat16).view(bench.B, bench.L).cpu()
+    return bench, cpu, got, w["ws_sh"].cpu(), request.param
 
 
 def test_step_finalize_outputs(step):
-    bench, cpu, got, _ = step
+    bench, cpu, got, _, _ = step
     ep, tp = cpu["ep"], cpu["tp"]
     for t in TOKENS:
         ref = oracle.ep_finalize(ep["rows"], ep["rows_per_slot"], ep["idx"][:, t:t + 1].contiguous(),
@@ -65,18 +71,31 @@ def test_step_finalize_outputs(step):
 
 
 def test_step_latent_tail_and_shared_expert(step):
-    bench, cpu, got, ws_sh = step
+    bench, cpu, got, ws_sh, mode = step
     lat, sh = cpu["lat"], cpu["sh"]
     B, L, H, I, TP = bench.B, bench.L, bench.H, bench.I, bench.TP
     h_gpu = ws_sh[: B * I * 2].view(torch.bfloat16).view(B, I)
-    d_gpu = got["shared9"][TP]
     for t in TOKENS:
         y_ref = oracle.latent_norm(lat["latent"][:, t:t + 1].contiguous(), lat["gamma"], 1e-6, 1, TP, L)
         assert torch.equal(got["y"][t:t + 1].view(torch.int16), y_ref.view(torch.int16)), f"y token {t}"
-        # the shared expert's d: a valid down projection of the GPU's h
-        d_ref = oracle.shared_down(h_gpu[t:t + 1].contiguous(), sh["w_down"], 1, H, I, accumulate=False)
-        close(d_gpu[t:t + 1], d_ref, f"d token {t}")
-        # the step's output: the up-projection of y plus all nine partials (d included)
-        out_ref = oracle.latent_up(got["y"][t:t + 1].contiguous(), lat["w_up"],
-                                   got["shared9"][:, t:t + 1].contiguous(), TP + 1, 1, L, H)
-        close(got["out"][t:t + 1], out_ref, f"out token {t}")
+        if mode == "two_branch":
+            # d: a valid down projection of the GPU's h; out: the up-projection of y
+            # plus all nine partials (d included)
+            d_gpu = got["shared9"][TP]
+            d_ref = oracle.shared_down(h_gpu[t:t + 1].contiguous(), sh["w_down"], 1, H, I, accumulate=False)
+            close(d_gpu[t:t + 1], d_ref, f"d token {t}")
+            out_ref = oracle.latent_up(got["y"][t:t + 1].contiguous(), lat["w_up"],
+                                       got["shared9"][:, t:t + 1].contiguous(), TP + 1, 1, L, H)
+            close(got["out"][t:t + 1], out_ref, f"out token {t}")
+        else:
+            # out = bf16(latent tail + bf16(down(h))): the latent tail's own output is
+            # not kept, so check out against the oracle's tail plus the oracle's down
+            # projection of the GPU's h, within the tail's GEMM bound plus d's rounding
+            tail = oracle.latent_up(got["y"][t:t + 1].contiguous(), lat["w_up"],
+                                    got["shared9"][:TP, t:t + 1].contiguous(), TP, 1, L, H)
+            d_ref = oracle.shared_down(h_gpu[t:t + 1].contiguous(), sh["w_down"], 1, H, I, accumulate=False)
+            ref = (tail.float() + d_ref.float()).to(torch.bfloat16)
+            g, r = got["out"][t:t + 1].float(), ref.float()
+            ulp = lambda v: torch.exp2(torch.floor(torch.log2(v.abs().clamp_min(2.0 ** -126))) - 7)
+            bound = 2 * ulp(r) + 2 * ulp(tail.float()) + 2 * ulp(d_ref.float()) + 2e-3
+            assert not bool(((g - r).abs() > bound).any()), f"sequential out token {t}"
