@@ -65,6 +65,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload isolated timings")
+    ap.add_argument("--composition", default="two_branch",
+                    choices=["two_branch", "norm_main", "norm_side_first", "norm_side_after"],
+                    help="how the step orders the weight-streaming calls (see run_step)")
     ap.add_argument("--sequential", action="store_true",
                     help="run the four calls in order on one stream (shared expert accumulating into out)")
     return ap.parse_args()
@@ -199,7 +202,7 @@ def make_workload(dev):
     return cpu, w
 
 
-EVENTS_PER_STEP = 10  # (start, end) of EP, TP, latent norm, up-projection, shared expert
+EVENTS_PER_STEP = 12  # (start, end) of EP, TP, latent norm, up-projection, shared gate/up (or all), down
 
 
 def run_step(mt, w, stream, events=None, side=None):
@@ -243,6 +246,8 @@ def run_step(mt, w, stream, events=None, side=None):
         mt.moe_shared_expert(w["x"], w["w_gate"], w["w_up_s"], w["w_down"], out, w["ws_sh"], accumulate=accumulate,
                              stream=st)
         rec(9, st)
+        rec(10, st)
+        rec(11, st)
 
     if side is None:
         ep(stream)
@@ -254,6 +259,43 @@ def run_step(mt, w, stream, events=None, side=None):
         rec(6, stream)
         rec(7, stream)
         shared_expert(stream, w["out"], True)
+        return
+    comp = w.get("composition", "two_branch")
+    if comp != "two_branch":
+        # the latent up-projection between the shared expert's gate/up and down
+        # projections; down then adds d into the latent tail's output
+        # (out = bf16(out + bf16(d)), the sequential composition's arithmetic)
+        w["fork"].record(stream)
+        side.wait_event(w["fork"])
+        ws_h = w["ws_sh"][: B * I * 2].view(torch.bfloat16).view(B, I)
+        norm_args = (w["latent"], w["lat_gamma"], w["y"])
+        if comp == "norm_side_first":
+            rec(4, side)
+            mt.moe_tail_latent_norm(*norm_args, eps=1e-6, inputs_ready=True, stream=side)
+            rec(5, side)
+        rec(8, side)
+        mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], ws_h, weights_static=True, stream=side)
+        rec(9, side)
+        if comp == "norm_side_after":
+            rec(4, side)
+            mt.moe_tail_latent_norm(*norm_args, eps=1e-6, inputs_ready=True, stream=side)
+            rec(5, side)
+        if comp == "norm_main":
+            rec(4, stream)
+            mt.moe_tail_latent_norm(*norm_args, eps=1e-6, inputs_ready=True, stream=stream)
+            rec(5, stream)
+            w["normed"].record(stream)
+            side.wait_event(w["normed"])
+        rec(6, side)
+        mt.moe_tail_up_project(w["y"], w["w_up"], w["shared"], w["out"], weights_static=True, stream=side)
+        rec(7, side)
+        rec(10, side)
+        mt.moe_shared_down(ws_h, w["w_down"], w["out"], accumulate=True, weights_static=True, stream=side)
+        rec(11, side)
+        w["join"].record(side)
+        ep(stream)
+        tp(stream)
+        stream.wait_event(w["join"])
         return
     w["fork"].record(stream)
     side.wait_event(w["fork"])
@@ -482,6 +524,7 @@ def cuda_arm(args, world, rank, local):
 
     mt.lib()
     cpu, w = make_workload(dev)
+    w["composition"] = args.composition
     # the routed finalize calls (latency-bound) on a high-priority stream, the
     # weight-streaming calls (shared expert, then latent tail) beside them
     stream = torch.cuda.Stream(dev, priority=-1)
@@ -538,14 +581,14 @@ def cuda_arm(args, world, rank, local):
     # per-call durations over the G steps of the last replay of the main graph
     per_call = {c: [] for c in CALLS}
     pairs = {"ep_finalize": [(0, 1)], "tp_finalize": [(2, 3)], "latent_up": [(4, 5), (6, 7)],
-             "shared_expert": [(8, 9)]}
+             "shared_expert": [(8, 9), (10, 11)]}
     for evs in main_ev:
         for c in CALLS:
             per_call[c].append(sum(evs[i].elapsed_time(evs[j]) for i, j in pairs[c]) * 1e3)  # us
     calls = {}
     hbm, bf16_tf, peak_kind = peaks()
     nbytes = dict(BYTES)
-    if side is not None:  # d written once and read once as a partial slot, instead of out read + written
+    if side is not None and args.composition == "two_branch":  # d written and read once as a partial slot
         nbytes["shared_expert"] = 3 * I * H * 2 + B * H * 2 + B * H * 2
         nbytes["latent_up"] = BYTES["latent_up"] + B * H * 2
     for c in CALLS:
@@ -581,7 +624,13 @@ def cuda_arm(args, world, rank, local):
         "config": dict(workload_config(), composition=(
             "sequential: EP, TP, latent tail, then the shared expert accumulating into out" if side is None else
             "two branches: on a side stream the shared expert writes d into an extra shared-partial slot, then the "
-            "latent norm and up-projection follow, adding all slots; EP and TP on a high-priority stream beside them")),
+            "latent norm and up-projection follow, adding all slots; EP and TP on a high-priority stream beside them"
+            if args.composition == "two_branch" else
+            f"two branches ({args.composition}): on a side stream the shared expert's gate/up, the latent "
+            "up-projection, then the shared expert's down projection adding d into out; the latent norm "
+            + {"norm_main": "first on the high-priority stream", "norm_side_first": "first on the side stream",
+               "norm_side_after": "on the side stream after gate/up"}[args.composition]
+            + "; EP and TP on the high-priority stream")),
         "roofline": roof, "calls": calls, "e2e": e2e,
         "step_roofline": {
             "algorithmic_bytes": sum(nbytes.values()),
@@ -719,7 +768,20 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
     out = torch.zeros((B, H), dtype=torch.bfloat16, device=dev)
     us = timed(lambda i: mt.moe_shared_expert(w["x"], *ws_[i], out, w["ws_sh"], accumulate=True, stream=stream), n)
     report("5_shared_expert_b64", us, nb, n, ">= 0.60 of the weight-stream roofline")
-    del ws_
+
+    # the composed layer of configs 4 and 5 at b = 64: the shared expert writes d into
+    # the latent tail's extra partial slot, then the latent tail's two calls follow
+    wl = [w["w_up"], w["w_up"].clone()]
+
+    def layer(i):
+        mt.moe_shared_expert(w["x"], *ws_[i], w["d_slot"], w["ws_sh"], accumulate=False, stream=stream)
+        mt.moe_tail_latent_norm(w["latent"], w["lat_gamma"], w["y"], eps=1e-6, inputs_ready=True, stream=stream)
+        mt.moe_tail_up_project(w["y"], wl[i], w["shared9"], w["out"], weights_static=True, stream=stream)
+
+    nb_layer = (3 * H * I * 2 + B * H * 2 + 2 * B * I * 2 + B * H * 2) + BYTES["latent_up"] + B * H * 2
+    us = timed(layer, 2)
+    report("4+5_latent_tail_and_shared_expert_b64", us, nb_layer, 2, "composed layer (report)")
+    del ws_, wl
     torch.cuda.synchronize()
 
     # the small-batch decode regime: each call at b = 1 and b = 8 (decode shapes of

@@ -180,6 +180,29 @@ int moe_shared_expert(const void* x, const void* w_gate, const void* w_up, const
                       size_t workspace_bytes, void* stream);
 
 /*
+ * The shared expert's two GEMMs as separate calls ([KS] module docstring), for
+ * callers that schedule other work between them -- e.g. the latent tail's
+ * up-projection between gate/up and down, with down then adding d into the
+ * tail's output.  moe_shared_expert is these two calls in a row, and each
+ * gives bit for bit the same result as that step there.
+ *
+ * moe_shared_gate_up:  h = the gate, up and h lines of moe_shared_expert.
+ *   x BF16 [b][H];  w_gate, w_up BF16 [I][H];  h BF16 [b][I] (written; must
+ *   not overlap an input).
+ * moe_shared_down:  out = the d and out lines of moe_shared_expert, from h.
+ *   h BF16 [b][I];  w_down BF16 [H][I];  out BF16 [b][H] (read as well when
+ *   accumulate != 0; must not overlap an input).
+ *   flags (both calls): 0, or MOE_TAIL_WEIGHTS_STATIC (as for
+ *   moe_tail_up_project: the first weight tiles are requested before the
+ *   kernel waits for the stream's preceding kernel).
+ *   Limits: 8 <= H, 8 <= I, H % 8 == 0, I % 8 == 0, b <= 65535.
+ */
+int moe_shared_gate_up(const void* x, const void* w_gate, const void* w_up, int b, int H, int I, void* h,
+                       int flags, void* stream);
+int moe_shared_down(const void* h, const void* w_down, int b, int H, int I, void* out, int accumulate,
+                    int flags, void* stream);
+
+/*
  * Latent tail without a workspace (no counterpart on the pages: an addition
  * of this library).  Same computation and arguments as moe_tail_latent_up,
  * minus the workspace: for callers that cannot allocate device memory -- a

@@ -19,6 +19,7 @@ __all__ = [
     "moe_shared_expert", "moe_tail_workspace_bytes", "moe_tail_status_str", "moe_tail_take_device_error",
     "moe_tail_latent_up_noalloc", "NOALLOC_SCRATCH_BYTES", "moe_tail_selftest_wait_timeout",
     "moe_tail_latent_norm", "moe_tail_up_project", "WEIGHTS_STATIC", "INPUTS_READY",
+    "moe_shared_gate_up", "moe_shared_down",
 ]
 
 OK, EINVAL, ECUDA, ENOTSUP = 0, 1, 2, 3
@@ -54,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.moe_tail_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
         L.moe_tail_latent_norm.argtypes = [P, P, f32, i32, i32, i32, P, i32, P]
         L.moe_tail_up_project.argtypes = [P, P, P, i32, i32, i32, i32, P, i32, P]
+        L.moe_shared_gate_up.argtypes = [P, P, P, i32, i32, i32, P, i32, P]
+        L.moe_shared_down.argtypes = [P, P, i32, i32, i32, P, i32, i32, P]
         L.moe_tail_workspace_bytes.argtypes = [i32, i32, i32]
         L.moe_tail_workspace_bytes.restype = sz
         L.moe_tail_status_str.argtypes = [i32]
@@ -61,7 +64,7 @@ def lib() -> ctypes.CDLL:
         L.moe_tail_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         for name in ("moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up", "moe_shared_expert",
                      "moe_tail_take_device_error", "moe_tail_latent_up_noalloc", "moe_tail_selftest_wait_timeout",
-                     "moe_tail_latent_norm", "moe_tail_up_project"):
+                     "moe_tail_latent_norm", "moe_tail_up_project", "moe_shared_gate_up", "moe_shared_down"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -167,6 +170,29 @@ def moe_tail_up_project(y, w_up, shared, out, *, weights_static=False, stream=No
     tp_s = 0 if shared is None else shared.shape[0]
     _check("moe_tail_up_project", lib().moe_tail_up_project(
         _p(y), _p(w_up), _p(shared), tp_s, b, L, H, _p(out), WEIGHTS_STATIC if weights_static else 0,
+        _stream(stream)))
+    return out
+
+
+def moe_shared_gate_up(x, w_gate, w_up, h, *, weights_static=False, stream=None) -> torch.Tensor:
+    """The shared expert's gate/up projection and SiLU into h (BF16 [b, I]):
+    x BF16 [b, H], w_gate and w_up BF16 [I, H]."""
+    _cuda(x, w_gate, w_up, h)
+    b, H = x.shape
+    I = w_gate.shape[0]
+    _check("moe_shared_gate_up", lib().moe_shared_gate_up(
+        _p(x), _p(w_gate), _p(w_up), b, H, I, _p(h), WEIGHTS_STATIC if weights_static else 0, _stream(stream)))
+    return h
+
+
+def moe_shared_down(h, w_down, out, *, accumulate=True, weights_static=False, stream=None) -> torch.Tensor:
+    """The shared expert's down projection of h (BF16 [b, I]) with w_down BF16
+    [H, I], written into out (BF16 [b, H]) or added into it (accumulate)."""
+    _cuda(h, w_down, out)
+    b, I = h.shape
+    H = w_down.shape[0]
+    _check("moe_shared_down", lib().moe_shared_down(
+        _p(h), _p(w_down), b, H, I, _p(out), int(bool(accumulate)), WEIGHTS_STATIC if weights_static else 0,
         _stream(stream)))
     return out
 

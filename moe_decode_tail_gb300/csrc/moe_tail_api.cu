@@ -291,11 +291,61 @@ MOE_API int moe_tail_up_project(const void* y, const void* w_up, const void* sha
 
 // ============================================================================ shared expert
 
+namespace {
+
+bool shared_sizes_ok(int b, int H, int I) {
+  return b >= 0 && b <= 65535 && H >= 8 && H % 8 == 0 && I >= 8 && I % 8 == 0 && H <= (1 << 24) && I <= (1 << 24);
+}
+
+// h = bf16(silu(bf16(x . w_gate^T)) * bf16(x . w_up^T)).  Arguments already checked.
+int launch_gate_up(const void* x, const void* w_gate, const void* w_up, int b, int H, int I, void* h,
+                   bool weights_before_wait, cudaStream_t st) {
+  const GemmPlan p1 = moetail::plan_gemm(moetail::kGemmGateUpSilu, I, H, b, device_sms());
+  CUtensorMap mg, mu, mx;
+  if (!encode_bf16_2d(&mg, w_gate, I, H, p1.tm / 2, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&mu, w_up, I, H, p1.tm / 2, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&mx, x, b, H, p1.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+    return MOE_TAIL_ECUDA;
+  GemmArgs g;
+  g.M = I;
+  g.K = H;
+  g.n_tok = b;
+  g.kblocks = (H + 63) / 64;
+  g.shared = nullptr;
+  g.tp_s = 0;
+  g.out = static_cast<uint16_t*>(h);
+  g.accumulate = 0;
+  g.weights_before_wait = weights_before_wait ? 1 : 0;
+  return finish(moetail::launch_decode_gemm(moetail::kGemmGateUpSilu, p1, mg, mu, mx, g, true, st));
+}
+
+// out = accumulate ? bf16(out + bf16(h . w_down^T)) : bf16(h . w_down^T).  Arguments already checked.
+int launch_down(const void* h, const void* w_down, int b, int H, int I, void* out, bool accumulate,
+                bool weights_before_wait, cudaStream_t st) {
+  const GemmPlan p2 = moetail::plan_gemm(moetail::kGemmDown, H, I, b, device_sms());
+  CUtensorMap md, mh;
+  if (!encode_bf16_2d(&md, w_down, H, I, p2.tm, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&mh, h, b, I, p2.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+    return MOE_TAIL_ECUDA;
+  GemmArgs d;
+  d.M = H;
+  d.K = I;
+  d.n_tok = b;
+  d.kblocks = (I + 63) / 64;
+  d.shared = nullptr;
+  d.tp_s = 0;
+  d.out = static_cast<uint16_t*>(out);
+  d.accumulate = accumulate ? 1 : 0;
+  d.weights_before_wait = weights_before_wait ? 1 : 0;
+  return finish(moetail::launch_decode_gemm(moetail::kGemmDown, p2, md, md, mh, d, true, st));
+}
+
+}  // namespace
+
 MOE_API int moe_shared_expert(const void* x, const void* w_gate, const void* w_up, const void* w_down, int b,
                               int H, int I, void* out, int accumulate, void* workspace, size_t workspace_bytes,
                               void* stream) {
-  if (b < 0 || b > 65535 || H < 8 || H % 8 || I < 8 || I % 8 || H > (1 << 24) || I > (1 << 24))
-    return MOE_TAIL_EINVAL;
+  if (!shared_sizes_ok(b, H, I)) return MOE_TAIL_EINVAL;
   if (b == 0) return MOE_TAIL_OK;
   if (!x || !w_gate || !w_up || !w_down || !out || !workspace) return MOE_TAIL_EINVAL;
   if (!aligned(x, 16) || !aligned(w_gate, 16) || !aligned(w_up, 16) || !aligned(w_down, 16) || !aligned(out, 16) ||
@@ -309,43 +359,39 @@ MOE_API int moe_shared_expert(const void* x, const void* w_gate, const void* w_u
   if (overlaps(o, rx) || overlaps(o, rg) || overlaps(o, ru) || overlaps(o, rd) || overlaps(o, ws) ||
       overlaps(ws, rx) || overlaps(ws, rg) || overlaps(ws, ru) || overlaps(ws, rd))
     return MOE_TAIL_EINVAL;
-
-  const int sms = device_sms();
-  const GemmPlan p1 = moetail::plan_gemm(moetail::kGemmGateUpSilu, I, H, b, sms);
-  const GemmPlan p2 = moetail::plan_gemm(moetail::kGemmDown, H, I, b, sms);
-  CUtensorMap mg, mu, mx, md, mh;
-  if (!encode_bf16_2d(&mg, w_gate, I, H, p1.tm / 2, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
-      !encode_bf16_2d(&mu, w_up, I, H, p1.tm / 2, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
-      !encode_bf16_2d(&mx, x, b, H, p1.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
-      !encode_bf16_2d(&md, w_down, H, I, p2.tm, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
-      !encode_bf16_2d(&mh, workspace, b, I, p2.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
-    return MOE_TAIL_ECUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // gate/up is the first kernel of the call: the caller may just have written the weights
+  const int rc = launch_gate_up(x, w_gate, w_up, b, H, I, workspace, false, st);
+  if (rc != MOE_TAIL_OK) return rc;
+  // the down projection follows this call's own gate/up kernel, which never writes w_down
+  return launch_down(workspace, w_down, b, H, I, out, accumulate != 0, true, st);
+}
 
-  GemmArgs g;
-  g.M = I;
-  g.K = H;
-  g.n_tok = b;
-  g.kblocks = (H + 63) / 64;
-  g.shared = nullptr;
-  g.tp_s = 0;
-  g.out = static_cast<uint16_t*>(workspace);
-  g.accumulate = 0;
-  g.weights_before_wait = 0;  // first kernel of the call: the caller may just have written the weights
-  cudaError_t e = moetail::launch_decode_gemm(moetail::kGemmGateUpSilu, p1, mg, mu, mx, g, true, st);
-  if (e != cudaSuccess) return finish(e);
+MOE_API int moe_shared_gate_up(const void* x, const void* w_gate, const void* w_up, int b, int H, int I, void* h,
+                               int flags, void* stream) {
+  if (!shared_sizes_ok(b, H, I) || (flags & ~MOE_TAIL_WEIGHTS_STATIC)) return MOE_TAIL_EINVAL;
+  if (b == 0) return MOE_TAIL_OK;
+  if (!x || !w_gate || !w_up || !h) return MOE_TAIL_EINVAL;
+  if (!aligned(x, 16) || !aligned(w_gate, 16) || !aligned(w_up, 16) || !aligned(h, 16)) return MOE_TAIL_EINVAL;
+  const Range rh = span(h, (size_t)b * I * 2);
+  if (overlaps(rh, span(x, (size_t)b * H * 2)) || overlaps(rh, span(w_gate, (size_t)I * H * 2)) ||
+      overlaps(rh, span(w_up, (size_t)I * H * 2)))
+    return MOE_TAIL_EINVAL;
+  return launch_gate_up(x, w_gate, w_up, b, H, I, h, (flags & MOE_TAIL_WEIGHTS_STATIC) != 0,
+                        static_cast<cudaStream_t>(stream));
+}
 
-  GemmArgs d;
-  d.M = H;
-  d.K = I;
-  d.n_tok = b;
-  d.kblocks = (I + 63) / 64;
-  d.shared = nullptr;
-  d.tp_s = 0;
-  d.out = static_cast<uint16_t*>(out);
-  d.accumulate = accumulate != 0;
-  d.weights_before_wait = 1;  // follows this call's own gate/up kernel
-  return finish(moetail::launch_decode_gemm(moetail::kGemmDown, p2, md, md, mh, d, true, st));
+MOE_API int moe_shared_down(const void* h, const void* w_down, int b, int H, int I, void* out, int accumulate,
+                            int flags, void* stream) {
+  if (!shared_sizes_ok(b, H, I) || (flags & ~MOE_TAIL_WEIGHTS_STATIC)) return MOE_TAIL_EINVAL;
+  if (b == 0) return MOE_TAIL_OK;
+  if (!h || !w_down || !out) return MOE_TAIL_EINVAL;
+  if (!aligned(h, 16) || !aligned(w_down, 16) || !aligned(out, 16)) return MOE_TAIL_EINVAL;
+  const Range o = span(out, (size_t)b * H * 2);
+  if (overlaps(o, span(h, (size_t)b * I * 2)) || overlaps(o, span(w_down, (size_t)H * I * 2)))
+    return MOE_TAIL_EINVAL;
+  return launch_down(h, w_down, b, H, I, out, accumulate != 0, (flags & MOE_TAIL_WEIGHTS_STATIC) != 0,
+                     static_cast<cudaStream_t>(stream));
 }
 
 // ============================================================================ misc

@@ -186,6 +186,44 @@ def test_shared_expert_refuses_bad_arguments(lib, bad):
     assert shared(lib, **bad) == EINVAL
 
 
+def gate_up(lib, **kw):
+    args = dict(x=a(), wg=a(1 << 28), wu=a(2 << 28), b=64, H=7168, I=6144, h=a(3 << 28), flags=0, stream=None)
+    args.update(kw)
+    return lib.moe_shared_gate_up(args["x"], args["wg"], args["wu"], args["b"], args["H"], args["I"], args["h"],
+                                  args["flags"], args["stream"])
+
+
+def down(lib, **kw):
+    args = dict(h=a(), wd=a(1 << 28), b=64, H=7168, I=6144, out=a(2 << 28), acc=1, flags=0, stream=None)
+    args.update(kw)
+    return lib.moe_shared_down(args["h"], args["wd"], args["b"], args["H"], args["I"], args["out"], args["acc"],
+                               args["flags"], args["stream"])
+
+
+@host_only
+@pytest.mark.parametrize("bad", [
+    dict(H=7169), dict(I=6142), dict(b=-1), dict(x=None), dict(wu=None), dict(h=None), dict(h=a(8)),
+    dict(h=a(16)), dict(flags=2), dict(wg=a(4)),  # h over x
+])
+def test_shared_gate_up_refuses_bad_arguments(lib, bad):
+    assert gate_up(lib, **bad) == EINVAL
+
+
+@host_only
+@pytest.mark.parametrize("bad", [
+    dict(H=4), dict(I=6150), dict(b=65536), dict(h=None), dict(wd=None), dict(out=None), dict(out=a(8)),
+    dict(out=a(16)), dict(flags=4), dict(h=a(2)),  # out over h
+])
+def test_shared_down_refuses_bad_arguments(lib, bad):
+    assert down(lib, **bad) == EINVAL
+
+
+@host_only
+def test_shared_steps_b_zero(lib):
+    assert gate_up(lib, b=0, x=None, h=None) == OK
+    assert down(lib, b=0, h=None, out=None, flags=1) == OK
+
+
 def test_workspace_bytes(lib):
     assert lib.moe_tail_workspace_bytes(0, 16, 3584) == 16 * 3584 * 2
     assert lib.moe_tail_workspace_bytes(1, 3, 100) == 768  # rounded up to 256 bytes

@@ -474,6 +474,37 @@ def test_shared_expert_down_stage_full_size_exact_h(mt):
         assert_accumulated_close(out[sl], out_ref, d_ref, f"accumulated token {t}")
 
 
+@pytest.mark.parametrize("kw", [dict(b=64, H=7168, I=6144), dict(b=5, H=264, I=200), dict(b=130, H=256, I=128)])
+@pytest.mark.parametrize("static", [False, True])
+def test_shared_expert_as_two_calls(mt, kw, static):
+    # moe_shared_gate_up then moe_shared_down on two streams joined by an event,
+    # with the latent-tail-like addend in out: bit-identical to the one call
+    s = synth.shared_expert_inputs(0x2C + kw["b"], **kw)
+    b, H, I = s["b"], s["H"], s["I"]
+    out_in = synth.bf16(synth.normal(0x2C, 5, b * H), (b, H))
+    h1, out1 = run_shared(mt, s, out_in, accumulate=True)
+    x, wg, wu, wd = (s[k].to(DEV) for k in ("x", "w_gate", "w_up", "w_down"))
+    h = torch.full((b, I), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out = out_in.to(DEV).clone()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    ready = torch.cuda.Event()
+    mt.moe_shared_gate_up(x, wg, wu, h, weights_static=static, stream=s1)
+    ready.record(s1)
+    s2.wait_event(ready)
+    mt.moe_shared_down(h, wd, out, accumulate=True, weights_static=static, stream=s2)
+    torch.cuda.synchronize()
+    assert_bitexact(h, h1, f"h {kw}")
+    assert_bitexact(out, out1, f"out {kw}")
+    d = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mt.moe_shared_down(h, wd, d, accumulate=False)
+    torch.cuda.synchronize()
+    t = min(3, b - 1)
+    assert_gemm_close(d[t:t + 1], oracle.shared_down(h[t:t + 1].cpu(), s["w_down"], 1, H, I, accumulate=False),
+                      f"d token {t} {kw}")
+    assert mt.moe_tail_take_device_error() == 0
+
+
 def test_shared_expert_zero_input_leaves_out(mt):
     s = synth.shared_expert_inputs(3, b=5, H=256, I=128)
     s["x"] = torch.zeros_like(s["x"])
