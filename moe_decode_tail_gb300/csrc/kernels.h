@@ -60,6 +60,13 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms);
 cudaError_t launch_decode_gemm(int mode, const GemmPlan& plan, const CUtensorMap& w0, const CUtensorMap& w1,
                                const CUtensorMap& x, const GemmArgs& a, bool pdl, cudaStream_t stream);
 
+// The latent tail's two steps, shared by its entry points (arguments already
+// checked; enqueue_up_project returns a moe_tail status).
+cudaError_t enqueue_latent_norm(const void* latent, const void* gamma, float eps, int b, int tp, int L, void* y,
+                                bool inputs_ready, cudaStream_t st);
+int enqueue_up_project(const void* y, const void* w_up, const void* shared, int tp_s, int b, int L, int H, void* out,
+                       bool weights_before_wait, cudaStream_t st);
+
 // Read and clear the device error word (synchronises with the device).
 cudaError_t take_device_error(unsigned* bits);
 // A one-thread kernel whose bounded wait expires after limit_ns.

@@ -177,13 +177,13 @@ MOE_API size_t moe_tail_workspace_bytes(int which, int b, int dim) {
   return round256((size_t)b * dim * 2);
 }
 
-namespace {
+namespace moetail {
 
 // Step 1 of the latent tail: y = RMS norm of the slot-summed latent (an
 // expert-TP finalize with one "route" per token: row = token, unit weight,
 // gain center 0).  Arguments already checked.
-cudaError_t launch_latent_norm(const void* latent, const void* gamma, float eps, int b, int tp, int L, void* y,
-                               bool inputs_ready, cudaStream_t st) {
+cudaError_t enqueue_latent_norm(const void* latent, const void* gamma, float eps, int b, int tp, int L, void* y,
+                                bool inputs_ready, cudaStream_t st) {
   FinalizeArgs n;
   n.inputs_before_wait = inputs_ready ? 1 : 0;
   n.rows = static_cast<const uint16_t*>(latent);
@@ -204,8 +204,8 @@ cudaError_t launch_latent_norm(const void* latent, const void* gamma, float eps,
 }
 
 // Step 2: out = y . w_up^T + sum_s shared[s].  Arguments already checked.
-int launch_up_project(const void* y, const void* w_up, const void* shared, int tp_s, int b, int L, int H, void* out,
-                      bool weights_before_wait, cudaStream_t st) {
+int enqueue_up_project(const void* y, const void* w_up, const void* shared, int tp_s, int b, int L, int H, void* out,
+                       bool weights_before_wait, cudaStream_t st) {
   const GemmPlan plan = moetail::plan_gemm(moetail::kGemmUpShared, H, L, b, device_sms());
   CUtensorMap mw, mx;
   if (!encode_bf16_2d(&mw, w_up, H, L, plan.tm, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
@@ -223,6 +223,13 @@ int launch_up_project(const void* y, const void* w_up, const void* shared, int t
   g.weights_before_wait = weights_before_wait ? 1 : 0;
   return finish(moetail::launch_decode_gemm(moetail::kGemmUpShared, plan, mw, mw, mx, g, true, st));
 }
+
+}  // namespace moetail
+
+namespace {
+
+using moetail::enqueue_latent_norm;
+using moetail::enqueue_up_project;
 
 bool latent_sizes_ok(int b, int tp, int L) {
   return b >= 0 && b <= 65535 && tp >= 1 && tp <= kMaxTp && L >= 8 && L <= kMaxP && L % 8 == 0;
@@ -255,9 +262,9 @@ MOE_API int moe_tail_latent_up(const void* latent, const void* gamma, float eps,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // 1. y (in the workspace), 2. the up-projection; the GEMM follows this
   // call's own norm kernel, which never writes w_up.
-  const cudaError_t e = launch_latent_norm(latent, gamma, eps, b, tp, L, workspace, false, st);
+  const cudaError_t e = enqueue_latent_norm(latent, gamma, eps, b, tp, L, workspace, false, st);
   if (e != cudaSuccess) return finish(e);
-  return launch_up_project(workspace, w_up, shared, tp_s, b, L, H, out, true, st);
+  return enqueue_up_project(workspace, w_up, shared, tp_s, b, L, H, out, true, st);
 }
 
 MOE_API int moe_tail_latent_norm(const void* latent, const void* gamma, float eps, int b, int tp, int L, void* y,
@@ -269,8 +276,8 @@ MOE_API int moe_tail_latent_norm(const void* latent, const void* gamma, float ep
   const Range yr = span(y, (size_t)b * L * 2);
   if (overlaps(yr, span(latent, (size_t)tp * b * L * 2)) || overlaps(yr, span(gamma, (size_t)L * 2)))
     return MOE_TAIL_EINVAL;
-  return finish(launch_latent_norm(latent, gamma, eps, b, tp, L, y, (flags & MOE_TAIL_INPUTS_READY) != 0,
-                                   static_cast<cudaStream_t>(stream)));
+  return finish(enqueue_latent_norm(latent, gamma, eps, b, tp, L, y, (flags & MOE_TAIL_INPUTS_READY) != 0,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 MOE_API int moe_tail_up_project(const void* y, const void* w_up, const void* shared, int tp_s, int b, int L, int H,
@@ -285,8 +292,8 @@ MOE_API int moe_tail_up_project(const void* y, const void* w_up, const void* sha
   if (overlaps(o, span(y, (size_t)b * L * 2)) || overlaps(o, span(w_up, (size_t)H * L * 2)) ||
       overlaps(o, span(shared, (size_t)tp_s * b * H * 2)))
     return MOE_TAIL_EINVAL;
-  return launch_up_project(y, w_up, shared, tp_s, b, L, H, out, (flags & MOE_TAIL_WEIGHTS_STATIC) != 0,
-                           static_cast<cudaStream_t>(stream));
+  return enqueue_up_project(y, w_up, shared, tp_s, b, L, H, out, (flags & MOE_TAIL_WEIGHTS_STATIC) != 0,
+                            static_cast<cudaStream_t>(stream));
 }
 
 // ============================================================================ shared expert

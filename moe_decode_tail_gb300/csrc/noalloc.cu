@@ -5,11 +5,11 @@
 // inference runtime gives only its input and output buffers, or a host
 // process whose device memory is entirely reserved by its own pool allocator.
 // Others must not call cudaMalloc on their hot path because it can
-// synchronise the device.  This entry point runs the same two kernels as
-// moe_tail_latent_up, but keeps the intermediate y rows in a fixed array in
-// device memory that is part of the library itself, so the caller passes only
-// inputs and outputs and nothing is allocated per call.
-#include <cuda.h>
+// synchronise the device.  This entry point enqueues the same two steps as
+// moe_tail_latent_up (through the same internal calls), but keeps the
+// intermediate y rows in a fixed array in device memory that is part of the
+// library itself, so the caller passes only inputs and outputs and nothing is
+// allocated per call.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -50,32 +50,6 @@ cudaError_t scratch_on_current_device(void** out) {
   return cudaSuccess;
 }
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows,
-                 CUtensorMapL2promotion promo) {
-  static EncodeTiled fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(p);
-  });
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
@@ -109,53 +83,13 @@ MOE_API int moe_tail_latent_up_noalloc(const void* latent, const void* gamma, fl
     (void)cudaGetLastError();
     return MOE_TAIL_ECUDA;
   }
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                cudaSuccess) {
-    (void)cudaGetLastError();
-    return MOE_TAIL_ECUDA;
-  }
-  const moetail::GemmPlan plan = moetail::plan_gemm(moetail::kGemmUpShared, H, L, b, sms);
-  CUtensorMap mw, mx;
-  if (!encode_rows(&mw, w_up, H, L, plan.tm, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
-      !encode_rows(&mx, y, b, L, plan.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
-    return MOE_TAIL_ECUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-  // 1. y (every element written, so nothing has to start at zero)
-  moetail::FinalizeArgs n;
-  n.rows = static_cast<const uint16_t*>(latent);
-  n.num_rows = b;
-  n.slot_stride = (int64_t)b * L;
-  n.idx = nullptr;
-  n.w = nullptr;
-  n.gamma = static_cast<const uint16_t*>(gamma);
-  n.gain_center = 0.0f;
-  n.eps = eps;
-  n.rcpP = (float)(1.0 / (double)L);
-  n.b = b;
-  n.tp = tp;
-  n.K = 1;
-  n.P = L;
-  n.out = static_cast<uint16_t*>(y);
-  e = moetail::launch_finalize(moetail::kFinalizeLatent, n, false, moetail::kWeightUnit, sms, st);
-  if (e == cudaSuccess) {
-    // 2. out = y . w_up^T + sum_s shared[s]
-    moetail::GemmArgs g;
-    g.M = H;
-    g.K = L;
-    g.n_tok = b;
-    g.kblocks = (L + 63) / 64;
-    g.shared = static_cast<const uint16_t*>(shared);
-    g.tp_s = tp_s;
-    g.out = static_cast<uint16_t*>(out);
-    g.accumulate = 0;
-    g.weights_before_wait = 1;
-    e = moetail::launch_decode_gemm(moetail::kGemmUpShared, plan, mw, mw, mx, g, true, st);
-  }
+  // 1. y (every element written, so nothing has to start at zero), 2. the
+  // up-projection, which follows this call's own norm kernel
+  e = moetail::enqueue_latent_norm(latent, gamma, eps, b, tp, L, y, false, st);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return MOE_TAIL_ECUDA;
   }
-  return MOE_TAIL_OK;
+  return moetail::enqueue_up_project(y, w_up, shared, tp_s, b, L, H, out, true, st);
 }
