@@ -39,12 +39,15 @@ _lib = None
 
 
 def lib() -> ctypes.CDLL:
-    """The loaded CUDA library (raises if it has not been built)."""
+    """The loaded CUDA library (raises if it has not been built).  The
+    MOE_TAIL_LIBRARY environment variable selects another build of it (the
+    trace build, see moe_decode_tail_gb300.trace) before the first call."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB):
-            raise RuntimeError(f"{LIB} is missing: build it with moe_decode_tail_gb300.build.build()")
-        L = ctypes.CDLL(LIB)
+        path = os.environ.get("MOE_TAIL_LIBRARY", LIB)
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with moe_decode_tail_gb300.build.build()")
+        L = ctypes.CDLL(path)
         P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
         fin = [P, i64, P, P, i32, P, f32, f32, i32, i32, i32, i32, i32, P, P]
         L.moe_tail_ep_finalize.argtypes = fin

@@ -18,6 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoetail.so")
+TRACE_LIB = os.path.join(BUILD, "libmoetail_trace.so")  # the same kernels with the per-CTA trace
 SOURCES = ["finalize.cu", "decode_gemm.cu", "moe_tail_api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
@@ -38,26 +39,30 @@ def _inputs() -> list[str]:
     files = [os.path.join(CSRC, s) for s in SOURCES]
     files += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     files.append(os.path.join(ROOT, "include", "moe_tail.h"))
+    files.append(os.path.join(ROOT, "include", "moe_tail_trace.h"))
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, trace: bool = False) -> str:
+    """Build libmoetail.so, or with trace=True libmoetail_trace.so (the same
+    kernels recording a per-CTA timeline; see include/moe_tail_trace.h)."""
+    lib = TRACE_LIB if trace else LIB
+    if not force and up_to_date(lib):
+        return lib
     os.makedirs(BUILD, exist_ok=True)
     exe = nvcc()
     tag = f".{os.getpid()}"
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src.replace(".cu", tag + ".o"))
-        cmd = [exe, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(BUILD, src.replace(".cu", tag + (".trace" if trace else "") + ".o"))
+        cmd = [exe, *NVCC_FLAGS, *(["-DMOE_TAIL_TRACE"] if trace else []), "-c", os.path.join(CSRC, src), "-o", obj]
         if ptxas_v:
             cmd += ["-Xptxas", "-v"]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -69,15 +74,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as pool:
         objs = list(pool.map(compile_one, SOURCES))
-    tmp = LIB + tag
+    tmp = lib + tag
     r = subprocess.run([exe, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     for o in objs:
         os.remove(o)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_v="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_v="-v" in sys.argv, trace="--trace" in sys.argv))

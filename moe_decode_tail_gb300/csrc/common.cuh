@@ -120,4 +120,61 @@ __device__ __forceinline__ void launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+
+// ---- per-CTA timeline trace (only in builds with MOE_TAIL_TRACE) -----------
+//
+// Thread 0 of every CTA records %globaltimer at kernel entry, at up to four
+// marks inside the kernel and at exit, with the kernel's id, the CTA index and
+// the SM, into a device buffer the host attaches.  Each translation unit has
+// its own copy of the buffer pointer; moe_tail_trace_attach sets them all.
+#ifdef MOE_TAIL_TRACE
+struct TraceRec {
+  unsigned long long t0, mark[4], t1, ids, pad;  // ids: kernel id << 48 | SM << 32 | CTA
+};
+static_assert(sizeof(TraceRec) == 64, "trace record layout");
+static __device__ TraceRec* g_trace_buf = nullptr;
+static __device__ unsigned g_trace_n = 0;
+static __device__ unsigned g_trace_cap = 0;
+struct TraceScope {
+  unsigned long long t0, mark[4];
+  unsigned kid;
+  __device__ explicit TraceScope(unsigned k) : t0(global_ns()), mark{0, 0, 0, 0}, kid(k) {}
+  __device__ ~TraceScope() {
+    if (threadIdx.x != 0 || g_trace_buf == nullptr) return;
+    const unsigned i = atomicAdd(&g_trace_n, 1u);
+    if (i >= g_trace_cap) return;
+    unsigned sm;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    g_trace_buf[i] = TraceRec{t0, {mark[0], mark[1], mark[2], mark[3]}, global_ns(),
+                              ((unsigned long long)kid << 48) | ((unsigned long long)sm << 32) | cta, 0};
+  }
+};
+// attach (or detach, buf = null) this translation unit's copy and reset its count
+static inline cudaError_t trace_attach_tu(void* buf, unsigned cap) {
+  unsigned zero = 0;
+  cudaError_t e = cudaMemcpyToSymbol(g_trace_buf, &buf, sizeof buf);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_trace_cap, &cap, sizeof cap);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_trace_n, &zero, sizeof zero);
+  return e;
+}
+static inline unsigned trace_count_tu() {
+  unsigned n = 0;
+  cudaMemcpyFromSymbol(&n, g_trace_n, sizeof n);
+  return n;
+}
+#define MOE_TRACE_SCOPE(kid) ::moetail::TraceScope moe_trace_scope_(kid)
+#define MOE_TRACE_MARK(k) \
+  do {                    \
+    if (threadIdx.x == 0) moe_trace_scope_.mark[k] = ::moetail::global_ns(); \
+  } while (0)
+#else
+#define MOE_TRACE_SCOPE(kid) \
+  do {                       \
+  } while (0)
+#define MOE_TRACE_MARK(k) \
+  do {                    \
+  } while (0)
+#endif
+
 }  // namespace moetail

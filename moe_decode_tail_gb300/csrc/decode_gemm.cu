@@ -178,6 +178,7 @@ template <int MODE, int N, int TM>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
                        const __grid_constant__ CUtensorMap map_x, const GemmArgs a, const int stages) {
+  MOE_TRACE_SCOPE(30 + MODE);
   extern __shared__ uint8_t smem_raw[];
   constexpr int kATile = TM * kBlockK * 2;
   constexpr int kBTileBytes = N * kBlockK * 2;
@@ -353,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     const bool got = mbar_wait(L.accum, 0);
+    MOE_TRACE_MARK(0);  // accumulator complete
     if (!got) {
       if (lane == 0) raise_error(kErrWaitAccum);
       *abort_ptr = 1;
@@ -381,7 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   const bool aborted = *abort_ptr != 0;
+  MOE_TRACE_MARK(1);                   // partial tile staged
   if (ksplit > 1) cluster_sync_all();  // every CTA's partial tile is staged
+  MOE_TRACE_MARK(2);
 
   // ---------------- rank-order reduction over the cluster + fused epilogue ----------------
   auto finish_item = [&](int item, float4 add) {
@@ -442,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         finish_item(item, has_addend ? addend(item) : make_float4(0.f, 0.f, 0.f, 0.f));
     }
   }
+  MOE_TRACE_MARK(3);                   // reduction and epilogue stores done
   if (ksplit > 1) cluster_sync_all();  // peers are done reading this CTA's staging tile
   __syncthreads();
   if (warp == 5) {
@@ -462,6 +467,11 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns) {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   if (!mbar_wait(b, 0, limit_ns)) raise_error(kErrWaitFull);
 }
+
+#ifdef MOE_TAIL_TRACE
+cudaError_t trace_attach_gemm(void* buf, unsigned cap) { return trace_attach_tu(buf, cap); }
+unsigned trace_count_gemm() { return trace_count_tu(); }
+#endif
 
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream) {
   selftest_wait_kernel<<<1, 32, 0, stream>>>(limit_ns);

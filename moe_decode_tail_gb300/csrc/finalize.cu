@@ -123,6 +123,7 @@ __device__ int load_route_list(const FinalizeArgs& a, FinalizeSmem& sm, int t) {
 
 template <int MODE, bool WBN, int WMODE>
 __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const FinalizeArgs a) {
+  MOE_TRACE_SCOPE(10 + MODE);
   extern __shared__ __align__(16) float prod[];  // [R][VB][8] products of a pass
   __shared__ FinalizeSmem sm;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -276,6 +277,7 @@ constexpr int kEpMaxThreads = 512;
 
 template <bool WBN, int WMODE>
 __global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const FinalizeArgs a) {
+  MOE_TRACE_SCOPE(40);
   __shared__ FinalizeSmem sm;
   const int tid = threadIdx.x, lane = tid & 31;
   const int t = blockIdx.y;
@@ -463,6 +465,7 @@ __device__ __forceinline__ bool next_route(const FinalizeArgs& a, RouteCursor& c
 
 template <bool WBN, int WMODE, bool LATENT>
 __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs a) {
+  MOE_TRACE_SCOPE(20 + (LATENT ? 1 : 0));
   extern __shared__ __align__(128) uint8_t ring_raw[];
   __shared__ StagedSmem sm;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -623,6 +626,11 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
     }
   }
 }
+
+#ifdef MOE_TAIL_TRACE
+cudaError_t trace_attach_finalize(void* buf, unsigned cap) { return trace_attach_tu(buf, cap); }
+unsigned trace_count_finalize() { return trace_count_tu(); }
+#endif
 
 cudaError_t take_finalize_error(unsigned* bits) {
   unsigned v = 0, zero = 0;

@@ -69,6 +69,12 @@ int enqueue_up_project(const void* y, const void* w_up, const void* shared, int 
 
 // Read and clear the device error word (synchronises with the device).
 cudaError_t take_device_error(unsigned* bits);
+#ifdef MOE_TAIL_TRACE
+cudaError_t trace_attach_gemm(void* buf, unsigned cap);
+unsigned trace_count_gemm();
+cudaError_t trace_attach_finalize(void* buf, unsigned cap);
+unsigned trace_count_finalize();
+#endif
 // A one-thread kernel whose bounded wait expires after limit_ns.
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
 

@@ -426,3 +426,24 @@ MOE_API int moe_tail_selftest_wait_timeout(unsigned int limit_us, void* stream) 
   if (limit_us < 1 || limit_us > 1000000) return MOE_TAIL_EINVAL;
   return finish(moetail::launch_selftest_wait((unsigned long long)limit_us * 1000ull, static_cast<cudaStream_t>(stream)));
 }
+
+#ifdef MOE_TAIL_TRACE
+#include "../../include/moe_tail_trace.h"
+
+MOE_API int moe_tail_trace_attach(void* buf, unsigned int capacity) {
+  if (buf && (!aligned(buf, 16) || capacity < 2)) return MOE_TAIL_EINVAL;
+  // GEMM records fill the buffer's first half, finalize records its second
+  const unsigned half = buf ? capacity / 2 : 0;
+  void* second = buf ? static_cast<uint8_t*>(buf) + (size_t)half * MOE_TAIL_TRACE_RECORD_BYTES : nullptr;
+  cudaError_t e = moetail::trace_attach_gemm(buf, half);
+  if (e == cudaSuccess) e = moetail::trace_attach_finalize(second, buf ? capacity - half : 0);
+  return finish(e);
+}
+
+MOE_API int moe_tail_trace_counts(unsigned int* gemm_records, unsigned int* finalize_records) {
+  if (!gemm_records || !finalize_records) return MOE_TAIL_EINVAL;
+  *gemm_records = moetail::trace_count_gemm();
+  *finalize_records = moetail::trace_count_finalize();
+  return finish(cudaGetLastError());
+}
+#endif
