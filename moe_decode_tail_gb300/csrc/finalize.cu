@@ -792,6 +792,10 @@ cudaError_t launch_finalize(int mode, const FinalizeArgs& args, bool wbn, int wm
   // expert-TP about two waves.  At most 8 bands (portable cluster size), one
   // band per chunk at most.
   int split = split_override();
+  if (mode == kModeEP) {  // tuning override for EP alone: MOE_TAIL_FIN_EP_SPLIT=<1|2|4|8>
+    const int s = env_int("MOE_TAIL_FIN_EP_SPLIT", 0);
+    if (s == 1 || s == 2 || s == 4 || s == 8) split = s;
+  }
   if (split == 0) {
     const int64_t target = mode == kModeTP ? 2 * (int64_t)sms : (3 * (int64_t)sms) / 4;
     split = 1;
