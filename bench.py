@@ -169,32 +169,39 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- workload
 
-def make_workload(dev):
+def make_workload(dev, b=B, weights=None):
+    """The step's inputs at b tokens (seeded; config 2's EP shape, config 3's
+    expert-TP shape, the latent tail and the shared expert), with the
+    workspaces, output buffers and events.  weights: a workload whose weight
+    tensors (W_up, W_gate, W_up of the shared expert, W_down) to share."""
     from moe_decode_tail_gb300 import synth
 
-    ep = synth.config(2)                                  # b=64, tp=8, P=4096, top-8 of 128
-    tp = synth.config(3, b=B)                             # expert-TP at b=64
-    lat = synth.latent_up_inputs(synth.SEED_BASE + 4, b=B)
-    sh = synth.config(5)                                  # b=64, H=7168, I=6144
+    ep = synth.config(2, b=b)                             # tp=8, P=4096, top-8 of 128
+    tp = synth.config(3, b=b)                             # expert-TP
+    lat = synth.latent_up_inputs(synth.SEED_BASE + 4, b=b, with_weight=weights is None)
+    sh = synth.config(5, b=b, with_weights=weights is None)  # H=7168, I=6144
     cpu = dict(ep=ep, tp=tp, lat=lat, sh=sh)
     g = lambda t: t.to(dev)
     w = dict(
         ep_rows=g(ep["rows"]), ep_idx=g(ep["idx"]), ep_w=g(ep["w"]), ep_gamma=g(ep["gamma"]),
         tp_part=g(tp["partials"]), tp_idx=g(tp["idx"]), tp_w=g(tp["w"]), tp_gamma=g(tp["gamma"]),
-        latent=g(lat["latent"]), lat_gamma=g(lat["gamma"]), w_up=g(lat["w_up"]), shared=g(lat["shared"]),
-        x=g(sh["x"]), w_gate=g(sh["w_gate"]), w_up_s=g(sh["w_up"]), w_down=g(sh["w_down"]),
+        latent=g(lat["latent"]), lat_gamma=g(lat["gamma"]), shared=g(lat["shared"]), x=g(sh["x"]),
     )
+    if weights is None:
+        w.update(w_up=g(lat["w_up"]), w_gate=g(sh["w_gate"]), w_up_s=g(sh["w_up"]), w_down=g(sh["w_down"]))
+    else:
+        w.update({k: weights[k] for k in ("w_up", "w_gate", "w_up_s", "w_down")})
     import moe_decode_tail_gb300 as mt
 
-    w["out_ep"] = torch.empty((B, P), dtype=torch.bfloat16, device=dev)
-    w["out_tp"] = torch.empty((B, P), dtype=torch.bfloat16, device=dev)
-    w["out"] = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
-    w["ws_lat"] = torch.empty(mt.moe_tail_workspace_bytes(0, B, L), dtype=torch.uint8, device=dev)
-    w["y"] = w["ws_lat"][: B * L * 2].view(torch.bfloat16).view(B, L)
-    w["ws_sh"] = torch.empty(mt.moe_tail_workspace_bytes(1, B, I), dtype=torch.uint8, device=dev)
+    w["out_ep"] = torch.empty((b, P), dtype=torch.bfloat16, device=dev)
+    w["out_tp"] = torch.empty((b, P), dtype=torch.bfloat16, device=dev)
+    w["out"] = torch.empty((b, H), dtype=torch.bfloat16, device=dev)
+    w["ws_lat"] = torch.empty(mt.moe_tail_workspace_bytes(0, b, L), dtype=torch.uint8, device=dev)
+    w["y"] = w["ws_lat"][: b * L * 2].view(torch.bfloat16).view(b, L)
+    w["ws_sh"] = torch.empty(mt.moe_tail_workspace_bytes(1, b, I), dtype=torch.uint8, device=dev)
     # the latent tail's shared partials plus one slot that receives the shared expert's output;
     # "shared" is a view of the first TP slots, so data copied into it reaches both compositions
-    w["shared9"] = torch.empty((TP + 1, B, H), dtype=torch.bfloat16, device=dev)
+    w["shared9"] = torch.empty((TP + 1, b, H), dtype=torch.bfloat16, device=dev)
     w["shared9"][:TP].copy_(w["shared"])
     w["shared"] = w["shared9"][:TP]
     w["d_slot"] = w["shared9"][TP]
@@ -645,6 +652,8 @@ def cuda_arm(args, world, rank, local):
         line["cpu_baseline"] = cpu_baseline(cpu)
     if not args.no_configs:
         line["configs_isolated"] = isolated_configs(mt, cpu, w, dev, stream)
+        line["step_by_batch"] = dict(step_by_batch(mt, w, dev, stream, side),
+                                     b64={"us_per_step": round(ms * 1e3, 2), "tokens_per_s": round(units / max_s, 1)})
     print(json.dumps(line), flush=True)
     return 0
 
@@ -830,6 +839,39 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
             "method": ("each call alone: a graph of max(20, copies) calls cycling over copies of the call's large "
                        "inputs (together > 2x L2, at most 256 copies), median of 7 replays"),
             "results": res, "small_batch_us": small}
+
+
+def step_by_batch(mt, w, dev, stream, side, sizes=(1, 8, 32, 128)) -> dict:
+    """The same composed step at other batch sizes (fresh seeded activations,
+    the b = 64 workload's resident weights): graphs of 20 steps, median of 7
+    replays, per-step time and tokens/s."""
+    res = {}
+    for b in sizes:
+        _, wb = make_workload(dev, b, weights=w)
+        wb["composition"] = w.get("composition", "two_branch")
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                run_step(mt, wb, stream, side=side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(20):
+                run_step(mt, wb, stream, side=side)
+        ts = []
+        with torch.cuda.stream(stream):
+            g.replay()
+            for _ in range(7):
+                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                e.record(stream)
+                e.synchronize()
+                ts.append(a.elapsed_time(e) * 1e3 / 20)
+        us = statistics.median(ts)
+        res[f"b{b}"] = {"us_per_step": round(us, 2), "tokens_per_s": round(b / (us * 1e-6), 1)}
+        del wb, g
+    torch.cuda.synchronize()
+    return res
 
 
 def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
