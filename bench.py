@@ -42,7 +42,7 @@ METRIC = "MoE-tail tokens/s and µs/layer at b; achieved HBM GB/s vs ~8 TB/s pea
 B = 64                    # decode tokens per step
 TP, P, K_ROUTES, E = 8, 4096, 8, 128
 L, H, I = 3584, 7168, 6144
-LAUNCHES_PER_STEP = 6     # EP 1, TP 1, latent 2 (norm, up GEMM), shared 2 (gate/up, down)
+LAUNCHES_PER_STEP = 6     # b = 64: EP 1, TP 1, latent 2 (norm, up GEMM), shared 2 (gate/up, down)
 
 # Algorithmic bytes per call (reads + writes the method needs; intermediates
 # such as y and h that a fused kernel would keep on chip are not counted).
@@ -66,7 +66,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload isolated timings")
     ap.add_argument("--composition", default="two_branch",
-                    choices=["two_branch", "norm_main", "norm_side_first", "norm_side_after"],
+                    choices=["two_branch", "two_branch_split", "norm_main", "norm_side_first", "norm_side_after"],
                     help="how the step orders the weight-streaming calls (see run_step)")
     ap.add_argument("--sequential", action="store_true",
                     help="run the four calls in order on one stream (shared expert accumulating into out)")
@@ -222,12 +222,14 @@ def run_step(mt, w, stream, events=None, side=None):
     finalize calls, as the Kimi-K3 tail runs its shared expert (its output is
     pushed into the tail's reduce-scatter partials): on the side stream
     moe_shared_expert writes d = bf16(down(h)) into the last of the latent
-    tail's shared-partial slots, then the latent tail follows as its two calls
-    -- moe_tail_latent_norm (inputs ready: it reads the latent partials while
-    the down projection drains) and moe_tail_up_project (static weights: its
-    first weight tiles are requested during the norm), which adds d with the
-    other slots in its epilogue; EP and expert-TP finalize run on the main
-    stream, which joins the side stream at the end of the step.  Without a
+    tail's shared-partial slots, then moe_tail_latent_up_flags follows with
+    both promises -- inputs ready (the latent partials are read while the down
+    projection drains) and static weights (the first weight tiles are
+    requested before that wait) -- and adds d with the other slots in its
+    epilogue; the call enqueues the norm and the up-projection
+    ("two_branch_split" makes the two split calls, moe_tail_latent_norm and
+    moe_tail_up_project, with the same promises).  EP and expert-TP finalize run on the main stream, which joins
+    the side stream at the end of the step.  Without a
     side stream the calls run in order (moe_tail_latent_up in one call) and
     the shared expert accumulates into the latent tail's output."""
     ev = events or [None] * EVENTS_PER_STEP
@@ -268,7 +270,7 @@ def run_step(mt, w, stream, events=None, side=None):
         shared_expert(stream, w["out"], True)
         return
     comp = w.get("composition", "two_branch")
-    if comp != "two_branch":
+    if comp not in ("two_branch", "two_branch_split"):
         # the latent up-projection between the shared expert's gate/up and down
         # projections; down then adds d into the latent tail's output
         # (out = bf16(out + bf16(d)), the sequential composition's arithmetic)
@@ -307,12 +309,20 @@ def run_step(mt, w, stream, events=None, side=None):
     w["fork"].record(stream)
     side.wait_event(w["fork"])
     shared_expert(side, w["d_slot"], False)
-    rec(4, side)
-    mt.moe_tail_latent_norm(w["latent"], w["lat_gamma"], w["y"], eps=1e-6, inputs_ready=True, stream=side)
-    rec(5, side)
-    rec(6, side)
-    mt.moe_tail_up_project(w["y"], w["w_up"], w["shared9"], w["out"], weights_static=True, stream=side)
-    rec(7, side)
+    if comp == "two_branch_split":
+        rec(4, side)
+        mt.moe_tail_latent_norm(w["latent"], w["lat_gamma"], w["y"], eps=1e-6, inputs_ready=True, stream=side)
+        rec(5, side)
+        rec(6, side)
+        mt.moe_tail_up_project(w["y"], w["w_up"], w["shared9"], w["out"], weights_static=True, stream=side)
+        rec(7, side)
+    else:
+        rec(4, side)
+        mt.moe_tail_latent_up_flags(w["latent"], w["lat_gamma"], w["w_up"], w["shared9"], w["out"], w["y"],
+                                    eps=1e-6, inputs_ready=True, weights_static=True, stream=side)
+        rec(5, side)
+        rec(6, side)
+        rec(7, side)
     w["join"].record(side)
     ep(stream)
     tp(stream)
@@ -595,7 +605,7 @@ def cuda_arm(args, world, rank, local):
     calls = {}
     hbm, bf16_tf, peak_kind = peaks()
     nbytes = dict(BYTES)
-    if side is not None and args.composition == "two_branch":  # d written and read once as a partial slot
+    if side is not None and args.composition in ("two_branch", "two_branch_split"):  # d: one partial slot
         nbytes["shared_expert"] = 3 * I * H * 2 + B * H * 2 + B * H * 2
         nbytes["latent_up"] = BYTES["latent_up"] + B * H * 2
     for c in CALLS:
@@ -631,8 +641,11 @@ def cuda_arm(args, world, rank, local):
         "config": dict(workload_config(), composition=(
             "sequential: EP, TP, latent tail, then the shared expert accumulating into out" if side is None else
             "two branches: on a side stream the shared expert writes d into an extra shared-partial slot, then the "
-            "latent norm and up-projection follow, adding all slots; EP and TP on a high-priority stream beside them"
+            "latent tail follows (its norm, then its up-projection), adding all slots; "
+            "EP and TP on a high-priority stream beside them"
             if args.composition == "two_branch" else
+            "two branches as two_branch, with the latent tail always as its two split calls"
+            if args.composition == "two_branch_split" else
             f"two branches ({args.composition}): on a side stream the shared expert's gate/up, the latent "
             "up-projection, then the shared expert's down projection adding d into out; the latent norm "
             + {"norm_main": "first on the high-priority stream", "norm_side_first": "first on the side stream",

@@ -160,6 +160,32 @@ int moe_tail_up_project(const void* y, const void* w_up, const void* shared, int
                         void* out, int flags, void* stream);
 
 /*
+ * The latent tail in one call with the scheduling promises of the split calls
+ * ([KT] module docstring, as moe_tail_latent_up).  Same arguments as
+ * moe_tail_latent_up, with y (BF16 [b][L], written, 16-byte aligned,
+ * overlapping no other argument) in place of the workspace, plus
+ *   flags: any of MOE_TAIL_INPUTS_READY (latent and gamma, as for
+ *   moe_tail_latent_norm) and MOE_TAIL_WEIGHTS_STATIC (w_up, as for
+ *   moe_tail_up_project); shared is always read, and y and out written, after
+ *   the wait for the stream's preceding kernel.
+ * It runs moe_tail_latent_norm then moe_tail_up_project.  With the variable
+ * MOE_TAIL_LATENT_FUSED=1 in the environment it runs instead, wherever the
+ * sizes allow (b <= 32, L <= 8192, tp <= 8 x the ring's stages), one kernel
+ * in the pages' fused-tail shape ([KT] WaveMoeTail keeps the normalised
+ * latent on chip): the up-projection's CTAs form y for their own K range in
+ * shared memory -- each CTA sums and squares the 256-column chunks its range
+ * touches and the cluster exchanges the chunk sums -- and then stream the
+ * weights.  It is slower on GB300 at every batch size and so not the default.
+ * Both forms give bit for bit the same y and out as the two split calls;
+ * moe_tail_latent_up and moe_tail_latent_up_noalloc take the same path with
+ * flags 0 (the one-kernel form of the latter does not touch its scratch
+ * array).  Limits: those of moe_tail_latent_up.
+ */
+int moe_tail_latent_up_flags(const void* latent, const void* gamma, float eps, const void* w_up,
+                             const void* shared, int tp_s, int b, int tp, int L, int H, void* out, void* y,
+                             int flags, void* stream);
+
+/*
  * Fused shared expert ([KS] module docstring, SharedUmma.owned_h,
  * SharedBase.push): gate/up projection, gated activation, down projection,
  * added into the tail's output:

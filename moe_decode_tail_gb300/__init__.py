@@ -19,7 +19,7 @@ __all__ = [
     "moe_shared_expert", "moe_tail_workspace_bytes", "moe_tail_status_str", "moe_tail_take_device_error",
     "moe_tail_latent_up_noalloc", "NOALLOC_SCRATCH_BYTES", "moe_tail_selftest_wait_timeout",
     "moe_tail_latent_norm", "moe_tail_up_project", "WEIGHTS_STATIC", "INPUTS_READY",
-    "moe_shared_gate_up", "moe_shared_down",
+    "moe_shared_gate_up", "moe_shared_down", "moe_tail_latent_up_flags",
 ]
 
 OK, EINVAL, ECUDA, ENOTSUP = 0, 1, 2, 3
@@ -58,6 +58,7 @@ def lib() -> ctypes.CDLL:
         L.moe_tail_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
         L.moe_tail_latent_norm.argtypes = [P, P, f32, i32, i32, i32, P, i32, P]
         L.moe_tail_up_project.argtypes = [P, P, P, i32, i32, i32, i32, P, i32, P]
+        L.moe_tail_latent_up_flags.argtypes = [P, P, f32, P, P, i32, i32, i32, i32, i32, P, P, i32, P]
         L.moe_shared_gate_up.argtypes = [P, P, P, i32, i32, i32, P, i32, P]
         L.moe_shared_down.argtypes = [P, P, i32, i32, i32, P, i32, i32, P]
         L.moe_tail_workspace_bytes.argtypes = [i32, i32, i32]
@@ -67,7 +68,8 @@ def lib() -> ctypes.CDLL:
         L.moe_tail_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         for name in ("moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up", "moe_shared_expert",
                      "moe_tail_take_device_error", "moe_tail_latent_up_noalloc", "moe_tail_selftest_wait_timeout",
-                     "moe_tail_latent_norm", "moe_tail_up_project", "moe_shared_gate_up", "moe_shared_down"):
+                     "moe_tail_latent_norm", "moe_tail_up_project", "moe_shared_gate_up", "moe_shared_down",
+                     "moe_tail_latent_up_flags"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -147,6 +149,25 @@ def moe_tail_latent_up(latent, gamma, w_up, shared, out, workspace, *, eps=1e-6,
     _check("moe_tail_latent_up", lib().moe_tail_latent_up(
         _p(latent), _p(gamma), eps, _p(w_up), _p(shared), tp_s, b, tp, L, H, _p(out), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def moe_tail_latent_up_flags(latent, gamma, w_up, shared, out, y, *, eps=1e-6, inputs_ready=False,
+                             weights_static=False, stream=None) -> torch.Tensor:
+    """The latent tail into out (BF16 [b, H]) and y (BF16 [b, L]), with the
+    split calls' promises: inputs_ready (latent and gamma, as for
+    moe_tail_latent_norm) and weights_static (w_up, as for moe_tail_up_project).
+    The norm and the up-projection, or with MOE_TAIL_LATENT_FUSED=1 in the
+    environment one kernel that forms y on chip (slower on GB300); the result
+    is bit for bit that of the two split calls either way."""
+    _cuda(latent, gamma, w_up, shared, out, y)
+    tp, b, L = latent.shape
+    H = w_up.shape[0]
+    tp_s = 0 if shared is None else shared.shape[0]
+    flags = (INPUTS_READY if inputs_ready else 0) | (WEIGHTS_STATIC if weights_static else 0)
+    _check("moe_tail_latent_up_flags", lib().moe_tail_latent_up_flags(
+        _p(latent), _p(gamma), eps, _p(w_up), _p(shared), tp_s, b, tp, L, H, _p(out), _p(y), flags,
+        _stream(stream)))
     return out
 
 

@@ -166,7 +166,50 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 struct GemmSmem {  // offsets from the 1024-aligned base of dynamic shared memory
   uint32_t ring, full, empty, accum, tmem_slot, abort_flag;
+  // latent tail in one kernel: y operand, chunk sums, 1/rms, gamma of the K
+  // range; y ready for the MMA; latent loads issued (the weights may follow)
+  uint32_t yop, ss, inv, gam, ybar, latbar;
 };
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+// Barrier 1 over the four epilogue warps only.
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Byte offset, in a K-major operand tile of 128-byte rows written with the
+// 128-byte swizzle, of the 16-byte unit u (columns 8u..8u+7) of row r: the
+// unit index is XORed with the row's position in its 8-row group, as a TMA
+// box lands with CU_TENSOR_MAP_SWIZZLE_128B (tile bases 1024-aligned).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int u) {
+  return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4));
+}
+
+// Cluster rank whose K range holds K block kb under the even split of
+// kblocks over ksplit ranks (the first kb_rem ranks take one more).
+__device__ __forceinline__ uint32_t kblock_owner(int kb, int kb_per, int kb_rem) {
+  const int big = kb_rem * (kb_per + 1);
+  return (uint32_t)(kb < big ? kb / (kb_per + 1) : kb_rem + (kb - big) / kb_per);
+}
 
 // TM = weight rows per CTA: 64 (one M=64 MMA), 128 (one M=128 MMA) or 256
 // (two M=128 MMAs per K step sharing the token tile, into two accumulators
@@ -174,15 +217,30 @@ struct GemmSmem {  // offsets from the 1024-aligned base of dynamic shared memor
 // in TMEM lane r; with M = 64 it sits in lane 32 * (r / 16) + r % 16 (lanes
 // 16..31 of each warp's quarter stay unused).  Gate/up tiles hold TM/2 gate
 // rows then the TM/2 matching up rows.
+//
+// kGemmLatentUp is the whole latent tail in one kernel (Kimi-K3 tail runtime
+// page, module docstring: latent sum over the slots, RMS norm, up-projection,
+// shared partials): instead of loading token tiles, the epilogue warps form y
+// for the CTA's K range in shared memory, in the swizzled operand layout, while
+// the weight ring fills.  Each CTA forms x (the slot sum, rounded to BF16) for
+// every 256-column chunk its K range touches, with the chunk's sum of squares
+// in the finalize kernels' canonical tree (lane l: columns 8l..8l+7 in order,
+// xor butterfly); after one cluster barrier each token's chunk sums are read
+// from the CTA that holds the chunk's first K block and added in chunk order
+// from +0, so y is bit for bit the norm kernel's y.  The K split and the MMA
+// sequence are the up-projection's, so out is bit for bit the two-kernel
+// result as well.
 template <int MODE, int N, int TM>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
                        const __grid_constant__ CUtensorMap map_x, const GemmArgs a, const int stages) {
   MOE_TRACE_SCOPE(30 + MODE);
   extern __shared__ uint8_t smem_raw[];
+  constexpr bool kFused = MODE == kGemmLatentUp;
+  constexpr bool kUp = MODE == kGemmUpShared || kFused;  // out = bf16(acc + slot sum of shared)
   constexpr int kATile = TM * kBlockK * 2;
   constexpr int kBTileBytes = N * kBlockK * 2;
-  constexpr int kStageBytes = kATile + kBTileBytes;
+  constexpr int kStageBytes = kFused ? kATile : kATile + kBTileBytes;
   constexpr int kMmaM = TM == 64 ? 64 : 128;
   constexpr int kNumAcc = TM / kMmaM;
   constexpr uint32_t kTmemCols = N * kNumAcc < 32 ? 32 : N * kNumAcc;
@@ -204,10 +262,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base_ptr = smem_raw + (base - raw);
   GemmSmem L;
   L.ring = base;
-  L.full = base + stages * kStageBytes;
+  uint32_t tail = base + stages * kStageBytes;
+  if (kFused) {  // y operand of the CTA's K range, chunk sums [N][chunks], 1/rms [N]
+    L.yop = tail;  // 1024-aligned: kATile is a multiple of 1024
+    tail += (uint32_t)((kb_per + (kb_rem > 0 ? 1 : 0)) * kBTileBytes);
+    L.ss = tail;
+    tail += (uint32_t)(4 * N * a.chunks);
+    L.inv = tail;
+    tail += 4u * N;
+    L.gam = tail;  // 16-aligned: the offsets before it are multiples of 64
+    tail = (tail + (uint32_t)((kb_per + (kb_rem > 0 ? 1 : 0)) * kBlockK * 2) + 7u) & ~7u;
+  }
+  L.full = tail;
   L.empty = L.full + 8 * stages;
   L.accum = L.empty + 8 * stages;
-  L.tmem_slot = L.accum + 8;
+  L.ybar = L.accum + 8;
+  L.latbar = L.accum + 16;
+  L.tmem_slot = L.accum + (kFused ? 24 : 8);
   L.abort_flag = L.tmem_slot + 4;
   volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (L.tmem_slot - base));
   volatile uint32_t* abort_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (L.abort_flag - base));
@@ -218,11 +289,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(L.empty + 8 * s, 1);
     }
     mbar_init(L.accum, 1);
+    if (kFused) {
+      mbar_init(L.ybar, 128);
+      mbar_init(L.latbar, 128);
+    }
     *abort_ptr = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_w0);
     if (MODE == kGemmGateUpSilu) prefetch_map(&map_w1);
-    prefetch_map(&map_x);
+    if (!kFused) prefetch_map(&map_x);
   }
   if (warp == 5) tmem_alloc(L.tmem_slot, kTmemCols);
   tc_fence_before();
@@ -230,6 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot_ptr;
   launch_dependents();  // the next kernel may be scheduled as this one's CTAs retire
+  // The epilogue warps exchange chunk sums over one cluster barrier; the
+  // producer and MMA warps take part in it without waiting here.
+  if (kFused && ksplit > 1 && warp >= 4) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   // Tokens whose outputs this CTA finishes (the tile's tokens split over the cluster).
   const int n_valid = min(N, a.n_tok - tok0);
@@ -243,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // depend on the accumulator, so the four epilogue warps gather it while the
   // K loop runs when each holds at most kPre items.
   constexpr int kPre = 4;
-  const bool has_addend = MODE == kGemmUpShared ? a.shared != nullptr : (MODE == kGemmDown && a.accumulate != 0);
+  const bool has_addend = kUp ? a.shared != nullptr : (MODE == kGemmDown && a.accumulate != 0);
   const bool pre = has_addend && n_items <= 128 * kPre;
   float4 pre_add[kPre];
   auto addend = [&](int item) -> float4 {
@@ -251,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = m_tile * kOutRows + 4 * (item % kQuads);
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (n >= a.M) return v;
-    if (MODE == kGemmUpShared) {  // slot order, from +0
+    if (kUp) {  // slot order, from +0
       for (int s = 0; s < a.tp_s; ++s) {
         const uint2 sv = *reinterpret_cast<const uint2*>(a.shared + ((int64_t)s * a.n_tok + tg) * a.M + n);
         v.x = __fadd_rn(v.x, bf16_lo(sv.x)); v.y = __fadd_rn(v.y, bf16_hi(sv.x));
@@ -275,6 +353,123 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
+  // Fused mode, the four epilogue warps: y of the tile's tokens over this
+  // CTA's K range into the operand tile, then release it to the MMA warp.
+  auto form_y = [&]() {
+    constexpr int kChunk = 256, kKbPerChunk = kChunk / kBlockK;
+    const int c_first = kb0 / kKbPerChunk;
+    const int ncc = nk > 0 ? (kb0 + nk - 1) / kKbPerChunk - c_first + 1 : 0;  // chunks the range touches
+    const int n_work = n_valid * ncc;                                          // (token, chunk) items
+    float* ss_sm = reinterpret_cast<float*>(base_ptr + (L.ss - base));
+    float* inv_sm = reinterpret_cast<float*>(base_ptr + (L.inv - base));
+    const int64_t slot_stride = (int64_t)a.n_tok * a.K;
+    if (!a.inputs_before_wait) grid_dependency_wait();
+    // gamma of the K range into shared memory, asynchronously (read in step 3)
+    const int gvecs = nk * (kBlockK / 8);
+    for (int v = threadIdx.x; v < gvecs; v += 128)
+      if (kb0 * kBlockK + 8 * v < a.K) cp_async_16(L.gam + 16u * v, a.gamma + kb0 * kBlockK + 8 * v);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    // 1. x = bf16(slot sum) of whole chunks (a warp per token and chunk; lane
+    //    l holds columns 8l..8l+7), the chunk's sum of squares, and x of the
+    //    CTA's own K blocks into the operand tile.  The latent rows are staged
+    //    with cp.async in the weight ring, which is still empty: each warp
+    //    takes a quarter of it, so a batch of items is one trip to memory made
+    //    before the CTA's weight stream starts.  Rows of padding tokens are left
+    //    as they are: they only feed accumulator columns that are never read.
+    const uint32_t quarter = (uint32_t)(stages * kStageBytes / 4) & ~511u;
+    const int per_batch = max(1, (int)(quarter / (uint32_t)(a.tp * 512)));  // the host keeps this >= 1
+    const uint32_t wstage = L.ring + (uint32_t)warp * quarter;
+    const int my_items = warp < n_work ? (n_work - warp + 3) / 4 : 0;  // items warp + 4j
+    for (int j0 = 0; j0 < my_items; j0 += per_batch) {
+      const int nb = min(per_batch, my_items - j0);
+      for (int j = 0; j < nb; ++j) {
+        const int it = warp + 4 * (j0 + j);
+        const int t = it / ncc, c = c_first + (it - t * ncc);
+        const int col = c * kChunk + 8 * lane;
+        if (col < a.K) {
+          const uint16_t* src = a.latent + (int64_t)(tok0 + t) * a.K + col;
+          for (int sl = 0; sl < a.tp; ++sl)
+            cp_async_16(wstage + (uint32_t)(((j * a.tp + sl) * 32 + lane) * 16), src + (int64_t)sl * slot_stride);
+        }
+      }
+      cp_async_wait_all();  // this lane's own copies (and gamma's)
+      for (int j = 0; j < nb; ++j) {
+        const int it = warp + 4 * (j0 + j);
+        const int t = it / ncc, c = c_first + (it - t * ncc);
+        const int col = c * kChunk + 8 * lane;
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = 0.0f;
+        if (col < a.K) {
+          for (int sl = 0; sl < a.tp; ++sl) {  // slot order, FP32 from +0
+            float f[8];
+            unpack8(ld_shared_v4(wstage + (uint32_t)(((j * a.tp + sl) * 32 + lane) * 16)), f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = __fadd_rn(x[i], f[i]);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = bf16_round(x[i]);
+        }
+        float acc = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, __fmul_rn(x[i], x[i]));
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+        if (lane == 0) ss_sm[t * a.chunks + c] = acc;
+        const int kb = c * kKbPerChunk + (lane >> 3);
+        if (kb >= kb0 && kb < kb0 + nk) {  // x is BF16-exact: the high half of each float is its BF16
+          uint4 pk;
+          pk.x = (__float_as_uint(x[0]) >> 16) | (__float_as_uint(x[1]) & 0xffff0000u);
+          pk.y = (__float_as_uint(x[2]) >> 16) | (__float_as_uint(x[3]) & 0xffff0000u);
+          pk.z = (__float_as_uint(x[4]) >> 16) | (__float_as_uint(x[5]) & 0xffff0000u);
+          pk.w = (__float_as_uint(x[6]) >> 16) | (__float_as_uint(x[7]) & 0xffff0000u);
+          st_shared_v4(L.yop + (uint32_t)((kb - kb0) * kBTileBytes) + sw128_offset(t, lane & 7), pk);
+        }
+      }
+      __syncwarp();  // the batch's staging is read before the next batch overwrites it
+    }
+    cp_async_wait_all();  // gamma, where this thread had no latent batch
+    // the ring is free for the weights (ordered before the async proxy's writes)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive(L.latbar);
+    MOE_TRACE_MARK(1);  // fused: latent rows read, x and chunk sums formed
+    if (ksplit > 1) cluster_sync_all();  // chunk sums published (producer and MMA warps arrived at entry)
+    else epilogue_bar();
+    // 2. per token: the chunk sums in chunk order from +0, then 1/rms; chunk c
+    //    is read from the CTA whose K range holds its first K block.
+    for (int t = warp; t < n_valid; t += 4) {
+      float v = 0.0f;
+      if (lane < a.chunks) {
+        const uint32_t owner = ksplit > 1 ? kblock_owner(kKbPerChunk * lane, kb_per, kb_rem) : 0u;
+        const int idx = t * a.chunks + lane;
+        v = owner == rank ? ss_sm[idx] : ld_cluster_f32(map_to_rank(L.ss + (uint32_t)(4 * idx), owner));
+      }
+      float ss = 0.0f;
+      for (int c = 0; c < a.chunks; ++c) ss = __fadd_rn(ss, __shfl_sync(0xffffffffu, v, c));
+      if (lane == 0) inv_sm[t] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, a.rcpK), a.eps)));
+    }
+    epilogue_bar();  // 1/rms and gamma (each thread waited for its copies) for every warp
+    // 3. y = bf16((x * inv) * gamma), -0 made +0, in place.
+    for (int it = warp; it < n_work; it += 4) {
+      const int t = it / ncc, c = c_first + (it - t * ncc);
+      const int kb = c * kKbPerChunk + (lane >> 3);
+      const int col = c * kChunk + 8 * lane;
+      if (kb < kb0 || kb >= kb0 + nk || col >= a.K) continue;  // outside the range, or zeros past K
+      const uint32_t addr = L.yop + (uint32_t)((kb - kb0) * kBTileBytes) + sw128_offset(t, lane & 7);
+      float x[8], g[8], yv[8];
+      unpack8(ld_shared_v4(addr), x);
+      unpack8(ld_shared_v4(L.gam + (uint32_t)(2 * (col - kb0 * kBlockK))), g);
+      const float inv = inv_sm[t];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) yv[i] = __fmul_rn(__fmul_rn(x[i], inv), __fadd_rn(g[i], 0.0f));
+      st_shared_v4(addr, make_uint4(pack_bf16x2_pz(yv[0], yv[1]), pack_bf16x2_pz(yv[2], yv[3]),
+                                    pack_bf16x2_pz(yv[4], yv[5]), pack_bf16x2_pz(yv[6], yv[7])));
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor-core reads
+    mbar_arrive(L.ybar);
+    MOE_TRACE_MARK(2);  // fused: y in the operand tile
+  };
+
   if (warp == 4) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
@@ -287,13 +482,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // for it; the first kernel of a call waits first.
       const int pre = min(nk, stages);
       if (!a.weights_before_wait) grid_dependency_wait();
+      if (kFused && !mbar_wait(L.latbar, 0)) {  // the ring holds the latent rows until y's inputs are read
+        raise_error(kErrWaitFull);
+        *abort_ptr = 1;
+      }
       for (int i = 0; i < pre; ++i) {
         mbar_expect_tx(L.full + 8 * i, kStageBytes);
         load_weights(L.ring + i * kStageBytes, L.full + 8 * i, kb0 + i, stream);
       }
-      if (a.weights_before_wait) grid_dependency_wait();
-      for (int i = 0; i < pre; ++i)
-        tma_load_2d(L.ring + i * kStageBytes + kATile, &map_x, L.full + 8 * i, (kb0 + i) * kBlockK, tok0, keep);
+      if (!kFused) {  // the token tiles are the preceding kernel's output
+        if (a.weights_before_wait) grid_dependency_wait();
+        for (int i = 0; i < pre; ++i)
+          tma_load_2d(L.ring + i * kStageBytes + kATile, &map_x, L.full + 8 * i, (kb0 + i) * kBlockK, tok0, keep);
+      }
       issued = pre;
       for (int i = pre; i < nk; ++i) {
         const int s = i % stages;
@@ -308,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bar = L.full + 8 * s;
         mbar_expect_tx(bar, kStageBytes);
         load_weights(st, bar, kb0 + i, stream);
-        tma_load_2d(st + kATile, &map_x, bar, (kb0 + i) * kBlockK, tok0, keep);
+        if (!kFused) tma_load_2d(st + kATile, &map_x, bar, (kb0 + i) * kBlockK, tok0, keep);
         ++issued;
       }
       if (!ok) {  // let the copies already in flight land before the CTA's memory goes away
@@ -319,9 +520,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
-    grid_dependency_wait();
+    if (!kFused) grid_dependency_wait();  // fused: reads shared memory only
     if (lane == 0) {
-      for (int i = 0; i < nk; ++i) {
+      bool ok = true;
+      if (kFused) {  // y is in shared memory (and visible to the tensor cores)
+        ok = mbar_wait(L.ybar, 0);
+        if (!ok) {
+          raise_error(kErrWaitFull);
+          *abort_ptr = 1;
+        }
+        tc_fence_after();
+      }
+      for (int i = 0; ok && i < nk; ++i) {
         const int s = i % stages;
         if (!mbar_wait(L.full + 8 * s, (uint32_t)(i / stages) & 1u)) {
           raise_error(kErrWaitFull);
@@ -331,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t st = L.ring + s * kStageBytes;
         const uint64_t adesc = smem_desc_sw128(st);
-        const uint64_t bdesc = smem_desc_sw128(st + kATile);
+        const uint64_t bdesc = smem_desc_sw128(kFused ? L.yop + (uint32_t)(i * kBTileBytes) : st + kATile);
 #pragma unroll
         for (int kk = 0; kk < kBlockK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
 #pragma unroll
@@ -344,13 +554,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- accumulator -> FP32 staging tile [N tokens][TM rows] ----------------
-    grid_dependency_wait();
+    // ---------------- (fused: y) accumulator -> FP32 staging tile [N tokens][TM rows] ----------------
+    if (kFused) {
+      form_y();
+      if (a.inputs_before_wait) grid_dependency_wait();  // before the shared partials and any store
+    } else {
+      grid_dependency_wait();
+    }
     if (pre) {
 #pragma unroll
       for (int j = 0; j < kPre; ++j) {
         const int item = threadIdx.x + 128 * j;
         if (item < n_items) pre_add[j] = addend(item);
+      }
+    }
+    if (kFused && a.y != nullptr && m_tile == 0) {  // y of the CTA's K range, from the operand tile
+      const int vecs = nk * (kBlockK / 8);
+      for (int e = threadIdx.x; e < n_valid * vecs; e += 128) {
+        const int t = e / vecs, v = e - t * vecs;
+        const int col = kb0 * kBlockK + 8 * v;
+        if (col < a.K)
+          st_v4(a.y + (int64_t)(tok0 + t) * a.K + col,
+                ld_shared_v4(L.yop + (uint32_t)((v >> 3) * kBTileBytes) + sw128_offset(t, v & 7)));
       }
     }
     const bool got = mbar_wait(L.accum, 0);
@@ -381,11 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
   }
+  if (kFused && ksplit > 1 && warp >= 4) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   __syncthreads();
   const bool aborted = *abort_ptr != 0;
-  MOE_TRACE_MARK(1);                   // partial tile staged
+  if (!kFused) MOE_TRACE_MARK(1);      // partial tile staged
   if (ksplit > 1) cluster_sync_all();  // every CTA's partial tile is staged
-  MOE_TRACE_MARK(2);
+  if (!kFused) MOE_TRACE_MARK(2);
 
   // ---------------- rank-order reduction over the cluster + fused epilogue ----------------
   auto finish_item = [&](int item, float4 add) {
@@ -419,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = m_tile * kOutRows + 4 * q;
       if (n >= a.M) return;
       const float ad[4] = {add.x, add.y, add.z, add.w};
-      if (MODE == kGemmUpShared) {  // out = bf16(acc + slot sum of the shared partials)
+      if (kUp) {  // out = bf16(acc + slot sum of the shared partials)
         if (has_addend) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) r[e] = __fadd_rn(r[e], ad[e]);
@@ -484,6 +710,7 @@ static int stage_bytes(int tm, int n_tile) { return tm * kBlockK * 2 + n_tile * 
 
 // Plan override for tuning: MOE_TAIL_GEMM_PLAN_<UP|GATEUP|DOWN>="tm,ksplit,stages".
 static bool plan_override(int mode, GemmPlan& p) {
+  if (mode < 0 || mode > 2) return false;
   const char* names[3] = {"MOE_TAIL_GEMM_PLAN_UP", "MOE_TAIL_GEMM_PLAN_GATEUP", "MOE_TAIL_GEMM_PLAN_DOWN"};
   const char* v = getenv(names[mode]);
   int tm = 0, ks = 0, st = 0;
@@ -532,15 +759,49 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms) {
   return p;
 }
 
-static size_t smem_bytes(const GemmPlan& p) {
+// Fused latent tail: everything but the weight ring (alignment slack, the y
+// operand of the longest K range, chunk sums, 1/rms, barriers and slots).
+static size_t fused_fixed_bytes(int n_tile, int kblocks, int ksplit, int chunks) {
+  const size_t per_cta = (size_t)((kblocks + ksplit - 1) / ksplit);
+  return 1024 + per_cta * n_tile * kBlockK * 2 + 4 * (size_t)n_tile * chunks + 4 * (size_t)n_tile +
+         per_cta * kBlockK * 2 + 8 + 8 + 8 + 8 + 8 + 64;
+}
+
+static size_t smem_bytes(const GemmPlan& p, int mode, const GemmArgs& a) {
+  if (mode == kGemmLatentUp)
+    return fused_fixed_bytes(p.n_tile, a.kblocks, p.ksplit, a.chunks) +
+           (size_t)p.stages * (p.tm * kBlockK * 2 + 16);
   return 1024 + (size_t)p.stages * stage_bytes(p.tm, p.n_tile) + 16 * (size_t)p.stages + 8 + 8 + 64;
+}
+
+// Two fused CTAs per SM: 2 x (this + the 1 KB the hardware keeps per CTA)
+// within an SM's 228 KB of shared memory.
+constexpr size_t kFusedSmemCap = 112 * 1024;
+
+bool plan_latent_fused(int H, int L, int b, int tp, int sms, GemmPlan* plan) {
+  const int chunks = (L + 255) / 256;
+  if (b < 1 || b > 32 || chunks > 32 || tp < 1) return false;
+  GemmPlan p = plan_gemm(kGemmUpShared, H, L, b, sms);  // the two-kernel tiles and K split
+  if (p.tm != 128 || p.n_tile > 32) return false;
+  const int kblocks = (L + kBlockK - 1) / kBlockK;
+  const size_t fixed = fused_fixed_bytes(p.n_tile, kblocks, p.ksplit, chunks);
+  const size_t a_tile = (size_t)p.tm * kBlockK * 2, per_stage = a_tile + 16;
+  if (fixed + 2 * per_stage > kFusedSmemCap) return false;
+  // as many stages as fit: the ring also stages the latent rows (a quarter per
+  // epilogue warp, which must hold one item's tp rows of 512 bytes)
+  p.stages = (int)std::min<size_t>((kFusedSmemCap - fixed) / per_stage, (size_t)kMaxStages);
+  if ((size_t)tp * 512 > (p.stages * a_tile / 4 & ~(size_t)511)) return false;
+  // the FP32 staging tile [n_tile][tm] reuses the ring
+  if ((size_t)p.stages * a_tile < (size_t)p.n_tile * p.tm * 4) return false;
+  *plan = p;
+  return true;
 }
 
 template <int MODE, int N, int TM>
 static cudaError_t launch_t(const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& x,
                             const GemmArgs& a, bool pdl, cudaStream_t stream) {
   auto kernel = decode_gemm_kernel<MODE, N, TM>;
-  const size_t smem = smem_bytes(p);
+  const size_t smem = smem_bytes(p, MODE, a);
   // Raise the kernel's shared-memory limit once per device (not per call, so
   // that a captured stream sees only launches).
   static int configured[64] = {0};
@@ -602,6 +863,11 @@ cudaError_t launch_decode_gemm(int mode, const GemmPlan& p, const CUtensorMap& w
     case kGemmUpShared: return launch_mode<kGemmUpShared>(p, w0, w1, x, a, pdl, stream);
     case kGemmGateUpSilu: return launch_mode<kGemmGateUpSilu>(p, w0, w1, x, a, pdl, stream);
     case kGemmDown: return launch_mode<kGemmDown>(p, w0, w1, x, a, pdl, stream);
+    case kGemmLatentUp:  // built for the small batches plan_latent_fused admits
+      if (p.tm != 128 || a.chunks < 1 || a.chunks > 32) return cudaErrorInvalidValue;
+      if (p.n_tile == 16) return launch_t<kGemmLatentUp, 16, 128>(p, w0, w1, x, a, pdl, stream);
+      if (p.n_tile == 32) return launch_t<kGemmLatentUp, 32, 128>(p, w0, w1, x, a, pdl, stream);
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }

@@ -34,7 +34,7 @@ cudaError_t take_finalize_error(unsigned* bits);
 
 // ---- decode GEMM (tcgen05) ---------------------------------------------------
 
-enum GemmMode { kGemmUpShared = 0, kGemmGateUpSilu = 1, kGemmDown = 2 };
+enum GemmMode { kGemmUpShared = 0, kGemmGateUpSilu = 1, kGemmDown = 2, kGemmLatentUp = 3 };
 
 struct GemmArgs {
   int M;             // output features of one weight (rows of W; gate/up: I)
@@ -46,6 +46,14 @@ struct GemmArgs {
   uint16_t* out;     // mode 0, 2: BF16 [b][M]; mode 1: h BF16 [b][M]
   int accumulate;    // mode 2: out = bf16(out + bf16(d))
   int weights_before_wait;  // 1 only when the preceding kernel is this library's own
+  // mode 3 (latent tail in one kernel: y formed in shared memory, then mode 0's product)
+  const uint16_t* latent = nullptr;  // BF16 [tp][n_tok][K]
+  const uint16_t* gamma = nullptr;   // BF16 [K]
+  uint16_t* y = nullptr;             // BF16 [n_tok][K], written by the first M tile's CTAs, or null
+  int tp = 0;
+  float eps = 0.f, rcpK = 0.f;
+  int chunks = 0;                    // 256-column chunks of K (at most 32)
+  int inputs_before_wait = 0;        // latent and gamma complete before the preceding kernel ends
 };
 
 struct GemmPlan {
@@ -57,6 +65,13 @@ struct GemmPlan {
 };
 
 GemmPlan plan_gemm(int mode, int M, int K, int b, int sms);
+// The one-kernel latent tail's plan at b tokens and tp slots: the
+// up-projection's tiles and K split (so the product is bit for bit the
+// two-kernel one) and a ring that fits beside the CTA's y operand and can
+// stage a token's tp latent rows per epilogue warp; false where that is not
+// possible (more than 32 tokens, more than 32 chunks of 256 columns, a plan
+// override with other tiles, too little shared memory).
+bool plan_latent_fused(int H, int L, int b, int tp, int sms, GemmPlan* plan);
 cudaError_t launch_decode_gemm(int mode, const GemmPlan& plan, const CUtensorMap& w0, const CUtensorMap& w1,
                                const CUtensorMap& x, const GemmArgs& a, bool pdl, cudaStream_t stream);
 
@@ -66,6 +81,17 @@ cudaError_t enqueue_latent_norm(const void* latent, const void* gamma, float eps
                                 bool inputs_ready, cudaStream_t st);
 int enqueue_up_project(const void* y, const void* w_up, const void* shared, int tp_s, int b, int L, int H, void* out,
                        bool weights_before_wait, cudaStream_t st);
+// The whole latent tail in one kernel (kGemmLatentUp)?  Only when the
+// variable MOE_TAIL_LATENT_FUSED=1 asks for it and plan_latent_fused finds a
+// plan at these sizes (the two-kernel form is faster on GB300).
+bool latent_tail_fused(int b, int tp, int L, int H, GemmPlan* plan);
+// Enqueue it (y: BF16 [b][L] written, or null); flags as moe_tail_latent_up_flags.
+int enqueue_latent_fused(const GemmPlan& plan, const void* latent, const void* gamma, float eps, const void* w_up,
+                         const void* shared, int tp_s, int b, int tp, int L, int H, void* out, void* y, int flags,
+                         cudaStream_t st);
+// Either form, as moe_tail_latent_up_flags (y required).
+int enqueue_latent_tail(const void* latent, const void* gamma, float eps, const void* w_up, const void* shared,
+                        int tp_s, int b, int tp, int L, int H, void* out, void* y, int flags, cudaStream_t st);
 
 // Read and clear the device error word (synchronises with the device).
 cudaError_t take_device_error(unsigned* bits);

@@ -224,6 +224,60 @@ int enqueue_up_project(const void* y, const void* w_up, const void* shared, int 
   return finish(moetail::launch_decode_gemm(moetail::kGemmUpShared, plan, mw, mw, mx, g, true, st));
 }
 
+// The one-kernel form is taken only on request (MOE_TAIL_LATENT_FUSED=1):
+// measured on GB300 it is slower than the norm kernel followed by the
+// up-projection at every batch size (b = 1: 14.5 vs 13.9 us in one call,
+// 12.3 vs 10.5 us with both promises).  Its CTAs form y on the MMA's critical
+// path -- a trip for the latent rows under the weight stream's load, the
+// cluster exchange, then y -- and every M tile's cluster re-reads the latent
+// partials, while the separate norm runs ahead of the weight stream under
+// programmatic dependent launch.
+bool latent_tail_fused(int b, int tp, int L, int H, GemmPlan* plan) {
+  const char* v = getenv("MOE_TAIL_LATENT_FUSED");
+  if (!(v && atoi(v) == 1)) return false;
+  return moetail::plan_latent_fused(H, L, b, tp, device_sms(), plan);
+}
+
+int enqueue_latent_fused(const GemmPlan& plan, const void* latent, const void* gamma, float eps, const void* w_up,
+                         const void* shared, int tp_s, int b, int tp, int L, int H, void* out, void* y, int flags,
+                         cudaStream_t st) {
+  CUtensorMap mw;
+  if (!encode_bf16_2d(&mw, w_up, H, L, plan.tm, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) return MOE_TAIL_ECUDA;
+  GemmArgs g;
+  g.M = H;
+  g.K = L;
+  g.n_tok = b;
+  g.kblocks = (L + 63) / 64;
+  g.shared = static_cast<const uint16_t*>(shared);
+  g.tp_s = tp_s;
+  g.out = static_cast<uint16_t*>(out);
+  g.accumulate = 0;
+  g.weights_before_wait = (flags & MOE_TAIL_WEIGHTS_STATIC) ? 1 : 0;
+  g.latent = static_cast<const uint16_t*>(latent);
+  g.gamma = static_cast<const uint16_t*>(gamma);
+  g.y = static_cast<uint16_t*>(y);
+  g.tp = tp;
+  g.eps = eps;
+  g.rcpK = (float)(1.0 / (double)L);
+  g.chunks = (L + 255) / 256;
+  g.inputs_before_wait = (flags & MOE_TAIL_INPUTS_READY) ? 1 : 0;
+  // the token-tile map is not used by this mode
+  return finish(moetail::launch_decode_gemm(moetail::kGemmLatentUp, plan, mw, mw, mw, g, true, st));
+}
+
+int enqueue_latent_tail(const void* latent, const void* gamma, float eps, const void* w_up, const void* shared,
+                        int tp_s, int b, int tp, int L, int H, void* out, void* y, int flags, cudaStream_t st) {
+  GemmPlan plan;
+  if (latent_tail_fused(b, tp, L, H, &plan))
+    return enqueue_latent_fused(plan, latent, gamma, eps, w_up, shared, tp_s, b, tp, L, H, out, y, flags, st);
+  // 1. y, 2. the up-projection; the GEMM follows this call's own norm kernel,
+  // which never writes w_up, so it requests its weights before waiting.
+  const cudaError_t e =
+      enqueue_latent_norm(latent, gamma, eps, b, tp, L, y, (flags & MOE_TAIL_INPUTS_READY) != 0, st);
+  if (e != cudaSuccess) return finish(e);
+  return enqueue_up_project(y, w_up, shared, tp_s, b, L, H, out, true, st);
+}
+
 }  // namespace moetail
 
 namespace {
@@ -259,12 +313,30 @@ MOE_API int moe_tail_latent_up(const void* latent, const void* gamma, float eps,
       overlaps(o, ws) || overlaps(ws, span(latent, (size_t)tp * b * L * 2)) || overlaps(ws, span(w_up, (size_t)H * L * 2)) ||
       overlaps(ws, span(shared, (size_t)tp_s * b * H * 2)) || overlaps(ws, span(gamma, (size_t)L * 2)))
     return MOE_TAIL_EINVAL;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // 1. y (in the workspace), 2. the up-projection; the GEMM follows this
-  // call's own norm kernel, which never writes w_up.
-  const cudaError_t e = enqueue_latent_norm(latent, gamma, eps, b, tp, L, workspace, false, st);
-  if (e != cudaSuccess) return finish(e);
-  return enqueue_up_project(workspace, w_up, shared, tp_s, b, L, H, out, true, st);
+  return moetail::enqueue_latent_tail(latent, gamma, eps, w_up, shared, tp_s, b, tp, L, H, out, workspace, 0,
+                                      static_cast<cudaStream_t>(stream));
+}
+
+MOE_API int moe_tail_latent_up_flags(const void* latent, const void* gamma, float eps, const void* w_up,
+                                     const void* shared, int tp_s, int b, int tp, int L, int H, void* out, void* y,
+                                     int flags, void* stream) {
+  if (!latent_sizes_ok(b, tp, L) || !up_sizes_ok(b, tp_s, L, H)) return MOE_TAIL_EINVAL;
+  if (flags & ~(MOE_TAIL_INPUTS_READY | MOE_TAIL_WEIGHTS_STATIC)) return MOE_TAIL_EINVAL;
+  if (b == 0) return MOE_TAIL_OK;
+  if (!latent || !gamma || !w_up || !out || !y) return MOE_TAIL_EINVAL;
+  if ((tp_s > 0) != (shared != nullptr)) return MOE_TAIL_EINVAL;
+  if (!aligned(latent, 16) || !aligned(gamma, 16) || !aligned(w_up, 16) || !aligned(out, 16) || !aligned(y, 16) ||
+      (shared && !aligned(shared, 16)))
+    return MOE_TAIL_EINVAL;
+  const Range o = span(out, (size_t)b * H * 2);
+  const Range yr = span(y, (size_t)b * L * 2);
+  if (overlaps(o, span(latent, (size_t)tp * b * L * 2)) || overlaps(o, span(gamma, (size_t)L * 2)) ||
+      overlaps(o, span(w_up, (size_t)H * L * 2)) || overlaps(o, span(shared, (size_t)tp_s * b * H * 2)) ||
+      overlaps(o, yr) || overlaps(yr, span(latent, (size_t)tp * b * L * 2)) || overlaps(yr, span(w_up, (size_t)H * L * 2)) ||
+      overlaps(yr, span(shared, (size_t)tp_s * b * H * 2)) || overlaps(yr, span(gamma, (size_t)L * 2)))
+    return MOE_TAIL_EINVAL;
+  return moetail::enqueue_latent_tail(latent, gamma, eps, w_up, shared, tp_s, b, tp, L, H, out, y, flags,
+                                      static_cast<cudaStream_t>(stream));
 }
 
 MOE_API int moe_tail_latent_norm(const void* latent, const void* gamma, float eps, int b, int tp, int L, void* y,

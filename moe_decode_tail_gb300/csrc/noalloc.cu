@@ -77,13 +77,18 @@ MOE_API int moe_tail_latent_up_noalloc(const void* latent, const void* gamma, fl
       overlaps(out, out_n, w_up, (size_t)H * L * 2) || overlaps(out, out_n, shared, (size_t)tp_s * b * H * 2))
     return MOE_TAIL_EINVAL;
 
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The one-kernel form, where requested, keeps y in shared memory (no scratch array).
+  moetail::GemmPlan plan;
+  if (moetail::latent_tail_fused(b, tp, L, H, &plan))
+    return moetail::enqueue_latent_fused(plan, latent, gamma, eps, w_up, shared, tp_s, b, tp, L, H, out, nullptr, 0,
+                                         st);
   void* y = nullptr;
   cudaError_t e = scratch_on_current_device(&y);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return MOE_TAIL_ECUDA;
   }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   // 1. y (every element written, so nothing has to start at zero), 2. the
   // up-projection, which follows this call's own norm kernel
   e = moetail::enqueue_latent_norm(latent, gamma, eps, b, tp, L, y, false, st);

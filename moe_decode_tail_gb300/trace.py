@@ -27,7 +27,7 @@ import torch
 
 KERNELS = {10: "ep_finalize (route-parallel)", 11: "tp_finalize (route-parallel)", 12: "latent_norm",
            20: "tp_finalize (staged)", 21: "latent_norm (staged)", 30: "up-projection GEMM", 31: "gate/up GEMM",
-           32: "down GEMM", 40: "ep_finalize"}
+           32: "down GEMM", 33: "latent tail (one kernel)", 40: "ep_finalize"}
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
@@ -82,7 +82,10 @@ def describe(group: list[tuple[int, int, list]]) -> list[str]:
         line = (f"{KERNELS.get(kid, kid):30s} CTAs {len(rs):4d}  first start {(min(r[3] for r in rs) - base) / 1e3:6.1f}"
                 f"  last start {(max(r[3] for r in rs) - base) / 1e3:6.1f}  end {(max(r[5] for r in rs) - base) / 1e3:6.1f}"
                 f"  CTA p50 {p50(lambda r: r[5] - r[3]):5.1f}")
-        if all(r[4][0] for r in rs):
+        if kid == 33 and all(r[4][0] and r[4][1] and r[4][2] for r in rs):  # marks 1, 2: x formed, y ready
+            line += (f"  x formed p50 {p50(lambda r: r[4][1] - r[3]):5.1f}  y ready {p50(lambda r: r[4][2] - r[3]):5.1f}"
+                     f"  accumulator {p50(lambda r: r[4][0] - r[3]):5.1f}")
+        elif all(r[4][0] for r in rs):
             line += f"  K loop p50 {p50(lambda r: r[4][0] - r[3]):5.1f}"
             if all(r[4][3] for r in rs):
                 line += (f"  epilogue: stage {p50(lambda r: r[4][1] - r[4][0]):.1f}"

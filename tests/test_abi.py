@@ -169,6 +169,30 @@ def test_latent_steps_b_zero(lib):
     assert up(lib, b=0, y=None, w=None, out=None, flags=1) == OK
 
 
+def latent_flags(lib, **kw):
+    args = dict(lat=a(), gamma=a(1 << 24), eps=1e-6, w=a(2 << 24), sh=a(3 << 24), tp_s=8, b=16, tp=8, L=3584,
+                H=7168, out=a(4 << 24), y=a(5 << 24), flags=3, stream=None)
+    args.update(kw)
+    return lib.moe_tail_latent_up_flags(args["lat"], args["gamma"], args["eps"], args["w"], args["sh"],
+                                        args["tp_s"], args["b"], args["tp"], args["L"], args["H"], args["out"],
+                                        args["y"], args["flags"], args["stream"])
+
+
+@host_only
+@pytest.mark.parametrize("bad", [
+    dict(tp=0), dict(tp_s=33), dict(L=3583), dict(H=7170), dict(b=-1), dict(sh=None), dict(tp_s=0),
+    dict(y=None), dict(lat=None), dict(out=None), dict(flags=4), dict(flags=-1), dict(y=a(8)),
+    dict(y=a(4 << 24)), dict(y=a(16)), dict(out=a(5 << 24)), dict(y=a(3 << 24)),  # y over out, latent, shared
+])
+def test_latent_up_flags_refuses_bad_arguments(lib, bad):
+    assert latent_flags(lib, **bad) == EINVAL
+
+
+@host_only
+def test_latent_up_flags_b_zero(lib):
+    assert latent_flags(lib, b=0, lat=None, w=None, out=None, y=None) == OK
+
+
 def shared(lib, **kw):
     args = dict(x=a(), wg=a(1 << 28), wu=a(2 << 28), wd=a(3 << 28), b=64, H=7168, I=6144, out=a(4 << 28), acc=1,
                 ws=a(5 << 28), wsb=64 * 6144 * 2, stream=None)

@@ -383,6 +383,94 @@ def test_latent_norm_inputs_ready_waits_before_writing_y(mt):
     assert mt.moe_tail_take_device_error() == 0
 
 
+@pytest.mark.parametrize("kw", [
+    dict(b=1, tp=8, tp_s=9, L=3584, H=7168),     # the decode step's latent tail: K split over 5-CTA clusters
+    dict(b=16, tp=8, tp_s=8, L=3584, H=7168),
+    dict(b=5, tp=3, tp_s=0, L=1000, H=520),      # split 8, ragged last chunk, M tail
+    dict(b=17, tp=2, tp_s=1, L=8192, H=264),     # N tile 32, 32 chunks, two ring stages
+    dict(b=32, tp=9, tp_s=2, L=256, H=136),      # one chunk shared by all four CTAs of a cluster
+    dict(b=8, tp=32, tp_s=32, L=8, H=8),         # one K block, no cluster
+    dict(b=12, tp=1, tp_s=0, L=8200, H=64),      # 33 chunks: the two-kernel form
+])
+@pytest.mark.parametrize("flags", [0, 1, 2, 3])
+def test_latent_one_kernel_matches_split_calls(mt, monkeypatch, kw, flags):
+    # moe_tail_latent_up_flags with its one-kernel form taken wherever it fits
+    # (up to 32 tokens): y and out bit for bit those of moe_tail_latent_norm +
+    # moe_tail_up_project, y bit-exact against the oracle's norm and out within
+    # the GEMM bound of the oracle's up-projection
+    d = synth.latent_up_inputs(0xF05E + kw["b"] + kw["L"], **kw)
+    b, L, H = d["b"], d["L"], d["H"]
+    lat, gam, w = d["latent"].to(DEV), d["gamma"].to(DEV), d["w_up"].to(DEV)
+    sh = None if d["shared"] is None else d["shared"].to(DEV)
+    y1 = torch.full((b, L), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out1 = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mt.moe_tail_latent_norm(lat, gam, y1, eps=d["eps"])
+    mt.moe_tail_up_project(y1, w, sh, out1)
+    monkeypatch.setenv("MOE_TAIL_LATENT_FUSED", "1")
+    y2 = torch.full((b, L), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out2 = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mt.moe_tail_latent_up_flags(lat, gam, w, sh, out2, y2, eps=d["eps"], inputs_ready=bool(flags & 2),
+                                weights_static=bool(flags & 1))
+    torch.cuda.synchronize()
+    assert mt.moe_tail_take_device_error() == 0
+    assert np.array_equal(bits(y2), bits(y1)), f"y one kernel vs split {kw}"
+    assert np.array_equal(bits(out2), bits(out1)), f"out one kernel vs split {kw}"
+    y_ref, out_ref = oracle.latent_tail(d["latent"], d["gamma"], d["eps"], d["w_up"], d["shared"], d["tp_s"],
+                                        b, d["tp"], L, H)
+    assert_bitexact(y2, y_ref, f"latent y {kw}")
+    assert_gemm_close(out2, out_ref, f"latent out {kw}")
+
+
+@pytest.mark.parametrize("choice", ["0", "1"])
+def test_latent_up_and_noalloc_take_either_form(mt, monkeypatch, choice):
+    # moe_tail_latent_up and the workspace-free call at b = 4, with the one-kernel
+    # form switched off and on: the same bits either way
+    monkeypatch.setenv("MOE_TAIL_LATENT_FUSED", choice)
+    d = synth.latent_up_inputs(0x0F4, b=4, tp=8, tp_s=9, L=3584, H=7168)
+    y, out = run_latent(mt, d)
+    out_na = torch.full((4, 7168), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mt.moe_tail_latent_up_noalloc(d["latent"].to(DEV), d["gamma"].to(DEV), d["w_up"].to(DEV),
+                                  d["shared"].to(DEV), out_na, eps=d["eps"])
+    torch.cuda.synchronize()
+    y_ref, out_ref = oracle.latent_tail(d["latent"], d["gamma"], d["eps"], d["w_up"], d["shared"], 9, 4, 8, 3584,
+                                        7168)
+    assert_bitexact(y, y_ref, "latent y b=4")
+    assert_gemm_close(out, out_ref, "latent out b=4")
+    assert np.array_equal(bits(out_na), bits(out))
+    assert mt.moe_tail_take_device_error() == 0
+
+
+@pytest.mark.parametrize("one_kernel", ["0", "1"])
+def test_latent_up_flags_inputs_ready_waits_before_writing_y(mt, monkeypatch, one_kernel):
+    # norm(A) -> up-projection reading y -> the flags call for B with
+    # inputs_ready into the same y, on one stream (both forms): B's first
+    # kernel may start while the up-projection still reads y, so y is written
+    # only after that kernel ends; outA must be A's up-projection and y, outB B's
+    monkeypatch.setenv("MOE_TAIL_LATENT_FUSED", one_kernel)
+    kw = dict(b=16, tp=8, tp_s=8, L=3584, H=7168)
+    A = synth.latent_up_inputs(0xA13, **kw)
+    B = synth.latent_up_inputs(0xB24, **kw)
+    yA_ref, outA_ref = oracle.latent_tail(A["latent"], A["gamma"], A["eps"], A["w_up"], A["shared"], 8, 16, 8,
+                                          3584, 7168)
+    yB_ref, outB_ref = oracle.latent_tail(B["latent"], B["gamma"], B["eps"], A["w_up"], B["shared"], 8, 16, 8,
+                                          3584, 7168)
+    y = torch.empty((16, 3584), dtype=torch.bfloat16, device=DEV)
+    outA = torch.full((16, 7168), float("nan"), dtype=torch.bfloat16, device=DEV)
+    outB = torch.full((16, 7168), float("nan"), dtype=torch.bfloat16, device=DEV)
+    w = A["w_up"].to(DEV)
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    mt.moe_tail_latent_norm(A["latent"].to(DEV), A["gamma"].to(DEV), y, eps=A["eps"], stream=st)
+    mt.moe_tail_up_project(y, w, A["shared"].to(DEV), outA, weights_static=True, stream=st)
+    mt.moe_tail_latent_up_flags(B["latent"].to(DEV), B["gamma"].to(DEV), w, B["shared"].to(DEV), outB, y,
+                                eps=B["eps"], inputs_ready=True, weights_static=True, stream=st)
+    torch.cuda.synchronize()
+    assert_gemm_close(outA, outA_ref, "up-projection of the first y")
+    assert_bitexact(y, yB_ref, "second y")
+    assert_gemm_close(outB, outB_ref, "latent tail of B")
+    assert mt.moe_tail_take_device_error() == 0
+
+
 # ------------------------------------------------------------------ shared expert
 #
 # gate and up are FP32 sums whose order the pages leave open, so bf16(gate),
