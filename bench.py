@@ -692,7 +692,8 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
     replays of a graph of max(20, copies) calls that cycles over copies of the
     call's large inputs (together more than twice the L2; at most 256 copies,
     so the smallest calls stay L2-resident), median of 7 replays.  Also each
-    call at b = 1 and b = 8 (the small-batch decode regime)."""
+    call at b = 1 and b = 8 (the small-batch decode regime), the latent tail
+    also with both promises and in its opt-in one-kernel form."""
     from moe_decode_tail_gb300 import synth
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -837,6 +838,25 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
         ws = torch.empty(mt.moe_tail_workspace_bytes(0, bs, L), dtype=torch.uint8, device=dev)
         row["latent_up"] = timed(lambda i: mt.moe_tail_latent_up(lat, w["lat_gamma"], wu[i], sh, out, ws,
                                                                  stream=stream), len(wu))
+        # the same through moe_tail_latent_up_flags with both promises, and both
+        # ways in the opt-in one-kernel form (MOE_TAIL_LATENT_FUSED=1)
+        yb = torch.empty((bs, L), dtype=torch.bfloat16, device=dev)
+
+        def flags_call(i, promises):
+            mt.moe_tail_latent_up_flags(lat, w["lat_gamma"], wu[i], sh, out, yb, inputs_ready=promises,
+                                        weights_static=promises, stream=stream)
+
+        row["latent_up_promises"] = timed(lambda i: flags_call(i, True), len(wu))
+        prev = os.environ.get("MOE_TAIL_LATENT_FUSED")
+        os.environ["MOE_TAIL_LATENT_FUSED"] = "1"
+        try:
+            row["latent_up_one_kernel"] = timed(lambda i: flags_call(i, False), len(wu))
+            row["latent_up_promises_one_kernel"] = timed(lambda i: flags_call(i, True), len(wu))
+        finally:
+            if prev is None:
+                os.environ.pop("MOE_TAIL_LATENT_FUSED", None)
+            else:
+                os.environ["MOE_TAIL_LATENT_FUSED"] = prev
         del wu
         x = w["x"][:bs].contiguous()
         sw = [(w["w_gate"], w["w_up_s"], w["w_down"])]
