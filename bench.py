@@ -66,7 +66,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload isolated timings")
     ap.add_argument("--composition", default="two_branch",
-                    choices=["two_branch", "two_branch_split", "norm_main", "norm_side_first", "norm_side_after"],
+                    choices=["two_branch", "two_branch_split", "two_branch_static", "norm_main", "norm_side_first",
+                             "norm_side_after"],
                     help="how the step orders the weight-streaming calls (see run_step)")
     ap.add_argument("--sequential", action="store_true",
                     help="run the four calls in order on one stream (shared expert accumulating into out)")
@@ -270,7 +271,7 @@ def run_step(mt, w, stream, events=None, side=None):
         shared_expert(stream, w["out"], True)
         return
     comp = w.get("composition", "two_branch")
-    if comp not in ("two_branch", "two_branch_split"):
+    if comp not in ("two_branch", "two_branch_split", "two_branch_static"):
         # the latent up-projection between the shared expert's gate/up and down
         # projections; down then adds d into the latent tail's output
         # (out = bf16(out + bf16(d)), the sequential composition's arithmetic)
@@ -308,7 +309,17 @@ def run_step(mt, w, stream, events=None, side=None):
         return
     w["fork"].record(stream)
     side.wait_event(w["fork"])
-    shared_expert(side, w["d_slot"], False)
+    if comp == "two_branch_static":  # the shared expert as its two calls, weights requested before each wait
+        bx = w["x"].shape[0]
+        ws_h = w["ws_sh"][: bx * I * 2].view(torch.bfloat16).view(bx, I)
+        rec(8, side)
+        mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], ws_h, weights_static=True, stream=side)
+        rec(9, side)
+        rec(10, side)
+        mt.moe_shared_down(ws_h, w["w_down"], w["d_slot"], accumulate=False, weights_static=True, stream=side)
+        rec(11, side)
+    else:
+        shared_expert(side, w["d_slot"], False)
     if comp == "two_branch_split":
         rec(4, side)
         mt.moe_tail_latent_norm(w["latent"], w["lat_gamma"], w["y"], eps=1e-6, inputs_ready=True, stream=side)
@@ -605,7 +616,7 @@ def cuda_arm(args, world, rank, local):
     calls = {}
     hbm, bf16_tf, peak_kind = peaks()
     nbytes = dict(BYTES)
-    if side is not None and args.composition in ("two_branch", "two_branch_split"):  # d: one partial slot
+    if side is not None and args.composition in ("two_branch", "two_branch_split", "two_branch_static"):  # d: a slot
         nbytes["shared_expert"] = 3 * I * H * 2 + B * H * 2 + B * H * 2
         nbytes["latent_up"] = BYTES["latent_up"] + B * H * 2
     for c in CALLS:
@@ -646,6 +657,8 @@ def cuda_arm(args, world, rank, local):
             if args.composition == "two_branch" else
             "two branches as two_branch, with the latent tail always as its two split calls"
             if args.composition == "two_branch_split" else
+            "two branches as two_branch, with the shared expert as its two calls with static weights"
+            if args.composition == "two_branch_static" else
             f"two branches ({args.composition}): on a side stream the shared expert's gate/up, the latent "
             "up-projection, then the shared expert's down projection adding d into out; the latent norm "
             + {"norm_main": "first on the high-priority stream", "norm_side_first": "first on the side stream",
