@@ -471,6 +471,38 @@ def test_latent_up_flags_inputs_ready_waits_before_writing_y(mt, monkeypatch, on
     assert mt.moe_tail_take_device_error() == 0
 
 
+# ------------------------------------------------------------------ the header's limits
+
+@pytest.mark.parametrize("case", ["ep_b_max", "tp_b_max", "ep_all_max", "tp_all_max", "latent_b_max",
+                                  "latent_L_max"])
+def test_maximum_sizes(mt, case):
+    # b = 65535 (one CTA row of the finalize grids per token: the grid's y
+    # limit), tp = K = 32 with P = 32768 together, and the latent tail at its
+    # largest b and L; finalize outputs and y bit-exact, out within the GEMM bound
+    if case == "ep_b_max":
+        d = synth.ep_finalize_inputs(0x3A1, b=65535, tp=1, P=8, K=1, num_experts=1)
+        assert_bitexact(run_ep(mt, d), ref_ep(d), case)
+    elif case == "tp_b_max":
+        d = synth.tp_finalize_inputs(0x3A2, b=65535, tp=1, P=8, K=1, num_experts=1)
+        assert_bitexact(run_tp(mt, d), ref_tp(d), case)
+    elif case == "ep_all_max":
+        d = synth.ep_finalize_inputs(0x3A3, b=2, tp=32, P=32768, K=32, num_experts=64)
+        assert_bitexact(run_ep(mt, d), ref_ep(d), case)
+    elif case == "tp_all_max":
+        d = synth.tp_finalize_inputs(0x3A4, b=2, tp=32, P=32768, K=32, num_experts=64)
+        assert_bitexact(run_tp(mt, d), ref_tp(d), case)
+    else:
+        kw = dict(b=65535, tp=1, tp_s=1, L=8, H=8) if case == "latent_b_max" else \
+            dict(b=2, tp=2, tp_s=32, L=32768, H=64)
+        d = synth.latent_up_inputs(0x3A5 + kw["L"], **kw)
+        y_ref, out_ref = oracle.latent_tail(d["latent"], d["gamma"], d["eps"], d["w_up"], d["shared"], d["tp_s"],
+                                            d["b"], d["tp"], d["L"], d["H"])
+        y, out = run_latent(mt, d)
+        assert_bitexact(y, y_ref, f"{case} y")
+        assert_gemm_close(out, out_ref, f"{case} out")
+    assert mt.moe_tail_take_device_error() == 0
+
+
 # ------------------------------------------------------------------ shared expert
 #
 # gate and up are FP32 sums whose order the pages leave open, so bf16(gate),
