@@ -90,6 +90,104 @@ def ref_ep(d, **kw):
                               a["eps"], a["weight_before_norm"], a["b"], a["tp"], a["K"], a["P"])
 
 
+def bf16_bits_pz(x32):
+    """BF16 bits (round to nearest even, -0 made +0) of float32 values."""
+    t = torch.from_numpy(np.ascontiguousarray(x32, dtype=np.float32)).to(torch.bfloat16)
+    b = t.view(torch.int16).numpy().astype(np.uint16)
+    b[b == 0x8000] = 0
+    return b
+
+
+def fp32_inv_rms(ss, P, eps=1e-6):
+    """1 / sqrt(ss * (float)(1/P) + eps), each step one FP32 operation."""
+    f = np.float32
+    return f(1.0) / np.sqrt(f(f(ss) * f(1.0 / P)) + f(eps))
+
+
+@pytest.mark.parametrize("wbn", [True, False])
+@pytest.mark.parametrize("wdtype", [torch.float32, torch.bfloat16])
+def test_ep_routing_marker_rows(mt, wbn, wdtype):
+    # Every route row is a marker: 1.0 at column s*R + j (slot s, row j), zeros
+    # elsewhere; route k has weight 2^-k and the gains are 1.  Token t's output
+    # then holds bf16(inv * 2^-k) at column s*R + j for each local route (s, k)
+    # with idx[s][t][k] = j -- inv = 1/sqrt(1/P + eps) in FP32 -- and zeros
+    # elsewhere.  The expected output is written here from the routing table
+    # alone (no oracle): a wrong slot, row, route weight or locality test shows
+    # up as a lit or dark column.
+    b, tp, R, K, P = 16, 4, 8, 4, 512
+    rng = np.random.default_rng(0x3A7)
+    idx = np.empty((tp, b, K), dtype=np.int32)
+    for s in range(tp):
+        for t in range(b):  # distinct per (slot, token): -3..-1 and R..R+2 are not local
+            idx[s, t] = rng.choice(np.arange(-3, R + 3), size=K, replace=False)
+    rows = torch.zeros((tp, R, P))
+    for s in range(tp):
+        for j in range(R):
+            rows[s, j, s * R + j] = 1.0
+    w = torch.tensor([[2.0 ** -k for k in range(K)]] * b, dtype=torch.float32).to(wdtype)
+    d = dict(rows=rows.to(torch.bfloat16), rows_per_slot=R, idx=torch.from_numpy(idx), w=w,
+             gamma=torch.zeros(P, dtype=torch.bfloat16), gain_center=1.0, eps=1e-6, weight_before_norm=wbn,
+             b=b, tp=tp, K=K, P=P)
+    inv = fp32_inv_rms(1.0, P)
+    expect = np.zeros((b, P), dtype=np.float32)
+    for s in range(tp):
+        for t in range(b):
+            for k in range(K):
+                j = idx[s, t, k]
+                if 0 <= j < R:
+                    expect[t, s * R + j] = inv * np.float32(2.0 ** -k)
+    out = run_ep(mt, d)
+    got = bits(out).astype(np.uint16)
+    assert np.array_equal(got, bf16_bits_pz(expect)), "EP marker rows: routing"
+    assert_bitexact(out, ref_ep(d), "EP marker rows vs oracle")
+
+
+@pytest.mark.parametrize("wbn", [True, False])
+def test_tp_routing_marker_rows(mt, wbn):
+    # Every slot's K-partial of row j holds 1.0 at column j, and slot s adds a
+    # slot marker 2^-s at column 256 + s; route k has weight 2^-k, gains 1.
+    # So x_j = tp at column j and 2^-s at 256 + s, ss = tp^2 + sum_s 4^-s
+    # exactly, and token t's output is bf16(tp * inv * 2^-k) at column
+    # idx[t][k] for each valid route, the route-ordered FP32 sum of
+    # (2^-s * inv) * 2^-k over the valid routes at column 256 + s (every slot
+    # must have been summed), and zeros elsewhere -- written out here from the
+    # routing table, without the oracle.
+    b, tp, K, P, rows_n = 16, 4, 4, 512, 32
+    rng = np.random.default_rng(0x3A8)
+    idx = np.stack([rng.choice(np.arange(-2, rows_n + 2), size=K, replace=False) for _ in range(b)])
+    idx = idx.astype(np.int32)
+    q = torch.zeros((tp, rows_n, P))
+    for s in range(tp):
+        for j in range(rows_n):
+            q[s, j, j] = 1.0
+            q[s, j, 256 + s] = 2.0 ** -s
+    d = dict(partials=q.to(torch.bfloat16), num_rows=rows_n, idx=torch.from_numpy(idx),
+             w=torch.tensor([[2.0 ** -k for k in range(K)]] * b, dtype=torch.float32),
+             gamma=torch.zeros(P, dtype=torch.bfloat16), gain_center=1.0, eps=1e-6, weight_before_norm=wbn,
+             b=b, tp=tp, K=K, P=P)
+    f = np.float32
+    ss = f(f(0.0) + f(tp * tp))  # chunk 0: the route column
+    marker_sq = f(0.0)
+    for s in range(tp):  # chunk 1: lane 0 squares columns 256.. in order
+        marker_sq = f(marker_sq + f(f(2.0 ** -s) * f(2.0 ** -s)))
+    ss = f(ss + marker_sq)
+    inv = fp32_inv_rms(ss, P)
+    expect = np.zeros((b, P), dtype=np.float32)
+    for t in range(b):
+        acc = np.zeros(tp, dtype=np.float32)
+        for k in range(K):
+            j = idx[t, k]
+            if 0 <= j < rows_n:
+                expect[t, j] = f(f(tp) * inv) * f(2.0 ** -k)
+                for s in range(tp):
+                    acc[s] = f(acc[s] + f(f(f(2.0 ** -s) * inv) * f(2.0 ** -k)))
+        expect[t, 256:256 + tp] = acc
+    out = run_tp(mt, d)
+    got = bits(out).astype(np.uint16)
+    assert np.array_equal(got, bf16_bits_pz(expect)), "TP marker rows: routing and slot sum"
+    assert_bitexact(out, ref_tp(d), "TP marker rows vs oracle")
+
+
 @pytest.mark.parametrize("wbn", [True, False])
 def test_ep_tiny(mt, wbn):
     d = synth.config(1, weight_before_norm=wbn)
