@@ -331,6 +331,31 @@ def test_ep_brute_force_double(wbn):
 
 # ------------------------------------------------------------- expert-TP finalize
 
+@pytest.mark.parametrize("kind", ["ep", "tp"])
+def test_single_route_is_textbook_rmsnorm(kind):
+    # One route per token, w = 1, tp = 1, gamma = 0 with gain center 1: the
+    # finalize is a plain RMS norm of the route row, x / sqrt(mean(x^2) + eps),
+    # computed here in double.  The oracle's FP32 steps round far below a BF16
+    # ulp, so every output is within one BF16 ulp of it (and nearly all equal
+    # its BF16 rounding).
+    P, b, eps = 512, 6, 1e-6
+    x = synth.bf16(synth.normal(0x7E, 1, b * P), (b, P))
+    common = dict(w=torch.ones((b, 1)), gamma=torch.zeros(P).to(torch.bfloat16), gain_center=1.0, eps=eps,
+                  weight_before_norm=True, b=b, tp=1, K=1, P=P)
+    if kind == "ep":  # token t's route is row t of the only slot
+        out = ep_call(dict(common, rows=x.reshape(1, b, P), rows_per_slot=b,
+                           idx=torch.arange(b, dtype=torch.int32).reshape(1, b, 1)))
+    else:
+        out = tp_call(dict(common, partials=x.reshape(1, b, P), num_rows=b,
+                           idx=torch.arange(b, dtype=torch.int32).reshape(b, 1)))
+    xd = x.double().numpy()
+    ref = xd / np.sqrt(np.mean(xd * xd, axis=1, keepdims=True) + eps)
+    got = out.double().numpy()
+    assert np.all(np.abs(got - ref) <= ulp_bf16(ref))
+    exact = bits(torch.from_numpy(ref).float().to(torch.bfloat16)) == bits(out)
+    assert exact.mean() > 0.99
+
+
 def test_tp_equals_ep_on_slot_summed_rows():
     # x_r = bf16(sum_s Q_s), then the EP formula on one slot with every route
     # local: the two statements of the method must agree bit for bit.
