@@ -63,6 +63,15 @@ __device__ __forceinline__ float route_weight(const void* w, int64_t i) {
   return ((const float*)w)[i];
 }
 
+// 1/rms of one route from its chunk sums of squares: the sums added in chunk
+// order from +0, then 1 / sqrt(ss * (1/P) + eps) with IEEE square root and
+// division.
+__device__ __forceinline__ float inv_rms_of_route(const float* chunk_ss, const FinalizeArgs& a) {
+  float ss = 0.0f;
+  for (int c = 0; c < a.chunks; ++c) ss = __fadd_rn(ss, chunk_ss[c]);
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, a.rcpP), a.eps)));
+}
+
 // The token's route weights into sm.w and its routes that have a row into
 // sm.list_* (EP in (slot, route) order over the slots' local routes, expert-TP
 // in route order; the latent norm has one "route", the token's own row);
@@ -334,13 +343,13 @@ __global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const Fin
       }
     }
     cluster_sync_all();
+    // lane q of every warp forms route q's 1/rms; the warp shares them
+    const float my_inv = inv_rms_of_route(ssp + (lane & (kEpRoutes - 1)) * kMaxChunks, a);
 #pragma unroll
     for (int q = 0; q < kEpRoutes; ++q) {
+      const float inv = __shfl_sync(0xffffffffu, my_inv, q);
       if (q < n_pass) {
         const int e = base + q;
-        float ss = 0.0f;
-        for (int c = 0; c < a.chunks; ++c) ss = __fadd_rn(ss, ssp[q * kMaxChunks + c]);
-        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, a.rcpP), a.eps)));
         const float w = sm.w[sm.list_route[e]];
         const int s = sm.list_slot[e];
         if (s != cur_slot) {  // slot boundary: its BF16 partial joins the slot sum
@@ -558,6 +567,8 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
           const int st = (int)(g % (uint32_t)S);
           sb_wait(smem_addr(&sm.full[st]), (g / S) & 1, abort_flag);
           ++g;
+          if (g == 1) MOE_TRACE_MARK(0);  // first route's rows landed
+          if (g == 4) MOE_TRACE_MARK(1);  // fourth route's rows landed
           if (valid) {
             const uint8_t* src = ring_raw + (size_t)st * stage_bytes + (size_t)vb * 16;
             for (int s = 0; s < a.tp; ++s, src += band_bytes) {  // slot order, FP32 from +0
@@ -584,20 +595,16 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
             st_cluster_f32(map_to_rank(smem_addr(&ss[rr * kMaxChunks + chunk]), (uint32_t)lane), sq);
         }
       }
+      if (g <= (uint32_t)kMaxRoutesPerPass) MOE_TRACE_MARK(2);  // first pass: all its routes consumed
       cluster_sync_all();
-      // fold the chunk sums of the pass's routes (independent chains side by side)
-      float tot[kMaxRoutesPerPass];
-#pragma unroll
-      for (int rr = 0; rr < kMaxRoutesPerPass; ++rr) tot[rr] = 0.0f;
-      for (int c = 0; c < a.chunks; ++c) {
-#pragma unroll
-        for (int rr = 0; rr < kMaxRoutesPerPass; ++rr)
-          if (has[rr]) tot[rr] = __fadd_rn(tot[rr], ss[rr * kMaxChunks + c]);
-      }
+      if (g <= (uint32_t)kMaxRoutesPerPass) MOE_TRACE_MARK(3);
+      // lane r of every warp folds route r's chunk sums in chunk order and forms
+      // its 1/rms (one square root and division per thread); the warp shares them
+      const float my_inv = inv_rms_of_route(ss + (lane & (kMaxRoutesPerPass - 1)) * kMaxChunks, a);
 #pragma unroll
       for (int rr = 0; rr < kMaxRoutesPerPass; ++rr) {
+        const float inv = __shfl_sync(0xffffffffu, my_inv, rr);
         if (has[rr]) {  // a route with no row contributes nothing
-          const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(tot[rr], a.rcpP), a.eps)));
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float x = xr[rr][i];
