@@ -67,8 +67,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload isolated timings")
     ap.add_argument("--composition", default="two_branch",
-                    choices=["two_branch", "two_branch_split", "two_branch_static", "norm_main", "norm_side_first",
-                             "norm_side_after"],
+                    choices=["two_branch", "two_branch_split", "two_branch_static", "latent_main", "norm_main",
+                             "norm_side_first", "norm_side_after"],
                     help="how the step orders the weight-streaming calls (see run_step)")
     ap.add_argument("--sequential", action="store_true",
                     help="run the four calls in order on one stream (shared expert accumulating into out)")
@@ -208,6 +208,7 @@ def make_workload(dev, b=B, weights=None):
     w["shared"] = w["shared9"][:TP]
     w["d_slot"] = w["shared9"][TP]
     w["fork"], w["join"], w["normed"] = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+    w["h_ready"] = torch.cuda.Event()
     return cpu, w
 
 
@@ -272,6 +273,32 @@ def run_step(mt, w, stream, events=None, side=None):
         shared_expert(stream, w["out"], True)
         return
     comp = w.get("composition", "two_branch")
+    if comp == "latent_main":
+        # the latent tail on the finalize stream after EP and TP, beside the
+        # shared expert's gate/up; the down projection then adds d into the
+        # latent tail's output (out = bf16(out + bf16(d)), the sequential
+        # composition's arithmetic) once both are done
+        bx = w["x"].shape[0]
+        ws_h = w["ws_sh"][: bx * I * 2].view(torch.bfloat16).view(bx, I)
+        w["fork"].record(stream)
+        side.wait_event(w["fork"])
+        rec(8, side)
+        mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], ws_h, weights_static=True, stream=side)
+        rec(9, side)
+        w["h_ready"].record(side)
+        ep(stream)
+        tp(stream)
+        rec(4, stream)
+        mt.moe_tail_latent_up_flags(w["latent"], w["lat_gamma"], w["w_up"], w["shared"], w["out"], w["y"], eps=1e-6,
+                                    inputs_ready=True, weights_static=True, stream=stream)
+        rec(5, stream)
+        rec(6, stream)
+        rec(7, stream)
+        stream.wait_event(w["h_ready"])
+        rec(10, stream)
+        mt.moe_shared_down(ws_h, w["w_down"], w["out"], accumulate=True, weights_static=True, stream=stream)
+        rec(11, stream)
+        return
     if comp not in ("two_branch", "two_branch_split", "two_branch_static"):
         # the latent up-projection between the shared expert's gate/up and down
         # projections; down then adds d into the latent tail's output
@@ -661,6 +688,9 @@ def cuda_arm(args, world, rank, local):
             if args.composition == "two_branch_split" else
             "two branches as two_branch, with the shared expert as its two calls with static weights"
             if args.composition == "two_branch_static" else
+            "two branches: the shared expert's gate/up on a side stream; EP, TP and the latent tail on a "
+            "high-priority stream beside it; then the down projection adds d into the latent tail's output"
+            if args.composition == "latent_main" else
             f"two branches ({args.composition}): on a side stream the shared expert's gate/up, the latent "
             "up-projection, then the shared expert's down projection adding d into out; the latent norm "
             + {"norm_main": "first on the high-priority stream", "norm_side_first": "first on the side stream",

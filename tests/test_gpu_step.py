@@ -1,8 +1,10 @@
 """The composed decode step exactly as bench.py times it (two branches: the
 shared expert then the latent tail on a side stream, EP and expert-TP
 finalize beside them; and the sequential composition, where the shared
-expert accumulates into the latent tail's output), checked against the
-oracle on sampled tokens:
+expert accumulates into the latent tail's output; and latent_main, where the
+latent tail runs beside the shared expert's gate/up and the down projection
+then accumulates into its output), checked against the oracle on sampled
+tokens:
 EP and expert-TP outputs and the latent norm's y bit for bit; the step's
 output against the oracle's up-projection of the GPU's y with the shared
 expert's BF16 output d as one more shared partial (GEMM bound); and d against
@@ -27,7 +29,7 @@ def close(got, ref, what):
     assert not bool(bad.any()), f"{what}: {int(bad.sum())} of {bad.numel()} out of tolerance"
 
 
-@pytest.fixture(scope="module", params=["two_branch", "sequential"])
+@pytest.fixture(scope="module", params=["two_branch", "sequential", "latent_main"])
 def step(request):
     from moe_decode_tail_gb300 import build as cuda_build
 
@@ -41,11 +43,13 @@ def step(request):
     dev = torch.device("cuda", 0)
     cpu, w = bench.make_workload(dev)
     stream = torch.cuda.Stream(dev, priority=-1)
-    side = torch.cuda.Stream(dev, priority=0) if request.param == "two_branch" else None
+    side = None if request.param == "sequential" else torch.cuda.Stream(dev, priority=0)
+    if side is not None:
+        w["composition"] = request.param
     for k in ("out_ep", "out_tp", "out", "y"):
         w[k].fill_(float("nan"))
     w["d_slot"].fill_(float("nan"))
-    if request.param == "sequential":  # the shared expert adds into the latent tail's output
+    if request.param == "sequential":  # the shared expert adds into the latent tail's output (after it)
         w["out"].zero_()
     with torch.cuda.stream(stream):
         bench.run_step(mt, w, stream, side=side)
