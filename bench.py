@@ -828,6 +828,10 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
 
     us = timed(split_call, n)
     report("4_latent_up_b16_two_calls", us, nb, n, ">= 0.60 of the weight-stream roofline")
+    # ... and as one call with the same promises (moe_tail_latent_up_flags)
+    us = timed(lambda i: mt.moe_tail_latent_up_flags(lat, gam, wu[i], sh, out, y, eps=d["eps"], inputs_ready=True,
+                                                     weights_static=True, stream=stream), n)
+    report("4_latent_up_b16_flags", us, nb, n, ">= 0.60 of the weight-stream roofline")
     del wu
 
     d = dict(b=B, H=H, I=I)
