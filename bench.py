@@ -605,14 +605,19 @@ def cuda_arm(args, world, rank, local):
                 run_step(mt, w, stream, evs[i] if evs else None, side=side)
         return g, [e for e in evs if e is not None] if evs else None
 
+    # The timed steps replay a graph without events; the last of the timed
+    # replays is the instrumented copy, whose event pairs give the per-call
+    # durations (so 1/10 of one replay's steps lose their overlap, not 1/10 of all)
+    clean_g = capture(G, False)[0]
     main_g, main_ev = capture(G, True)
     rest = K % G
     rest_g = capture(rest, False)[0] if rest else None
     torch.cuda.synchronize()
-    # warm-up: W steps from the same graph (replay() launches on the current stream)
+    # warm-up: W steps from the same graphs (replay() launches on the current stream)
     with torch.cuda.stream(stream):
+        main_g.replay()
         for _ in range(max(1, -(-W // G))):
-            main_g.replay()
+            clean_g.replay()
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
@@ -623,8 +628,8 @@ def cuda_arm(args, world, rank, local):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         start.record(stream)
-        for _ in range(K // G):
-            main_g.replay()
+        for r in range(K // G):
+            (main_g if r == K // G - 1 else clean_g).replay()
         if rest_g is not None:
             rest_g.replay()
         stop.record(stream)
@@ -670,8 +675,8 @@ def cuda_arm(args, world, rank, local):
         "frac": round(calls[dom]["achieved_gbs"] / hbm, 4), "traffic": traffic,
         "algorithmic_bytes_per_call": nbytes[dom], "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
         "note": "per-call CUDA events on the launch stream, recorded as graph nodes in every tenth step of the "
-                "timed graph replays (those steps lose the overlap between calls, so the per-call figures are "
-                "conservative)",
+                "last timed graph replay (those steps lose the overlap between calls, so the per-call figures are "
+                "conservative; the other timed replays carry no events)",
     }
     ms = max_s * 1e3 / K
     line = {
