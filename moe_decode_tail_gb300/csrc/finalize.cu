@@ -799,14 +799,19 @@ cudaError_t launch_finalize(int mode, const FinalizeArgs& args, bool wbn, int wm
   // expert-TP about two waves.  At most 8 bands (portable cluster size), one
   // band per chunk at most.
   int split = split_override();
-  if (mode == kModeEP) {  // tuning override for EP alone: MOE_TAIL_FIN_EP_SPLIT=<1|2|4|8>
-    const int s = env_int("MOE_TAIL_FIN_EP_SPLIT", 0);
+  if (mode == kModeEP || mode == kModeLatent) {  // tuning overrides for EP or the latent norm alone
+    const int s = env_int(mode == kModeEP ? "MOE_TAIL_FIN_EP_SPLIT" : "MOE_TAIL_FIN_LATENT_SPLIT", 0);
     if (s == 1 || s == 2 || s == 4 || s == 8) split = s;
   }
   if (split == 0) {
     const int64_t target = mode == kModeTP ? 2 * (int64_t)sms : (3 * (int64_t)sms) / 4;
     split = 1;
     while (split < 8 && split < a.chunks && (int64_t)a.b * split < target) split *= 2;
+    // The latent norm of up to 4 tokens in at most 2 bands: its 2-CTA clusters
+    // hand over to the up-projection sooner (one call at b = 1: 12.4 vs 13.7
+    // us; b = 4: 13.5 vs 14.6).  From b = 8 the wide bands are far slower
+    // there (~20 us), and the composed step is the same either way.
+    if (mode == kModeLatent && a.b <= 4) split = std::min(split, 2);
   }
   while (split < 8 && (a.chunks + split - 1) / split > kMaxThreads / 32) split *= 2;
   a.band_vectors = 32 * ((a.chunks + split - 1) / split);
