@@ -24,6 +24,8 @@
 //                   rows in one M tile; owned_h rounds gate and up to BF16)
 //   kGemmDown       out = bf16(out + bf16(d)) or bf16(d)  (the down projection
 //                   pushed as BF16, -0 made +0, added into the tail's output)
+//   kGemmLatentUp   kGemmUpShared with y formed on chip from the latent partials
+//                   (the latent tail in one kernel; taken only on request)
 //
 // Every wait is bounded in time; on expiry the kernel raises a bit in the
 // device error word, drains what it started, frees its tensor memory and

@@ -33,10 +33,10 @@ bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a
 int device_sms() {
   static int cache[64] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
   if (dev < 64 && cache[dev]) return cache[dev];
   int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
   if (dev < 64) cache[dev] = sms;
   return sms;
 }
