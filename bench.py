@@ -966,23 +966,51 @@ def step_by_batch(mt, w, dev, stream, side, sizes=(1, 8, 32, 128)) -> dict:
 def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
     """The same step through the public API with host buffers: every step
     copies its activations from pinned host memory and reads its outputs back
-    (weights stay resident, as in serving).  Two sets of activation and output
-    buffers alternate, so step i+1's host-to-device copies (on their own
-    stream) run while step i computes, and step i's outputs are read back on a
-    third stream; every step still moves all of its inputs and outputs."""
-    inputs = ["ep_rows", "ep_idx", "ep_w", "tp_part", "tp_idx", "tp_w", "latent", "shared", "x"]
+    (weights stay resident, as in serving).  A step's activations sit in one
+    pinned host buffer and, on the device, in one buffer whose tensors the
+    calls take as views (256-byte aligned), so a step moves them with one
+    host-to-device copy; its three outputs come back the same way, in one copy.
+    Two sets of device buffers alternate, so step i+1's host-to-device copy
+    (on its own stream) runs while step i computes, and step i's outputs are
+    read back on a third stream; every step still moves all of its inputs and
+    outputs."""
+    inputs = ["ep_rows", "ep_idx", "ep_w", "tp_part", "tp_idx", "tp_w", "latent", "x"]
     outputs = ["out_ep", "out_tp", "out"]
-    host_in = {k: w[k].cpu().pin_memory() for k in inputs}
-    host_out = [{k: torch.empty(w[k].shape, dtype=w[k].dtype).pin_memory() for k in outputs} for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
-    sets = [w, dict(w)]
-    second = sets[1]
-    for k in inputs + outputs:
-        if k != "shared":
-            second[k] = torch.empty_like(w[k])
-    second["shared9"] = torch.empty_like(w["shared9"])
-    second["shared"], second["d_slot"] = second["shared9"][:TP], second["shared9"][TP]
+
+    def layout(keys, extra=()):
+        offs, off = {}, 0
+        for k, t in [(k, w[k]) for k in keys] + list(extra):
+            offs[k] = off
+            off = (off + t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, off
+
+    def view(buf, offs, k, like):
+        n = like.numel() * like.element_size()
+        return buf[offs[k]: offs[k] + n].view(like.dtype).view(like.shape)
+
+    # inputs, then the latent tail's shared-partial slots with the shared expert's
+    # slot last: the copy covers every input and stops before that slot
+    in_offs, in_total = layout(inputs, [("shared9", w["shared9"])])
+    h2d = in_offs["shared9"] + w["shared"].numel() * w["shared"].element_size()
+    host_in = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+    for k in inputs:
+        view(host_in, in_offs, k, w[k]).copy_(w[k].cpu())
+    view(host_in, in_offs, "shared9", w["shared"]).copy_(w["shared"].cpu())
+    out_offs, out_total = layout(outputs)
+    host_out = [torch.empty(out_total, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    d2h = out_total
+    sets = []
+    for _ in range(2):
+        s = dict(w)  # weights, workspaces and events shared: the steps run in stream order
+        s["packed_in"] = torch.empty(in_total, dtype=torch.uint8, device=dev)
+        s["packed_out"] = torch.empty(out_total, dtype=torch.uint8, device=dev)
+        for k in inputs:
+            s[k] = view(s["packed_in"], in_offs, k, w[k])
+        s["shared9"] = view(s["packed_in"], in_offs, "shared9", w["shared9"])
+        s["shared"], s["d_slot"] = s["shared9"][:TP], s["shared9"][TP]
+        for k in outputs:
+            s[k] = view(s["packed_out"], out_offs, k, w[k])
+        sets.append(s)
     h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()
     computed, read_back = [ev(), ev()], [ev(), ev()]
@@ -995,8 +1023,7 @@ def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
         if i >= 2:
             h2d_stream.wait_event(computed[buf])  # step i-2 is done with these inputs
         with torch.cuda.stream(h2d_stream):
-            for k in inputs:
-                s[k].copy_(host_in[k], non_blocking=True)
+            s["packed_in"][:h2d].copy_(host_in, non_blocking=True)
             ready.record(h2d_stream)
         stream.wait_event(ready)
         if i >= 2:
@@ -1005,8 +1032,7 @@ def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
         computed[buf].record(stream)
         d2h_stream.wait_event(computed[buf])
         with torch.cuda.stream(d2h_stream):
-            for k in outputs:
-                host_out[buf][k].copy_(s[k], non_blocking=True)
+            host_out[buf].copy_(s["packed_out"], non_blocking=True)
             read_back[buf].record(d2h_stream)
         issued[0] += 1
 
@@ -1027,7 +1053,8 @@ def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
     s, units = aggregate(a.elapsed_time(b) / 1e3, float(B * steps), dist, dev)
     return {"value": units / s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": s * 1e3 / steps,
-            "pipelining": "double-buffered activations: step i+1's H2D copies overlap step i's compute"}
+            "pipelining": "double-buffered activations: step i+1's host-to-device copy overlaps step i's compute; "
+                          "one copy each way per step (activations and outputs packed in one buffer)"}
 
 
 def main():
