@@ -67,8 +67,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload isolated timings")
     ap.add_argument("--composition", default="two_branch",
-                    choices=["two_branch", "two_branch_split", "two_branch_static", "latent_main", "norm_main",
-                             "norm_side_first", "norm_side_after"],
+                    choices=["two_branch", "two_branch_one_call", "two_branch_split", "tp_after_gateup", "latent_main",
+                             "norm_main", "norm_side_first", "norm_side_after"],
                     help="how the step orders the weight-streaming calls (see run_step)")
     ap.add_argument("--sequential", action="store_true",
                     help="run the four calls in order on one stream (shared expert accumulating into out)")
@@ -223,18 +223,21 @@ def run_step(mt, w, stream, events=None, side=None):
 
     With a side stream the weight-streaming calls run beside the routed
     finalize calls, as the Kimi-K3 tail runs its shared expert (its output is
-    pushed into the tail's reduce-scatter partials): on the side stream
-    moe_shared_expert writes d = bf16(down(h)) into the last of the latent
-    tail's shared-partial slots, then moe_tail_latent_up_flags follows with
-    both promises -- inputs ready (the latent partials are read while the down
-    projection drains) and static weights (the first weight tiles are
-    requested before that wait) -- and adds d with the other slots in its
-    epilogue; the call enqueues the norm and the up-projection
-    ("two_branch_split" makes the two split calls, moe_tail_latent_norm and
-    moe_tail_up_project, with the same promises).  EP and expert-TP finalize run on the main stream, which joins
-    the side stream at the end of the step.  Without a
-    side stream the calls run in order (moe_tail_latent_up in one call) and
-    the shared expert accumulates into the latent tail's output."""
+    pushed into the tail's reduce-scatter partials): on the side stream the
+    shared expert's two calls, moe_shared_gate_up and moe_shared_down, with
+    static weights (each requests its first weight tiles before waiting for
+    the preceding kernel), write d = bf16(down(h)) into the last of the
+    latent tail's shared-partial slots ("two_branch_one_call": one
+    moe_shared_expert call instead); then moe_tail_latent_up_flags follows
+    with both promises -- inputs ready (the latent partials are read while
+    the down projection drains) and static weights -- and adds d with the
+    other slots in its epilogue; the call enqueues the norm and the
+    up-projection ("two_branch_split" makes the two split calls,
+    moe_tail_latent_norm and moe_tail_up_project, with the same promises).
+    EP and expert-TP finalize run on the main stream, which joins the side
+    stream at the end of the step.  Without a side stream the calls run in
+    order (moe_tail_latent_up in one call) and the shared expert accumulates
+    into the latent tail's output."""
     ev = events or [None] * EVENTS_PER_STEP
 
     def rec(i, st):
@@ -299,7 +302,34 @@ def run_step(mt, w, stream, events=None, side=None):
         mt.moe_shared_down(ws_h, w["w_down"], w["out"], accumulate=True, weights_static=True, stream=stream)
         rec(11, stream)
         return
-    if comp not in ("two_branch", "two_branch_split", "two_branch_static"):
+    if comp == "tp_after_gateup":
+        # as two_branch, with the shared expert as its two calls and expert-TP
+        # finalize started once gate/up has streamed its weights, so its rows
+        # share HBM with the down projection instead of with gate/up
+        bx = w["x"].shape[0]
+        ws_h = w["ws_sh"][: bx * I * 2].view(torch.bfloat16).view(bx, I)
+        w["fork"].record(stream)
+        side.wait_event(w["fork"])
+        rec(8, side)
+        mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], ws_h, weights_static=True, stream=side)
+        rec(9, side)
+        w["h_ready"].record(side)
+        rec(10, side)
+        mt.moe_shared_down(ws_h, w["w_down"], w["d_slot"], accumulate=False, weights_static=True, stream=side)
+        rec(11, side)
+        rec(4, side)
+        mt.moe_tail_latent_up_flags(w["latent"], w["lat_gamma"], w["w_up"], w["shared9"], w["out"], w["y"],
+                                    eps=1e-6, inputs_ready=True, weights_static=True, stream=side)
+        rec(5, side)
+        rec(6, side)
+        rec(7, side)
+        w["join"].record(side)
+        ep(stream)
+        stream.wait_event(w["h_ready"])
+        tp(stream)
+        stream.wait_event(w["join"])
+        return
+    if comp not in ("two_branch", "two_branch_split", "two_branch_one_call"):
         # the latent up-projection between the shared expert's gate/up and down
         # projections; down then adds d into the latent tail's output
         # (out = bf16(out + bf16(d)), the sequential composition's arithmetic)
@@ -337,14 +367,14 @@ def run_step(mt, w, stream, events=None, side=None):
         return
     w["fork"].record(stream)
     side.wait_event(w["fork"])
-    if comp == "two_branch_static":  # the shared expert as its two calls, weights requested before each wait
+    if comp != "two_branch_one_call":  # the shared expert as its two calls, weights requested before each wait
         bx = w["x"].shape[0]
         ws_h = w["ws_sh"][: bx * I * 2].view(torch.bfloat16).view(bx, I)
-        rec(8, side)
+        rec(8, side)  # one interval over both calls: an event between them would break their overlap
         mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], ws_h, weights_static=True, stream=side)
+        mt.moe_shared_down(ws_h, w["w_down"], w["d_slot"], accumulate=False, weights_static=True, stream=side)
         rec(9, side)
         rec(10, side)
-        mt.moe_shared_down(ws_h, w["w_down"], w["d_slot"], accumulate=False, weights_static=True, stream=side)
         rec(11, side)
     else:
         shared_expert(side, w["d_slot"], False)
@@ -649,7 +679,8 @@ def cuda_arm(args, world, rank, local):
     calls = {}
     hbm, bf16_tf, peak_kind = peaks()
     nbytes = dict(BYTES)
-    if side is not None and args.composition in ("two_branch", "two_branch_split", "two_branch_static"):  # d: a slot
+    if side is not None and args.composition in ("two_branch", "two_branch_split", "two_branch_one_call",
+                                                 "tp_after_gateup"):  # d: a slot
         nbytes["shared_expert"] = 3 * I * H * 2 + B * H * 2 + B * H * 2
         nbytes["latent_up"] = BYTES["latent_up"] + B * H * 2
     for c in CALLS:
@@ -685,14 +716,17 @@ def cuda_arm(args, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64 + Box-Muller; random-init weights)",
         "config": dict(workload_config(), composition=(
             "sequential: EP, TP, latent tail, then the shared expert accumulating into out" if side is None else
-            "two branches: on a side stream the shared expert writes d into an extra shared-partial slot, then the "
+            "two branches: on a side stream the shared expert (gate/up, then down, both with static weights) writes "
+            "d into an extra shared-partial slot, then the "
             "latent tail follows (its norm, then its up-projection), adding all slots; "
             "EP and TP on a high-priority stream beside them"
             if args.composition == "two_branch" else
             "two branches as two_branch, with the latent tail always as its two split calls"
             if args.composition == "two_branch_split" else
-            "two branches as two_branch, with the shared expert as its two calls with static weights"
-            if args.composition == "two_branch_static" else
+            "two branches as two_branch, with the shared expert as one moe_shared_expert call"
+            if args.composition == "two_branch_one_call" else
+            "two branches as two_branch, with expert-TP finalize started once gate/up is done"
+            if args.composition == "tp_after_gateup" else
             "two branches: the shared expert's gate/up on a side stream; EP, TP and the latent tail on a "
             "high-priority stream beside it; then the down projection adds d into the latent tail's output"
             if args.composition == "latent_main" else

@@ -1,6 +1,7 @@
 """The composed decode step exactly as bench.py times it (two branches: the
-shared expert then the latent tail on a side stream, EP and expert-TP
-finalize beside them; and the sequential composition, where the shared
+shared expert -- as its two calls, or as one -- then the latent tail on a
+side stream, EP and expert-TP finalize beside them; and the sequential
+composition, where the shared
 expert accumulates into the latent tail's output; and latent_main, where the
 latent tail runs beside the shared expert's gate/up and the down projection
 then accumulates into its output), checked against the oracle on sampled
@@ -29,7 +30,7 @@ def close(got, ref, what):
     assert not bool(bad.any()), f"{what}: {int(bad.sum())} of {bad.numel()} out of tolerance"
 
 
-@pytest.fixture(scope="module", params=["two_branch", "sequential", "latent_main"])
+@pytest.fixture(scope="module", params=["two_branch", "two_branch_one_call", "sequential", "latent_main"])
 def step(request):
     from moe_decode_tail_gb300 import build as cuda_build
 
@@ -82,7 +83,7 @@ def test_step_latent_tail_and_shared_expert(step):
     for t in TOKENS:
         y_ref = oracle.latent_norm(lat["latent"][:, t:t + 1].contiguous(), lat["gamma"], 1e-6, 1, TP, L)
         assert torch.equal(got["y"][t:t + 1].view(torch.int16), y_ref.view(torch.int16)), f"y token {t}"
-        if mode == "two_branch":
+        if mode.startswith("two_branch"):
             # d: a valid down projection of the GPU's h; out: the up-projection of y
             # plus all nine partials (d included)
             d_gpu = got["shared9"][TP]
