@@ -70,6 +70,9 @@ def parse_args():
                     choices=["two_branch", "two_branch_one_call", "two_branch_split", "tp_after_gateup", "latent_main",
                              "norm_main", "norm_side_first", "norm_side_after"],
                     help="how the step orders the weight-streaming calls (see run_step)")
+    ap.add_argument("--only-config", type=int, choices=[1, 2, 3, 4, 5], default=None,
+                    help="run one workload's call alone --calls times and exit (for profiling the call)")
+    ap.add_argument("--calls", type=int, default=4)
     ap.add_argument("--sequential", action="store_true",
                     help="run the four calls in order on one stream (shared expert accumulating into out)")
     return ap.parse_args()
@@ -1091,6 +1094,51 @@ def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
                           "one copy each way per step (activations and outputs packed in one buffer)"}
 
 
+def only_config(args) -> int:
+    """One workload's call, eagerly, --calls times on cuda:0 (for ncu): configs
+    1-2 EP finalize, 3 expert-TP finalize, 4 the latent tail (moe_tail_latent_up
+    and then moe_tail_latent_up_flags with both promises), 5 the shared expert
+    added into out."""
+    import moe_decode_tail_gb300 as mt
+    from moe_decode_tail_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n = args.only_config
+    d = synth.config(n)
+    g = lambda t: t.to(dev)
+    if n in (1, 2):
+        rows, idx, wt, gam = g(d["rows"]), g(d["idx"]), g(d["w"]), g(d["gamma"])
+        out = torch.empty((d["b"], d["P"]), dtype=torch.bfloat16, device=dev)
+        calls = [lambda: mt.moe_tail_ep_finalize(rows, idx, wt, gam, out, gain_center=d["gain_center"], eps=d["eps"],
+                                                 weight_before_norm=d["weight_before_norm"])]
+    elif n == 3:
+        parts, idx, wt, gam = g(d["partials"]), g(d["idx"]), g(d["w"]), g(d["gamma"])
+        out = torch.empty((d["b"], d["P"]), dtype=torch.bfloat16, device=dev)
+        calls = [lambda: mt.moe_tail_tp_finalize(parts, idx, wt, gam, out, gain_center=d["gain_center"], eps=d["eps"],
+                                                 weight_before_norm=d["weight_before_norm"])]
+    elif n == 4:
+        lat, gam, wu, sh = g(d["latent"]), g(d["gamma"]), g(d["w_up"]), g(d["shared"])
+        out = torch.empty((d["b"], d["H"]), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(mt.moe_tail_workspace_bytes(0, d["b"], d["L"]), dtype=torch.uint8, device=dev)
+        y = ws[: d["b"] * d["L"] * 2].view(torch.bfloat16).view(d["b"], d["L"])
+        calls = [lambda: mt.moe_tail_latent_up(lat, gam, wu, sh, out, ws, eps=d["eps"]),
+                 lambda: mt.moe_tail_latent_up_flags(lat, gam, wu, sh, out, y, eps=d["eps"], inputs_ready=True,
+                                                     weights_static=True)]
+    else:
+        x, wg, wu, wd = g(d["x"]), g(d["w_gate"]), g(d["w_up"]), g(d["w_down"])
+        out = torch.zeros((d["b"], d["H"]), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(mt.moe_tail_workspace_bytes(1, d["b"], d["I"]), dtype=torch.uint8, device=dev)
+        calls = [lambda: mt.moe_shared_expert(x, wg, wu, wd, out, ws, accumulate=True)]
+    for call in calls:
+        for _ in range(args.calls):
+            call()
+    torch.cuda.synchronize()
+    print(json.dumps({"only_config": n, "calls_each": args.calls, "forms": len(calls),
+                      "device_error": mt.moe_tail_take_device_error()}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
@@ -1098,6 +1146,8 @@ def main():
         return reference_arm(args, world, rank)
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device (the CUDA arm has no CPU fallback)")
+    if args.only_config is not None:
+        return only_config(args)
     return cuda_arm(args, world, rank, local)
 
 
