@@ -41,6 +41,17 @@ def test_header_declares_the_four_calls_and_helpers():
         assert n in names
 
 
+@pytest.mark.parametrize("lang", [["gcc", "-std=c99", "-x", "c"], ["g++", "-std=c++17", "-x", "c++"]])
+def test_headers_compile_as_c_and_cxx(tmp_path, lang):
+    # a plain C (and C++) consumer of the ABI: both headers, no warnings
+    src = tmp_path / "consumer.c"
+    src.write_text('#include "moe_tail.h"\n#include "moe_tail_trace.h"\n'
+                   "int main(void) { return moe_tail_workspace_bytes(0, 1, 8) == 0 ? 1 : 0; }\n")
+    inc = os.path.join(ROOT, "include")
+    subprocess.run(lang[:2] + ["-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only", "-I", inc] + lang[2:]
+                   + [str(src)], check=True, capture_output=True)
+
+
 def test_library_exports_every_declared_symbol(lib):
     for n in declared():
         assert hasattr(lib, n), n
