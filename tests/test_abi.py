@@ -52,6 +52,33 @@ def test_headers_compile_as_c_and_cxx(tmp_path, lang):
                    + [str(src)], check=True, capture_output=True)
 
 
+def test_c_program_links_and_calls_the_host_entries(tmp_path, lib):
+    # a C program linked against the library calls the entries that need no
+    # device: workspace sizes, status strings, and a refused call (b = 0 with
+    # null pointers succeeds; a bad size is refused before any CUDA call)
+    src = tmp_path / "host.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "moe_tail.h"
+int main(void) {
+  if (moe_tail_workspace_bytes(0, 16, 3584) < (size_t)16 * 3584 * 2) return 1;
+  if (moe_tail_workspace_bytes(2, 16, 3584) != 0) return 2;
+  if (strlen(moe_tail_status_str(MOE_TAIL_EINVAL)) == 0) return 3;
+  if (moe_tail_latent_up(0, 0, 1e-6f, 0, 0, 0, 0, 1, 8, 8, 0, 0, 0, 0) != MOE_TAIL_OK) return 4;
+  if (moe_tail_latent_up(0, 0, 1e-6f, 0, 0, 0, 1, 0, 8, 8, 0, 0, 0, 0) != MOE_TAIL_EINVAL) return 5;
+  puts("ok");
+  return 0;
+}
+""")
+    exe = tmp_path / "host"
+    libdir = os.path.dirname(cuda_build.LIB)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-o", str(exe), cuda_build.LIB, "-Wl,-rpath," + libdir], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)
+
+
 def test_library_exports_every_declared_symbol(lib):
     for n in declared():
         assert hasattr(lib, n), n
