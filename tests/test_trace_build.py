@@ -59,3 +59,43 @@ def test_traced_calls_leave_one_record_per_cta(trace_lib):
     r = subprocess.run([sys.executable, "-c", CHILD], capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "trace ok" in r.stdout
+
+
+def _rec(kid, cta, sm, t0, marks, t1):
+    return (kid, cta, sm, t0, tuple(marks), t1)
+
+
+def test_launches_cut_records_into_grids():
+    # two launches of a 3-CTA kernel and one of a 2-CTA kernel, records out of
+    # order: grouped per kernel by start time, in consecutive grid-sized groups
+    from moe_decode_tail_gb300.trace import launches
+
+    recs = [_rec(40, 1, 0, 1010, [0] * 4, 2000), _rec(31, 0, 3, 100, [0] * 4, 900),
+            _rec(40, 0, 1, 1000, [0] * 4, 2100), _rec(40, 2, 2, 5, [0] * 4, 800),
+            _rec(40, 0, 2, 0, [0] * 4, 700), _rec(40, 1, 5, 3, [0] * 4, 650), _rec(40, 2, 4, 1020, [0] * 4, 2050),
+            _rec(31, 1, 4, 110, [0] * 4, 950)]
+    ls = launches(recs)
+    by_kernel = {}
+    for kid, ordinal, rs in ls:
+        by_kernel.setdefault(kid, []).append((ordinal, sorted(r[1] for r in rs), min(r[3] for r in rs)))
+    assert sorted(by_kernel) == [31, 40]
+    assert by_kernel[31] == [(0, [0, 1], 100)]
+    assert sorted(by_kernel[40]) == [(0, [0, 1, 2], 0), (1, [0, 1, 2], 1000)]
+
+
+def test_describe_reads_gemm_and_one_kernel_marks():
+    # a GEMM launch: marks 0 (accumulator), 1 (staged), 2 (peers), 3 (stores);
+    # the one-kernel latent tail: marks 1 (x formed), 2 (y ready), 0 (accumulator)
+    from moe_decode_tail_gb300.trace import describe
+
+    gemm = [_rec(30, c, c, 1000 * c, [1000 * c + 9000, 1000 * c + 9400, 1000 * c + 10400, 1000 * c + 12400],
+                 1000 * c + 13800) for c in range(3)]
+    fused = [_rec(33, c, c, 500 * c, [500 * c + 11000, 500 * c + 2000, 500 * c + 6500, 0], 500 * c + 14000)
+             for c in range(3)]
+    lines = describe([(30, 0, gemm), (33, 0, fused)])
+    gemm_line = next(line for line in lines if line.startswith("up-projection GEMM"))
+    fused_line = next(line for line in lines if line.startswith("latent tail (one kernel)"))
+    assert "K loop p50   9.0" in gemm_line
+    assert "stage 0.4 peers 1.0 reduce 2.0 barrier+exit 1.4" in gemm_line
+    assert "x formed p50   2.0  y ready   6.5  accumulator  11.0" in fused_line
+    assert "CTAs    3" in gemm_line and "CTA p50  13.8" in gemm_line
