@@ -247,16 +247,20 @@ def run_step(mt, w, stream, events=None, side=None):
         if ev[i] is not None:
             ev[i].record(st)
 
+    ready = w.get("finalize_ready", False)  # EP and TP with the inputs-ready promise
+
     def ep(st):
         rec(0, st)
-        mt.moe_tail_ep_finalize(w["ep_rows"], w["ep_idx"], w["ep_w"], w["ep_gamma"], w["out_ep"], gain_center=1.0,
-                                eps=1e-6, weight_before_norm=True, stream=st)
+        mt.moe_tail_ep_finalize_flags(w["ep_rows"], w["ep_idx"], w["ep_w"], w["ep_gamma"], w["out_ep"],
+                                      gain_center=1.0, eps=1e-6, weight_before_norm=True, inputs_ready=ready,
+                                      stream=st)
         rec(1, st)
 
     def tp(st):
         rec(2, st)
-        mt.moe_tail_tp_finalize(w["tp_part"], w["tp_idx"], w["tp_w"], w["tp_gamma"], w["out_tp"], gain_center=1.0,
-                                eps=1e-6, weight_before_norm=True, stream=st)
+        mt.moe_tail_tp_finalize_flags(w["tp_part"], w["tp_idx"], w["tp_w"], w["tp_gamma"], w["out_tp"],
+                                      gain_center=1.0, eps=1e-6, weight_before_norm=True, inputs_ready=ready,
+                                      stream=st)
         rec(3, st)
 
     def shared_expert(st, out, accumulate):
@@ -820,7 +824,7 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
                     "hbm_frac": round(gbs / hbm, 4), "hbm_frac_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
                     "input_copies": copies, "target": target}
 
-    def ep_like(key, d, target, n=None):
+    def ep_like(key, d, target, n=None, ready_key=None):
         nb = config_bytes("ep", d)
         n = n or copies_for(nb)
         rows = [d["rows"].to(dev)] + [None] * (n - 1)
@@ -832,9 +836,14 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
                                                      eps=d["eps"], weight_before_norm=d["weight_before_norm"],
                                                      stream=stream), n)
         report(key, us, nb, n, target)
+        if ready_key:  # the same call with the inputs-ready promise (moe_tail_ep_finalize_flags)
+            us = timed(lambda i: mt.moe_tail_ep_finalize_flags(
+                rows[i], idx, wt, gam, out, gain_center=d["gain_center"], eps=d["eps"],
+                weight_before_norm=d["weight_before_norm"], inputs_ready=True, stream=stream), n)
+            report(ready_key, us, nb, n, target)
 
     ep_like("1_ep_tiny_b4_P512", synth.config(1), "parity; latency-bound (report us; inputs L2-resident)", n=1)
-    ep_like("2_ep_b64_P4096", cpu["ep"], ">= 0.70 of HBM (hard at 4.7 MB)")
+    ep_like("2_ep_b64_P4096", cpu["ep"], ">= 0.70 of HBM (hard at 4.7 MB)", ready_key="2_ep_b64_P4096_ready")
 
     d = synth.config(3)
     nb = config_bytes("tp", d)
@@ -847,6 +856,12 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
                                                  eps=d["eps"], weight_before_norm=d["weight_before_norm"],
                                                  stream=stream), n)
     report("3_tp_b128_P4096", us, nb, n, ">= 0.70 of HBM")
+    # ... with the inputs-ready promise (moe_tail_tp_finalize_flags): each call reads its
+    # partials while the previous call drains
+    us = timed(lambda i: mt.moe_tail_tp_finalize_flags(parts[i], idx, wt, gam, out, gain_center=d["gain_center"],
+                                                       eps=d["eps"], weight_before_norm=d["weight_before_norm"],
+                                                       inputs_ready=True, stream=stream), n)
+    report("3_tp_b128_P4096_ready", us, nb, n, ">= 0.70 of HBM")
     del parts
 
     d = synth.config(4)

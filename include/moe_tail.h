@@ -101,6 +101,28 @@ int moe_tail_tp_finalize(const void* partials, int64_t num_rows, const int32_t* 
                          int P, void* out, void* stream);
 
 /*
+ * The two finalize calls with a scheduling promise (no counterpart on the
+ * pages as calls): the same arguments, results and refusals as
+ * moe_tail_ep_finalize / moe_tail_tp_finalize, plus
+ *   flags: 0, or MOE_TAIL_INPUTS_READY (defined below) -- a promise that the
+ *   rows or partials, the indices, the route weights and gamma are not being
+ *   written by work still in flight on the stream when the call is enqueued.
+ *   The kernel then reads them while the stream's preceding kernel still runs
+ *   (with programmatic dependent launch) and waits for that kernel only
+ *   before it writes out, which in-flight work may still be reading.
+ * Back to back on static inputs this hides most of a call's first trip to
+ * memory behind the previous call.
+ */
+int moe_tail_ep_finalize_flags(const void* rows, int64_t rows_per_slot, const int32_t* permuted_idx,
+                               const void* route_weights, int weight_dtype, const void* gamma,
+                               float gain_center, float eps, int weight_before_norm, int b, int tp, int K,
+                               int P, void* out, int flags, void* stream);
+int moe_tail_tp_finalize_flags(const void* partials, int64_t num_rows, const int32_t* permuted_idx,
+                               const void* route_weights, int weight_dtype, const void* gamma,
+                               float gain_center, float eps, int weight_before_norm, int b, int tp, int K,
+                               int P, void* out, int flags, void* stream);
+
+/*
  * Latent tail ([KT] module docstring): the latent partials of the tp slots
  * are summed, RMS-normalised per row, up-projected and the shared expert's
  * partials are added:

@@ -19,7 +19,8 @@ __all__ = [
     "moe_shared_expert", "moe_tail_workspace_bytes", "moe_tail_status_str", "moe_tail_take_device_error",
     "moe_tail_latent_up_noalloc", "NOALLOC_SCRATCH_BYTES", "moe_tail_selftest_wait_timeout",
     "moe_tail_latent_norm", "moe_tail_up_project", "WEIGHTS_STATIC", "INPUTS_READY",
-    "moe_shared_gate_up", "moe_shared_down", "moe_tail_latent_up_flags",
+    "moe_shared_gate_up", "moe_shared_down", "moe_tail_latent_up_flags", "moe_tail_ep_finalize_flags",
+    "moe_tail_tp_finalize_flags",
 ]
 
 OK, EINVAL, ECUDA, ENOTSUP = 0, 1, 2, 3
@@ -52,6 +53,9 @@ def lib() -> ctypes.CDLL:
         fin = [P, i64, P, P, i32, P, f32, f32, i32, i32, i32, i32, i32, P, P]
         L.moe_tail_ep_finalize.argtypes = fin
         L.moe_tail_tp_finalize.argtypes = fin
+        fin_flags = fin[:-1] + [i32, P]
+        L.moe_tail_ep_finalize_flags.argtypes = fin_flags
+        L.moe_tail_tp_finalize_flags.argtypes = fin_flags
         L.moe_tail_latent_up.argtypes = [P, P, f32, P, P, i32, i32, i32, i32, i32, P, P, sz, P]
         L.moe_shared_expert.argtypes = [P, P, P, P, i32, i32, i32, P, i32, P, sz, P]
         L.moe_tail_latent_up_noalloc.argtypes = [P, P, f32, P, P, i32, i32, i32, i32, i32, P, P]
@@ -69,7 +73,7 @@ def lib() -> ctypes.CDLL:
         for name in ("moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up", "moe_shared_expert",
                      "moe_tail_take_device_error", "moe_tail_latent_up_noalloc", "moe_tail_selftest_wait_timeout",
                      "moe_tail_latent_norm", "moe_tail_up_project", "moe_shared_gate_up", "moe_shared_down",
-                     "moe_tail_latent_up_flags"):
+                     "moe_tail_latent_up_flags", "moe_tail_ep_finalize_flags", "moe_tail_tp_finalize_flags"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -131,6 +135,34 @@ def moe_tail_tp_finalize(partials, permuted_idx, route_weights, gamma, out, *, g
     _check("moe_tail_tp_finalize", lib().moe_tail_tp_finalize(
         _p(partials), num_rows, _p(permuted_idx), _p(route_weights), _weights(route_weights), _p(gamma),
         gain_center, eps, int(bool(weight_before_norm)), b, tp, K, P, _p(out), _stream(stream)))
+    return out
+
+
+def moe_tail_ep_finalize_flags(rows, permuted_idx, route_weights, gamma, out, *, gain_center=1.0, eps=1e-6,
+                               weight_before_norm=True, inputs_ready=False, stream=None) -> torch.Tensor:
+    """moe_tail_ep_finalize with the promise inputs_ready: rows, indices, route
+    weights and gamma are not written by work still in flight on the stream."""
+    _cuda(rows, permuted_idx, route_weights, gamma, out)
+    tp, rows_per_slot, P = rows.shape
+    b, K = route_weights.shape
+    _check("moe_tail_ep_finalize_flags", lib().moe_tail_ep_finalize_flags(
+        _p(rows), rows_per_slot, _p(permuted_idx), _p(route_weights), _weights(route_weights), _p(gamma),
+        gain_center, eps, int(bool(weight_before_norm)), b, tp, K, P, _p(out), INPUTS_READY if inputs_ready else 0,
+        _stream(stream)))
+    return out
+
+
+def moe_tail_tp_finalize_flags(partials, permuted_idx, route_weights, gamma, out, *, gain_center=1.0, eps=1e-6,
+                               weight_before_norm=True, inputs_ready=False, stream=None) -> torch.Tensor:
+    """moe_tail_tp_finalize with the promise inputs_ready: partials, indices,
+    route weights and gamma are not written by work still in flight on the stream."""
+    _cuda(partials, permuted_idx, route_weights, gamma, out)
+    tp, num_rows, P = partials.shape
+    b, K = route_weights.shape
+    _check("moe_tail_tp_finalize_flags", lib().moe_tail_tp_finalize_flags(
+        _p(partials), num_rows, _p(permuted_idx), _p(route_weights), _weights(route_weights), _p(gamma),
+        gain_center, eps, int(bool(weight_before_norm)), b, tp, K, P, _p(out), INPUTS_READY if inputs_ready else 0,
+        _stream(stream)))
     return out
 
 

@@ -100,59 +100,27 @@ int check_finalize_common(const void* w, int weight_dtype, const void* gamma, in
 
 // ============================================================================ EP finalize
 
-MOE_API int moe_tail_ep_finalize(const void* rows, int64_t rows_per_slot, const int32_t* permuted_idx,
-                                 const void* route_weights, int weight_dtype, const void* gamma,
-                                 float gain_center, float eps, int weight_before_norm, int b, int tp, int K,
-                                 int P, void* out, void* stream) {
-  int rc = check_finalize_common(route_weights, weight_dtype, gamma, b, tp, K, P, out);
-  if (rc != MOE_TAIL_OK || b == 0) return rc;
-  if (rows_per_slot < 0 || rows_per_slot > ((int64_t)1 << 31) - 1) return MOE_TAIL_EINVAL;
-  if (!permuted_idx || !aligned(permuted_idx, 4)) return MOE_TAIL_EINVAL;
-  if (rows_per_slot > 0 && (!rows || !aligned(rows, 16))) return MOE_TAIL_EINVAL;
-  const Range o = span(out, (size_t)b * P * 2);
-  const size_t wsz = weight_dtype == MOE_TAIL_W_FP32 ? 4 : 2;
-  if (overlaps(o, span(rows, (size_t)tp * rows_per_slot * P * 2)) ||
-      overlaps(o, span(permuted_idx, (size_t)tp * b * K * 4)) || overlaps(o, span(route_weights, (size_t)b * K * wsz)) ||
-      overlaps(o, span(gamma, (size_t)P * 2)))
-    return MOE_TAIL_EINVAL;
-  FinalizeArgs a;
-  a.rows = static_cast<const uint16_t*>(rows);
-  a.num_rows = rows_per_slot;
-  a.slot_stride = rows_per_slot * P;
-  a.idx = permuted_idx;
-  a.w = route_weights;
-  a.gamma = static_cast<const uint16_t*>(gamma);
-  a.gain_center = gain_center;
-  a.eps = eps;
-  a.rcpP = (float)(1.0 / (double)P);
-  a.b = b;
-  a.tp = tp;
-  a.K = K;
-  a.P = P;
-  a.out = static_cast<uint16_t*>(out);
-  return finish(moetail::launch_finalize(moetail::kFinalizeEP, a, weight_before_norm != 0, weight_dtype,
-                                         device_sms(), static_cast<cudaStream_t>(stream)));
-}
+namespace {
 
-// ============================================================================ expert-TP finalize
-
-MOE_API int moe_tail_tp_finalize(const void* partials, int64_t num_rows, const int32_t* permuted_idx,
-                                 const void* route_weights, int weight_dtype, const void* gamma,
-                                 float gain_center, float eps, int weight_before_norm, int b, int tp, int K,
-                                 int P, void* out, void* stream) {
+// EP or expert-TP finalize after the common checks; flags: 0 or MOE_TAIL_INPUTS_READY.
+int finalize_call(int mode, const void* rows, int64_t num_rows, const int32_t* permuted_idx,
+                  const void* route_weights, int weight_dtype, const void* gamma, float gain_center, float eps,
+                  int weight_before_norm, int b, int tp, int K, int P, void* out, int flags, void* stream) {
   int rc = check_finalize_common(route_weights, weight_dtype, gamma, b, tp, K, P, out);
+  if (rc == MOE_TAIL_OK && (flags & ~MOE_TAIL_INPUTS_READY)) rc = MOE_TAIL_EINVAL;
   if (rc != MOE_TAIL_OK || b == 0) return rc;
   if (num_rows < 0 || num_rows > ((int64_t)1 << 31) - 1) return MOE_TAIL_EINVAL;
   if (!permuted_idx || !aligned(permuted_idx, 4)) return MOE_TAIL_EINVAL;
-  if (num_rows > 0 && (!partials || !aligned(partials, 16))) return MOE_TAIL_EINVAL;
+  if (num_rows > 0 && (!rows || !aligned(rows, 16))) return MOE_TAIL_EINVAL;
   const Range o = span(out, (size_t)b * P * 2);
   const size_t wsz = weight_dtype == MOE_TAIL_W_FP32 ? 4 : 2;
-  if (overlaps(o, span(partials, (size_t)tp * num_rows * P * 2)) ||
-      overlaps(o, span(permuted_idx, (size_t)b * K * 4)) || overlaps(o, span(route_weights, (size_t)b * K * wsz)) ||
-      overlaps(o, span(gamma, (size_t)P * 2)))
+  const size_t idx_count = (mode == moetail::kFinalizeEP ? (size_t)tp : 1) * b * K;  // EP: [tp][b][K]
+  if (overlaps(o, span(rows, (size_t)tp * num_rows * P * 2)) || overlaps(o, span(permuted_idx, idx_count * 4)) ||
+      overlaps(o, span(route_weights, (size_t)b * K * wsz)) || overlaps(o, span(gamma, (size_t)P * 2)))
     return MOE_TAIL_EINVAL;
   FinalizeArgs a;
-  a.rows = static_cast<const uint16_t*>(partials);
+  a.inputs_before_wait = (flags & MOE_TAIL_INPUTS_READY) ? 1 : 0;
+  a.rows = static_cast<const uint16_t*>(rows);
   a.num_rows = num_rows;
   a.slot_stride = num_rows * P;
   a.idx = permuted_idx;
@@ -166,8 +134,44 @@ MOE_API int moe_tail_tp_finalize(const void* partials, int64_t num_rows, const i
   a.K = K;
   a.P = P;
   a.out = static_cast<uint16_t*>(out);
-  return finish(moetail::launch_finalize(moetail::kFinalizeTP, a, weight_before_norm != 0, weight_dtype,
-                                         device_sms(), static_cast<cudaStream_t>(stream)));
+  return finish(moetail::launch_finalize(mode, a, weight_before_norm != 0, weight_dtype, device_sms(),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+MOE_API int moe_tail_ep_finalize(const void* rows, int64_t rows_per_slot, const int32_t* permuted_idx,
+                                 const void* route_weights, int weight_dtype, const void* gamma,
+                                 float gain_center, float eps, int weight_before_norm, int b, int tp, int K,
+                                 int P, void* out, void* stream) {
+  return finalize_call(moetail::kFinalizeEP, rows, rows_per_slot, permuted_idx, route_weights, weight_dtype, gamma,
+                       gain_center, eps, weight_before_norm, b, tp, K, P, out, 0, stream);
+}
+
+MOE_API int moe_tail_ep_finalize_flags(const void* rows, int64_t rows_per_slot, const int32_t* permuted_idx,
+                                       const void* route_weights, int weight_dtype, const void* gamma,
+                                       float gain_center, float eps, int weight_before_norm, int b, int tp, int K,
+                                       int P, void* out, int flags, void* stream) {
+  return finalize_call(moetail::kFinalizeEP, rows, rows_per_slot, permuted_idx, route_weights, weight_dtype, gamma,
+                       gain_center, eps, weight_before_norm, b, tp, K, P, out, flags, stream);
+}
+
+// ============================================================================ expert-TP finalize
+
+MOE_API int moe_tail_tp_finalize(const void* partials, int64_t num_rows, const int32_t* permuted_idx,
+                                 const void* route_weights, int weight_dtype, const void* gamma,
+                                 float gain_center, float eps, int weight_before_norm, int b, int tp, int K,
+                                 int P, void* out, void* stream) {
+  return finalize_call(moetail::kFinalizeTP, partials, num_rows, permuted_idx, route_weights, weight_dtype, gamma,
+                       gain_center, eps, weight_before_norm, b, tp, K, P, out, 0, stream);
+}
+
+MOE_API int moe_tail_tp_finalize_flags(const void* partials, int64_t num_rows, const int32_t* permuted_idx,
+                                       const void* route_weights, int weight_dtype, const void* gamma,
+                                       float gain_center, float eps, int weight_before_norm, int b, int tp, int K,
+                                       int P, void* out, int flags, void* stream) {
+  return finalize_call(moetail::kFinalizeTP, partials, num_rows, permuted_idx, route_weights, weight_dtype, gamma,
+                       gain_center, eps, weight_before_norm, b, tp, K, P, out, flags, stream);
 }
 
 // ============================================================================ latent tail

@@ -142,6 +142,29 @@ def test_bf16_weights_need_only_2_byte_alignment_but_fp32_need_4(lib):
     assert ep(lib, w=a(2), wd=1, out=a(0), rps=0, rows=None) == EINVAL
 
 
+def fin_flags(lib, which, **kw):
+    args = dict(rows=a(), n=8, idx=a(1 << 24), w=a(2 << 24), wd=0, gamma=a(3 << 24), gc=1.0, eps=1e-6, wbn=1, b=4,
+                tp=2, K=4, P=512, out=a(4 << 24), flags=2, stream=None)
+    args.update(kw)
+    fn = lib.moe_tail_ep_finalize_flags if which == "ep" else lib.moe_tail_tp_finalize_flags
+    return fn(args["rows"], args["n"], args["idx"], args["w"], args["wd"], args["gamma"], args["gc"], args["eps"],
+              args["wbn"], args["b"], args["tp"], args["K"], args["P"], args["out"], args["flags"], args["stream"])
+
+
+@host_only
+@pytest.mark.parametrize("which", ["ep", "tp"])
+@pytest.mark.parametrize("bad", [dict(flags=1), dict(flags=4), dict(flags=-1), dict(tp=0), dict(P=100),
+                                 dict(idx=None), dict(out=a(3 << 24))])
+def test_finalize_flags_refuse_bad_arguments(lib, which, bad):
+    assert fin_flags(lib, which, **bad) == EINVAL
+
+
+@host_only
+@pytest.mark.parametrize("which", ["ep", "tp"])
+def test_finalize_flags_b_zero(lib, which):
+    assert fin_flags(lib, which, b=0, rows=None, idx=None, w=None, out=None) == OK
+
+
 def latent(lib, **kw):
     args = dict(lat=a(), gamma=a(1 << 24), eps=1e-6, w=a(2 << 24), sh=a(3 << 24), tp_s=8, b=16, tp=8, L=3584, H=7168,
                 out=a(4 << 24), ws=a(5 << 24), wsb=16 * 3584 * 2, stream=None)

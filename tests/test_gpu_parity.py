@@ -370,6 +370,66 @@ def test_tp_both_kernels(mt, monkeypatch, staged, b):
     assert_bitexact(run_tp(mt, d), ref_tp(d), f"TP b={b} staged={staged}")
 
 
+@pytest.mark.parametrize("kind", ["ep", "tp_staged", "tp_route_parallel"])
+def test_finalize_flags_call_matches_plain_call(mt, monkeypatch, kind):
+    # the calls with MOE_TAIL_INPUTS_READY give the plain calls' bits
+    if kind == "ep":
+        d = synth.config(2)
+        plain = run_ep(mt, d)
+        out = torch.full_like(plain, float("nan"))
+        mt.moe_tail_ep_finalize_flags(d["rows"].to(DEV), d["idx"].to(DEV), d["w"].to(DEV), d["gamma"].to(DEV), out,
+                                      gain_center=d["gain_center"], eps=d["eps"],
+                                      weight_before_norm=d["weight_before_norm"], inputs_ready=True)
+        ref = ref_ep(d)
+    else:
+        monkeypatch.setenv("MOE_TAIL_FIN_STAGED", "1" if kind == "tp_staged" else "0")
+        d = synth.config(3, b=64)
+        plain = run_tp(mt, d)
+        out = torch.full_like(plain, float("nan"))
+        mt.moe_tail_tp_finalize_flags(d["partials"].to(DEV), d["idx"].to(DEV), d["w"].to(DEV), d["gamma"].to(DEV),
+                                      out, gain_center=d["gain_center"], eps=d["eps"],
+                                      weight_before_norm=d["weight_before_norm"], inputs_ready=True)
+        ref = ref_tp(d)
+    torch.cuda.synchronize()
+    assert_bitexact(out, plain, f"{kind} flags call vs plain call")
+    assert_bitexact(out, ref, f"{kind} flags call vs oracle")
+    assert mt.moe_tail_take_device_error() == 0
+
+
+@pytest.mark.parametrize("staged", ["0", "1"])
+def test_tp_flags_inputs_ready_waits_before_writing_out(mt, monkeypatch, staged):
+    # on one stream: TP(Q1) -> X; TP reading X as its partials -> Y; then TP with
+    # inputs_ready from Q3 into X.  The last call may start while the second
+    # still reads X, so it writes X only after that call ends: Y is the
+    # finalize of TP(Q1), X that of Q3.
+    monkeypatch.setenv("MOE_TAIL_FIN_STAGED", staged)
+    b, tp, K, P = 64, 8, 8, 4096
+    d1 = synth.tp_finalize_inputs(0xC1, b=b, tp=tp, P=P, K=K)
+    d3 = synth.tp_finalize_inputs(0xC3, b=b, tp=tp, P=P, K=K)
+    b2, K2 = 16, 4
+    idx2 = torch.from_numpy((synth.u64(0xC2, 1, b2 * K2) % b).astype(np.int32).reshape(b2, K2))
+    w2 = synth.softmax_weights(0xC2, 2, b2, K2)
+    x1_ref = ref_tp(d1)
+    d2 = dict(partials=x1_ref.reshape(1, b, P), num_rows=b, idx=idx2, w=w2, gamma=d1["gamma"], gain_center=1.0,
+              eps=1e-6, weight_before_norm=True, b=b2, tp=1, K=K2, P=P)
+    y_ref = ref_tp(d2)
+    x3_ref = ref_tp(d3)
+    X = torch.empty((b, P), dtype=torch.bfloat16, device=DEV)
+    Y = torch.full((b2, P), float("nan"), dtype=torch.bfloat16, device=DEV)
+    q1, q3 = d1["partials"].to(DEV), d3["partials"].to(DEV)
+    idx1, idx3, i2 = d1["idx"].to(DEV), d3["idx"].to(DEV), idx2.to(DEV)
+    w1, w3, ww2, gam = d1["w"].to(DEV), d3["w"].to(DEV), w2.to(DEV), d1["gamma"].to(DEV)
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    mt.moe_tail_tp_finalize(q1, idx1, w1, gam, X, stream=st)
+    mt.moe_tail_tp_finalize(X.view(1, b, P), i2, ww2, gam, Y, stream=st)
+    mt.moe_tail_tp_finalize_flags(q3, idx3, w3, d3["gamma"].to(DEV), X, inputs_ready=True, stream=st)
+    torch.cuda.synchronize()
+    assert_bitexact(Y, y_ref, "the call reading X saw the first X")
+    assert_bitexact(X, x3_ref, "X is the last call's output")
+    assert mt.moe_tail_take_device_error() == 0
+
+
 # ------------------------------------------------------------------ latent tail
 
 def run_latent(mt, d):
