@@ -899,6 +899,16 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
     out = torch.zeros((B, H), dtype=torch.bfloat16, device=dev)
     us = timed(lambda i: mt.moe_shared_expert(w["x"], *ws_[i], out, w["ws_sh"], accumulate=True, stream=stream), n)
     report("5_shared_expert_b64", us, nb, n, ">= 0.60 of the weight-stream roofline")
+    # ... as its two calls with static weights: each gate/up requests its first
+    # weight tiles while the previous call's down projection drains
+    h_ = w["ws_sh"][: B * I * 2].view(torch.bfloat16).view(B, I)
+
+    def shared_static(i):
+        mt.moe_shared_gate_up(w["x"], ws_[i][0], ws_[i][1], h_, weights_static=True, stream=stream)
+        mt.moe_shared_down(h_, ws_[i][2], out, accumulate=True, weights_static=True, stream=stream)
+
+    us = timed(shared_static, n)
+    report("5_shared_expert_b64_static", us, nb, n, ">= 0.60 of the weight-stream roofline")
 
     # the composed layer of configs 4 and 5 at b = 64: the shared expert writes d into
     # the latent tail's extra partial slot, then the latent tail's two calls follow
