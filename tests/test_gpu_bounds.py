@@ -58,7 +58,10 @@ def test_ep_finalize(mt, kw):
     rows, idx, w, gam = dev(d, "rows", "idx", "w", "gamma")
     mt.moe_tail_ep_finalize(rows, idx, w, gam, out.t, gain_center=d["gain_center"], eps=d["eps"],
                             weight_before_norm=True)
-    assert out.intact()
+    out2 = Guarded((d["b"], d["P"]))
+    mt.moe_tail_ep_finalize_flags(rows, idx, w, gam, out2.t, gain_center=d["gain_center"], eps=d["eps"],
+                                  weight_before_norm=True, inputs_ready=True)
+    assert out.intact() and out2.intact()
     assert mt.moe_tail_take_device_error() == 0
 
 
@@ -71,7 +74,10 @@ def test_tp_finalize(mt, monkeypatch, staged, kw):
     parts, idx, w, gam = dev(d, "partials", "idx", "w", "gamma")
     mt.moe_tail_tp_finalize(parts, idx, w, gam, out.t, gain_center=d["gain_center"], eps=d["eps"],
                             weight_before_norm=False)
-    assert out.intact()
+    out2 = Guarded((d["b"], d["P"]))
+    mt.moe_tail_tp_finalize_flags(parts, idx, w, gam, out2.t, gain_center=d["gain_center"], eps=d["eps"],
+                                  weight_before_norm=False, inputs_ready=True)
+    assert out.intact() and out2.intact()
     assert mt.moe_tail_take_device_error() == 0
 
 
