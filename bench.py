@@ -1025,6 +1025,17 @@ def step_by_batch(mt, w, dev, stream, side, sizes=(1, 8, 32, 128)) -> dict:
     return res
 
 
+def packed_layout(named):
+    """Byte offsets of tensors packed one after another in one buffer, each
+    256-byte aligned (the calls want 16), and the buffer's size: named is a
+    list of (name, tensor)."""
+    offs, off = {}, 0
+    for k, t in named:
+        offs[k] = off
+        off = (off + t.numel() * t.element_size() + 255) // 256 * 256
+    return offs, off
+
+
 def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
     """The same step through the public API with host buffers: every step
     copies its activations from pinned host memory and reads its outputs back
@@ -1039,26 +1050,19 @@ def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
     inputs = ["ep_rows", "ep_idx", "ep_w", "tp_part", "tp_idx", "tp_w", "latent", "x"]
     outputs = ["out_ep", "out_tp", "out"]
 
-    def layout(keys, extra=()):
-        offs, off = {}, 0
-        for k, t in [(k, w[k]) for k in keys] + list(extra):
-            offs[k] = off
-            off = (off + t.numel() * t.element_size() + 255) // 256 * 256
-        return offs, off
-
     def view(buf, offs, k, like):
         n = like.numel() * like.element_size()
         return buf[offs[k]: offs[k] + n].view(like.dtype).view(like.shape)
 
     # inputs, then the latent tail's shared-partial slots with the shared expert's
     # slot last: the copy covers every input and stops before that slot
-    in_offs, in_total = layout(inputs, [("shared9", w["shared9"])])
+    in_offs, in_total = packed_layout([(k, w[k]) for k in inputs] + [("shared9", w["shared9"])])
     h2d = in_offs["shared9"] + w["shared"].numel() * w["shared"].element_size()
     host_in = torch.empty(h2d, dtype=torch.uint8).pin_memory()
     for k in inputs:
         view(host_in, in_offs, k, w[k]).copy_(w[k].cpu())
     view(host_in, in_offs, "shared9", w["shared"]).copy_(w["shared"].cpu())
-    out_offs, out_total = layout(outputs)
+    out_offs, out_total = packed_layout([(k, w[k]) for k in outputs])
     host_out = [torch.empty(out_total, dtype=torch.uint8).pin_memory() for _ in range(2)]
     d2h = out_total
     sets = []

@@ -1,0 +1,45 @@
+"""Host-side pieces of bench.py that need no GPU: the argument defaults keep
+the timing contract, and the end-to-end leg's packed buffers lay the step's
+activations out aligned, without overlap, with the copied region ending before
+the shared expert's output slot."""
+import importlib.util
+import os
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_host", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_defaults_keep_the_timing_contract(bench, monkeypatch):
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse_args()
+    assert a.gpus == 1 and a.impl == "cuda" and a.warmup >= 3 and a.steps >= 1000
+    assert a.composition == "two_branch" and not a.sequential
+
+
+def test_packed_layout_of_the_step_inputs(bench):
+    B, TP, P, K, L, H = bench.B, bench.TP, bench.P, bench.K_ROUTES, bench.L, bench.H
+    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+    named = [("ep_rows", torch.empty((TP, 65, P), dtype=bf)), ("ep_idx", torch.empty((TP, B, K), dtype=i32)),
+             ("ep_w", torch.empty((B, K), dtype=f32)), ("tp_part", torch.empty((TP, B * K, P), dtype=bf)),
+             ("tp_idx", torch.empty((B, K), dtype=i32)), ("tp_w", torch.empty((B, K), dtype=f32)),
+             ("latent", torch.empty((TP, B, L), dtype=bf)), ("x", torch.empty((B, H), dtype=bf)),
+             ("shared9", torch.empty((TP + 1, B, H), dtype=bf))]
+    offs, total = bench.packed_layout(named)
+    spans = sorted((offs[k], offs[k] + t.numel() * t.element_size()) for k, t in named)
+    assert all(o % 256 == 0 for o in offs.values())
+    assert all(a_end <= b_start for (_, a_end), (b_start, _) in zip(spans, spans[1:]))
+    assert spans[-1][1] <= total < spans[-1][1] + 256
+    # the step copies everything up to the end of the latent tail's TP shared slots
+    h2d = offs["shared9"] + TP * B * H * 2
+    assert h2d == spans[-1][1] - B * H * 2
