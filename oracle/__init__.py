@@ -27,7 +27,12 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (contraction off: no fused multiply-add)."""
+    """Compile the oracle with gcc (contraction off: no fused multiply-add).
+    MOE_TAIL_ORACLE_LIBRARY names another build of it to use instead (the
+    tests that plant mistakes in a copy of the source use this)."""
+    other = os.environ.get("MOE_TAIL_ORACLE_LIBRARY")
+    if other:
+        return other
     if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < os.path.getmtime(_SRC):
         os.makedirs(_BUILD, exist_ok=True)
         tmp = LIB_PATH + f".tmp{os.getpid()}"
@@ -39,8 +44,7 @@ def build(force: bool = False) -> str:
 def lib():
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(LIB_PATH)
+        L = ctypes.CDLL(build())
         P, i32, i64, f32, f64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double
         L.oracle_ep_finalize.argtypes = [P, i64, P, P, i32, P, f32, f32, i32, i32, i32, i32, i32, P]
         L.oracle_tp_finalize.argtypes = [P, i64, P, P, i32, P, f32, f32, i32, i32, i32, i32, i32, P]
@@ -50,6 +54,8 @@ def lib():
         L.oracle_shared_down.argtypes = [P, P, i32, i32, i32, P, i32]
         L.oracle_sum_of_squares.argtypes = [P, i32]
         L.oracle_sum_of_squares.restype = f32
+        L.oracle_inverse_rms.argtypes = [f32, i32, f32]
+        L.oracle_inverse_rms.restype = f32
         L.oracle_bf16_from_f32.argtypes = [f32]
         L.oracle_bf16_from_f32.restype = ctypes.c_uint16
         L.oracle_bf16_from_f64.argtypes = [f64]
@@ -158,6 +164,11 @@ def shared_down(h, w_down, b, H, I, out_in=None, accumulate=True):
 def sum_of_squares(v: np.ndarray) -> float:
     v = np.ascontiguousarray(v, dtype=np.float32)
     return float(lib().oracle_sum_of_squares(v.ctypes.data_as(ctypes.c_void_p), v.size))
+
+
+def inverse_rms(ss: float, P: int, eps: float) -> float:
+    """1 / sqrt(ss * (float)(1/P) + eps), each step one FP32 operation."""
+    return float(lib().oracle_inverse_rms(ss, P, eps))
 
 
 def bf16_from_f32(x: float) -> int:

@@ -125,6 +125,9 @@ static float inverse_rms(float ss, int P, float eps) {
     return 1.0f / sqrtf(den);
 }
 
+/* The inverse RMS on its own, for the pins of its rounding steps. */
+float oracle_inverse_rms(float ss, int P, float eps) { return inverse_rms(ss, P, eps); }
+
 static float route_weight(const void* w, int w_is_bf16, int64_t i) {
     return w_is_bf16 ? oracle_f32_from_bf16(((const uint16_t*)w)[i]) : ((const float*)w)[i];
 }

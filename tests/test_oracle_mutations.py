@@ -1,0 +1,86 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a copy of oracle/moe_tail_oracle.c (a sum in
+the wrong order, a rounding dropped or added, a term, a sign or an operand
+moved), builds the copy with the oracle's flags, and runs the pins
+(tests/test_oracle_pins.py) against it in a child process, which must fail.
+The unchanged copy must pass.  Only the copy is changed; the oracle itself is
+not touched."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "moe_tail_oracle.c")
+PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
+
+# (what the mistake is, text in the oracle, what it becomes); the first match is changed
+MUTATIONS = [
+    ("EP slots summed in reverse order",
+     "for (int s = 0; s < tp; ++s) {\n            for (int c = 0; c < P; ++c) part[c] = 0.0f;",
+     "for (int s = tp - 1; s >= 0; --s) {\n            for (int c = 0; c < P; ++c) part[c] = 0.0f;"),
+    ("EP slot partial not rounded to BF16", "o[c] = o[c] + bf16_round(part[c]);", "o[c] = o[c] + part[c];"),
+    ("EP routes summed in reverse order",
+     "for (int k = 0; k < K; ++k) {\n                int32_t j = idx[((int64_t)s * b + t) * K + k];",
+     "for (int k = K - 1; k >= 0; --k) {\n                int32_t j = idx[((int64_t)s * b + t) * K + k];"),
+    ("gain placement of weight_before_norm swapped", "float n = wbn ? v[c] * inv : (x[c] * inv) * g[c];",
+     "float n = wbn ? (x[c] * inv) * g[c] : v[c] * inv;"),
+    ("product order (x * inv) * g changed", "float n = wbn ? v[c] * inv : (x[c] * inv) * g[c];",
+     "float n = wbn ? v[c] * inv : x[c] * (inv * g[c]);"),
+    ("lane columns strided instead of contiguous", "int col = 256 * c + 8 * l + i;", "int col = 256 * c + l + 32 * i;"),
+    ("butterfly offsets in reverse order", "for (int off = 1; off < 32; off <<= 1) {",
+     "for (int off = 16; off >= 1; off >>= 1) {"),
+    ("chunk sums folded in reverse order",
+     "for (int c = 0; c < chunks; ++c) {\n        float a[32], nb[32];",
+     "for (int c = chunks - 1; c >= 0; --c) {\n        float a[32], nb[32];"),
+    ("a lane's columns added in reverse order", "for (int i = 0; i < 8; ++i) {\n                int col",
+     "for (int i = 7; i >= 0; --i) {\n                int col"),
+    ("eps dropped", "float den = mean + eps;", "float den = mean;"),
+    ("mean by division instead of the rounded reciprocal", "float mean = ss * rcp;", "float mean = ss / (float)P;"),
+    ("inverse RMS as sqrt of a reciprocal", "return 1.0f / sqrtf(den);", "return sqrtf(1.0f / den);"),
+    ("-0 not made +0 in the expert-TP output", "out[(int64_t)t * P + c] = pz(oracle_bf16_from_f32(acc[c]));",
+     "out[(int64_t)t * P + c] = oracle_bf16_from_f32(acc[c]);"),
+    ("row 0 treated as not local", "if (j < 0 || (int64_t)j >= rows_per_slot) continue;",
+     "if (j <= 0 || (int64_t)j >= rows_per_slot) continue;"),
+    ("gain center not added", "for (int c = 0; c < P; ++c) g[c] = oracle_f32_from_bf16(gamma[c]) + gain_center;",
+     "for (int c = 0; c < P; ++c) g[c] = oracle_f32_from_bf16(gamma[c]);"),
+    ("expert-TP slot sum not rounded to BF16",
+     "                x[c] = bf16_round(sum);\n            }\n            add_normalised_route",
+     "                x[c] = sum;\n            }\n            add_normalised_route"),
+    ("latent tail skips the first shared slot", "for (int s = 0; s < tp_s; ++s)", "for (int s = 1; s < tp_s; ++s)"),
+    ("SiLU with the wrong sign", "double silu = gate / (1.0 + exp(-gate));", "double silu = gate / (1.0 + exp(gate));"),
+    ("h multiplies gate instead of up", "pz(oracle_bf16_from_f64(silu * up))", "pz(oracle_bf16_from_f64(silu * gate))"),
+    ("d added into out before its BF16 rounding",
+     "float sum = oracle_f32_from_bf16(*o) + oracle_f32_from_bf16(db);", "float sum = oracle_f32_from_bf16(*o) + (float)acc;"),
+]
+
+
+def build_copy(tmp_path, source: str, name: str) -> str:
+    src = tmp_path / f"{name}.c"
+    src.write_text(source)
+    lib = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", str(lib), str(src), "-lm"], check=True, capture_output=True)
+    return str(lib)
+
+
+def run_pins(lib: str) -> subprocess.CompletedProcess:
+    env = dict(os.environ, MOE_TAIL_ORACLE_LIBRARY=lib, PYTHONPATH=ROOT)
+    return subprocess.run([sys.executable, "-m", "pytest", PINS, "-x", "-q", "-p", "no:cacheprovider"],
+                          capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
+
+
+def test_unchanged_copy_passes_the_pins(tmp_path):
+    r = run_pins(build_copy(tmp_path, open(SRC).read(), "unchanged"))
+    assert r.returncode == 0, r.stdout[-2000:]
+
+
+@pytest.mark.parametrize("what,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_the_mistake(tmp_path, what, old, new):
+    source = open(SRC).read()
+    assert old in source, f"mutation site not found: {what}"
+    r = run_pins(build_copy(tmp_path, source.replace(old, new, 1), "mutant"))
+    assert r.returncode != 0, f"no pin fails with: {what}"

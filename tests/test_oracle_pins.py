@@ -151,6 +151,35 @@ def test_sum_of_squares_lanes_combine_by_butterfly():
     assert oracle.sum_of_squares(v) == 16777216.0 + 30.0
 
 
+def test_sum_of_squares_butterfly_pairs_adjacent_lanes_first():
+    # lane 0 holds 2^24, lanes 1 and 17 hold 1.  Offsets 1, 2, 4, 8, 16: lane 0
+    # meets lane 1 first (2^24 + 1 is a tie back to 2^24) and lanes 16-31 later
+    # bring 1 (again back to 2^24): the total stays 2^24.  Offsets 16 first would
+    # pair lanes 1 and 17 (1 + 1 = 2) and end at 2^24 + 2.
+    v = np.zeros(256, dtype=np.float32)
+    v[0] = 4096.0
+    v[8] = 1.0
+    v[136] = 1.0
+    assert oracle.sum_of_squares(v) == 16777216.0
+
+
+@pytest.mark.parametrize("ss,expect,other", [
+    # ss * (float)(1/3584), then 1/sqrt: 45.38468933105469; the mean as ss / 3584
+    # (one rounding instead of two) gives 45.38469314575195
+    (1.74, 45.38468933105469, 45.38469314575195),
+    # 1 / sqrt(mean): 41.21381378173828; sqrt(1 / mean) gives 41.213809967041016
+    (2.11, 41.21381378173828, 41.213809967041016),
+])
+def test_inverse_rms_rounding_steps(ss, expect, other):
+    # the values were found with numpy's IEEE float32 operations; each step of
+    # the definition is one rounding, and the neighbouring formulas differ
+    f = np.float32
+    got = oracle.inverse_rms(float(f(ss)), 3584, 0.0)
+    assert got == expect and got != other
+    mean = f(f(ss) * f(1.0 / 3584))
+    assert float(f(1.0) / np.sqrt(mean)) == expect
+
+
 def test_sum_of_squares_chunks_fold_in_order():
     # chunk 0 holds 2^24, chunks 1..15 hold 1 each.  Folding chunks in order
     # from +0: every +1 is a tie back to 2^24.  A pairwise fold would give
@@ -219,6 +248,19 @@ def test_ep_normalisation_product_order_with_subnormals():
     off = ep_call(constant_ep([[1.0]], row_value=x, gamma=gamma, gc=0.0, eps=2.0 ** -100, wbn=False))
     assert torch.equal(on.float(), torch.full((1, 256), 1.5 * 2.0 ** -97))
     assert torch.equal(off.float(), torch.full((1, 256), 1.421875 * 2.0 ** -97))
+
+
+def test_ep_product_order_after_the_norm_at_a_bf16_boundary():
+    # P = 8, one route of weight 1, row (2.3125, 0.8125, 0, ...), gamma[0] = 2.828125,
+    # gain center 0, eps 0, gain after the norm: ss = 2.3125^2 + 0.8125^2 = 6.0078125
+    # and inv = 1/sqrt(ss/8) = 1.1539495 in FP32.  (x*inv)*g = 7.546875 rounds to the
+    # BF16 0x40F2; x*(inv*g) = 7.5468745 would round to 0x40F1.
+    row = torch.tensor([2.3125, 0.8125, 0, 0, 0, 0, 0, 0]).to(torch.bfloat16).reshape(1, 1, 8)
+    gamma = torch.tensor([2.828125, 1, 1, 1, 1, 1, 1, 1]).to(torch.bfloat16)
+    d = dict(rows=row, rows_per_slot=1, idx=torch.zeros((1, 1, 1), dtype=torch.int32),
+             w=torch.ones((1, 1)), gamma=gamma, gain_center=0.0, eps=0.0, weight_before_norm=False,
+             b=1, tp=1, K=1, P=8)
+    assert int(bits(ep_call(d))[0, 0]) == 0x40F2
 
 
 def test_ep_inverse_rms_uses_eps():
@@ -398,6 +440,17 @@ def test_tp_non_local_route_contributes_nothing():
         keep_rows.append(tp_call(d, idx=idx[t:t + 1, keep].contiguous(), w=d["w"][t:t + 1, keep].contiguous(),
                                  b=1, K=len(keep)))
     assert np.array_equal(bits(a), bits(torch.cat(keep_rows)))
+
+
+def test_tp_tiny_negative_output_is_positive_zero():
+    # one route of weight -2^-140, rows of 1, gains 1, eps 0: n = 1, the route
+    # sum is -2^-140, below half the smallest BF16 subnormal (2^-133), so it
+    # rounds to -0, which is written as +0
+    d = dict(partials=torch.ones((1, 1, 256)).to(torch.bfloat16), num_rows=1,
+             idx=torch.zeros((1, 1), dtype=torch.int32), w=torch.full((1, 1), -2.0 ** -140),
+             gamma=torch.zeros(256).to(torch.bfloat16), gain_center=1.0, eps=0.0, weight_before_norm=True,
+             b=1, tp=1, K=1, P=256)
+    assert np.all(bits(tp_call(d)) == 0)
 
 
 def test_tp_routes_sum_in_route_order():
