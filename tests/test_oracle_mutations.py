@@ -56,6 +56,28 @@ MUTATIONS = [
     ("h multiplies gate instead of up", "pz(oracle_bf16_from_f64(silu * up))", "pz(oracle_bf16_from_f64(silu * gate))"),
     ("d added into out before its BF16 rounding",
      "float sum = oracle_f32_from_bf16(*o) + oracle_f32_from_bf16(db);", "float sum = oracle_f32_from_bf16(*o) + (float)acc;"),
+    ("BF16 ties rounded away from zero", "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1u;",
+     "if (rest >= 0x8000u) keep += 1u;"),
+    ("BF16 from binary64 through a plain binary32 rounding", "        u |= 1u; /* the odd one of the two neighbours */",
+     "        u |= 0u;"),
+    ("latent slot sum not rounded to BF16",
+     "            x[c] = bf16_round(sum);\n        }\n        float inv",
+     "            x[c] = sum;\n        }\n        float inv"),
+    ("latent y as x * (inv * gamma)", "float n = (x[c] * inv) * oracle_f32_from_bf16(gamma[c]);",
+     "float n = x[c] * (inv * oracle_f32_from_bf16(gamma[c]));"),
+    ("latent y without gamma", "float n = (x[c] * inv) * oracle_f32_from_bf16(gamma[c]);", "float n = x[c] * inv;"),
+    ("expert-TP routes summed in reverse order",
+     "for (int k = 0; k < K; ++k) {\n            int32_t j = idx[(int64_t)t * K + k];",
+     "for (int k = K - 1; k >= 0; --k) {\n            int32_t j = idx[(int64_t)t * K + k];"),
+    ("expert-TP slots summed in reverse order",
+     "for (int s = 0; s < tp; ++s)\n                    sum = sum + oracle_f32_from_bf16(partials",
+     "for (int s = tp - 1; s >= 0; --s)\n                    sum = sum + oracle_f32_from_bf16(partials"),
+    ("BF16 route weights read as FP32", "return w_is_bf16 ? oracle_f32_from_bf16(((const uint16_t*)w)[i]) : ((const float*)w)[i];",
+     "return ((const float*)w)[i / 2];"),
+    ("up-projection rounds through FP32", "out[(int64_t)t * H + n] = pz(oracle_bf16_from_f64(acc));",
+     "out[(int64_t)t * H + n] = pz(oracle_bf16_from_f32((float)acc));"),
+    ("gate not rounded to BF16 before SiLU", "double gate = oracle_f32_from_bf16(oracle_bf16_from_f64(ga));",
+     "double gate = ga;"),
 ]
 
 

@@ -483,6 +483,44 @@ def test_latent_norm_matches_textbook_rmsnorm():
     assert np.all(np.abs(y - ref) <= ulp_bf16(ref))
 
 
+def _latent_pair(col0_slots, col1, gamma0):
+    lat = torch.zeros((2, 1, 8))
+    lat[0, 0, 0], lat[1, 0, 0], lat[0, 0, 1] = col0_slots[0], col0_slots[1], col1
+    gamma = torch.ones(8)
+    gamma[0] = gamma0
+    return lat.to(torch.bfloat16), gamma.to(torch.bfloat16)
+
+
+def test_latent_norm_rounds_the_slot_sum_to_bf16():
+    # column 0 holds 2.578125 and -0.00640869140625 in the two slots, column 1
+    # holds 3.546875, gamma[0] = 1.2734375, eps 0.  The slot sum rounded to BF16
+    # (2.5625) gives y[0] = 0x4008; the unrounded sum (2.57171...) would give
+    # 0x4007.  (Found with numpy float32, each step one rounding.)
+    lat, gamma = _latent_pair((2.578125, -0.00640869140625), 3.546875, 1.2734375)
+    y = oracle.latent_norm(lat, gamma, 0.0, 1, 2, 8)
+    assert int(bits(y)[0, 0]) == 0x4008
+
+
+def test_latent_norm_product_order():
+    # slots (3.609375, -0.041015625) in column 0, 0.55859375 in column 1,
+    # gamma[0] = 1.3671875, eps 0: (x * inv) * gamma rounds to 0x4074 and
+    # x * (inv * gamma) would round to 0x4075
+    lat, gamma = _latent_pair((3.609375, -0.041015625), 0.55859375, 1.3671875)
+    y = oracle.latent_norm(lat, gamma, 0.0, 1, 2, 8)
+    assert int(bits(y)[0, 0]) == 0x4074
+
+
+def test_latent_up_rounds_the_double_sum_straight_to_bf16():
+    # y = (1, 2^-8, 2^-30, 0, ...), one output row of ones: the sum is exactly
+    # 1 + 2^-8 + 2^-30 in double, above the tie between 1 and 1 + 2^-7, so it
+    # rounds up to 0x3F81.  Through binary32 it would first become the tie
+    # 1 + 2^-8 and then round to even, 0x3F80.
+    y = torch.tensor([[1.0, 2.0 ** -8, 2.0 ** -30, 0, 0, 0, 0, 0]]).to(torch.bfloat16)
+    w = torch.ones((1, 8)).to(torch.bfloat16)
+    out = oracle.latent_up(y, w, None, 0, 1, 8, 1)
+    assert int(bits(out)[0, 0]) == 0x3F81
+
+
 def test_latent_up_identity_weight_reproduces_y():
     L, H, b = 256, 512, 3
     y = synth.bf16(synth.normal(1, 1, b * L), (b, L))
