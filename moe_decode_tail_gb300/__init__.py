@@ -104,6 +104,57 @@ def _cuda(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
+def _dims(name: str, t, n: int) -> tuple:
+    """The shape of t, which must have n dimensions."""
+    if t.dim() != n:
+        raise ValueError(f"{name} must have {n} dimensions, got shape {tuple(t.shape)}")
+    return tuple(t.shape)
+
+
+def _like(name: str, t, dtype, shape) -> None:
+    """t must be dtype with exactly this shape: the C entry points receive only
+    a pointer and take the layout from the sizes, so a tensor of another type
+    or shape would be read (or written) as if it had this one."""
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _finalize_args(kind: str, src, permuted_idx, route_weights, gamma, out) -> tuple:
+    """Shapes of a finalize call: src [tp, rows, P] BF16, route weights [b, K]
+    FP32 or BF16, permuted_idx int32 [tp, b, K] (EP) or [b, K] (expert-TP),
+    gamma BF16 [P], out BF16 [b, P].  Returns (tp, rows, P, b, K)."""
+    tp, rows, P = _dims(kind, src, 3)
+    b, K = _dims("route_weights", route_weights, 2)
+    _like(kind, src, torch.bfloat16, (tp, rows, P))
+    _weights(route_weights)
+    _like("permuted_idx", permuted_idx, torch.int32, (tp, b, K) if kind == "rows" else (b, K))
+    _like("gamma", gamma, torch.bfloat16, (P,))
+    _like("out", out, torch.bfloat16, (b, P))
+    _cuda(src, permuted_idx, route_weights, gamma, out)
+    return tp, rows, P, b, K
+
+
+def _latent_args(latent, gamma, w_up, shared, out, y) -> tuple:
+    """Shapes of a latent-tail call: latent BF16 [tp, b, L], gamma BF16 [L],
+    w_up BF16 [H, L], shared BF16 [tp_s, b, H] or None, out BF16 [b, H], y
+    BF16 [b, L] or None.  Returns (tp, b, L, H, tp_s)."""
+    tp, b, L = _dims("latent", latent, 3)
+    H, _ = _dims("w_up", w_up, 2)
+    tp_s = 0 if shared is None else _dims("shared", shared, 3)[0]
+    _like("latent", latent, torch.bfloat16, (tp, b, L))
+    _like("gamma", gamma, torch.bfloat16, (L,))
+    _like("w_up", w_up, torch.bfloat16, (H, L))
+    if shared is not None:
+        _like("shared", shared, torch.bfloat16, (tp_s, b, H))
+    _like("out", out, torch.bfloat16, (b, H))
+    if y is not None:
+        _like("y", y, torch.bfloat16, (b, L))
+    _cuda(latent, gamma, w_up, shared, out, y)
+    return tp, b, L, H, tp_s
+
+
 def _weights(w: torch.Tensor) -> int:
     if w.dtype == torch.float32:
         return W_FP32
@@ -116,9 +167,7 @@ def moe_tail_ep_finalize(rows, permuted_idx, route_weights, gamma, out, *, gain_
                          weight_before_norm=True, stream=None) -> torch.Tensor:
     """EP finalize into out (BF16 [b, P]); rows BF16 [tp, rows_per_slot, P],
     permuted_idx int32 [tp, b, K], route_weights [b, K], gamma BF16 [P]."""
-    _cuda(rows, permuted_idx, route_weights, gamma, out)
-    tp, rows_per_slot, P = rows.shape
-    b, K = route_weights.shape
+    tp, rows_per_slot, P, b, K = _finalize_args("rows", rows, permuted_idx, route_weights, gamma, out)
     _check("moe_tail_ep_finalize", lib().moe_tail_ep_finalize(
         _p(rows), rows_per_slot, _p(permuted_idx), _p(route_weights), _weights(route_weights), _p(gamma),
         gain_center, eps, int(bool(weight_before_norm)), b, tp, K, P, _p(out), _stream(stream)))
@@ -129,9 +178,7 @@ def moe_tail_tp_finalize(partials, permuted_idx, route_weights, gamma, out, *, g
                          weight_before_norm=True, stream=None) -> torch.Tensor:
     """Expert-TP finalize into out (BF16 [b, P]); partials BF16 [tp, num_rows, P],
     permuted_idx int32 [b, K], route_weights [b, K], gamma BF16 [P]."""
-    _cuda(partials, permuted_idx, route_weights, gamma, out)
-    tp, num_rows, P = partials.shape
-    b, K = route_weights.shape
+    tp, num_rows, P, b, K = _finalize_args("partials", partials, permuted_idx, route_weights, gamma, out)
     _check("moe_tail_tp_finalize", lib().moe_tail_tp_finalize(
         _p(partials), num_rows, _p(permuted_idx), _p(route_weights), _weights(route_weights), _p(gamma),
         gain_center, eps, int(bool(weight_before_norm)), b, tp, K, P, _p(out), _stream(stream)))
@@ -142,9 +189,7 @@ def moe_tail_ep_finalize_flags(rows, permuted_idx, route_weights, gamma, out, *,
                                weight_before_norm=True, inputs_ready=False, stream=None) -> torch.Tensor:
     """moe_tail_ep_finalize with the promise inputs_ready: rows, indices, route
     weights and gamma are not written by work still in flight on the stream."""
-    _cuda(rows, permuted_idx, route_weights, gamma, out)
-    tp, rows_per_slot, P = rows.shape
-    b, K = route_weights.shape
+    tp, rows_per_slot, P, b, K = _finalize_args("rows", rows, permuted_idx, route_weights, gamma, out)
     _check("moe_tail_ep_finalize_flags", lib().moe_tail_ep_finalize_flags(
         _p(rows), rows_per_slot, _p(permuted_idx), _p(route_weights), _weights(route_weights), _p(gamma),
         gain_center, eps, int(bool(weight_before_norm)), b, tp, K, P, _p(out), INPUTS_READY if inputs_ready else 0,
@@ -156,9 +201,7 @@ def moe_tail_tp_finalize_flags(partials, permuted_idx, route_weights, gamma, out
                                weight_before_norm=True, inputs_ready=False, stream=None) -> torch.Tensor:
     """moe_tail_tp_finalize with the promise inputs_ready: partials, indices,
     route weights and gamma are not written by work still in flight on the stream."""
-    _cuda(partials, permuted_idx, route_weights, gamma, out)
-    tp, num_rows, P = partials.shape
-    b, K = route_weights.shape
+    tp, num_rows, P, b, K = _finalize_args("partials", partials, permuted_idx, route_weights, gamma, out)
     _check("moe_tail_tp_finalize_flags", lib().moe_tail_tp_finalize_flags(
         _p(partials), num_rows, _p(permuted_idx), _p(route_weights), _weights(route_weights), _p(gamma),
         gain_center, eps, int(bool(weight_before_norm)), b, tp, K, P, _p(out), INPUTS_READY if inputs_ready else 0,
@@ -174,10 +217,8 @@ def moe_tail_latent_up(latent, gamma, w_up, shared, out, workspace, *, eps=1e-6,
     """Latent tail into out (BF16 [b, H]): latent BF16 [tp, b, L], gamma BF16 [L],
     w_up BF16 [H, L], shared BF16 [tp_s, b, H] or None, workspace uint8 CUDA
     tensor of at least moe_tail_workspace_bytes(0, b, L) bytes (y after the call)."""
-    _cuda(latent, gamma, w_up, shared, out, workspace)
-    tp, b, L = latent.shape
-    H = w_up.shape[0]
-    tp_s = 0 if shared is None else shared.shape[0]
+    tp, b, L, H, tp_s = _latent_args(latent, gamma, w_up, shared, out, None)
+    _cuda(workspace)
     _check("moe_tail_latent_up", lib().moe_tail_latent_up(
         _p(latent), _p(gamma), eps, _p(w_up), _p(shared), tp_s, b, tp, L, H, _p(out), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
@@ -192,10 +233,7 @@ def moe_tail_latent_up_flags(latent, gamma, w_up, shared, out, y, *, eps=1e-6, i
     The norm and the up-projection, or with MOE_TAIL_LATENT_FUSED=1 in the
     environment one kernel that forms y on chip (slower on GB300); the result
     is bit for bit that of the two split calls either way."""
-    _cuda(latent, gamma, w_up, shared, out, y)
-    tp, b, L = latent.shape
-    H = w_up.shape[0]
-    tp_s = 0 if shared is None else shared.shape[0]
+    tp, b, L, H, tp_s = _latent_args(latent, gamma, w_up, shared, out, y)
     flags = (INPUTS_READY if inputs_ready else 0) | (WEIGHTS_STATIC if weights_static else 0)
     _check("moe_tail_latent_up_flags", lib().moe_tail_latent_up_flags(
         _p(latent), _p(gamma), eps, _p(w_up), _p(shared), tp_s, b, tp, L, H, _p(out), _p(y), flags,
@@ -208,8 +246,11 @@ def moe_tail_latent_norm(latent, gamma, y, *, eps=1e-6, inputs_ready=False, stre
     BF16 [tp, b, L], RMS-normalised and scaled by gamma BF16 [L].
     inputs_ready: latent and gamma are not written by work still in flight on
     the stream, so the kernel may read them before the preceding kernel ends."""
+    tp, b, L = _dims("latent", latent, 3)
+    _like("latent", latent, torch.bfloat16, (tp, b, L))
+    _like("gamma", gamma, torch.bfloat16, (L,))
+    _like("y", y, torch.bfloat16, (b, L))
     _cuda(latent, gamma, y)
-    tp, b, L = latent.shape
     _check("moe_tail_latent_norm", lib().moe_tail_latent_norm(
         _p(latent), _p(gamma), eps, b, tp, L, _p(y), INPUTS_READY if inputs_ready else 0, _stream(stream)))
     return y
@@ -220,10 +261,15 @@ def moe_tail_up_project(y, w_up, shared, out, *, weights_static=False, stream=No
     w_up BF16 [H, L] transposed, plus shared BF16 [tp_s, b, H] (or None).
     weights_static: w_up is not written by work still in flight on the stream,
     so the kernel may request weight tiles before the preceding kernel ends."""
+    b, L = _dims("y", y, 2)
+    H, _ = _dims("w_up", w_up, 2)
+    tp_s = 0 if shared is None else _dims("shared", shared, 3)[0]
+    _like("y", y, torch.bfloat16, (b, L))
+    _like("w_up", w_up, torch.bfloat16, (H, L))
+    if shared is not None:
+        _like("shared", shared, torch.bfloat16, (tp_s, b, H))
+    _like("out", out, torch.bfloat16, (b, H))
     _cuda(y, w_up, shared, out)
-    b, L = y.shape
-    H = w_up.shape[0]
-    tp_s = 0 if shared is None else shared.shape[0]
     _check("moe_tail_up_project", lib().moe_tail_up_project(
         _p(y), _p(w_up), _p(shared), tp_s, b, L, H, _p(out), WEIGHTS_STATIC if weights_static else 0,
         _stream(stream)))
@@ -233,9 +279,13 @@ def moe_tail_up_project(y, w_up, shared, out, *, weights_static=False, stream=No
 def moe_shared_gate_up(x, w_gate, w_up, h, *, weights_static=False, stream=None) -> torch.Tensor:
     """The shared expert's gate/up projection and SiLU into h (BF16 [b, I]):
     x BF16 [b, H], w_gate and w_up BF16 [I, H]."""
+    b, H = _dims("x", x, 2)
+    I, _ = _dims("w_gate", w_gate, 2)
+    _like("x", x, torch.bfloat16, (b, H))
+    _like("w_gate", w_gate, torch.bfloat16, (I, H))
+    _like("w_up", w_up, torch.bfloat16, (I, H))
+    _like("h", h, torch.bfloat16, (b, I))
     _cuda(x, w_gate, w_up, h)
-    b, H = x.shape
-    I = w_gate.shape[0]
     _check("moe_shared_gate_up", lib().moe_shared_gate_up(
         _p(x), _p(w_gate), _p(w_up), b, H, I, _p(h), WEIGHTS_STATIC if weights_static else 0, _stream(stream)))
     return h
@@ -244,9 +294,12 @@ def moe_shared_gate_up(x, w_gate, w_up, h, *, weights_static=False, stream=None)
 def moe_shared_down(h, w_down, out, *, accumulate=True, weights_static=False, stream=None) -> torch.Tensor:
     """The shared expert's down projection of h (BF16 [b, I]) with w_down BF16
     [H, I], written into out (BF16 [b, H]) or added into it (accumulate)."""
+    b, I = _dims("h", h, 2)
+    H, _ = _dims("w_down", w_down, 2)
+    _like("h", h, torch.bfloat16, (b, I))
+    _like("w_down", w_down, torch.bfloat16, (H, I))
+    _like("out", out, torch.bfloat16, (b, H))
     _cuda(h, w_down, out)
-    b, I = h.shape
-    H = w_down.shape[0]
     _check("moe_shared_down", lib().moe_shared_down(
         _p(h), _p(w_down), b, H, I, _p(out), int(bool(accumulate)), WEIGHTS_STATIC if weights_static else 0,
         _stream(stream)))
@@ -261,13 +314,10 @@ def moe_tail_latent_up_noalloc(latent, gamma, w_up, shared, out, *, eps=1e-6, st
     the library, shared by every call.  Same arguments as moe_tail_latent_up
     minus the workspace; b * L * 2 must not exceed NOALLOC_SCRATCH_BYTES.
     Calls that may overlap on the GPU race on the shared array."""
-    _cuda(latent, gamma, w_up, shared, out)
-    tp, b, L = latent.shape
-    H = w_up.shape[0]
+    tp, b, L, H, tp_s = _latent_args(latent, gamma, w_up, shared, out, None)
     if b * L * 2 > NOALLOC_SCRATCH_BYTES:
         raise ValueError(f"moe_tail_latent_up_noalloc: y needs {b * L * 2} bytes, more than the library's "
                          f"built-in {NOALLOC_SCRATCH_BYTES}-byte scratch; use moe_tail_latent_up with a workspace")
-    tp_s = 0 if shared is None else shared.shape[0]
     _check("moe_tail_latent_up_noalloc", lib().moe_tail_latent_up_noalloc(
         _p(latent), _p(gamma), eps, _p(w_up), _p(shared), tp_s, b, tp, L, H, _p(out), _stream(stream)))
     return out
@@ -277,9 +327,14 @@ def moe_shared_expert(x, w_gate, w_up, w_down, out, workspace, *, accumulate=Tru
     """Fused shared expert into out (BF16 [b, H]): x BF16 [b, H], w_gate/w_up BF16
     [I, H], w_down BF16 [H, I], workspace of at least moe_tail_workspace_bytes(1, b, I)
     bytes (h after the call); out += down(...) when accumulate."""
+    b, H = _dims("x", x, 2)
+    I, _ = _dims("w_gate", w_gate, 2)
+    _like("x", x, torch.bfloat16, (b, H))
+    _like("w_gate", w_gate, torch.bfloat16, (I, H))
+    _like("w_up", w_up, torch.bfloat16, (I, H))
+    _like("w_down", w_down, torch.bfloat16, (H, I))
+    _like("out", out, torch.bfloat16, (b, H))
     _cuda(x, w_gate, w_up, w_down, out, workspace)
-    b, H = x.shape
-    I = w_gate.shape[0]
     _check("moe_shared_expert", lib().moe_shared_expert(
         _p(x), _p(w_gate), _p(w_up), _p(w_down), b, H, I, _p(out), int(bool(accumulate)), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
