@@ -78,6 +78,16 @@ MUTATIONS = [
      "out[(int64_t)t * H + n] = pz(oracle_bf16_from_f32((float)acc));"),
     ("gate not rounded to BF16 before SiLU", "double gate = oracle_f32_from_bf16(oracle_bf16_from_f64(ga));",
      "double gate = ga;"),
+    ("latent y keeps -0", "y[(int64_t)t * L + c] = pz(oracle_bf16_from_f32(n));",
+     "y[(int64_t)t * L + c] = oracle_bf16_from_f32(n);"),
+    ("h rounded through binary32", "h_out[(int64_t)t * I + i] = pz(oracle_bf16_from_f64(silu * up));",
+     "h_out[(int64_t)t * I + i] = pz(oracle_bf16_from_f32((float)(silu * up)));"),
+    ("down output keeps -0", "uint16_t db = pz(oracle_bf16_from_f64(acc));", "uint16_t db = oracle_bf16_from_f64(acc);"),
+    ("expert-TP ignores weight_before_norm",
+     "add_normalised_route(x, g, wbn, eps, route_weight(w, w_is_bf16, (int64_t)t * K + k), P,",
+     "add_normalised_route(x, g, 1, eps, route_weight(w, w_is_bf16, (int64_t)t * K + k), P,"),
+    ("expert-TP row num_rows treated as local", "if (j < 0 || (int64_t)j >= num_rows) continue;",
+     "if (j < 0 || (int64_t)j > num_rows) continue;"),
 ]
 
 

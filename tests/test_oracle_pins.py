@@ -398,10 +398,12 @@ def test_single_route_is_textbook_rmsnorm(kind):
     assert exact.mean() > 0.99
 
 
-def test_tp_equals_ep_on_slot_summed_rows():
+@pytest.mark.parametrize("wbn", [True, False])
+def test_tp_equals_ep_on_slot_summed_rows(wbn):
     # x_r = bf16(sum_s Q_s), then the EP formula on one slot with every route
-    # local: the two statements of the method must agree bit for bit.
-    d = synth.config(3, b=6, P=512, tp=4)
+    # local: the two statements of the method must agree bit for bit, with the
+    # gains before the norm or after it (gamma is random, so the two differ).
+    d = synth.config(3, b=6, P=512, tp=4, weight_before_norm=wbn)
     acc = torch.zeros(d["partials"].shape[1:], dtype=torch.float32)
     for s in range(d["tp"]):  # slot order, one FP32 add per slot
         acc = acc + d["partials"][s].float()
@@ -433,6 +435,7 @@ def test_tp_non_local_route_contributes_nothing():
     idx = d["idx"].clone()
     idx[1, 3] = -1
     idx[2, 0] = d["num_rows"] + 5
+    idx[0, 1] = d["num_rows"]  # one past the last row
     keep_rows = []
     a = tp_call(d, idx=idx)
     for t in range(d["b"]):
@@ -510,6 +513,15 @@ def test_latent_norm_product_order():
     assert int(bits(y)[0, 0]) == 0x4074
 
 
+def test_latent_norm_zero_column_with_negative_gamma_is_positive_zero():
+    # column 0's slots cancel (1 and -1: x = +0) and gamma[0] = -1.5, so
+    # (x * inv) * gamma = +0 * -1.5 = -0, which y (a BF16 output) stores as +0.
+    # Column 1 (x = 1) gives ss = 1, inv = sqrt(8), y[1] = bf16(2.828...) = 0x4035.
+    lat, gamma = _latent_pair((1.0, -1.0), 1.0, -1.5)
+    y = bits(oracle.latent_norm(lat, gamma, 0.0, 1, 2, 8))
+    assert int(y[0, 0]) == 0x0000 and int(y[0, 1]) == 0x4035
+
+
 def test_latent_up_rounds_the_double_sum_straight_to_bf16():
     # y = (1, 2^-8, 2^-30, 0, ...), one output row of ones: the sum is exactly
     # 1 + 2^-8 + 2^-30 in double, above the tie between 1 and 1 + 2^-7, so it
@@ -576,6 +588,29 @@ def test_shared_activation_special_values():
     assert bits(h)[0, 0] == 0 and bits(h)[0, 1] == bits(bf([48.0]))[0]
     for i in (2, 3, 4):
         assert int(bits(h)[0, i]) == _nearest_bf16_exact(expect[i])
+
+
+def test_shared_h_rounds_the_double_product_straight_to_bf16():
+    # gate = -0.7578125, up = 1.5546875 (both BF16): silu(gate) * up in double
+    # is -0.37597656760..., just beyond the tie -0.3759765625 between BF16
+    # -0.375 (0xBEC0) and -0.376953125 (0xBEC1), by 1.4e-8 relative (far above
+    # the error of exp).  Rounded straight to BF16 it gives 0xBEC1; rounded to
+    # binary32 first it would land on the tie and go to the even 0xBEC0.
+    x, wg, wu, wd = _onehot_shared([-0.7578125], [1.5546875])
+    h, _ = oracle.shared_expert(x, wg, wu, wd, 1, 16, 1, out_in=torch.zeros((1, 16)).to(torch.bfloat16))
+    assert int(bits(h)[0, 0]) == 0xBEC1
+
+
+def test_shared_down_tiny_negative_is_positive_zero():
+    # h = silu(64) * 2^-76 = 2^-70 (silu(64) = 64 up to 1e-26), one down weight
+    # -2^-70: d = -2^-140, below half the smallest BF16 subnormal (2^-133), so
+    # bf16(d) = -0, which is written as +0 when out is overwritten
+    down = torch.zeros((16, 1))
+    down[5, 0] = -2.0 ** -70
+    x, wg, wu, wd = _onehot_shared([64.0], [2.0 ** -76], down=down)
+    h, out = oracle.shared_expert(x, wg, wu, wd, 1, 16, 1, accumulate=False)
+    assert int(bits(h)[0, 0]) == 0x1C80
+    assert np.all(bits(out) == 0)
 
 
 def test_shared_down_selects_h():
