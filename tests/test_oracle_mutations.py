@@ -88,7 +88,30 @@ MUTATIONS = [
      "add_normalised_route(x, g, 1, eps, route_weight(w, w_is_bf16, (int64_t)t * K + k), P,"),
     ("expert-TP row num_rows treated as local", "if (j < 0 || (int64_t)j >= num_rows) continue;",
      "if (j < 0 || (int64_t)j > num_rows) continue;"),
+    ("latent out keeps -0", "out[(int64_t)t * H + n] = pz(oracle_bf16_from_f64(acc));",
+     "out[(int64_t)t * H + n] = oracle_bf16_from_f64(acc);"),
+    ("latent shared slots accumulated in binary32",
+     "acc += (double)oracle_f32_from_bf16(shared[((int64_t)s * b + t) * H + n]);",
+     "acc = (float)(acc + (double)oracle_f32_from_bf16(shared[((int64_t)s * b + t) * H + n]));"),
+    ("latent norm without eps", "float inv = inverse_rms(oracle_sum_of_squares(x, L), L, eps);",
+     "float inv = inverse_rms(oracle_sum_of_squares(x, L), L, 0.0f);"),
+    ("h keeps -0", "h_out[(int64_t)t * I + i] = pz(oracle_bf16_from_f64(silu * up));",
+     "h_out[(int64_t)t * I + i] = oracle_bf16_from_f64(silu * up);"),
+    ("SiLU rounded to binary32", "double silu = gate / (1.0 + exp(-gate));",
+     "double silu = (float)(gate / (1.0 + exp(-gate)));"),
+    ("gate rounded through binary32", "double gate = oracle_f32_from_bf16(oracle_bf16_from_f64(ga));",
+     "double gate = oracle_f32_from_bf16(oracle_bf16_from_f32((float)ga));"),
+    ("up rounded through binary32", "double up = oracle_f32_from_bf16(oracle_bf16_from_f64(ua));",
+     "double up = oracle_f32_from_bf16(oracle_bf16_from_f32((float)ua));"),
+    ("d rounded through binary32", "uint16_t db = pz(oracle_bf16_from_f64(acc));",
+     "uint16_t db = pz(oracle_bf16_from_f32((float)acc));"),
 ]
+# Mistakes that cannot change any result are not listed.  Examples: dropping
+# the -0 -> +0 step of the EP output or of the accumulated down output (both
+# sums start from +0 and add BF16 values, so neither can be -0 or a nonzero
+# value below the smallest BF16 subnormal); starting the expert-TP slot sum
+# from -0 (a -0 row changes neither the sum of squares nor the +0-started
+# route sum).
 
 
 def build_copy(tmp_path, source: str, name: str) -> str:

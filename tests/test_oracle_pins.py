@@ -494,6 +494,15 @@ def _latent_pair(col0_slots, col1, gamma0):
     return lat.to(torch.bfloat16), gamma.to(torch.bfloat16)
 
 
+def test_latent_norm_uses_eps():
+    # tp = 2 slots of 1 -> x = 2 over L = 8 columns: ss = 32, mean = 32 * 0.125
+    # = 4; eps = 12 makes the denominator 16, inv = 1/4 and y = 2 * 1/4 * 1 =
+    # 0.5 exactly (without eps, y would be 1)
+    lat = torch.ones((2, 1, 8)).to(torch.bfloat16)
+    y = oracle.latent_norm(lat, torch.ones(8).to(torch.bfloat16), 12.0, 1, 2, 8)
+    assert torch.equal(y.float(), torch.full((1, 8), 0.5))
+
+
 def test_latent_norm_rounds_the_slot_sum_to_bf16():
     # column 0 holds 2.578125 and -0.00640869140625 in the two slots, column 1
     # holds 3.546875, gamma[0] = 1.2734375, eps 0.  The slot sum rounded to BF16
@@ -531,6 +540,28 @@ def test_latent_up_rounds_the_double_sum_straight_to_bf16():
     w = torch.ones((1, 8)).to(torch.bfloat16)
     out = oracle.latent_up(y, w, None, 0, 1, 8, 1)
     assert int(bits(out)[0, 0]) == 0x3F81
+
+
+def test_latent_up_adds_the_shared_slots_in_double():
+    # y = (1, 2^-8, 0, ...) against a row of ones gives exactly 1 + 2^-8 (the
+    # BF16 tie between 1 and 1 + 2^-7); one shared slot of 2^-30 moves the
+    # double sum above the tie, so out rounds up to 0x3F81.  Accumulated in
+    # binary32, 1 + 2^-8 + 2^-30 would fall back onto the tie and give 0x3F80.
+    y = torch.tensor([[1.0, 2.0 ** -8, 0, 0, 0, 0, 0, 0]]).to(torch.bfloat16)
+    shared = torch.full((1, 1, 1), 2.0 ** -30).to(torch.bfloat16)
+    out = oracle.latent_up(y, torch.ones((1, 8)).to(torch.bfloat16), shared, 1, 1, 8, 1)
+    assert int(bits(out)[0, 0]) == 0x3F81
+
+
+def test_latent_up_tiny_negative_is_positive_zero():
+    # y[0] = 2^-70 times a weight -2^-70: the sum -2^-140 is below half the
+    # smallest BF16 subnormal (2^-133), rounds to -0 and is written as +0
+    y = torch.zeros((1, 8))
+    y[0, 0] = 2.0 ** -70
+    w = torch.zeros((1, 8))
+    w[0, 0] = -2.0 ** -70
+    out = oracle.latent_up(y.to(torch.bfloat16), w.to(torch.bfloat16), None, 0, 1, 8, 1)
+    assert int(bits(out)[0, 0]) == 0x0000
 
 
 def test_latent_up_identity_weight_reproduces_y():
@@ -599,6 +630,55 @@ def test_shared_h_rounds_the_double_product_straight_to_bf16():
     x, wg, wu, wd = _onehot_shared([-0.7578125], [1.5546875])
     h, _ = oracle.shared_expert(x, wg, wu, wd, 1, 16, 1, out_in=torch.zeros((1, 16)).to(torch.bfloat16))
     assert int(bits(h)[0, 0]) == 0xBEC1
+
+
+def test_shared_h_of_a_zero_gate_is_positive_zero():
+    # silu(0) = 0 / (1 + 1) = +0; times up = -1 gives -0, which h stores as +0
+    x, wg, wu, wd = _onehot_shared([0.0], [-1.0])
+    h, _ = oracle.shared_expert(x, wg, wu, wd, 1, 16, 1, out_in=torch.zeros((1, 16)).to(torch.bfloat16))
+    assert int(bits(h)[0, 0]) == 0x0000
+
+
+def test_shared_h_keeps_silu_in_double():
+    # gate = 18.75, up = 1.25: silu(18.75) = 18.75 (1 - 7.2e-9), so in double
+    # h = 23.4375 (1 - 7.2e-9) = 23.43749983..., just under the BF16 tie 23.4375
+    # between 23.375 (0x41BB) and 23.5 (0x41BC): it rounds down to 0x41BB.  With
+    # silu rounded to binary32 first (to 18.75 exactly) the product would be the
+    # tie itself and round to the even 0x41BC.
+    x, wg, wu, wd = _onehot_shared([18.75], [1.25])
+    h, _ = oracle.shared_expert(x, wg, wu, wd, 1, 16, 1, out_in=torch.zeros((1, 16)).to(torch.bfloat16))
+    assert int(bits(h)[0, 0]) == 0x41BB
+
+
+def test_shared_gate_and_up_round_their_double_sums_straight_to_bf16():
+    # x = (1, 2^-8, 2^-30, 1, 0, ...).  Unit 0: gate = x . (1, 1, 1, 0, ...) =
+    # 1 + 2^-8 + 2^-30 exactly in double, which rounds up to 1.0078125, and up =
+    # 1, so h = bf16(silu(1.0078125)) = bf16(0.73832) = 0x3F3D (through binary32
+    # the gate would be 1.0 and h = bf16(0.73106) = 0x3F3B).  Unit 1: gate = 64
+    # (silu = 64 up to 1e-26) and up = 1 + 2^-8 + 2^-30 -> 1.0078125, so h =
+    # 64.5 = 0x4281 (through binary32: 64 = 0x4280).
+    H, I = 16, 2
+    x = torch.zeros((1, H))
+    x[0, :4] = torch.tensor([1.0, 2.0 ** -8, 2.0 ** -30, 1.0])
+    wg, wu = torch.zeros((I, H)), torch.zeros((I, H))
+    wg[0, :3], wu[0, 0] = 1.0, 1.0
+    wg[1, 3], wu[1, :3] = 64.0, 1.0
+    bf16 = torch.bfloat16
+    h, _ = oracle.shared_expert(x.to(bf16), wg.to(bf16), wu.to(bf16), torch.zeros((H, I)).to(bf16), 1, H, I,
+                                out_in=torch.zeros((1, H)).to(bf16))
+    assert [int(v) for v in bits(h)[0]] == [0x3F3D, 0x4281]
+
+
+def test_shared_down_rounds_its_double_sum_straight_to_bf16():
+    # gate 64 and ups 2^-6, 2^-14, 2^-36 make h = (1, 2^-8, 2^-30) exactly;
+    # a down row of ones sums them to 1 + 2^-8 + 2^-30, which rounds up to
+    # 0x3F81 (through binary32 it would be the tie 1 + 2^-8 and give 0x3F80)
+    down = torch.zeros((16, 3))
+    down[7, :] = 1.0
+    x, wg, wu, wd = _onehot_shared([64.0, 64.0, 64.0], [2.0 ** -6, 2.0 ** -14, 2.0 ** -36], down=down)
+    h, out = oracle.shared_expert(x, wg, wu, wd, 1, 16, 3, accumulate=False)
+    assert [int(v) for v in bits(h)[0]] == [0x3F80, 0x3B80, 0x3080]
+    assert int(bits(out)[0, 7]) == 0x3F81
 
 
 def test_shared_down_tiny_negative_is_positive_zero():
