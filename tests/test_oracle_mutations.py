@@ -4,8 +4,8 @@ Each case plants one mistake in a copy of oracle/moe_tail_oracle.c (a sum in
 the wrong order, a rounding dropped or added, a term, a sign or an operand
 moved), builds the copy with the oracle's flags, and runs the pins
 (tests/test_oracle_pins.py) against it in a child process, which must fail.
-The unchanged copy must pass.  Only the copy is changed; the oracle itself is
-not touched."""
+The unchanged copy must pass.  The copies run side by side, one child
+each.  Only the copies are changed; the oracle itself is not touched."""
 import os
 import subprocess
 import sys
@@ -106,6 +106,49 @@ MUTATIONS = [
     ("d rounded through binary32", "uint16_t db = pz(oracle_bf16_from_f64(acc));",
      "uint16_t db = pz(oracle_bf16_from_f32((float)acc));"),
 ]
+# indexing, layout and formula slips
+MUTATIONS += [
+    ("sum of squares over the gained row when the gains follow the norm",
+     "for (int c = 0; c < P; ++c) v[c] = wbn ? x[c] * g[c] : x[c];", "for (int c = 0; c < P; ++c) v[c] = x[c] * g[c];"),
+    ("gains dropped after the norm", "float n = wbn ? v[c] * inv : (x[c] * inv) * g[c];",
+     "float n = wbn ? v[c] * inv : (x[c] * inv);"),
+    ("gains applied twice before the norm", "float n = wbn ? v[c] * inv : (x[c] * inv) * g[c];",
+     "float n = wbn ? (v[c] * inv) * g[c] : (x[c] * inv) * g[c];"),
+    ("expert-TP sum not reset per token", "        for (int c = 0; c < P; ++c) acc[c] = 0.0f;\n", ""),
+    ("EP output sum not reset per token", "        for (int c = 0; c < P; ++c) o[c] = 0.0f;\n", ""),
+    ("EP slot partial not reset per slot", "            for (int c = 0; c < P; ++c) part[c] = 0.0f;\n", ""),
+    ("EP index of token 0", "int32_t j = idx[((int64_t)s * b + t) * K + k];", "int32_t j = idx[((int64_t)s * b) * K + k];"),
+    ("EP index token-major", "int32_t j = idx[((int64_t)s * b + t) * K + k];",
+     "int32_t j = idx[((int64_t)t * tp + s) * K + k];"),
+    ("EP rows of slot 0 for every slot", "const uint16_t* row = rows + ((int64_t)s * rows_per_slot + j) * P;",
+     "const uint16_t* row = rows + ((int64_t)j) * P;"),
+    ("expert-TP index of token 0", "int32_t j = idx[(int64_t)t * K + k];", "int32_t j = idx[(int64_t)k];"),
+    ("expert-TP partials of slot 0 for every slot",
+     "sum = sum + oracle_f32_from_bf16(partials[((int64_t)s * num_rows + j) * P + c]);",
+     "sum = sum + oracle_f32_from_bf16(partials[((int64_t)j) * P + c]);"),
+    ("route weight divides", "        float p = n * w;\n", "        float p = n / w;\n"),
+    ("latent gamma of column 0", "float n = (x[c] * inv) * oracle_f32_from_bf16(gamma[c]);",
+     "float n = (x[c] * inv) * oracle_f32_from_bf16(gamma[0]);"),
+    ("latent mean over L + 1", "float inv = inverse_rms(oracle_sum_of_squares(x, L), L, eps);",
+     "float inv = inverse_rms(oracle_sum_of_squares(x, L), L + 1, eps);"),
+    ("W_up read transposed",
+     "const uint16_t* wr = w_up + (int64_t)n * L;\n            double acc = 0.0;\n"
+     "            for (int c = 0; c < L; ++c) acc += yd[c] * (double)oracle_f32_from_bf16(wr[c]);",
+     "const uint16_t* wr = w_up + (int64_t)n;\n            double acc = 0.0;\n"
+     "            for (int c = 0; c < L; ++c) acc += yd[c] * (double)oracle_f32_from_bf16(wr[(int64_t)c * H]);"),
+    ("W_gate and W_up swapped",
+     "const uint16_t* gr = w_gate + (int64_t)i * H;\n            const uint16_t* ur = w_up + (int64_t)i * H;",
+     "const uint16_t* gr = w_up + (int64_t)i * H;\n            const uint16_t* ur = w_gate + (int64_t)i * H;"),
+    ("W_down read transposed",
+     "const uint16_t* dr = w_down + (int64_t)n * I;\n            double acc = 0.0;\n"
+     "            for (int i = 0; i < I; ++i) acc += hd[i] * (double)oracle_f32_from_bf16(dr[i]);",
+     "const uint16_t* dr = w_down + (int64_t)n;\n            double acc = 0.0;\n"
+     "            for (int i = 0; i < I; ++i) acc += hd[i] * (double)oracle_f32_from_bf16(dr[(int64_t)i * H]);"),
+    ("accumulate drops the old out", "float sum = oracle_f32_from_bf16(*o) + oracle_f32_from_bf16(db);",
+     "float sum = oracle_f32_from_bf16(db);"),
+    ("SiLU's exponent taken of up", "double silu = gate / (1.0 + exp(-gate));", "double silu = gate / (1.0 + exp(-up));"),
+]
+
 # Mistakes that cannot change any result are not listed.  Examples: dropping
 # the -0 -> +0 step of the EP output or of the accumulated down output (both
 # sums start from +0 and add BF16 values, so neither can be -0 or a nonzero
@@ -128,14 +171,34 @@ def run_pins(lib: str) -> subprocess.CompletedProcess:
                           capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
 
 
-def test_unchanged_copy_passes_the_pins(tmp_path):
-    r = run_pins(build_copy(tmp_path, open(SRC).read(), "unchanged"))
+@pytest.fixture(scope="module")
+def outcomes(tmp_path_factory):
+    """Every copy (the unchanged one under the key None, then each mutant)
+    built and run against the pins, the child processes side by side."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    source = open(SRC).read()
+    names = [m[0] for m in MUTATIONS]
+    assert len(set(names)) == len(names), "two mutations share a name"
+    copies = [(None, source)]
+    for what, old, new in MUTATIONS:
+        assert old in source, f"mutation site not found: {what}"
+        copies.append((what, source.replace(old, new, 1)))
+    tmp = tmp_path_factory.mktemp("oracle_copies")
+
+    def run(i_copy):
+        i, (what, text) = i_copy
+        return what, run_pins(build_copy(tmp, text, f"copy{i}"))
+
+    with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as pool:
+        return dict(pool.map(run, enumerate(copies)))
+
+
+def test_unchanged_copy_passes_the_pins(outcomes):
+    r = outcomes[None]
     assert r.returncode == 0, r.stdout[-2000:]
 
 
-@pytest.mark.parametrize("what,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_pins_catch_the_mistake(tmp_path, what, old, new):
-    source = open(SRC).read()
-    assert old in source, f"mutation site not found: {what}"
-    r = run_pins(build_copy(tmp_path, source.replace(old, new, 1), "mutant"))
-    assert r.returncode != 0, f"no pin fails with: {what}"
+@pytest.mark.parametrize("what", [m[0] for m in MUTATIONS])
+def test_pins_catch_the_mistake(outcomes, what):
+    assert outcomes[what].returncode != 0, f"no pin fails with: {what}"
