@@ -373,6 +373,40 @@ def test_ep_brute_force_double(wbn):
 
 # ------------------------------------------------------------- expert-TP finalize
 
+@pytest.mark.parametrize("wbn", [True, False])
+def test_tp_brute_force_double(wbn):
+    # The expert-TP formula recomputed on tiny inputs: each route row's slot sum
+    # in binary32 from +0 in slot order, rounded to BF16 (the method fixes both),
+    # then the norm, the gains and the weighted route sum in double.  The
+    # oracle's binary32 steps must land within one BF16 ulp of it, plus the
+    # binary32 rounding of a route sum that cancels.
+    d = synth.config(3, b=4, P=264, tp=3, K=3, weight_before_norm=wbn)
+    idx = d["idx"].clone()
+    idx[1, 2] = -1  # one route without a row
+    Q = d["partials"].float().numpy()
+    g = d["gamma"].double().numpy() + d["gain_center"]
+    w = d["w"].double().numpy()
+    ref = np.zeros((d["b"], d["P"]))
+    mag = np.zeros((d["b"], d["P"]))
+    for t in range(d["b"]):
+        for k in range(d["K"]):
+            j = int(idx[t, k])
+            if not 0 <= j < d["num_rows"]:
+                continue
+            xs = np.zeros(d["P"], dtype=np.float32)
+            for s in range(d["tp"]):
+                xs = (xs + Q[s, j]).astype(np.float32)
+            x = torch.from_numpy(xs).to(torch.bfloat16).double().numpy()
+            v = x * g if wbn else x
+            n = v / np.sqrt(np.mean(v * v) + d["eps"])
+            if not wbn:
+                n = n * g
+            ref[t] += w[t, k] * n
+            mag[t] += np.abs(w[t, k] * n)
+    got = tp_call(d, idx=idx).double().numpy()
+    assert np.all(np.abs(got - ref) <= ulp_bf16(ref) + 2.0 ** -20 * mag)
+
+
 @pytest.mark.parametrize("kind", ["ep", "tp"])
 def test_single_route_is_textbook_rmsnorm(kind):
     # One route per token, w = 1, tp = 1, gamma = 0 with gain center 1: the
@@ -501,6 +535,26 @@ def test_latent_norm_uses_eps():
     lat = torch.ones((2, 1, 8)).to(torch.bfloat16)
     y = oracle.latent_norm(lat, torch.ones(8).to(torch.bfloat16), 12.0, 1, 2, 8)
     assert torch.equal(y.float(), torch.full((1, 8), 0.5))
+
+
+def test_latent_norm_brute_force_double():
+    # The latent norm recomputed on tiny inputs (ragged chunk: L = 264): the
+    # slot sum in binary32 from +0 in slot order, rounded to BF16 (as the
+    # method fixes), then x / sqrt(mean(x^2) + eps) * gamma in double.  The
+    # oracle's y must be within one BF16 ulp of it.
+    b, tp, L = 3, 3, 264
+    d = synth.latent_up_inputs(0x1B, b=b, tp=tp, L=L, H=8, tp_s=0)
+    lat = d["latent"].float().numpy()
+    gamma = d["gamma"].double().numpy()
+    ref = np.zeros((b, L))
+    for t in range(b):
+        xs = np.zeros(L, dtype=np.float32)
+        for s in range(tp):
+            xs = (xs + lat[s, t]).astype(np.float32)
+        x = torch.from_numpy(xs).to(torch.bfloat16).double().numpy()
+        ref[t] = x / np.sqrt(np.mean(x * x) + d["eps"]) * gamma
+    got = oracle.latent_norm(d["latent"], d["gamma"], d["eps"], b, tp, L).double().numpy()
+    assert np.all(np.abs(got - ref) <= ulp_bf16(ref))
 
 
 def test_latent_norm_rounds_the_slot_sum_to_bf16():
