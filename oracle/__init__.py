@@ -87,6 +87,8 @@ def _weights(w: torch.Tensor):
 
 
 def _check(rc: int, name: str) -> None:
+    if rc == -2:
+        raise MemoryError(f"{name}: host allocation failed")
     if rc != 0:
         raise ValueError(f"{name}: arguments refused ({rc})")
 

@@ -44,6 +44,9 @@
  *  - latent tail: the slot sum is rounded to BF16 before the norm; the norm
  *    has gain center 0, y = bf16((x * inv) * gamma).
  *  - shared expert activation: SiLU, silu(g) = g / (1 + exp(-g)).
+ *
+ * Every entry returns 0 on success, -1 when its sizes are refused and -2 when
+ * a host allocation fails (nothing is written then).
  */
 #include <math.h>
 #include <stdint.h>
@@ -164,6 +167,10 @@ int oracle_ep_finalize(const uint16_t* rows, int64_t rows_per_slot, const int32_
     float* v = malloc(sizeof(float) * P);
     float* part = malloc(sizeof(float) * P);
     float* o = malloc(sizeof(float) * P);
+    if (!g || !x || !v || !part || !o) {
+        free(g); free(x); free(v); free(part); free(o);
+        return -2;
+    }
     for (int c = 0; c < P; ++c) g[c] = oracle_f32_from_bf16(gamma[c]) + gain_center;
     for (int t = 0; t < b; ++t) {
         for (int c = 0; c < P; ++c) o[c] = 0.0f;
@@ -200,6 +207,10 @@ int oracle_tp_finalize(const uint16_t* partials, int64_t num_rows, const int32_t
     float* x = malloc(sizeof(float) * P);
     float* v = malloc(sizeof(float) * P);
     float* acc = malloc(sizeof(float) * P);
+    if (!g || !x || !v || !acc) {
+        free(g); free(x); free(v); free(acc);
+        return -2;
+    }
     for (int c = 0; c < P; ++c) g[c] = oracle_f32_from_bf16(gamma[c]) + gain_center;
     for (int t = 0; t < b; ++t) {
         for (int c = 0; c < P; ++c) acc[c] = 0.0f;
@@ -228,6 +239,7 @@ int oracle_latent_norm(const uint16_t* latent, const uint16_t* gamma, float eps,
                        int L, uint16_t* y) {
     if (b < 0 || tp < 1 || L < 1) return -1;
     float* x = malloc(sizeof(float) * L);
+    if (!x) return -2;
     for (int t = 0; t < b; ++t) {
         for (int c = 0; c < L; ++c) {
             float sum = 0.0f;
@@ -252,6 +264,7 @@ int oracle_latent_up(const uint16_t* y, const uint16_t* w_up, const uint16_t* sh
                      int b, int L, int H, uint16_t* out) {
     if (b < 0 || L < 1 || H < 1 || tp_s < 0) return -1;
     double* yd = malloc(sizeof(double) * L);
+    if (!yd) return -2;
     for (int t = 0; t < b; ++t) {
         for (int c = 0; c < L; ++c) yd[c] = oracle_f32_from_bf16(y[(int64_t)t * L + c]);
         for (int n = 0; n < H; ++n) {
@@ -275,6 +288,7 @@ int oracle_shared_down(const uint16_t* h, const uint16_t* w_down, int b, int H, 
                        int accumulate) {
     if (b < 0 || H < 1 || I < 1) return -1;
     double* hd = malloc(sizeof(double) * I);
+    if (!hd) return -2;
     for (int t = 0; t < b; ++t) {
         for (int i = 0; i < I; ++i) hd[i] = oracle_f32_from_bf16(h[(int64_t)t * I + i]);
         for (int n = 0; n < H; ++n) {
@@ -305,6 +319,7 @@ int oracle_shared_expert(const uint16_t* x, const uint16_t* w_gate, const uint16
                          uint16_t* out, int accumulate) {
     if (b < 0 || H < 1 || I < 1 || !h_out) return -1;
     double* xd = malloc(sizeof(double) * H);
+    if (!xd) return -2;
     for (int t = 0; t < b; ++t) {
         for (int c = 0; c < H; ++c) xd[c] = oracle_f32_from_bf16(x[(int64_t)t * H + c]);
         for (int i = 0; i < I; ++i) {
