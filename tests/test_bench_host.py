@@ -1,7 +1,9 @@
 """Host-side pieces of bench.py that need no GPU: the argument defaults keep
-the timing contract, and the end-to-end leg's packed buffers lay the step's
+the timing contract, the end-to-end leg's packed buffers lay the step's
 activations out aligned, without overlap, with the copied region ending before
-the shared expert's output slot."""
+the shared expert's output slot, the reference arm (the oracle on the host)
+prints one contract line on rank 0 only, and the CUDA arm refuses to run
+without a device."""
 import importlib.util
 import os
 import sys
@@ -43,3 +45,43 @@ def test_packed_layout_of_the_step_inputs(bench):
     # the step copies everything up to the end of the latent tail's TP shared slots
     h2d = offs["shared9"] + TP * B * H * 2
     assert h2d == spans[-1][1] - B * H * 2
+
+
+def _run_bench(*argv, env=None):
+    import subprocess
+
+    e = dict(os.environ)
+    e.update(env or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *argv], capture_output=True, text=True,
+                          env=e, cwd=ROOT, timeout=600)
+
+
+def test_reference_arm_prints_one_contract_line():
+    # the oracle timed on the host cores: one JSON line with the contract's
+    # keys, its cpu_baseline describing this run and an e2e of its own value
+    import json
+
+    r = _run_bench("--impl", "reference", "--steps", "1", "--warmup", "3", env={"WORLD_SIZE": "1", "RANK": "0"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
+    assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    r = _run_bench("--impl", "reference", "--steps", "1", "--warmup", "3",
+                   env={"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the refusal without a CUDA device")
+def test_cuda_arm_refuses_to_run_without_a_device():
+    # no CPU fallback: the CUDA arm exits non-zero and says why
+    r = _run_bench("--steps", "1", "--warmup", "3")
+    assert r.returncode != 0 and "no CUDA device" in (r.stderr + r.stdout)
