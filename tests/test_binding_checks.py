@@ -199,3 +199,20 @@ def test_shared_split_calls_refuse_a_wrong_h():
         mt.moe_shared_down(torch.empty((3, 136)), wd, out)
     with pytest.raises(ValueError, match="^(w_down|out) "):
         mt.moe_shared_down(torch.empty((3, 135), dtype=BF), wd, out)
+
+
+def test_missing_library_fails_loudly():
+    # no CPU path: without the CUDA library every call that reaches it raises
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import moe_decode_tail_gb300 as mt\n"
+            "try:\n"
+            "    mt.moe_tail_workspace_bytes(0, 4, 512)\n"
+            "except RuntimeError as e:\n"
+            "    print('refused:', e)\n")
+    env = dict(os.environ, MOE_TAIL_LIBRARY=os.path.join(root, "no_such_libmoetail.so"), PYTHONPATH=root)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=root, timeout=300)
+    assert r.returncode == 0 and "refused:" in r.stdout and "is missing" in r.stdout, r.stdout + r.stderr
