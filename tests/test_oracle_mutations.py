@@ -149,12 +149,30 @@ MUTATIONS += [
     ("SiLU's exponent taken of up", "double silu = gate / (1.0 + exp(-gate));", "double silu = gate / (1.0 + exp(-up));"),
 ]
 
+# roundings fused or moved
+MUTATIONS += [
+    ("each square fused into the lane's add", "                float sq = e * e;\n                acc = acc + sq;",
+     "                acc = (float)((double)acc + (double)e * (double)e);"),
+    ("EP running slot sum rounded to BF16", "o[c] = o[c] + bf16_round(part[c]);", "o[c] = bf16_round(o[c] + part[c]);"),
+    ("expert-TP running slot sum rounded to BF16",
+     "sum = sum + oracle_f32_from_bf16(partials[((int64_t)s * num_rows + j) * P + c]);",
+     "sum = bf16_round(sum + oracle_f32_from_bf16(partials[((int64_t)s * num_rows + j) * P + c]));"),
+    ("route product rounded to BF16", "        float p = n * w;\n", "        float p = bf16_round(n * w);\n"),
+    ("normalised value rounded to BF16", "        float n = wbn ? v[c] * inv : (x[c] * inv) * g[c];\n",
+     "        float n = bf16_round(wbn ? v[c] * inv : (x[c] * inv) * g[c]);\n"),
+    ("gains rounded to BF16", "for (int c = 0; c < P; ++c) g[c] = oracle_f32_from_bf16(gamma[c]) + gain_center;",
+     "for (int c = 0; c < P; ++c) g[c] = bf16_round(oracle_f32_from_bf16(gamma[c]) + gain_center);"),
+    ("inverse RMS in double", "    return 1.0f / sqrtf(den);", "    return (float)(1.0 / sqrt((double)den));"),
+]
+
 # Mistakes that cannot change any result are not listed.  Examples: dropping
 # the -0 -> +0 step of the EP output or of the accumulated down output (both
 # sums start from +0 and add BF16 values, so neither can be -0 or a nonzero
 # value below the smallest BF16 subnormal); starting the expert-TP slot sum
 # from -0 (a -0 row changes neither the sum of squares nor the +0-started
-# route sum).
+# route sum); forming 1/P or mean + eps in double and rounding once to
+# binary32 (double carries more than 2 * 24 + 2 bits, so one operation
+# rounded twice is still correctly rounded).
 
 
 def build_copy(tmp_path, source: str, name: str) -> str:

@@ -131,6 +131,17 @@ def test_sum_of_squares_exact_on_small_integers(P):
     assert oracle.sum_of_squares(v) == float(np.sum(v.astype(np.int64) ** 2))
 
 
+def test_sum_of_squares_rounds_each_square_before_adding():
+    # v = (1, 1 + 2^-12 + 2^-23, 0, ...): the second square is
+    # 1 + 2^-11 + 2^-22 + 2^-24 + 2^-34 + 2^-46, rounded to binary32 it is
+    # 1 + 2^-11 + 3 * 2^-23.  Added to 1 that is 2 + 2^-11 + 1.5 ulp (ulp 2^-22
+    # at 2): a tie, to even, 2 + 2^-11 + 2^-21.  Squaring and adding in one
+    # rounding (a fused multiply-add) would give 2 + 2^-11 + 2^-22.
+    v = np.zeros(8, dtype=np.float32)
+    v[0], v[1] = 1.0, 1.0 + 2.0 ** -12 + 2.0 ** -23
+    assert oracle.sum_of_squares(v) == 2.0 + 2.0 ** -11 + 2.0 ** -21
+
+
 def test_sum_of_squares_lane_adds_columns_in_order():
     # lane 0: 4096^2 = 2^24 then seven 1s.  In column order each +1 is a tie
     # that rounds back to 2^24 (even), so the total is 2^24.  Any other order
@@ -206,6 +217,16 @@ def test_ep_slot_partials_are_rounded_to_bf16_before_the_slot_sum():
     # per-slot rounding the sum 1 + 2^-7 + 2^-20 would round to 1.0078125.
     d = constant_ep([[1.0 + 2.0 ** -8 + 2.0 ** -20], [2.0 ** -8]])
     assert torch.equal(ep_call(d).float(), torch.full((1, 256), 1.015625))
+
+
+def test_ep_slot_sum_stays_in_binary32():
+    # three slots with one route each on rows of 1 (n = 1): partials 1,
+    # 3 * 2^-10, 3 * 2^-10, all exact in BF16.  Summed in binary32 they give
+    # 1 + 1.5 * 2^-8, above the BF16 tie 1 + 2^-8, so out = 1 + 2^-7 (0x3F81).
+    # Rounding the running sum to BF16 after each slot would drop each
+    # 3 * 2^-10 (below the tie) and give 1.0.
+    d = constant_ep([[1.0], [3 * 2.0 ** -10], [3 * 2.0 ** -10]])
+    assert np.all(bits(ep_call(d)) == 0x3F81)
 
 
 def test_ep_slots_sum_in_rank_order():
