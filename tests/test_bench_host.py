@@ -85,3 +85,24 @@ def test_cuda_arm_refuses_to_run_without_a_device():
     # no CPU fallback: the CUDA arm exits non-zero and says why
     r = _run_bench("--steps", "1", "--warmup", "3")
     assert r.returncode != 0 and "no CUDA device" in (r.stderr + r.stdout)
+
+
+def test_traffic_is_reported_only_for_the_sources_it_was_measured_on(bench, monkeypatch, tmp_path):
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "roofline_traffic.txt").write_text(
+        "# comment lines are skipped\nsources_sha256 abc123\ntraffic_bytes_per_call 270426112\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_sources_hash", lambda: "abc123")
+    assert bench.traffic_record() == 270426112
+    monkeypatch.setattr(bench, "kernel_sources_hash", lambda: "changed")
+    assert bench.traffic_record() is None
+    (tmp_path / "profiles" / "roofline_traffic.txt").unlink()
+    assert bench.traffic_record() is None
+
+
+def test_kernel_sources_hash_covers_the_gemm_sources(bench):
+    # the hash is of the files that define the measured kernels and their launch
+    csrc = os.path.join(ROOT, "moe_decode_tail_gb300", "csrc")
+    assert all(os.path.exists(os.path.join(csrc, f)) for f in bench.GEMM_SOURCES)
+    assert {"decode_gemm.cu", "moe_tail_api.cu"} <= set(bench.GEMM_SOURCES)
+    assert len(bench.kernel_sources_hash()) == 64
