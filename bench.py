@@ -159,16 +159,22 @@ class ClockSampler:
             if len(parts) < 8:
                 continue
             try:
-                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+                sm, sm_max = float(parts[0]), float(parts[1])
             except ValueError:
                 continue
+            try:
+                power = float(parts[2])
+            except ValueError:  # "[N/A]": the clock sample still counts
+                power = None
+            rows.append((sm, sm_max, power, parts[3:]))
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3][1:5]) if v.lower() == "active"})
+        powers = [r[2] for r in rows if r[2] is not None]
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+                "power_w_max": max(powers) if powers else None, "samples": len(rows), "reasons": reasons}
 
 
 # ----------------------------------------------------------------------------- workload

@@ -106,3 +106,34 @@ def test_kernel_sources_hash_covers_the_gemm_sources(bench):
     assert all(os.path.exists(os.path.join(csrc, f)) for f in bench.GEMM_SOURCES)
     assert {"decode_gemm.cu", "moe_tail_api.cu"} <= set(bench.GEMM_SOURCES)
     assert len(bench.kernel_sources_hash()) == 64
+
+
+def test_clock_samples_summarised(bench, tmp_path):
+    # nvidia-smi's CSV (noheader, nounits): clocks.sm, clocks.max.sm, power.draw,
+    # reasons.active, hw_slowdown, hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap
+    csv = tmp_path / "clocks.csv"
+    csv.write_text("2070, 2070, 900.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n"
+                   "2055, 2070, 1010.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n"
+                   "2070, 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active\n"
+                   "garbage line\n"
+                   "2040, 2070, 980.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n")
+
+    class Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    s = bench.ClockSampler(0)
+    s.proc, s.path = Done(), str(csv)
+    r = s.stop()
+    # four samples (the one without a power reading still counts its clock), median 2062.5
+    assert r["samples"] == 4 and r["sm_mhz"] == 2062.5 and r["sm_max_mhz"] == 2070 and r["power_w_max"] == 1010.0
+    assert r["reasons"] == ["sw_power_cap"]
+    assert not csv.exists()
+
+
+def test_clock_sampler_without_nvidia_smi_says_so(bench):
+    s = bench.ClockSampler(0)
+    assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
