@@ -166,8 +166,8 @@ def test_finalize_flags_b_zero(lib, which):
 
 
 def latent(lib, **kw):
-    args = dict(lat=a(), gamma=a(1 << 24), eps=1e-6, w=a(2 << 24), sh=a(3 << 24), tp_s=8, b=16, tp=8, L=3584, H=7168,
-                out=a(4 << 24), ws=a(5 << 24), wsb=16 * 3584 * 2, stream=None)
+    args = dict(lat=a(), gamma=a(1 << 28), eps=1e-6, w=a(2 << 28), sh=a(3 << 28), tp_s=8, b=16, tp=8, L=3584, H=7168,
+                out=a(4 << 28), ws=a(5 << 28), wsb=16 * 3584 * 2, stream=None)
     args.update(kw)
     return lib.moe_tail_latent_up(args["lat"], args["gamma"], args["eps"], args["w"], args["sh"], args["tp_s"],
                                   args["b"], args["tp"], args["L"], args["H"], args["out"], args["ws"], args["wsb"],
@@ -177,8 +177,8 @@ def latent(lib, **kw):
 @host_only
 @pytest.mark.parametrize("bad", [
     dict(tp=0), dict(tp_s=-1), dict(tp_s=33), dict(L=3583), dict(H=7170), dict(L=4), dict(b=-2),
-    dict(sh=None), dict(tp_s=0), dict(ws=None), dict(wsb=16 * 3584 * 2 - 1), dict(out=a(5 << 24)),
-    dict(ws=a(4 << 24)), dict(lat=a(3)), dict(w=a(8)), dict(L=40000),
+    dict(sh=None), dict(tp_s=0), dict(ws=None), dict(wsb=16 * 3584 * 2 - 1), dict(out=a(5 << 28)),
+    dict(ws=a(4 << 28)), dict(lat=a(3)), dict(w=a(8)), dict(L=40000),
 ])
 def test_latent_up_refuses_bad_arguments(lib, bad):
     assert latent(lib, **bad) == EINVAL
@@ -207,7 +207,7 @@ def test_latent_norm_refuses_bad_arguments(lib, bad):
 
 
 def up(lib, **kw):
-    args = dict(y=a(), w=a(1 << 24), sh=a(2 << 24), tp_s=8, b=16, L=3584, H=7168, out=a(3 << 24), flags=0,
+    args = dict(y=a(), w=a(1 << 28), sh=a(2 << 28), tp_s=8, b=16, L=3584, H=7168, out=a(3 << 28), flags=0,
                 stream=None)
     args.update(kw)
     return lib.moe_tail_up_project(args["y"], args["w"], args["sh"], args["tp_s"], args["b"], args["L"], args["H"],
@@ -218,7 +218,7 @@ def up(lib, **kw):
 @pytest.mark.parametrize("bad", [
     dict(tp_s=-1), dict(tp_s=33), dict(L=3583), dict(H=7170), dict(H=4), dict(b=-2), dict(sh=None), dict(tp_s=0),
     dict(y=None), dict(w=None), dict(out=None), dict(flags=2), dict(flags=-1), dict(out=a(8)),
-    dict(out=a(2 << 24)), dict(out=a(16)),  # out over shared, over y
+    dict(out=a(2 << 28)), dict(out=a(16)),  # out over shared, over y
 ])
 def test_up_project_refuses_bad_arguments(lib, bad):
     assert up(lib, **bad) == EINVAL
@@ -231,8 +231,8 @@ def test_latent_steps_b_zero(lib):
 
 
 def latent_flags(lib, **kw):
-    args = dict(lat=a(), gamma=a(1 << 24), eps=1e-6, w=a(2 << 24), sh=a(3 << 24), tp_s=8, b=16, tp=8, L=3584,
-                H=7168, out=a(4 << 24), y=a(5 << 24), flags=3, stream=None)
+    args = dict(lat=a(), gamma=a(1 << 28), eps=1e-6, w=a(2 << 28), sh=a(3 << 28), tp_s=8, b=16, tp=8, L=3584,
+                H=7168, out=a(4 << 28), y=a(5 << 28), flags=3, stream=None)
     args.update(kw)
     return lib.moe_tail_latent_up_flags(args["lat"], args["gamma"], args["eps"], args["w"], args["sh"],
                                         args["tp_s"], args["b"], args["tp"], args["L"], args["H"], args["out"],
@@ -243,7 +243,7 @@ def latent_flags(lib, **kw):
 @pytest.mark.parametrize("bad", [
     dict(tp=0), dict(tp_s=33), dict(L=3583), dict(H=7170), dict(b=-1), dict(sh=None), dict(tp_s=0),
     dict(y=None), dict(lat=None), dict(out=None), dict(flags=4), dict(flags=-1), dict(y=a(8)),
-    dict(y=a(4 << 24)), dict(y=a(16)), dict(out=a(5 << 24)), dict(y=a(3 << 24)),  # y over out, latent, shared
+    dict(y=a(4 << 28)), dict(y=a(16)), dict(out=a(5 << 28)), dict(y=a(3 << 28)),  # y over out, latent, shared
 ])
 def test_latent_up_flags_refuses_bad_arguments(lib, bad):
     assert latent_flags(lib, **bad) == EINVAL
@@ -252,6 +252,32 @@ def test_latent_up_flags_refuses_bad_arguments(lib, bad):
 @host_only
 def test_latent_up_flags_b_zero(lib):
     assert latent_flags(lib, b=0, lat=None, w=None, out=None, y=None) == OK
+
+
+def noalloc(lib, **kw):
+    args = dict(lat=a(), gamma=a(1 << 28), eps=1e-6, w=a(2 << 28), sh=a(3 << 28), tp_s=8, b=16, tp=8, L=3584,
+                H=7168, out=a(4 << 28), stream=None)
+    args.update(kw)
+    return lib.moe_tail_latent_up_noalloc(args["lat"], args["gamma"], args["eps"], args["w"], args["sh"],
+                                          args["tp_s"], args["b"], args["tp"], args["L"], args["H"], args["out"],
+                                          args["stream"])
+
+
+@host_only
+@pytest.mark.parametrize("bad", [
+    dict(tp=0), dict(tp=33), dict(tp_s=-1), dict(tp_s=33), dict(L=3583), dict(L=4), dict(L=40000), dict(H=7170),
+    dict(H=4), dict(H=(1 << 24) + 8), dict(b=-2), dict(b=65536), dict(sh=None), dict(tp_s=0), dict(lat=None),
+    dict(gamma=None), dict(w=None), dict(out=None), dict(lat=a(3)), dict(w=a(8)), dict(out=a(8)),
+    dict(out=a(16)), dict(out=a(3 << 28)),  # out over the latent, over shared
+    dict(b=147),  # y (147 x 3584 BF16) larger than the built-in 1 MiB scratch
+])
+def test_latent_up_noalloc_refuses_bad_arguments(lib, bad):
+    assert noalloc(lib, **bad) == EINVAL
+
+
+@host_only
+def test_latent_up_noalloc_b_zero(lib):
+    assert noalloc(lib, b=0, lat=None, gamma=None, w=None, out=None) == OK
 
 
 def shared(lib, **kw):
@@ -320,3 +346,18 @@ def test_status_strings(lib):
     assert lib.moe_tail_status_str(0) == b"ok"
     assert lib.moe_tail_status_str(1) == b"invalid argument"
     assert lib.moe_tail_status_str(99) == b"unknown status"
+
+
+@host_only
+@pytest.mark.parametrize("name", ["ep", "tp", "fin_flags_ep", "fin_flags_tp", "latent", "norm", "up", "latent_flags",
+                                  "noalloc", "shared", "gate_up", "down"])
+def test_default_arguments_pass_every_check(lib, name):
+    # Each refusal test changes one argument of these defaults, so the defaults
+    # themselves must be accepted: with no GPU visible the call then fails at its
+    # first CUDA call (MOE_TAIL_ECUDA, or ENOTSUP where a tensor map cannot be
+    # encoded), never with EINVAL.
+    if name.startswith("fin_flags_"):
+        rc = fin_flags(lib, name[len("fin_flags_"):])
+    else:
+        rc = globals()[name](lib)
+    assert rc in (2, 3), rc
