@@ -37,7 +37,10 @@ def test_oracle_reproduces_the_stored_outputs():
     import oracle
 
     oracle.build()
-    for name, desc, tensors in make_golden.cases():
+    cases = list(make_golden.cases())
+    # every stored fixture is recomputed (none silently skipped)
+    assert sorted(c[0] for c in cases) == sorted(f[:-4] for f in os.listdir(HERE) if f.endswith(".txt"))
+    for name, desc, tensors in cases:
         expect = open(os.path.join(HERE, f"{name}.txt")).read()
         assert make_golden.render(name, desc, tensors) == expect, f"{name}: the oracle's output changed"
 
