@@ -26,6 +26,14 @@ def test_selftest_rejects_limits_out_of_range(mt):
     assert mt.lib().moe_tail_selftest_wait_timeout(1000001, None) == mt.EINVAL
 
 
+@pytest.mark.skipif(torch.cuda.is_available(), reason="with a GPU a valid limit launches the self-test")
+def test_selftest_accepts_the_limits_at_the_ends_of_its_range(mt):
+    # 1 us and 1 s pass the host checks; with no GPU visible the call then
+    # fails at its first CUDA call instead of being refused
+    assert mt.lib().moe_tail_selftest_wait_timeout(1, None) == mt.ECUDA
+    assert mt.lib().moe_tail_selftest_wait_timeout(1000000, None) == mt.ECUDA
+
+
 @pytest.mark.gpu
 def test_expired_wait_is_reported_and_the_device_stays_usable(mt):
     assert mt.moe_tail_take_device_error() == 0
