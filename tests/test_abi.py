@@ -361,3 +361,11 @@ def test_default_arguments_pass_every_check(lib, name):
     else:
         rc = globals()[name](lib)
     assert rc in (2, 3), rc
+
+
+def test_binding_has_every_declared_call_under_the_same_name():
+    import moe_decode_tail_gb300 as mt
+
+    missing = [n for n in declared() if not callable(getattr(mt, n, None))]
+    assert not missing, missing
+    assert set(declared()) <= set(mt.__all__)
