@@ -137,8 +137,8 @@ int moe_tail_tp_finalize_flags(const void* partials, int64_t num_rows, const int
  *   out        BF16 [b][H]
  *   workspace  >= moe_tail_workspace_bytes(0, b, L) bytes, 16-byte aligned;
  *              holds y (BF16 [b][L]) after the call
- * Limits: 1 <= tp <= 32, 0 <= tp_s <= 32, 8 <= L <= 32768, 8 <= H, L % 8 == 0,
- * H % 8 == 0, b <= 65535.
+ * Limits: 1 <= tp <= 32, 0 <= tp_s <= 32, 8 <= L <= 32768, 8 <= H <= 16777216,
+ * L % 8 == 0, H % 8 == 0, b <= 65535.
  */
 int moe_tail_latent_up(const void* latent, const void* gamma, float eps, const void* w_up,
                        const void* shared, int tp_s, int b, int tp, int L, int H, void* out,
@@ -171,8 +171,8 @@ int moe_tail_latent_up(const void* latent, const void* gamma, float eps, const v
  *   first weight tiles before it waits for the stream's preceding kernel, so
  *   with programmatic dependent launch the weight stream starts while that
  *   kernel drains; y and shared are always read after the wait.
- *   Limits: 0 <= tp_s <= 32, 8 <= L <= 32768, 8 <= H, L % 8 == 0,
- *   H % 8 == 0, b <= 65535.
+ *   Limits: 0 <= tp_s <= 32, 8 <= L <= 32768, 8 <= H <= 16777216,
+ *   L % 8 == 0, H % 8 == 0, b <= 65535.
  */
 #define MOE_TAIL_WEIGHTS_STATIC 1
 #define MOE_TAIL_INPUTS_READY 2
@@ -221,7 +221,8 @@ int moe_tail_latent_up_flags(const void* latent, const void* gamma, float eps, c
  *   out        BF16 [b][H] (read as well when accumulate != 0)
  *   workspace  >= moe_tail_workspace_bytes(1, b, I) bytes, 16-byte aligned;
  *              holds h (BF16 [b][I]) after the call
- * Limits: 8 <= H, 8 <= I, H % 8 == 0, I % 8 == 0.
+ * Limits: 8 <= H <= 16777216, 8 <= I <= 16777216, H % 8 == 0, I % 8 == 0,
+ * b <= 65535.
  */
 int moe_shared_expert(const void* x, const void* w_gate, const void* w_up, const void* w_down,
                       int b, int H, int I, void* out, int accumulate, void* workspace,
@@ -243,7 +244,8 @@ int moe_shared_expert(const void* x, const void* w_gate, const void* w_up, const
  *   flags (both calls): 0, or MOE_TAIL_WEIGHTS_STATIC (as for
  *   moe_tail_up_project: the first weight tiles are requested before the
  *   kernel waits for the stream's preceding kernel).
- *   Limits: 8 <= H, 8 <= I, H % 8 == 0, I % 8 == 0, b <= 65535.
+ *   Limits: 8 <= H <= 16777216, 8 <= I <= 16777216, H % 8 == 0, I % 8 == 0,
+ *   b <= 65535.
  */
 int moe_shared_gate_up(const void* x, const void* w_gate, const void* w_up, int b, int H, int I, void* h,
                        int flags, void* stream);

@@ -369,3 +369,32 @@ def test_binding_has_every_declared_call_under_the_same_name():
     missing = [n for n in declared() if not callable(getattr(mt, n, None))]
     assert not missing, missing
     assert set(declared()) <= set(mt.__all__)
+
+
+@host_only
+def test_width_caps_are_exact(lib):
+    # H (and I) up to 2^24 pass the checks and 2^24 + 8 is refused, as the
+    # header states; shapes are kept small elsewhere (L = 8, b = 1, no shared
+    # partials) so that no buffer overlaps another at the cap
+    cap = 1 << 24
+    for n, want in ((cap, (2, 3)), (cap + 8, (EINVAL,))):
+        assert latent(lib, H=n, L=8, b=1, tp_s=0, sh=None, wsb=lib.moe_tail_workspace_bytes(0, 1, 8)) in want
+        assert up(lib, H=n, L=8, b=1, tp_s=0, sh=None) in want
+        assert latent_flags(lib, H=n, L=8, b=1, tp_s=0, sh=None) in want
+        assert noalloc(lib, H=n, L=8, b=1, tp_s=0, sh=None) in want
+        assert shared(lib, H=n, I=8, b=1, wsb=lib.moe_tail_workspace_bytes(1, 1, 8)) in want
+        assert shared(lib, H=8, I=n, b=1, wsb=max(256, 2 * n)) in want
+        assert gate_up(lib, H=n, I=8, b=1) in want
+        assert gate_up(lib, H=8, I=n, b=1) in want
+        assert down(lib, H=n, I=8, b=1) in want
+        assert down(lib, H=8, I=n, b=1) in want
+
+
+@host_only
+def test_token_cap_is_exact(lib):
+    for b, want in ((65535, (2, 3)), (65536, (EINVAL,))):
+        assert ep(lib, b=b, out=a(1 << 30)) in want
+        assert norm(lib, b=b, L=8, y=a(1 << 30)) in want
+        assert shared(lib, b=b, H=8, I=8, wsb=-(-16 * b // 256) * 256) in want
+        assert gate_up(lib, b=b, H=8, I=8) in want
+        assert down(lib, b=b, H=8, I=8) in want
