@@ -65,13 +65,14 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload isolated timings")
-    ap.add_argument("--composition", default="two_branch",
-                    choices=["two_branch", "two_branch_one_call", "two_branch_split", "tp_after_gateup", "latent_main",
-                             "norm_main", "norm_side_first", "norm_side_after"],
+    ap.add_argument("--composition", default="two_branch", choices=["two_branch", "two_branch_one_call", "latent_main"],
                     help="how the step orders the weight-streaming calls (see run_step)")
     ap.add_argument("--only-config", type=int, choices=[1, 2, 3, 4, 5], default=None,
                     help="run one workload's call alone --calls times and exit (for profiling the call)")
     ap.add_argument("--calls", type=int, default=4)
+    ap.add_argument("--trace", choices=["step", "latent"], default=None,
+                    help="per-CTA timeline from the trace build: ten decode steps as one graph (step), or the latent "
+                         "tail's one-kernel form alone at b = 1, 4, 16 (latent)")
     ap.add_argument("--sequential", action="store_true",
                     help="run the four calls in order on one stream (shared expert accumulating into out)")
     return ap.parse_args()
@@ -240,8 +241,9 @@ def run_step(mt, w, stream, events=None, side=None):
     with both promises -- inputs ready (the latent partials are read while
     the down projection drains) and static weights -- and adds d with the
     other slots in its epilogue; the call enqueues the norm and the
-    up-projection ("two_branch_split" makes the two split calls,
-    moe_tail_latent_norm and moe_tail_up_project, with the same promises).
+    up-projection.  With "latent_main" the latent tail runs on the main
+    stream after the finalize calls, beside the shared expert's gate/up, and
+    the down projection then adds d into its output.
     EP and expert-TP finalize run on the main stream, which joins the side
     stream at the end of the step.  Without a side stream the calls run in
     order (moe_tail_latent_up in one call) and the shared expert accumulates
@@ -314,69 +316,6 @@ def run_step(mt, w, stream, events=None, side=None):
         mt.moe_shared_down(ws_h, w["w_down"], w["out"], accumulate=True, weights_static=True, stream=stream)
         rec(11, stream)
         return
-    if comp == "tp_after_gateup":
-        # as two_branch, with the shared expert as its two calls and expert-TP
-        # finalize started once gate/up has streamed its weights, so its rows
-        # share HBM with the down projection instead of with gate/up
-        bx = w["x"].shape[0]
-        ws_h = w["ws_sh"][: bx * I * 2].view(torch.bfloat16).view(bx, I)
-        w["fork"].record(stream)
-        side.wait_event(w["fork"])
-        rec(8, side)
-        mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], ws_h, weights_static=True, stream=side)
-        rec(9, side)
-        w["h_ready"].record(side)
-        rec(10, side)
-        mt.moe_shared_down(ws_h, w["w_down"], w["d_slot"], accumulate=False, weights_static=True, stream=side)
-        rec(11, side)
-        rec(4, side)
-        mt.moe_tail_latent_up_flags(w["latent"], w["lat_gamma"], w["w_up"], w["shared9"], w["out"], w["y"],
-                                    eps=1e-6, inputs_ready=True, weights_static=True, stream=side)
-        rec(5, side)
-        rec(6, side)
-        rec(7, side)
-        w["join"].record(side)
-        ep(stream)
-        stream.wait_event(w["h_ready"])
-        tp(stream)
-        stream.wait_event(w["join"])
-        return
-    if comp not in ("two_branch", "two_branch_split", "two_branch_one_call"):
-        # the latent up-projection between the shared expert's gate/up and down
-        # projections; down then adds d into the latent tail's output
-        # (out = bf16(out + bf16(d)), the sequential composition's arithmetic)
-        w["fork"].record(stream)
-        side.wait_event(w["fork"])
-        ws_h = w["ws_sh"][: B * I * 2].view(torch.bfloat16).view(B, I)
-        norm_args = (w["latent"], w["lat_gamma"], w["y"])
-        if comp == "norm_side_first":
-            rec(4, side)
-            mt.moe_tail_latent_norm(*norm_args, eps=1e-6, inputs_ready=True, stream=side)
-            rec(5, side)
-        rec(8, side)
-        mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], ws_h, weights_static=True, stream=side)
-        rec(9, side)
-        if comp == "norm_side_after":
-            rec(4, side)
-            mt.moe_tail_latent_norm(*norm_args, eps=1e-6, inputs_ready=True, stream=side)
-            rec(5, side)
-        if comp == "norm_main":
-            rec(4, stream)
-            mt.moe_tail_latent_norm(*norm_args, eps=1e-6, inputs_ready=True, stream=stream)
-            rec(5, stream)
-            w["normed"].record(stream)
-            side.wait_event(w["normed"])
-        rec(6, side)
-        mt.moe_tail_up_project(w["y"], w["w_up"], w["shared"], w["out"], weights_static=True, stream=side)
-        rec(7, side)
-        rec(10, side)
-        mt.moe_shared_down(ws_h, w["w_down"], w["out"], accumulate=True, weights_static=True, stream=side)
-        rec(11, side)
-        w["join"].record(side)
-        ep(stream)
-        tp(stream)
-        stream.wait_event(w["join"])
-        return
     w["fork"].record(stream)
     side.wait_event(w["fork"])
     if comp != "two_branch_one_call":  # the shared expert as its two calls, weights requested before each wait
@@ -390,20 +329,12 @@ def run_step(mt, w, stream, events=None, side=None):
         rec(11, side)
     else:
         shared_expert(side, w["d_slot"], False)
-    if comp == "two_branch_split":
-        rec(4, side)
-        mt.moe_tail_latent_norm(w["latent"], w["lat_gamma"], w["y"], eps=1e-6, inputs_ready=True, stream=side)
-        rec(5, side)
-        rec(6, side)
-        mt.moe_tail_up_project(w["y"], w["w_up"], w["shared9"], w["out"], weights_static=True, stream=side)
-        rec(7, side)
-    else:
-        rec(4, side)
-        mt.moe_tail_latent_up_flags(w["latent"], w["lat_gamma"], w["w_up"], w["shared9"], w["out"], w["y"],
-                                    eps=1e-6, inputs_ready=True, weights_static=True, stream=side)
-        rec(5, side)
-        rec(6, side)
-        rec(7, side)
+    rec(4, side)
+    mt.moe_tail_latent_up_flags(w["latent"], w["lat_gamma"], w["w_up"], w["shared9"], w["out"], w["y"],
+                                eps=1e-6, inputs_ready=True, weights_static=True, stream=side)
+    rec(5, side)
+    rec(6, side)
+    rec(7, side)
     w["join"].record(side)
     ep(stream)
     tp(stream)
@@ -647,19 +578,21 @@ def cuda_arm(args, world, rank, local):
                 run_step(mt, w, stream, evs[i] if evs else None, side=side)
         return g, [e for e in evs if e is not None] if evs else None
 
-    # The timed steps replay a graph without events; the last of the timed
-    # replays is the instrumented copy, whose event pairs give the per-call
-    # durations (so 1/10 of one replay's steps lose their overlap, not 1/10 of all)
+    # The timed region replays graphs without events only: K // G replays of a
+    # G-step graph and one graph of the K % G remaining steps.  A copy of the
+    # G-step graph with per-call events replays after the timed region and
+    # gives each call's duration.
     clean_g = capture(G, False)[0]
-    main_g, main_ev = capture(G, True)
     rest = K % G
     rest_g = capture(rest, False)[0] if rest else None
+    inst_g, inst_ev = capture(G, True)
     torch.cuda.synchronize()
-    # warm-up: W steps from the same graphs (replay() launches on the current stream)
+    # warm-up: at least W steps from the timed graphs (replay() launches on the current stream)
     with torch.cuda.stream(stream):
-        main_g.replay()
         for _ in range(max(1, -(-W // G))):
             clean_g.replay()
+        if rest_g is not None:
+            rest_g.replay()
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
@@ -670,8 +603,8 @@ def cuda_arm(args, world, rank, local):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         start.record(stream)
-        for r in range(K // G):
-            (main_g if r == K // G - 1 else clean_g).replay()
+        for _ in range(K // G):
+            clean_g.replay()
         if rest_g is not None:
             rest_g.replay()
         stop.record(stream)
@@ -680,19 +613,22 @@ def cuda_arm(args, world, rank, local):
     clocks = sampler.stop() if rank == 0 else None
     seconds = start.elapsed_time(stop) / 1e3
     max_s, units = aggregate(seconds, float(B * K), dist, dev)
+    # the instrumented copy, outside the timed region
+    with torch.cuda.stream(stream):
+        inst_g.replay()
+    torch.cuda.synchronize()
 
-    # per-call durations over the G steps of the last replay of the main graph
+    # per-call durations over the instrumented steps of that replay
     per_call = {c: [] for c in CALLS}
     pairs = {"ep_finalize": [(0, 1)], "tp_finalize": [(2, 3)], "latent_up": [(4, 5), (6, 7)],
              "shared_expert": [(8, 9), (10, 11)]}
-    for evs in main_ev:
+    for evs in inst_ev:
         for c in CALLS:
             per_call[c].append(sum(evs[i].elapsed_time(evs[j]) for i, j in pairs[c]) * 1e3)  # us
     calls = {}
     hbm, bf16_tf, peak_kind = peaks()
     nbytes = dict(BYTES)
-    if side is not None and args.composition in ("two_branch", "two_branch_split", "two_branch_one_call",
-                                                 "tp_after_gateup"):  # d: a slot
+    if side is not None and args.composition in ("two_branch", "two_branch_one_call"):  # d: a slot
         nbytes["shared_expert"] = 3 * I * H * 2 + B * H * 2 + B * H * 2
         nbytes["latent_up"] = BYTES["latent_up"] + B * H * 2
     for c in CALLS:
@@ -717,9 +653,9 @@ def cuda_arm(args, world, rank, local):
         "achieved": calls[dom]["achieved_gbs"], "peak": hbm, "unit": "GB/s",
         "frac": round(calls[dom]["achieved_gbs"] / hbm, 4), "traffic": traffic,
         "algorithmic_bytes_per_call": nbytes[dom], "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
-        "note": "per-call CUDA events on the launch stream, recorded as graph nodes in every tenth step of the "
-                "last timed graph replay (those steps lose the overlap between calls, so the per-call figures are "
-                "conservative; the other timed replays carry no events)",
+        "note": "per-call CUDA events on the launch stream, recorded as graph nodes in every tenth step of a "
+                "replay made after the timed region (those steps lose the overlap between calls, so the per-call "
+                "figures are conservative; the timed replays carry no events)",
     }
     ms = max_s * 1e3 / K
     line = {
@@ -729,24 +665,13 @@ def cuda_arm(args, world, rank, local):
         "config": dict(workload_config(), composition=(
             "sequential: EP, TP, latent tail, then the shared expert accumulating into out" if side is None else
             "two branches: on a side stream the shared expert (gate/up, then down, both with static weights) writes "
-            "d into an extra shared-partial slot, then the "
-            "latent tail follows (its norm, then its up-projection), adding all slots; "
-            "EP and TP on a high-priority stream beside them"
+            "d into an extra shared-partial slot, then the latent tail follows (its norm, then its up-projection), "
+            "adding all slots; EP and TP on a high-priority stream beside them"
             if args.composition == "two_branch" else
-            "two branches as two_branch, with the latent tail always as its two split calls"
-            if args.composition == "two_branch_split" else
             "two branches as two_branch, with the shared expert as one moe_shared_expert call"
             if args.composition == "two_branch_one_call" else
-            "two branches as two_branch, with expert-TP finalize started once gate/up is done"
-            if args.composition == "tp_after_gateup" else
             "two branches: the shared expert's gate/up on a side stream; EP, TP and the latent tail on a "
-            "high-priority stream beside it; then the down projection adds d into the latent tail's output"
-            if args.composition == "latent_main" else
-            f"two branches ({args.composition}): on a side stream the shared expert's gate/up, the latent "
-            "up-projection, then the shared expert's down projection adding d into out; the latent norm "
-            + {"norm_main": "first on the high-priority stream", "norm_side_first": "first on the side stream",
-               "norm_side_after": "on the side stream after gate/up"}[args.composition]
-            + "; EP and TP on the high-priority stream")),
+            "high-priority stream beside it; then the down projection adds d into the latent tail's output")),
         "roofline": roof, "calls": calls, "e2e": e2e,
         "step_roofline": {
             "algorithmic_bytes": sum(nbytes.values()),
@@ -962,7 +887,7 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
         row["latent_up"] = timed(lambda i: mt.moe_tail_latent_up(lat, w["lat_gamma"], wu[i], sh, out, ws,
                                                                  stream=stream), len(wu))
         # the same through moe_tail_latent_up_flags with both promises, and both
-        # ways in the opt-in one-kernel form (MOE_TAIL_LATENT_FUSED=1)
+        # ways in the opt-in one-kernel form
         yb = torch.empty((bs, L), dtype=torch.bfloat16, device=dev)
 
         def flags_call(i, promises):
@@ -970,16 +895,9 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
                                         weights_static=promises, stream=stream)
 
         row["latent_up_promises"] = timed(lambda i: flags_call(i, True), len(wu))
-        prev = os.environ.get("MOE_TAIL_LATENT_FUSED")
-        os.environ["MOE_TAIL_LATENT_FUSED"] = "1"
-        try:
+        with mt.kernel_form(mt.FORM_LATENT, mt.FORM_LATENT_ONE_KERNEL):
             row["latent_up_one_kernel"] = timed(lambda i: flags_call(i, False), len(wu))
             row["latent_up_promises_one_kernel"] = timed(lambda i: flags_call(i, True), len(wu))
-        finally:
-            if prev is None:
-                os.environ.pop("MOE_TAIL_LATENT_FUSED", None)
-            else:
-                os.environ["MOE_TAIL_LATENT_FUSED"] = prev
         del wu
         x = w["x"][:bs].contiguous()
         sw = [(w["w_gate"], w["w_up_s"], w["w_down"])]
@@ -1122,10 +1040,33 @@ def e2e_leg(mt, w, stream, steps, dist, dev, side=None):
         b.record(stream)
         torch.cuda.synchronize()
     s, units = aggregate(a.elapsed_time(b) / 1e3, float(B * steps), dist, dev)
+    link = link_rates(sets[0]["packed_in"][:h2d], host_in, sets[0]["packed_out"], host_out[0], h2d_stream)
+    step_s = s / steps
     return {"value": units / s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "ms_per_step": s * 1e3 / steps,
+            "steps": steps, "ms_per_step": step_s * 1e3,
+            "h2d_gbs": round(h2d / step_s / 1e9, 1),
+            "link_peak_gbs": link,
+            "h2d_frac_of_link": round(h2d / step_s / 1e9 / link["h2d"], 4),
             "pipelining": "double-buffered activations: step i+1's host-to-device copy overlaps step i's compute; "
                           "one copy each way per step (activations and outputs packed in one buffer)"}
+
+
+def link_rates(dev_in, host_in, dev_out, host_out, stream, reps=10) -> dict:
+    """GB/s of plain pinned copies of the e2e step's own buffers, alone on one
+    stream (host to device: the step's packed inputs; device to host: its packed
+    outputs): the link rate the e2e figure is bounded by."""
+    res = {}
+    for name, dst, src in (("h2d", dev_in, host_in), ("d2h", host_out, dev_out)):
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                dst.copy_(src, non_blocking=True)
+            b.record(stream)
+        b.synchronize()
+        res[name] = round(reps * src.numel() * src.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9, 1)
+    return res
 
 
 def only_config(args) -> int:
@@ -1173,6 +1114,84 @@ def only_config(args) -> int:
     return 0
 
 
+def trace_run(args) -> int:
+    """Per-CTA timeline from the trace build (libmoetail_trace.so, loaded
+    through MOE_TAIL_LIBRARY before the first library call).  "step": ten
+    decode steps as one graph replay, as the timed region runs them, and the
+    launches of two steps in its middle; "latent": the latent tail's opt-in
+    one-kernel form (pinned with moe_tail_set_kernel_form) at b = 1, 4, 16, each call alone,
+    without and with both promises."""
+    from moe_decode_tail_gb300 import build as cuda_build
+
+    os.environ["MOE_TAIL_LIBRARY"] = cuda_build.build(trace=True)
+    import moe_decode_tail_gb300 as mt
+    from moe_decode_tail_gb300.trace import Tracer, describe, launches
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.trace == "latent":
+        g = torch.Generator(device=dev).manual_seed(7)
+        wc = [(0.02 * torch.randn(H, L, device=dev, generator=g)).to(torch.bfloat16) for _ in range(6)]
+        gamma = (1 + 0.05 * torch.randn(L, device=dev, generator=g)).to(torch.bfloat16)
+        tracer = Tracer(mt)
+        mt.moe_tail_set_kernel_form(mt.FORM_LATENT, mt.FORM_LATENT_ONE_KERNEL)
+        for b in (1, 4, 16):
+            lat = (0.5 * torch.randn(TP, b, L, device=dev, generator=g)).to(torch.bfloat16)
+            sh = (0.5 * torch.randn(TP + 1, b, H, device=dev, generator=g)).to(torch.bfloat16)
+            y = torch.empty((b, L), dtype=torch.bfloat16, device=dev)
+            out = torch.empty((b, H), dtype=torch.bfloat16, device=dev)
+            for promises in (False, True):
+                def call(i):
+                    mt.moe_tail_latent_up_flags(lat, gamma, wc[i % len(wc)], sh, out, y, inputs_ready=promises,
+                                                weights_static=promises)
+                for i in range(6):  # warm-up
+                    call(i)
+                torch.cuda.synchronize()
+                tracer.attach()
+                for i in range(6):
+                    call(i)
+                    torch.cuda.synchronize()
+                print(f"-- b = {b}, promises {promises}")
+                for kid, i, rs in launches(tracer.records())[1:3]:
+                    print("  " + describe([(kid, i, rs)])[0])
+    else:
+        _, w = make_workload(dev)
+        w["composition"] = args.composition
+        stream = torch.cuda.Stream(dev, priority=-1)
+        side = torch.cuda.Stream(dev, priority=0)
+        tracer = Tracer(mt)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                run_step(mt, w, stream, side=side)
+        torch.cuda.synchronize()
+        steps = 10
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(steps):
+                run_step(mt, w, stream, side=side)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+        torch.cuda.synchronize()
+        tracer.attach()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        print(f"{steps} steps: {a.elapsed_time(b) * 1e3 / steps:.1f} us per step (trace build)")
+        ls = launches(tracer.records())
+        for step in (steps // 2 - 1, steps // 2):
+            print(f"-- step {step}")
+            for line in describe([x for x in ls if x[1] == step]):
+                print("  " + line)
+    if mt.moe_tail_take_device_error() != 0:
+        raise RuntimeError("a kernel wait expired")
+    return 0
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
@@ -1182,6 +1201,8 @@ def main():
         raise SystemExit("bench.py: no CUDA device (the CUDA arm has no CPU fallback)")
     if args.only_config is not None:
         return only_config(args)
+    if args.trace is not None:
+        return trace_run(args)
     return cuda_arm(args, world, rank, local)
 
 

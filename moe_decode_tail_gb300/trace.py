@@ -2,26 +2,18 @@
 
 The trace build (build.build(trace=True) -> _build/libmoetail_trace.so,
 include/moe_tail_trace.h) has every CTA record %globaltimer at entry, at up to
-four marks and at exit.  This module attaches a record buffer, runs work, and
-turns the records into per-launch spans and the GEMM epilogue's phases.
-
-    python -m moe_decode_tail_gb300.trace          # one bench.py decode step (b = 64), timed as the bench times it
-    python -m moe_decode_tail_gb300.trace --latent-one-kernel   # the latent tail's one-kernel form, b = 1, 4, 16
-
-prints, for one step in the middle of a graph replay of ten steps: each
-kernel launch's first and last CTA start and its end (µs from the step's
-first CTA), the median CTA duration, and for the GEMMs the median time from
-CTA start to accumulator complete (the K loop) and the median epilogue
-phases (staging, waiting for cluster peers, reduction and stores, second
-barrier, exit).  Set MOE_TAIL_LIBRARY before the first library call, as
-main() does; records are 64 bytes.
+four marks and at exit.  Tracer attaches a record buffer and reads the
+records back; launches() groups them into launches and describe() prints
+each launch's first and last CTA start and its end (µs from the earliest
+CTA), the median CTA duration, and for the GEMMs the median time from CTA
+start to accumulator complete (the K loop) and the median epilogue phases.
+Load the trace build by setting MOE_TAIL_LIBRARY before the first library
+call; records are 64 bytes.  bench.py --trace runs it on the decode step.
 """
 from __future__ import annotations
 
 import collections
 import ctypes
-import importlib.util
-import os
 import statistics
 
 import torch
@@ -29,7 +21,6 @@ import torch
 KERNELS = {10: "ep_finalize (route-parallel)", 11: "tp_finalize (route-parallel)", 12: "latent_norm",
            20: "tp_finalize (staged)", 21: "latent_norm (staged)", 30: "up-projection GEMM", 31: "gate/up GEMM",
            32: "down GEMM", 33: "latent tail (one kernel)", 40: "ep_finalize"}
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 class Tracer:
@@ -97,103 +88,3 @@ def describe(group: list[tuple[int, int, list]]) -> list[str]:
                          f" barrier+exit {p50(lambda r: r[5] - r[4][3]):.1f}")
         lines.append(line)
     return lines
-
-
-def latent_one_kernel(mt, sizes=(1, 4, 16), calls: int = 6) -> None:
-    """The latent tail's one-kernel form (MOE_TAIL_LATENT_FUSED=1) at the decode
-    shape (tp = 8 latent slots, L = 3584, H = 7168, 9 shared slots), each call
-    alone (synchronised after it), without and with both promises: per call the
-    CTA spans and the median times from CTA start to x formed, y ready and
-    accumulator complete.  The weights rotate over six copies (> 2x L2)."""
-    dev = torch.device("cuda", 0)
-    L, H, TP, TPS = 3584, 7168, 8, 9
-    g = torch.Generator(device=dev).manual_seed(7)
-    wc = [(0.02 * torch.randn(H, L, device=dev, generator=g)).to(torch.bfloat16) for _ in range(6)]
-    gamma = (1 + 0.05 * torch.randn(L, device=dev, generator=g)).to(torch.bfloat16)
-    tracer = Tracer(mt)
-    prev = os.environ.get("MOE_TAIL_LATENT_FUSED")
-    os.environ["MOE_TAIL_LATENT_FUSED"] = "1"
-    try:
-        for b in sizes:
-            lat = (0.5 * torch.randn(TP, b, L, device=dev, generator=g)).to(torch.bfloat16)
-            sh = (0.5 * torch.randn(TPS, b, H, device=dev, generator=g)).to(torch.bfloat16)
-            y = torch.empty((b, L), dtype=torch.bfloat16, device=dev)
-            out = torch.empty((b, H), dtype=torch.bfloat16, device=dev)
-            for promises in (False, True):
-                def call(i):
-                    mt.moe_tail_latent_up_flags(lat, gamma, wc[i % len(wc)], sh, out, y, inputs_ready=promises,
-                                                weights_static=promises)
-                for i in range(calls):  # warm-up
-                    call(i)
-                torch.cuda.synchronize()
-                tracer.attach()
-                for i in range(calls):
-                    call(i)
-                    torch.cuda.synchronize()
-                print(f"-- b = {b}, promises {promises}")
-                for kid, i, rs in launches(tracer.records())[1:3]:
-                    print("  " + describe([(kid, i, rs)])[0])
-    finally:
-        if prev is None:
-            os.environ.pop("MOE_TAIL_LATENT_FUSED", None)
-        else:
-            os.environ["MOE_TAIL_LATENT_FUSED"] = prev
-
-
-def main() -> None:
-    import sys
-
-    from moe_decode_tail_gb300 import build as cuda_build
-
-    os.environ["MOE_TAIL_LIBRARY"] = cuda_build.build(trace=True)
-    import moe_decode_tail_gb300 as mt
-
-    if "--latent-one-kernel" in sys.argv[1:]:
-        torch.cuda.set_device(0)
-        latent_one_kernel(mt)
-        if mt.moe_tail_take_device_error() != 0:
-            raise RuntimeError("a kernel wait expired")
-        return
-
-    spec = importlib.util.spec_from_file_location("bench_trace", os.path.join(ROOT, "bench.py"))
-    bench = importlib.util.module_from_spec(spec)
-    spec.loader.exec_module(bench)
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    cpu, w = bench.make_workload(dev)
-    stream = torch.cuda.Stream(dev, priority=-1)
-    side = torch.cuda.Stream(dev, priority=0)
-    tracer = Tracer(mt)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            bench.run_step(mt, w, stream, side=side)
-    torch.cuda.synchronize()
-    steps = 10
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for _ in range(steps):
-            bench.run_step(mt, w, stream, side=side)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            g.replay()
-    torch.cuda.synchronize()
-    tracer.attach()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        a.record(stream)
-        g.replay()
-        b.record(stream)
-    torch.cuda.synchronize()
-    print(f"{steps} steps: {a.elapsed_time(b) * 1e3 / steps:.1f} us per step (trace build)")
-    ls = launches(tracer.records())
-    for step in (steps // 2 - 1, steps // 2):
-        print(f"-- step {step}")
-        for line in describe([x for x in ls if x[1] == step]):
-            print("  " + line)
-    if mt.moe_tail_take_device_error() != 0:
-        raise RuntimeError("a kernel wait expired")
-
-
-if __name__ == "__main__":
-    main()
