@@ -190,9 +190,10 @@ int moe_tail_up_project(const void* y, const void* w_up, const void* shared, int
  *   moe_tail_latent_norm) and MOE_TAIL_WEIGHTS_STATIC (w_up, as for
  *   moe_tail_up_project); shared is always read, and y and out written, after
  *   the wait for the stream's preceding kernel.
- * It runs moe_tail_latent_norm then moe_tail_up_project.  With the variable
- * MOE_TAIL_LATENT_FUSED=1 in the environment it runs instead, wherever the
- * sizes allow (b <= 32, L <= 8192, tp <= 8 x the ring's stages), one kernel
+ * It runs moe_tail_latent_norm then moe_tail_up_project.  With the latent
+ * tail's kernel form pinned to MOE_TAIL_FORM_LATENT_ONE_KERNEL
+ * (moe_tail_set_kernel_form) it runs instead, wherever the sizes allow
+ * (b <= 32, L <= 8192, tp <= 8 x the ring's stages), one kernel
  * in the pages' fused-tail shape ([KT] WaveMoeTail keeps the normalised
  * latent on chip): the up-projection's CTAs form y for their own K range in
  * shared memory -- each CTA sums and squares the 256-column chunks its range
@@ -268,7 +269,10 @@ int moe_shared_down(const void* h, const void* w_down, int b, int H, int I, void
  * returns MOE_TAIL_EINVAL before anything runs.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture.  If the device's context has been replaced since (a
+ *     cudaDeviceReset), the next call looks the address up again.
+ *   - The array is private to the library, so no caller buffer can overlap
+ *     it; the call still refuses one that does, as it would a workspace.
  *   - All calls share the one array and each overwrites all of the y rows it
  *     uses, so nothing has to start at zero; calls that may run at the same
  *     time on the GPU (different streams, or different host threads) race on
@@ -278,6 +282,32 @@ int moe_shared_down(const void* h, const void* w_down, int b, int H, int I, void
 int moe_tail_latent_up_noalloc(const void* latent, const void* gamma, float eps, const void* w_up,
                                const void* shared, int tp_s, int b, int tp, int L, int H, void* out,
                                void* stream);
+
+/*
+ * Kernel form of a call (no counterpart on the pages: a choice between
+ * kernels of this library that compute the same bits).  Some calls have more
+ * than one kernel form; the library picks one per call from the sizes unless
+ * a form is pinned here.  Every form of a call gives bit for bit the same
+ * outputs, so a pin only changes speed; it exists for tests that run every
+ * form and for measurements.  The setting is process-wide (all devices and
+ * host threads) and applies to calls made after it returns.
+ *   call MOE_TAIL_FORM_EP      (moe_tail_ep_finalize, _flags):
+ *        1 token-resident kernel (a token's routes held in registers),
+ *        2 route-parallel kernel (route groups of a CTA, products in shared memory)
+ *   call MOE_TAIL_FORM_TP      (moe_tail_tp_finalize, _flags):
+ *        1 staged kernel (route rows streamed into a shared-memory ring),
+ *        2 route-parallel kernel
+ *   call MOE_TAIL_FORM_LATENT  (moe_tail_latent_up, _flags, _noalloc):
+ *        MOE_TAIL_FORM_LATENT_ONE_KERNEL (1): the latent tail as one kernel
+ *        wherever the sizes allow (b <= 32, L <= 8192, tp within the ring),
+ *        the norm and the up-projection as two kernels elsewhere;
+ *        2: always the two kernels
+ *   form 0 (every call): the library's choice (the default).
+ * Returns MOE_TAIL_EINVAL for an unknown call or form, else MOE_TAIL_OK.
+ */
+enum { MOE_TAIL_FORM_EP = 0, MOE_TAIL_FORM_TP = 1, MOE_TAIL_FORM_LATENT = 2 };
+#define MOE_TAIL_FORM_LATENT_ONE_KERNEL 1
+int moe_tail_set_kernel_form(int call, int form);
 
 /* Workspace bytes of moe_tail_latent_up (which = 0, dim = L) or
  * moe_shared_expert (which = 1, dim = I) at b tokens; 0 for bad arguments. */

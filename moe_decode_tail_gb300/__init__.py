@@ -20,7 +20,8 @@ __all__ = [
     "moe_tail_latent_up_noalloc", "NOALLOC_SCRATCH_BYTES", "moe_tail_selftest_wait_timeout",
     "moe_tail_latent_norm", "moe_tail_up_project", "WEIGHTS_STATIC", "INPUTS_READY",
     "moe_shared_gate_up", "moe_shared_down", "moe_tail_latent_up_flags", "moe_tail_ep_finalize_flags",
-    "moe_tail_tp_finalize_flags",
+    "moe_tail_tp_finalize_flags", "moe_tail_set_kernel_form", "kernel_form", "FORM_EP", "FORM_TP", "FORM_LATENT",
+    "FORM_LATENT_ONE_KERNEL",
 ]
 
 OK, EINVAL, ECUDA, ENOTSUP = 0, 1, 2, 3
@@ -28,6 +29,8 @@ NOALLOC_SCRATCH_BYTES = 1 << 20  # MOE_TAIL_NOALLOC_SCRATCH_BYTES
 W_FP32, W_BF16 = 0, 1
 WEIGHTS_STATIC = 1  # MOE_TAIL_WEIGHTS_STATIC
 INPUTS_READY = 2  # MOE_TAIL_INPUTS_READY
+FORM_EP, FORM_TP, FORM_LATENT = 0, 1, 2  # MOE_TAIL_FORM_*: the calls whose kernel form can be pinned
+FORM_LATENT_ONE_KERNEL = 1  # MOE_TAIL_FORM_LATENT_ONE_KERNEL
 
 
 class MoeTailError(RuntimeError):
@@ -70,10 +73,12 @@ def lib() -> ctypes.CDLL:
         L.moe_tail_status_str.argtypes = [i32]
         L.moe_tail_status_str.restype = ctypes.c_char_p
         L.moe_tail_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        L.moe_tail_set_kernel_form.argtypes = [i32, i32]
         for name in ("moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up", "moe_shared_expert",
                      "moe_tail_take_device_error", "moe_tail_latent_up_noalloc", "moe_tail_selftest_wait_timeout",
                      "moe_tail_latent_norm", "moe_tail_up_project", "moe_shared_gate_up", "moe_shared_down",
-                     "moe_tail_latent_up_flags", "moe_tail_ep_finalize_flags", "moe_tail_tp_finalize_flags"):
+                     "moe_tail_latent_up_flags", "moe_tail_ep_finalize_flags", "moe_tail_tp_finalize_flags",
+                     "moe_tail_set_kernel_form"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -230,9 +235,10 @@ def moe_tail_latent_up_flags(latent, gamma, w_up, shared, out, y, *, eps=1e-6, i
     """The latent tail into out (BF16 [b, H]) and y (BF16 [b, L]), with the
     split calls' promises: inputs_ready (latent and gamma, as for
     moe_tail_latent_norm) and weights_static (w_up, as for moe_tail_up_project).
-    The norm and the up-projection, or with MOE_TAIL_LATENT_FUSED=1 in the
-    environment one kernel that forms y on chip (slower on GB300); the result
-    is bit for bit that of the two split calls either way."""
+    The norm and the up-projection, or with the latent tail's kernel form
+    pinned to one kernel (moe_tail_set_kernel_form(FORM_LATENT, FORM_LATENT_ONE_KERNEL)) one kernel
+    that forms y on chip (slower on GB300); the result is bit for bit that of
+    the two split calls either way."""
     tp, b, L, H, tp_s = _latent_args(latent, gamma, w_up, shared, out, y)
     flags = (INPUTS_READY if inputs_ready else 0) | (WEIGHTS_STATIC if weights_static else 0)
     _check("moe_tail_latent_up_flags", lib().moe_tail_latent_up_flags(
@@ -350,6 +356,29 @@ def moe_tail_take_device_error() -> int:
     bits = ctypes.c_uint(0)
     _check("moe_tail_take_device_error", lib().moe_tail_take_device_error(ctypes.byref(bits)))
     return int(bits.value)
+
+
+def moe_tail_set_kernel_form(call: int, form: int) -> None:
+    """Pin the kernel form of a call (FORM_EP, FORM_TP, FORM_LATENT; form 0 is
+    the library's choice, see include/moe_tail.h).  Every form of a call gives
+    the same bits; the setting is process-wide."""
+    _check("moe_tail_set_kernel_form", lib().moe_tail_set_kernel_form(call, form))
+
+
+class kernel_form:
+    """Context manager: the call's kernel form pinned inside the block, the
+    library's choice again after it."""
+
+    def __init__(self, call: int, form: int):
+        self.call, self.form = call, form
+
+    def __enter__(self):
+        moe_tail_set_kernel_form(self.call, self.form)
+        return self
+
+    def __exit__(self, *exc):
+        moe_tail_set_kernel_form(self.call, 0)
+        return False
 
 
 def moe_tail_selftest_wait_timeout(limit_us: int, stream=None) -> None:

@@ -710,17 +710,14 @@ cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t strea
 
 static int stage_bytes(int tm, int n_tile) { return tm * kBlockK * 2 + n_tile * kBlockK * 2; }
 
-// Plan override for tuning: MOE_TAIL_GEMM_PLAN_<UP|GATEUP|DOWN>="tm,ksplit,stages".
+// Plan override for tuning (tm, ksplit, stages; read once from the environment).
 static bool plan_override(int mode, GemmPlan& p) {
   if (mode < 0 || mode > 2) return false;
-  const char* names[3] = {"MOE_TAIL_GEMM_PLAN_UP", "MOE_TAIL_GEMM_PLAN_GATEUP", "MOE_TAIL_GEMM_PLAN_DOWN"};
-  const char* v = getenv(names[mode]);
-  int tm = 0, ks = 0, st = 0;
-  if (!v || sscanf(v, "%d,%d,%d", &tm, &ks, &st) != 3) return false;
-  if ((tm != 64 && tm != 128 && tm != 256) || ks < 1 || ks > 8 || st < 2 || st > kMaxStages) return false;
-  p.tm = tm;
-  p.ksplit = ks;
-  p.stages = st;
+  const int* v = tuning().gemm_plan[mode];
+  if (v[0] == 0) return false;
+  p.tm = v[0];
+  p.ksplit = v[1];
+  p.stages = v[2];
   return true;
 }
 
@@ -806,16 +803,8 @@ static cudaError_t launch_t(const GemmPlan& p, const CUtensorMap& w0, const CUte
   const size_t smem = smem_bytes(p, MODE, a);
   // Raise the kernel's shared-memory limit once per device (not per call, so
   // that a captured stream sees only launches).
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const cudaError_t e = ensure_smem_limit((const void*)kernel, 220 * 1024);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
   if (smem > 220 * 1024) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.ksplit, p.m_tiles, (a.n_tok + N - 1) / N);

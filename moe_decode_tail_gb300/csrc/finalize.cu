@@ -649,27 +649,12 @@ cudaError_t take_finalize_error(unsigned* bits) {
 
 // ---------------------------------------------------------------- launcher
 
-// Tuning override of the column split: MOE_TAIL_FIN_SPLIT=<1|2|4|8>.
-static int split_override() {
-  const char* v = getenv("MOE_TAIL_FIN_SPLIT");
-  const int s = v ? atoi(v) : 0;
-  return (s == 1 || s == 2 || s == 4 || s == 8) ? s : 0;
-}
-
 template <int MODE, bool WBN, int WMODE>
 static cudaError_t launch_t(const FinalizeArgs& a, int split, cudaStream_t stream) {
   auto k = finalize_kernel<MODE, WBN, WMODE>;
   const size_t smem = (size_t)a.routes_per_pass * a.band_vectors * 32;
-  static int configured[64] = {0};  // raise the limit once per device, not per call
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = ensure_smem_limit((const void*)k, 64 * 1024);  // once per device, not per call
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(split, a.b, 1);
   cfg.blockDim = dim3(a.routes_per_pass * a.band_vectors, 1, 1);
@@ -711,16 +696,8 @@ static cudaError_t launch_ep_t(const FinalizeArgs& a, int split, cudaStream_t st
 template <bool WBN, int WMODE, bool LATENT>
 static cudaError_t launch_staged_t(const FinalizeArgs& a, int split, int groups, size_t smem, cudaStream_t stream) {
   auto k = staged_finalize_kernel<WBN, WMODE, LATENT>;
-  static int configured[64] = {0};  // raise the limit once per device, not per call
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = ensure_smem_limit((const void*)k, 192 * 1024);  // once per device, not per call
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 192 * 1024);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(split, groups, 1);
   cfg.blockDim = dim3(a.band_vectors, 1, 1);
@@ -738,11 +715,6 @@ static cudaError_t launch_staged_t(const FinalizeArgs& a, int split, int groups,
   return cudaLaunchKernelEx(&cfg, k, a);
 }
 
-static int env_int(const char* name, int fallback) {
-  const char* v = getenv(name);
-  return v ? atoi(v) : fallback;
-}
-
 // Expert-TP and latent with the rows staged in shared memory; returns
 // cudaErrorNotSupported when a stage (one route's rows of a band in every
 // slot) does not fit, so the caller can fall back to finalize_kernel.
@@ -753,7 +725,7 @@ static cudaError_t launch_staged(int mode, const FinalizeArgs& args, bool wbn, i
   // every slot) within 32 KB, then more while the batch leaves over half of
   // the SMs idle (measured on GB300: tp = 8, P = 4096 is best at 2 bands for
   // b = 64 and b = 128).
-  int split = split_override();
+  int split = tuning().fin_split;
   if (split == 0) {
     split = 1;
     while (split < 8 && split < a.chunks && (size_t)a.tp * ((a.P + split - 1) / split) * 2 > 32 * 1024) split *= 2;
@@ -763,10 +735,10 @@ static cudaError_t launch_staged(int mode, const FinalizeArgs& args, bool wbn, i
   a.band_vectors = 32 * ((a.chunks + split - 1) / split);
   if (a.band_vectors > 512) return cudaErrorNotSupported;
   const size_t stage_bytes = (size_t)a.tp * a.band_vectors * 16;
-  const size_t budget = (size_t)env_int("MOE_TAIL_FIN_RING_KB", 64) * 1024;
+  const size_t budget = (size_t)(tuning().fin_ring_kb > 0 ? tuning().fin_ring_kb : 64) * 1024;
   a.stages = (int)std::min<size_t>(16, budget / stage_bytes);
   if (a.stages < 2) return cudaErrorNotSupported;
-  const int group_cap = env_int("MOE_TAIL_FIN_GROUPS", 0);  // tuning override: CTAs along the tokens
+  const int group_cap = tuning().fin_groups;  // tuning override: CTAs along the tokens
   const int groups = (int)std::min<int64_t>(
       a.b, group_cap > 0 ? group_cap : std::max<int64_t>(1, 2 * (int64_t)sms / split));
   const size_t smem = (size_t)a.stages * stage_bytes;
@@ -782,10 +754,10 @@ cudaError_t launch_finalize(int mode, const FinalizeArgs& args, bool wbn, int wm
   // enough routes to keep the ring streaming (measured: b * K >= 512, i.e.
   // b >= 64 at top-8); fewer routes finish sooner on the route-parallel
   // kernel's single trip (b = 1: 4.6 vs 13.5 us).  The latent norm (one route
-  // per token) is faster on the route-parallel kernel.  MOE_TAIL_FIN_STAGED
-  // = 1 / 0 forces either kernel.
-  const int staged = env_int("MOE_TAIL_FIN_STAGED", -1);
-  if (mode == kModeTP && (staged == 1 || (staged != 0 && (int64_t)args.b * args.K >= 512))) {
+  // per token) is faster on the route-parallel kernel.  A pinned kernel form
+  // (1 staged, 2 route-parallel) takes precedence.
+  const int staged = kernel_form(kFormCallTP);
+  if (mode == kModeTP && (staged == 1 || (staged != 2 && (int64_t)args.b * args.K >= 512))) {
     const cudaError_t e = launch_staged(mode, args, wbn, wmode, sms, stream);
     if (e != cudaErrorNotSupported) return e;
   }
@@ -798,11 +770,9 @@ cudaError_t launch_finalize(int mode, const FinalizeArgs& args, bool wbn, int wm
   // at b = 64 with 2 bands instead of 8 shortened the composed step by 1.3 us);
   // expert-TP about two waves.  At most 8 bands (portable cluster size), one
   // band per chunk at most.
-  int split = split_override();
-  if (mode == kModeEP || mode == kModeLatent) {  // tuning overrides for EP or the latent norm alone
-    const int s = env_int(mode == kModeEP ? "MOE_TAIL_FIN_EP_SPLIT" : "MOE_TAIL_FIN_LATENT_SPLIT", 0);
-    if (s == 1 || s == 2 || s == 4 || s == 8) split = s;
-  }
+  int split = tuning().fin_split;
+  if (mode == kModeEP && tuning().fin_ep_split) split = tuning().fin_ep_split;  // tuning overrides for EP
+  if (mode == kModeLatent && tuning().fin_latent_split) split = tuning().fin_latent_split;  // or the latent norm alone
   if (split == 0) {
     const int64_t target = mode == kModeTP ? 2 * (int64_t)sms : (3 * (int64_t)sms) / 4;
     split = 1;
@@ -820,9 +790,9 @@ cudaError_t launch_finalize(int mode, const FinalizeArgs& args, bool wbn, int wm
   if (mode == kModeEP) {  // a token has about K local rows in all: more groups would idle
     a.routes_per_pass = std::max(1, std::min(a.routes_per_pass, a.K));
   }
-  const int routes_cap = env_int("MOE_TAIL_FIN_ROUTES", 0);  // tuning override
+  const int routes_cap = tuning().fin_routes;  // tuning override
   if (routes_cap >= 1 && routes_cap <= kMaxRoutesPerPass) a.routes_per_pass = std::min(a.routes_per_pass, routes_cap);
-  if (mode == kModeEP && a.band_vectors <= kEpMaxThreads && env_int("MOE_TAIL_FIN_EP_REGS", 1)) {
+  if (mode == kModeEP && a.band_vectors <= kEpMaxThreads && kernel_form(kFormCallEP) != 2) {
     if (wbn) return wmode == kWeightBF16 ? launch_ep_t<true, kWeightBF16>(a, split, stream)
                                          : launch_ep_t<true, kWeightF32>(a, split, stream);
     return wmode == kWeightBF16 ? launch_ep_t<false, kWeightBF16>(a, split, stream)

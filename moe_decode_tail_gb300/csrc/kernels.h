@@ -9,6 +9,19 @@ namespace moetail {
 
 enum { kWeightF32 = 0, kWeightBF16 = 1, kWeightUnit = 2 };
 
+// Limits of the C ABI's sizes (every entry point checks against these).
+constexpr int kMaxTp = 32, kMaxK = 32, kMaxP = 32768, kMaxTokens = 65535, kMaxWidth = 1 << 24;
+
+// The latent tail's sizes: tp latent slots of b tokens, width L.
+inline bool latent_sizes_ok(int b, int tp, int L) {
+  return b >= 0 && b <= kMaxTokens && tp >= 1 && tp <= kMaxTp && L >= 8 && L <= kMaxP && L % 8 == 0;
+}
+// The up-projection's sizes: tp_s shared slots, y of width L, output width H.
+inline bool up_sizes_ok(int b, int tp_s, int L, int H) {
+  return b >= 0 && b <= kMaxTokens && tp_s >= 0 && tp_s <= kMaxTp && L >= 8 && L <= kMaxP && L % 8 == 0 &&
+         H >= 8 && H % 8 == 0 && H <= kMaxWidth;
+}
+
 // Rows of one finalize call: slot s's row j starts at rows + s * slot_stride + j * P.
 struct FinalizeArgs {
   const uint16_t* rows;   // EP: GEMM2 rows [tp][num_rows][P]; TP: K-partials; latent: [tp][b][L]
@@ -82,8 +95,8 @@ cudaError_t enqueue_latent_norm(const void* latent, const void* gamma, float eps
 int enqueue_up_project(const void* y, const void* w_up, const void* shared, int tp_s, int b, int L, int H, void* out,
                        bool weights_before_wait, cudaStream_t st);
 // The whole latent tail in one kernel (kGemmLatentUp)?  Only when the
-// variable MOE_TAIL_LATENT_FUSED=1 asks for it and plan_latent_fused finds a
-// plan at these sizes (the two-kernel form is faster on GB300).
+// latent-tail kernel form is pinned to it and plan_latent_fused finds a plan
+// at these sizes (the two-kernel form is faster on GB300).
 bool latent_tail_fused(int b, int tp, int L, int H, GemmPlan* plan);
 // Enqueue it (y: BF16 [b][L] written, or null); flags as moe_tail_latent_up_flags.
 int enqueue_latent_fused(const GemmPlan& plan, const void* latent, const void* gamma, float eps, const void* w_up,
@@ -95,6 +108,33 @@ int enqueue_latent_tail(const void* latent, const void* gamma, float eps, const 
 
 // Read and clear the device error word (synchronises with the device).
 cudaError_t take_device_error(unsigned* bits);
+
+// ---- host-side configuration -------------------------------------------------
+
+// Kernel forms a caller may pin with moe_tail_set_kernel_form (the values of
+// the MOE_TAIL_FORM_* constants of the public header); 0: the library's choice.
+enum { kFormCallEP = 0, kFormCallTP = 1, kFormCallLatent = 2, kFormCalls = 3 };
+int kernel_form(int call);
+
+// Tuning overrides for sweeps, read from the environment once (at the first
+// call that needs them), never per call.  0 means "not set".
+struct Tuning {
+  int fin_split;         // MOE_TAIL_FIN_SPLIT: column bands per token (1, 2, 4 or 8), any finalize
+  int fin_ep_split;      // MOE_TAIL_FIN_EP_SPLIT: the same for EP finalize alone
+  int fin_latent_split;  // MOE_TAIL_FIN_LATENT_SPLIT: the same for the latent norm alone
+  int fin_ring_kb;       // MOE_TAIL_FIN_RING_KB: staged finalize ring budget (KB)
+  int fin_groups;        // MOE_TAIL_FIN_GROUPS: staged finalize CTAs along the tokens
+  int fin_routes;        // MOE_TAIL_FIN_ROUTES: route-parallel finalize routes per pass
+  int gemm_plan[3][3];   // MOE_TAIL_GEMM_PLAN_<UP|GATEUP|DOWN> = "tm,ksplit,stages"
+};
+const Tuning& tuning();
+
+// Raise a kernel's dynamic shared-memory limit on the current device, once
+// per (kernel, device) and safe to call from several host threads.
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+
+// Multiprocessors of the current device (cached per device).
+int device_sms();
 #ifdef MOE_TAIL_TRACE
 cudaError_t trace_attach_gemm(void* buf, unsigned cap);
 unsigned trace_count_gemm();

@@ -4,23 +4,116 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "../../include/moe_tail.h"
 #include "kernels.h"
 
 #define MOE_API extern "C" __attribute__((visibility("default")))
 
+// ============================================================================ host-side configuration
+
+namespace moetail {
+
+namespace {
+std::atomic<int> g_forms[kFormCalls];  // zero-initialised: the library's choice
+
+int env_int(const char* name) {
+  const char* v = getenv(name);
+  return v ? atoi(v) : 0;
+}
+
+int env_split(const char* name) {
+  const int s = env_int(name);
+  return (s == 1 || s == 2 || s == 4 || s == 8) ? s : 0;
+}
+
+void env_plan(const char* name, int (&plan)[3]) {
+  plan[0] = plan[1] = plan[2] = 0;
+  const char* v = getenv(name);
+  int tm = 0, ks = 0, st = 0;
+  if (!v || sscanf(v, "%d,%d,%d", &tm, &ks, &st) != 3) return;
+  if ((tm != 64 && tm != 128 && tm != 256) || ks < 1 || ks > 8 || st < 2 || st > 12) return;
+  plan[0] = tm;
+  plan[1] = ks;
+  plan[2] = st;
+}
+}  // namespace
+
+int kernel_form(int call) { return call >= 0 && call < kFormCalls ? g_forms[call].load(std::memory_order_relaxed) : 0; }
+
+const Tuning& tuning() {
+  static const Tuning t = [] {
+    Tuning r{};
+    r.fin_split = env_split("MOE_TAIL_FIN_SPLIT");
+    r.fin_ep_split = env_split("MOE_TAIL_FIN_EP_SPLIT");
+    r.fin_latent_split = env_split("MOE_TAIL_FIN_LATENT_SPLIT");
+    r.fin_ring_kb = env_int("MOE_TAIL_FIN_RING_KB");
+    r.fin_groups = env_int("MOE_TAIL_FIN_GROUPS");
+    r.fin_routes = env_int("MOE_TAIL_FIN_ROUTES");
+    env_plan("MOE_TAIL_GEMM_PLAN_UP", r.gemm_plan[0]);
+    env_plan("MOE_TAIL_GEMM_PLAN_GATEUP", r.gemm_plan[1]);
+    env_plan("MOE_TAIL_GEMM_PLAN_DOWN", r.gemm_plan[2]);
+    return r;
+  }();
+  return t;
+}
+
+cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
+  static std::mutex m;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(m);
+  if (done.count({kernel, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({kernel, dev});
+  return e;
+}
+
+int device_sms() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
+  if (dev < 64) cache[dev].store(sms, std::memory_order_relaxed);
+  return sms;
+}
+
+}  // namespace moetail
+
+MOE_API int moe_tail_set_kernel_form(int call, int form) {
+  static const int kForms[moetail::kFormCalls] = {3, 3, 3};  // forms 0..2 of each call
+  if (call < 0 || call >= moetail::kFormCalls || form < 0 || form >= kForms[call]) return MOE_TAIL_EINVAL;
+  moetail::g_forms[call].store(form, std::memory_order_relaxed);
+  return MOE_TAIL_OK;
+}
+
 namespace {
 
+using moetail::device_sms;
 using moetail::FinalizeArgs;
 using moetail::GemmArgs;
 using moetail::GemmPlan;
 
-constexpr int kMaxTp = 32, kMaxK = 32, kMaxP = 32768;
+using moetail::kMaxK;
+using moetail::kMaxP;
+using moetail::kMaxTokens;
+using moetail::kMaxTp;
+using moetail::kMaxWidth;
 
 bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
@@ -29,17 +122,6 @@ struct Range {
 };
 Range span(const void* p, size_t bytes) { return Range{(uintptr_t)p, (uintptr_t)p + bytes}; }
 bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
-
-int device_sms() {
-  static int cache[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
-  if (dev < 64 && cache[dev]) return cache[dev];
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
-  if (dev < 64) cache[dev] = sms;
-  return sms;
-}
 
 int finish(cudaError_t e) {
   if (e == cudaSuccess) return MOE_TAIL_OK;
@@ -87,7 +169,7 @@ size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
 int check_finalize_common(const void* w, int weight_dtype, const void* gamma, int b, int tp, int K, int P,
                           void* out) {
   if (b < 0 || tp < 1 || tp > kMaxTp || K < 1 || K > kMaxK || P < 8 || P > kMaxP || P % 8) return MOE_TAIL_EINVAL;
-  if (b > 65535) return MOE_TAIL_EINVAL;
+  if (b > kMaxTokens) return MOE_TAIL_EINVAL;
   if (weight_dtype != MOE_TAIL_W_FP32 && weight_dtype != MOE_TAIL_W_BF16) return MOE_TAIL_EINVAL;
   if (b == 0) return MOE_TAIL_OK;
   if (!w || !gamma || !out) return MOE_TAIL_EINVAL;
@@ -228,7 +310,7 @@ int enqueue_up_project(const void* y, const void* w_up, const void* shared, int 
   return finish(moetail::launch_decode_gemm(moetail::kGemmUpShared, plan, mw, mw, mx, g, true, st));
 }
 
-// The one-kernel form is taken only on request (MOE_TAIL_LATENT_FUSED=1):
+// The one-kernel form is taken only on request (moe_tail_set_kernel_form):
 // measured on GB300 it is slower than the norm kernel followed by the
 // up-projection at every batch size (b = 1: 14.5 vs 13.9 us in one call,
 // 12.3 vs 10.5 us with both promises).  Its CTAs form y on the MMA's critical
@@ -237,8 +319,7 @@ int enqueue_up_project(const void* y, const void* w_up, const void* shared, int 
 // partials, while the separate norm runs ahead of the weight stream under
 // programmatic dependent launch.
 bool latent_tail_fused(int b, int tp, int L, int H, GemmPlan* plan) {
-  const char* v = getenv("MOE_TAIL_LATENT_FUSED");
-  if (!(v && atoi(v) == 1)) return false;
+  if (kernel_form(kFormCallLatent) != MOE_TAIL_FORM_LATENT_ONE_KERNEL) return false;
   return moetail::plan_latent_fused(H, L, b, tp, device_sms(), plan);
 }
 
@@ -289,13 +370,8 @@ namespace {
 using moetail::enqueue_latent_norm;
 using moetail::enqueue_up_project;
 
-bool latent_sizes_ok(int b, int tp, int L) {
-  return b >= 0 && b <= 65535 && tp >= 1 && tp <= kMaxTp && L >= 8 && L <= kMaxP && L % 8 == 0;
-}
-bool up_sizes_ok(int b, int tp_s, int L, int H) {
-  return b >= 0 && b <= 65535 && tp_s >= 0 && tp_s <= kMaxTp && L >= 8 && L <= kMaxP && L % 8 == 0 && H >= 8 &&
-         H % 8 == 0 && H <= (1 << 24);
-}
+using moetail::latent_sizes_ok;
+using moetail::up_sizes_ok;
 
 }  // namespace
 
@@ -377,7 +453,8 @@ MOE_API int moe_tail_up_project(const void* y, const void* w_up, const void* sha
 namespace {
 
 bool shared_sizes_ok(int b, int H, int I) {
-  return b >= 0 && b <= 65535 && H >= 8 && H % 8 == 0 && I >= 8 && I % 8 == 0 && H <= (1 << 24) && I <= (1 << 24);
+  return b >= 0 && b <= kMaxTokens && H >= 8 && H % 8 == 0 && I >= 8 && I % 8 == 0 && H <= kMaxWidth &&
+         I <= kMaxWidth;
 }
 
 // h = bf16(silu(bf16(x . w_gate^T)) * bf16(x . w_up^T)).  Arguments already checked.

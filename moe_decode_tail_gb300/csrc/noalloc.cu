@@ -10,6 +10,7 @@
 // intermediate y rows in a fixed array in device memory that is part of the
 // library itself, so the caller passes only inputs and outputs and nothing is
 // allocated per call.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,24 +30,48 @@ namespace {
 static __device__ __align__(256) uint8_t g_noalloc_y[MOE_TAIL_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch[kMaxDevices] = {nullptr};
+struct ScratchAddress {
+  CUcontext ctx;  // the context the address belongs to
+  void* ptr;
+};
+ScratchAddress g_scratch[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
 
-// The device address of g_noalloc_y on the current device, looked up once
-// per device (the first call on a device does this).
+using CtxGetCurrent = CUresult (*)(CUcontext*);
+
+// The calling thread's current context, or null when it has none yet.
+CUcontext current_context() {
+  static const CtxGetCurrent fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrent>(p);
+    return static_cast<CtxGetCurrent>(nullptr);
+  }();
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
+// The device address of g_noalloc_y on the current device.  It is looked up
+// with cudaGetSymbolAddress once per device (the first call on a device does
+// this), and again only if the device's context has changed since -- after a
+// cudaDeviceReset the library's module is loaded anew and the array may move.
 cudaError_t scratch_on_current_device(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch[dev]) {
+  const CUcontext ctx = current_context();
+  if (!g_scratch[dev].ptr || !ctx || g_scratch[dev].ctx != ctx) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_y);
+    e = cudaGetSymbolAddress(&p, g_noalloc_y);  // with the device current; creates its context if needed
     if (e != cudaSuccess) return e;
-    g_scratch[dev] = p;
+    g_scratch[dev] = ScratchAddress{current_context(), p};
   }
-  *out = g_scratch[dev];
+  *out = g_scratch[dev].ptr;
   return cudaSuccess;
 }
 
@@ -62,8 +87,8 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
 MOE_API int moe_tail_latent_up_noalloc(const void* latent, const void* gamma, float eps, const void* w_up,
                                        const void* shared, int tp_s, int b, int tp, int L, int H, void* out,
                                        void* stream) {
-  if (b < 0 || b > 65535 || tp < 1 || tp > 32 || tp_s < 0 || tp_s > 32) return MOE_TAIL_EINVAL;
-  if (L < 8 || L > 32768 || L % 8 || H < 8 || H % 8 || H > (1 << 24)) return MOE_TAIL_EINVAL;
+  // the limits of moe_tail_latent_up (one definition for both)
+  if (!moetail::latent_sizes_ok(b, tp, L) || !moetail::up_sizes_ok(b, tp_s, L, H)) return MOE_TAIL_EINVAL;
   if (b == 0) return MOE_TAIL_OK;
   // y must fit the library's fixed scratch array
   if ((size_t)b * (size_t)L * 2 > (size_t)MOE_TAIL_NOALLOC_SCRATCH_BYTES) return MOE_TAIL_EINVAL;
@@ -78,7 +103,7 @@ MOE_API int moe_tail_latent_up_noalloc(const void* latent, const void* gamma, fl
     return MOE_TAIL_EINVAL;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The one-kernel form, where requested, keeps y in shared memory (no scratch array).
+  // The one-kernel form, where pinned, keeps y in shared memory (no scratch array).
   moetail::GemmPlan plan;
   if (moetail::latent_tail_fused(b, tp, L, H, &plan))
     return moetail::enqueue_latent_fused(plan, latent, gamma, eps, w_up, shared, tp_s, b, tp, L, H, out, nullptr, 0,
@@ -89,6 +114,13 @@ MOE_API int moe_tail_latent_up_noalloc(const void* latent, const void* gamma, fl
     (void)cudaGetLastError();
     return MOE_TAIL_ECUDA;
   }
+  // The array belongs to the library, so no caller buffer can legitimately
+  // overlap it; check anyway, with the same rule as a caller's workspace.
+  const size_t y_n = (size_t)b * L * 2;
+  if (overlaps(y, y_n, out, out_n) || overlaps(y, y_n, latent, (size_t)tp * b * L * 2) ||
+      overlaps(y, y_n, gamma, (size_t)L * 2) || overlaps(y, y_n, w_up, (size_t)H * L * 2) ||
+      overlaps(y, y_n, shared, (size_t)tp_s * b * H * 2))
+    return MOE_TAIL_EINVAL;
   // 1. y (every element written, so nothing has to start at zero), 2. the
   // up-projection, which follows this call's own norm kernel
   e = moetail::enqueue_latent_norm(latent, gamma, eps, b, tp, L, y, false, st);

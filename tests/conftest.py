@@ -25,3 +25,20 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture
+def pin():
+    """pin(call, form): pin a call's kernel form (moe_tail_set_kernel_form) for
+    one test; the library's choice is restored afterwards."""
+    import moe_decode_tail_gb300 as mt
+
+    calls = []
+
+    def _pin(call, form):
+        mt.moe_tail_set_kernel_form(call, form)
+        calls.append(call)
+
+    yield _pin
+    for c in calls:
+        mt.moe_tail_set_kernel_form(c, 0)

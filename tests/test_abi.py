@@ -398,3 +398,16 @@ def test_token_cap_is_exact(lib):
         assert shared(lib, b=b, H=8, I=8, wsb=-(-16 * b // 256) * 256) in want
         assert gate_up(lib, b=b, H=8, I=8) in want
         assert down(lib, b=b, H=8, I=8) in want
+
+
+def test_kernel_form_accepts_known_forms_and_refuses_the_rest(lib):
+    # host-side only: the setting is a process-wide value, no CUDA call
+    lib.moe_tail_set_kernel_form.argtypes = [ctypes.c_int, ctypes.c_int]
+    for call in (0, 1, 2):  # MOE_TAIL_FORM_EP, _TP, _LATENT
+        for form in (0, 1, 2):
+            assert lib.moe_tail_set_kernel_form(call, form) == OK
+        assert lib.moe_tail_set_kernel_form(call, 3) == EINVAL
+        assert lib.moe_tail_set_kernel_form(call, -1) == EINVAL
+        assert lib.moe_tail_set_kernel_form(call, 0) == OK  # back to the library's choice
+    assert lib.moe_tail_set_kernel_form(3, 0) == EINVAL
+    assert lib.moe_tail_set_kernel_form(-1, 0) == EINVAL

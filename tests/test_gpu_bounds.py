@@ -67,8 +67,8 @@ def test_ep_finalize(mt, kw):
 
 @pytest.mark.parametrize("staged", ["0", "1"])
 @pytest.mark.parametrize("kw", [dict(b=9, tp=3, P=264, K=5), dict(b=70, tp=2, P=1000, K=8)])
-def test_tp_finalize(mt, monkeypatch, staged, kw):
-    monkeypatch.setenv("MOE_TAIL_FIN_STAGED", staged)
+def test_tp_finalize(mt, pin, staged, kw):
+    pin(mt.FORM_TP, 1 if staged == "1" else 2)
     d = synth.tp_finalize_inputs(0xB1 + kw["b"], num_experts=16, **kw)
     out = Guarded((d["b"], d["P"]))
     parts, idx, w, gam = dev(d, "partials", "idx", "w", "gamma")
@@ -86,7 +86,7 @@ LATENT = [dict(b=5, tp=3, tp_s=2, L=264, H=200), dict(b=17, tp=2, tp_s=1, L=1000
 
 
 @pytest.mark.parametrize("kw", LATENT)
-def test_latent_tail_calls(mt, monkeypatch, kw):
+def test_latent_tail_calls(mt, pin, kw):
     d = synth.latent_up_inputs(0xB2 + kw["b"], **kw)
     b, L, H = d["b"], d["L"], d["H"]
     lat, gam, wu = dev(d, "latent", "gamma", "w_up")
@@ -103,7 +103,7 @@ def test_latent_tail_calls(mt, monkeypatch, kw):
     guards += [y, out2]
     # the flags call in both forms, and the call without a workspace
     for one_kernel in ("0", "1"):
-        monkeypatch.setenv("MOE_TAIL_LATENT_FUSED", one_kernel)
+        pin(mt.FORM_LATENT, 1 if one_kernel == "1" else 2)
         y3, out3 = Guarded((b, L)), Guarded((b, H))
         mt.moe_tail_latent_up_flags(lat, gam, wu, sh, out3.t, y3.t, eps=d["eps"], inputs_ready=True,
                                     weights_static=True)

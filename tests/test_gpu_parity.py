@@ -243,11 +243,11 @@ def test_ep_many_local_routes_per_slot(mt):
 
 
 @pytest.mark.parametrize("regs", ["0", "1"])
-def test_ep_both_kernels(mt, monkeypatch, regs):
+def test_ep_both_kernels(mt, pin, regs):
     # the register-resident EP kernel (default) and the route-parallel one
-    # (MOE_TAIL_FIN_EP_REGS=0) on the decode shape and on one token with more
+    # (kernel form 2) on the decode shape and on one token with more
     # local routes than a pass holds
-    monkeypatch.setenv("MOE_TAIL_FIN_EP_REGS", regs)
+    pin(mt.FORM_EP, 1 if regs == "1" else 2)
     d = synth.config(2, weight_before_norm=False)
     assert_bitexact(run_ep(mt, d), ref_ep(d), f"EP b=64 kernel regs={regs}")
     d = synth.ep_finalize_inputs(0xE11, b=9, tp=4, P=2048, K=24, num_experts=24)
@@ -362,16 +362,16 @@ def test_tp_shapes(mt, kw):
 
 @pytest.mark.parametrize("staged", ["0", "1"])
 @pytest.mark.parametrize("b", [3, 64])
-def test_tp_both_kernels(mt, monkeypatch, staged, b):
+def test_tp_both_kernels(mt, pin, staged, b):
     # the staged kernel (chosen from b * K >= 512) and the route-parallel one
     # (chosen below), each forced on a batch the other would take
-    monkeypatch.setenv("MOE_TAIL_FIN_STAGED", staged)
+    pin(mt.FORM_TP, 1 if staged == "1" else 2)
     d = synth.config(3, b=b, weight_before_norm=(b == 3))
     assert_bitexact(run_tp(mt, d), ref_tp(d), f"TP b={b} staged={staged}")
 
 
 @pytest.mark.parametrize("kind", ["ep", "tp_staged", "tp_route_parallel"])
-def test_finalize_flags_call_matches_plain_call(mt, monkeypatch, kind):
+def test_finalize_flags_call_matches_plain_call(mt, pin, kind):
     # the calls with MOE_TAIL_INPUTS_READY give the plain calls' bits
     if kind == "ep":
         d = synth.config(2)
@@ -382,7 +382,7 @@ def test_finalize_flags_call_matches_plain_call(mt, monkeypatch, kind):
                                       weight_before_norm=d["weight_before_norm"], inputs_ready=True)
         ref = ref_ep(d)
     else:
-        monkeypatch.setenv("MOE_TAIL_FIN_STAGED", "1" if kind == "tp_staged" else "0")
+        pin(mt.FORM_TP, 1 if kind == "tp_staged" else 2)
         d = synth.config(3, b=64)
         plain = run_tp(mt, d)
         out = torch.full_like(plain, float("nan"))
@@ -397,12 +397,12 @@ def test_finalize_flags_call_matches_plain_call(mt, monkeypatch, kind):
 
 
 @pytest.mark.parametrize("staged", ["0", "1"])
-def test_tp_flags_inputs_ready_waits_before_writing_out(mt, monkeypatch, staged):
+def test_tp_flags_inputs_ready_waits_before_writing_out(mt, pin, staged):
     # on one stream: TP(Q1) -> X; TP reading X as its partials -> Y; then TP with
     # inputs_ready from Q3 into X.  The last call may start while the second
     # still reads X, so it writes X only after that call ends: Y is the
     # finalize of TP(Q1), X that of Q3.
-    monkeypatch.setenv("MOE_TAIL_FIN_STAGED", staged)
+    pin(mt.FORM_TP, 1 if staged == "1" else 2)
     b, tp, K, P = 64, 8, 8, 4096
     d1 = synth.tp_finalize_inputs(0xC1, b=b, tp=tp, P=P, K=K)
     d3 = synth.tp_finalize_inputs(0xC3, b=b, tp=tp, P=P, K=K)
@@ -551,7 +551,7 @@ def test_latent_norm_inputs_ready_waits_before_writing_y(mt):
     dict(b=12, tp=1, tp_s=0, L=8200, H=64),      # 33 chunks: the two-kernel form
 ])
 @pytest.mark.parametrize("flags", [0, 1, 2, 3])
-def test_latent_one_kernel_matches_split_calls(mt, monkeypatch, kw, flags):
+def test_latent_one_kernel_matches_split_calls(mt, pin, kw, flags):
     # moe_tail_latent_up_flags with its one-kernel form taken wherever it fits
     # (up to 32 tokens): y and out bit for bit those of moe_tail_latent_norm +
     # moe_tail_up_project, y bit-exact against the oracle's norm and out within
@@ -564,7 +564,7 @@ def test_latent_one_kernel_matches_split_calls(mt, monkeypatch, kw, flags):
     out1 = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
     mt.moe_tail_latent_norm(lat, gam, y1, eps=d["eps"])
     mt.moe_tail_up_project(y1, w, sh, out1)
-    monkeypatch.setenv("MOE_TAIL_LATENT_FUSED", "1")
+    pin(mt.FORM_LATENT, 1)
     y2 = torch.full((b, L), float("nan"), dtype=torch.bfloat16, device=DEV)
     out2 = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
     mt.moe_tail_latent_up_flags(lat, gam, w, sh, out2, y2, eps=d["eps"], inputs_ready=bool(flags & 2),
@@ -580,10 +580,10 @@ def test_latent_one_kernel_matches_split_calls(mt, monkeypatch, kw, flags):
 
 
 @pytest.mark.parametrize("choice", ["0", "1"])
-def test_latent_up_and_noalloc_take_either_form(mt, monkeypatch, choice):
+def test_latent_up_and_noalloc_take_either_form(mt, pin, choice):
     # moe_tail_latent_up and the workspace-free call at b = 4, with the one-kernel
     # form switched off and on: the same bits either way
-    monkeypatch.setenv("MOE_TAIL_LATENT_FUSED", choice)
+    pin(mt.FORM_LATENT, 1 if choice == "1" else 2)
     d = synth.latent_up_inputs(0x0F4, b=4, tp=8, tp_s=9, L=3584, H=7168)
     y, out = run_latent(mt, d)
     out_na = torch.full((4, 7168), float("nan"), dtype=torch.bfloat16, device=DEV)
@@ -599,12 +599,12 @@ def test_latent_up_and_noalloc_take_either_form(mt, monkeypatch, choice):
 
 
 @pytest.mark.parametrize("one_kernel", ["0", "1"])
-def test_latent_up_flags_inputs_ready_waits_before_writing_y(mt, monkeypatch, one_kernel):
+def test_latent_up_flags_inputs_ready_waits_before_writing_y(mt, pin, one_kernel):
     # norm(A) -> up-projection reading y -> the flags call for B with
     # inputs_ready into the same y, on one stream (both forms): B's first
     # kernel may start while the up-projection still reads y, so y is written
     # only after that kernel ends; outA must be A's up-projection and y, outB B's
-    monkeypatch.setenv("MOE_TAIL_LATENT_FUSED", one_kernel)
+    pin(mt.FORM_LATENT, 1 if one_kernel == "1" else 2)
     kw = dict(b=16, tp=8, tp_s=8, L=3584, H=7168)
     A = synth.latent_up_inputs(0xA13, **kw)
     B = synth.latent_up_inputs(0xB24, **kw)

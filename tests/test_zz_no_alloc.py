@@ -82,3 +82,20 @@ def test_noalloc_refuses_a_problem_larger_than_its_array(mt):
         mt.moe_tail_latent_up_noalloc(d["latent"], d["gamma"], d["w_up"], None, out)
     torch.cuda.synchronize()
     assert bool((out.float() == 0).all())  # nothing ran
+
+
+def test_noalloc_in_the_one_kernel_form(mt, pin):
+    # with the latent tail's one-kernel form pinned, the call keeps y on chip and
+    # passes the kernel no y pointer at all; at a batch that form takes (b = 8)
+    # its output must still match the workspace entry point's, and no bounded
+    # wait may have expired
+    pin(mt.FORM_LATENT, mt.FORM_LATENT_ONE_KERNEL)
+    d = inputs(0x5EED0048, b=8)
+    got = without_workspace(mt, d)
+    torch.cuda.synchronize()
+    assert mt.moe_tail_take_device_error() == 0
+    pin(mt.FORM_LATENT, 2)  # the reference: the workspace entry point as its two kernels
+    ref = with_workspace(mt, d)
+    torch.cuda.synchronize()
+    assert close(got, ref)
+    assert mt.moe_tail_take_device_error() == 0
