@@ -709,6 +709,66 @@ def config_bytes(name: str, d: dict) -> int:
     return 3 * H_ * I_ * 2 + b * H_ * 2 + 2 * b * I_ * 2 + 2 * b * H_ * 2
 
 
+def floor_lib():
+    """The latency-floor kernels (include/moe_tail_floor.h), built on first use."""
+    import ctypes
+
+    from moe_decode_tail_gb300 import build as cuda_build
+
+    L_ = ctypes.CDLL(cuda_build.build(floor=True))
+    P_, i32 = ctypes.c_void_p, ctypes.c_int
+    L_.moe_tail_floor_empty.argtypes = [i32, i32, i32, i32, P_]
+    L_.moe_tail_floor_read.argtypes = [P_, ctypes.c_size_t, i32, i32, i32, i32, P_, P_]
+    L_.moe_tail_floor_gather.argtypes = [P_, i32, P_, ctypes.c_int64, i32, i32, i32, i32, P_, P_]
+    return L_
+
+
+def ep_floor(d, dev, timed, copies_for, ep_us) -> dict:
+    """Latency floors of the EP finalize call at config 2, on its own grid (two
+    column bands of 256 threads per token, clusters of two, b = 64 tokens):
+    an empty kernel (launch and dependency wait), one trip reading the call's
+    algorithmic bytes, and the two dependent trips of its access pattern (the
+    token's route indices, then its 8 local rows' bands).  Each is timed as
+    the call is (a graph of back-to-back launches, inputs rotated past L2)."""
+    import ctypes
+
+    fl = floor_lib()
+    gx, gy, thr, cl = 2, d["b"], 256, 2
+    st = torch.cuda.current_stream(dev)
+    sptr = lambda: ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    sink = torch.zeros(gx * gy, dtype=torch.int32, device=dev)
+    nbytes = config_bytes("ep", d)
+    nbytes -= nbytes % 16
+    n = copies_for(nbytes)
+    bufs = [torch.empty(nbytes, dtype=torch.uint8, device=dev).random_(0, 255) for _ in range(n)]
+    # the gather: each token's 8 local routes as (slot, row) -> a row of the [tp * rows_per_slot, P] table
+    tp, K, R = d["tp"], d["K"], d["rows_per_slot"]
+    idx = d["idx"].numpy()
+    flat = []
+    for t in range(d["b"]):
+        flat.append([s * R + int(j) for s in range(tp) for j in idx[s, t] if 0 <= j < R][:K])
+    gidx = torch.tensor(flat, dtype=torch.int32, device=dev)
+    rows = [d["rows"].to(dev)] + [None] * (copies_for(d["rows"].numel() * 2) - 1)
+    for i in range(1, len(rows)):
+        rows[i] = rows[0].clone()
+
+    def call(rc):
+        assert rc == 0, rc
+
+    out = {"grid": f"{gx} x {gy} CTAs of {thr} threads, clusters of {cl}"}
+    out["empty_us"] = round(timed(lambda i: call(fl.moe_tail_floor_empty(gx, gy, thr, cl, sptr())), 1), 3)
+    out["read_us"] = round(timed(lambda i: call(fl.moe_tail_floor_read(
+        ctypes.c_void_p(bufs[i].data_ptr()), nbytes, gx, gy, thr, cl, ctypes.c_void_p(sink.data_ptr()), sptr())),
+        n), 3)
+    out["gather_us"] = round(timed(lambda i: call(fl.moe_tail_floor_gather(
+        ctypes.c_void_p(gidx.data_ptr()), K, ctypes.c_void_p(rows[i].data_ptr()), tp * R, gx, gy, thr, cl,
+        ctypes.c_void_p(sink.data_ptr()), sptr())), len(rows)), 3)
+    out["ep_over_read"] = round(ep_us / out["read_us"], 3)
+    out["ep_over_gather"] = round(ep_us / out["gather_us"], 3)
+    del bufs, rows, st
+    return out
+
+
 def isolated_configs(mt, cpu, w, dev, stream) -> dict:
     """Each workload timed alone: one call per graph node, CUDA events around
     replays of a graph of max(20, copies) calls that cycles over copies of the
@@ -774,6 +834,7 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
 
     ep_like("1_ep_tiny_b4_P512", synth.config(1), "parity; latency-bound (report us; inputs L2-resident)", n=1)
     ep_like("2_ep_b64_P4096", cpu["ep"], ">= 0.70 of HBM (hard at 4.7 MB)", ready_key="2_ep_b64_P4096_ready")
+    res["2_ep_b64_P4096"]["floor"] = ep_floor(cpu["ep"], dev, timed, copies_for, res["2_ep_b64_P4096"]["us"])
 
     d = synth.config(3)
     nb = config_bytes("tp", d)

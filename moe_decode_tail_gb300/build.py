@@ -19,7 +19,9 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoetail.so")
 TRACE_LIB = os.path.join(BUILD, "libmoetail_trace.so")  # the same kernels with the per-CTA trace
+FLOOR_LIB = os.path.join(BUILD, "libmoetail_floor.so")  # latency-floor kernels (measurement only)
 SOURCES = ["finalize.cu", "decode_gemm.cu", "moe_tail_api.cu", "noalloc.cu"]
+FLOOR_SOURCES = ["floor.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
@@ -35,26 +37,31 @@ def nvcc() -> str:
     return exe
 
 
-def _inputs() -> list[str]:
-    files = [os.path.join(CSRC, s) for s in SOURCES]
+def _inputs(sources=SOURCES) -> list[str]:
+    files = [os.path.join(CSRC, s) for s in sources]
     files += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     files.append(os.path.join(ROOT, "include", "moe_tail.h"))
     files.append(os.path.join(ROOT, "include", "moe_tail_trace.h"))
+    files.append(os.path.join(ROOT, "include", "moe_tail_floor.h"))
     return files
 
 
-def up_to_date(lib: str = LIB) -> bool:
+def up_to_date(lib: str = LIB, sources=SOURCES) -> bool:
     if not os.path.exists(lib):
         return False
     t = os.path.getmtime(lib)
-    return all(os.path.getmtime(f) <= t for f in _inputs())
+    return all(os.path.getmtime(f) <= t for f in _inputs(sources))
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, trace: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, trace: bool = False,
+          floor: bool = False) -> str:
     """Build libmoetail.so, or with trace=True libmoetail_trace.so (the same
-    kernels recording a per-CTA timeline; see include/moe_tail_trace.h)."""
-    lib = TRACE_LIB if trace else LIB
-    if not force and up_to_date(lib):
+    kernels recording a per-CTA timeline; see include/moe_tail_trace.h), or
+    with floor=True libmoetail_floor.so (the latency-floor kernels of
+    include/moe_tail_floor.h, used by bench.py only)."""
+    lib = FLOOR_LIB if floor else TRACE_LIB if trace else LIB
+    sources = FLOOR_SOURCES if floor else SOURCES
+    if not force and up_to_date(lib, sources):
         return lib
     os.makedirs(BUILD, exist_ok=True)
     exe = nvcc()
@@ -72,8 +79,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, tra
             sys.stderr.write(r.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as pool:
-        objs = list(pool.map(compile_one, SOURCES))
+    with ThreadPoolExecutor(max_workers=len(sources)) as pool:
+        objs = list(pool.map(compile_one, sources))
     tmp = lib + tag
     r = subprocess.run([exe, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     for o in objs:
@@ -85,4 +92,5 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, tra
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_v="-v" in sys.argv, trace="--trace" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_v="-v" in sys.argv, trace="--trace" in sys.argv,
+                floor="--floor" in sys.argv))

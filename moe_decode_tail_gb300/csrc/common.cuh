@@ -52,6 +52,48 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
+// ---- paired FP32 arithmetic ----------------------------------------------------
+//
+// Eight consecutive values as four pairs (2k, 2k + 1).  add.rn.f32x2 and
+// mul.rn.f32x2 do two binary32 operations in one instruction, each component
+// rounded to nearest even as add.rn.f32 / mul.rn.f32 round it, so the paired
+// loops give the bits of the scalar ones -- with one rule: a paired product
+// never feeds a paired add.  Measured on GB300, such a pair is fused into one
+// multiply-add (a single rounding) despite the explicit rounding modes and
+// with contraction switched off; a product that goes into a sum is formed by
+// mul_each (two __fmul_rn, which are never merged) instead.
+__device__ __forceinline__ void unpack8p(const uint4& v, float2 (&f)[4]) {
+  f[0] = make_float2(bf16_lo(v.x), bf16_hi(v.x));
+  f[1] = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+  f[2] = make_float2(bf16_lo(v.z), bf16_hi(v.z));
+  f[3] = make_float2(bf16_lo(v.w), bf16_hi(v.w));
+}
+__device__ __forceinline__ uint64_t pair_bits(float2 v) {
+  return ((uint64_t)__float_as_uint(v.y) << 32) | __float_as_uint(v.x);
+}
+__device__ __forceinline__ float2 pair_of(uint64_t b) {
+  return make_float2(__uint_as_float((uint32_t)b), __uint_as_float((uint32_t)(b >> 32)));
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pair_bits(a)), "l"(pair_bits(b)));
+  return pair_of(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pair_bits(a)), "l"(pair_bits(b)));
+  return pair_of(d);
+}
+// Each component times s, as two scalar products that are never merged into a
+// following add (the form to use for a product that is summed).
+__device__ __forceinline__ float2 mul_each(float2 v, float s) { return make_float2(__fmul_rn(v.x, s), __fmul_rn(v.y, s)); }
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+__device__ __forceinline__ float2 bf16_round2(float2 v) { return make_float2(bf16_round(v.x), bf16_round(v.y)); }
+__device__ __forceinline__ uint4 pack8p_pz(const float2 (&o)[4]) {
+  return make_uint4(pack_bf16x2_pz(o[0].x, o[0].y), pack_bf16x2_pz(o[1].x, o[1].y), pack_bf16x2_pz(o[2].x, o[2].y),
+                    pack_bf16x2_pz(o[3].x, o[3].y));
+}
+
 // 16-byte streaming load of data read once (no L1 allocation).
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;

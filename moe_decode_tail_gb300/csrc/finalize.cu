@@ -24,8 +24,9 @@
 // leaves the product in shared memory; the first route group then adds the
 // products in route order (EP: per slot, each slot's partial rounded to BF16,
 // slots summed in order).  All arithmetic is single IEEE binary32 operations
-// (__fmul_rn / __fadd_rn: never contracted into an FMA), the inverse RMS is
-// 1 / sqrt(.) with IEEE square root and division, and subnormals are kept.
+// (__fmul_rn / __fadd_rn and the paired mul.rn.f32x2 / add.rn.f32x2, which
+// round each component alike: never contracted into an FMA), the inverse RMS
+// is 1 / sqrt(.) with IEEE square root and division, and subnormals are kept.
 #include <stdlib.h>
 
 #include <algorithm>
@@ -154,13 +155,13 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
   const uint4 gv = valid ? ld_v4(a.gamma + col) : make_uint4(0, 0, 0, 0);
   const int count = load_route_list<MODE, WMODE>(a, sm, t);
 
-  float g[8];
-  unpack8(gv, g);
+  float2 g[4];
+  unpack8p(gv, g);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) g[i] = __fadd_rn(g[i], a.gain_center);
-  float o[8], part[8];
+  for (int k = 0; k < 4; ++k) g[k] = add2(g[k], splat2(a.gain_center));
+  float2 o[4], part[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] = part[i] = 0.0f;
+  for (int k = 0; k < 4; ++k) o[k] = part[k] = splat2(0.0f);
   int cur_slot = -1;
 
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // peers started: DSMEM is live
@@ -168,14 +169,14 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
   for (int base = 0, pass = 0; base < count; base += R, ++pass) {
     const int e = base + r_local;  // this thread's route in the pass
     const bool active = e < count;
-    float x[8];
+    float2 x[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = 0.0f;
+    for (int k = 0; k < 4; ++k) x[k] = splat2(0.0f);
     if (active && valid) {
       const int64_t row = sm.list_row[e];
       if (MODE == kModeEP) {
         const uint4 v = ld_stream_v4(a.rows + (int64_t)sm.list_slot[e] * a.slot_stride + row * a.P + col);
-        unpack8(v, x);
+        unpack8p(v, x);
       } else {
         const uint16_t* src = a.rows + row * a.P + col;
         for (int s0 = 0; s0 < a.tp; s0 += 8) {  // eight slots in flight at a time
@@ -186,25 +187,26 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             if (s0 + q < a.tp) {  // slot order, FP32 from +0
-              float f[8];
-              unpack8(v[q], f);
+              float2 f[4];
+              unpack8p(v[q], f);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) x[i] = __fadd_rn(x[i], f[i]);
+              for (int k = 0; k < 4; ++k) x[k] = add2(x[k], f[k]);
             }
           }
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = bf16_round(x[i]);
+        for (int k = 0; k < 4; ++k) x[k] = bf16_round2(x[k]);
       }
     }
     // this warp's chunk sum of squares, published to every CTA of the cluster
     float* ssp = sm.ss[pass & 1][r_local];
     {
-      float acc = 0.0f;
+      float acc = 0.0f;  // the lane's eight squares, added in column order
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float v = WBN ? __fmul_rn(x[i], g[i]) : x[i];
-        acc = __fadd_rn(acc, __fmul_rn(v, v));
+      for (int k = 0; k < 4; ++k) {
+        const float2 v = WBN ? mul2(x[k], g[k]) : x[k];
+        const float2 sq = mul2(v, v);
+        acc = __fadd_rn(__fadd_rn(acc, sq.x), sq.y);
       }
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
@@ -217,15 +219,16 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
       for (int c = 0; c < a.chunks; ++c) ss = __fadd_rn(ss, ssp[c]);
       const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, a.rcpP), a.eps)));
       const float w = MODE == kModeLatent ? 1.0f : sm.w[sm.list_route[e]];
+      const float2 inv2 = splat2(inv);
       float4* dst = reinterpret_cast<float4*>(prod + ((size_t)r_local * VB + vb) * 8);
-      float p[8];
+      float2 p[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float nv = WBN ? __fmul_rn(__fmul_rn(x[i], g[i]), inv) : __fmul_rn(__fmul_rn(x[i], inv), g[i]);
-        p[i] = __fmul_rn(nv, w);  // each product rounded alone
+      for (int k = 0; k < 4; ++k) {
+        const float2 nv = WBN ? mul2(mul2(x[k], g[k]), inv2) : mul2(mul2(x[k], inv2), g[k]);
+        p[k] = mul_each(nv, w);  // each product rounded alone (summed after the barrier)
       }
-      dst[0] = make_float4(p[0], p[1], p[2], p[3]);
-      dst[1] = make_float4(p[4], p[5], p[6], p[7]);
+      dst[0] = make_float4(p[0].x, p[0].y, p[1].x, p[1].y);
+      dst[1] = make_float4(p[2].x, p[2].y, p[3].x, p[3].y);
     }
     __syncthreads();
     if (r_local == 0) {  // the route sum, in route order
@@ -233,24 +236,25 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
       for (int rr = 0; rr < n_pass; ++rr) {
         const float4* src = reinterpret_cast<const float4*>(prod + ((size_t)rr * VB + vb) * 8);
         const float4 p0 = src[0], p1 = src[1];
-        const float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        const float2 p[4] = {make_float2(p0.x, p0.y), make_float2(p0.z, p0.w), make_float2(p1.x, p1.y),
+                             make_float2(p1.z, p1.w)};
         if (MODE == kModeEP) {
           const int s = sm.list_slot[base + rr];
           if (s != cur_slot) {  // slot boundary: its BF16 partial joins the slot sum
             if (cur_slot >= 0) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                o[i] = __fadd_rn(o[i], bf16_round(part[i]));
-                part[i] = 0.0f;
+              for (int k = 0; k < 4; ++k) {
+                o[k] = add2(o[k], bf16_round2(part[k]));
+                part[k] = splat2(0.0f);
               }
             }
             cur_slot = s;
           }
 #pragma unroll
-          for (int i = 0; i < 8; ++i) part[i] = __fadd_rn(part[i], p[i]);
+          for (int k = 0; k < 4; ++k) part[k] = add2(part[k], p[k]);
         } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) o[i] = __fadd_rn(o[i], p[i]);
+          for (int k = 0; k < 4; ++k) o[k] = add2(o[k], p[k]);
         }
       }
     }
@@ -258,14 +262,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
   }
   if (MODE == kModeEP && cur_slot >= 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = __fadd_rn(o[i], bf16_round(part[i]));
+    for (int k = 0; k < 4; ++k) o[k] = add2(o[k], bf16_round2(part[k]));
   }
   if (r_local == 0 && valid) {
-    uint4 r;
-    r.x = pack_bf16x2_pz(o[0], o[1]);
-    r.y = pack_bf16x2_pz(o[2], o[3]);
-    r.z = pack_bf16x2_pz(o[4], o[5]);
-    r.w = pack_bf16x2_pz(o[6], o[7]);
+    const uint4 r = pack8p_pz(o);
     if (a.inputs_before_wait) grid_dependency_wait();  // the preceding kernel may still read out
     st_v4(a.out + (int64_t)t * a.P + col, r);
   }
@@ -302,13 +302,13 @@ __global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const Fin
 
   const uint4 gv = valid ? ld_v4(a.gamma + col) : make_uint4(0, 0, 0, 0);
   const int count = load_route_list<kModeEP, WMODE>(a, sm, t);
-  float g[8];
-  unpack8(gv, g);
+  float2 g[4];
+  unpack8p(gv, g);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) g[i] = __fadd_rn(g[i], a.gain_center);
-  float o[8], part[8];
+  for (int k = 0; k < 4; ++k) g[k] = add2(g[k], splat2(a.gain_center));
+  float2 o[4], part[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] = part[i] = 0.0f;
+  for (int k = 0; k < 4; ++k) o[k] = part[k] = splat2(0.0f);
   int cur_slot = -1;
 
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // peers started: DSMEM is live
@@ -328,13 +328,14 @@ __global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const Fin
 #pragma unroll
     for (int q = 0; q < kEpRoutes; ++q) {
       if (q < n_pass) {
-        float x[8];
-        unpack8(raw[q], x);
-        float acc = 0.0f;
+        float2 x[4];
+        unpack8p(raw[q], x);
+        float acc = 0.0f;  // the lane's eight squares, added in column order
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float v = WBN ? __fmul_rn(x[i], g[i]) : x[i];
-          acc = __fadd_rn(acc, __fmul_rn(v, v));
+        for (int k = 0; k < 4; ++k) {
+          const float2 v = WBN ? mul2(x[k], g[k]) : x[k];
+          const float2 sq = mul2(v, v);
+          acc = __fadd_rn(__fadd_rn(acc, sq.x), sq.y);
         }
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
@@ -355,33 +356,30 @@ __global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const Fin
         if (s != cur_slot) {  // slot boundary: its BF16 partial joins the slot sum
           if (cur_slot >= 0) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              o[i] = __fadd_rn(o[i], bf16_round(part[i]));
-              part[i] = 0.0f;
+            for (int k = 0; k < 4; ++k) {
+              o[k] = add2(o[k], bf16_round2(part[k]));
+              part[k] = splat2(0.0f);
             }
           }
           cur_slot = s;
         }
-        float x[8];
-        unpack8(raw[q], x);
+        float2 x[4];
+        unpack8p(raw[q], x);
+        const float2 inv2 = splat2(inv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float nv = WBN ? __fmul_rn(__fmul_rn(x[i], g[i]), inv) : __fmul_rn(__fmul_rn(x[i], inv), g[i]);
-          part[i] = __fadd_rn(part[i], __fmul_rn(nv, w));  // each product rounded alone
+        for (int k = 0; k < 4; ++k) {
+          const float2 nv = WBN ? mul2(mul2(x[k], g[k]), inv2) : mul2(mul2(x[k], inv2), g[k]);
+          part[k] = add2(part[k], mul_each(nv, w));  // each product rounded alone
         }
       }
     }
   }
   if (cur_slot >= 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = __fadd_rn(o[i], bf16_round(part[i]));
+    for (int k = 0; k < 4; ++k) o[k] = add2(o[k], bf16_round2(part[k]));
   }
   if (valid) {
-    uint4 r;
-    r.x = pack_bf16x2_pz(o[0], o[1]);
-    r.y = pack_bf16x2_pz(o[2], o[3]);
-    r.z = pack_bf16x2_pz(o[4], o[5]);
-    r.w = pack_bf16x2_pz(o[6], o[7]);
+    const uint4 r = pack8p_pz(o);
     if (a.inputs_before_wait) grid_dependency_wait();
     st_v4(a.out + (int64_t)t * a.P + col, r);
   }
@@ -534,23 +532,23 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
   const int vec = band * VB + vb;
   const bool valid = vec * 8 < a.P;
   const int chunk = vec >> 5;
-  float g8[8];
+  float2 g8[4];
   {
     const uint4 gv = valid ? ld_v4(a.gamma + vec * 8) : make_uint4(0, 0, 0, 0);
-    unpack8(gv, g8);
+    unpack8p(gv, g8);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) g8[i] = __fadd_rn(g8[i], a.gain_center);
+    for (int k = 0; k < 4; ++k) g8[k] = add2(g8[k], splat2(a.gain_center));
   }
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // peers started: DSMEM is live
 
   uint32_t g = 0;  // stages consumed
   int pass = 0;
   for (int t = blockIdx.y; t < a.b; t += gridDim.y) {
-    float acc[8];
+    float2 acc[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int k = 0; k < 4; ++k) acc[k] = splat2(0.0f);
     for (int base = 0; base < a.K; base += kMaxRoutesPerPass, ++pass) {
-      float xr[kMaxRoutesPerPass][8];
+      float2 xr[kMaxRoutesPerPass][4];
       bool has[kMaxRoutesPerPass];
       float wr[kMaxRoutesPerPass];
       float* ss = &sm.ss[pass & 1][0][0];
@@ -562,7 +560,7 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
         has[rr] = k < a.K && j >= 0 && j < a.num_rows;
         wr[rr] = has[rr] ? route_weight<WMODE>(a.w, (int64_t)t * a.K + k) : 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) xr[rr][i] = 0.0f;
+        for (int k = 0; k < 4; ++k) xr[rr][k] = splat2(0.0f);
         if (has[rr]) {
           const int st = (int)(g % (uint32_t)S);
           sb_wait(smem_addr(&sm.full[st]), (g / S) & 1, abort_flag);
@@ -572,22 +570,23 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
           if (valid) {
             const uint8_t* src = ring_raw + (size_t)st * stage_bytes + (size_t)vb * 16;
             for (int s = 0; s < a.tp; ++s, src += band_bytes) {  // slot order, FP32 from +0
-              float f[8];
-              unpack8(*reinterpret_cast<const uint4*>(src), f);
+              float2 f[4];
+              unpack8p(*reinterpret_cast<const uint4*>(src), f);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) xr[rr][i] = __fadd_rn(xr[rr][i], f[i]);
+              for (int k = 0; k < 4; ++k) xr[rr][k] = add2(xr[rr][k], f[k]);
             }
           }
           __syncwarp();
           if (lane == 0) sb_arrive(smem_addr(&sm.empty[st]));
           if (issuer) issue_next();  // refill the stage just consumed
 #pragma unroll
-          for (int i = 0; i < 8; ++i) xr[rr][i] = bf16_round(xr[rr][i]);
-          float sq = 0.0f;
+          for (int k = 0; k < 4; ++k) xr[rr][k] = bf16_round2(xr[rr][k]);
+          float sq = 0.0f;  // the lane's eight squares, added in column order
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float v = WBN ? __fmul_rn(xr[rr][i], g8[i]) : xr[rr][i];
-            sq = __fadd_rn(sq, __fmul_rn(v, v));
+          for (int k = 0; k < 4; ++k) {
+            const float2 v = WBN ? mul2(xr[rr][k], g8[k]) : xr[rr][k];
+            const float2 s2 = mul2(v, v);
+            sq = __fadd_rn(__fadd_rn(sq, s2.x), s2.y);
           }
 #pragma unroll
           for (int off = 1; off < 32; off <<= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, off));
@@ -605,21 +604,18 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
       for (int rr = 0; rr < kMaxRoutesPerPass; ++rr) {
         const float inv = __shfl_sync(0xffffffffu, my_inv, rr);
         if (has[rr]) {  // a route with no row contributes nothing
+          const float2 inv2 = splat2(inv);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float x = xr[rr][i];
-            const float nv = WBN ? __fmul_rn(__fmul_rn(x, g8[i]), inv) : __fmul_rn(__fmul_rn(x, inv), g8[i]);
-            acc[i] = __fadd_rn(acc[i], __fmul_rn(nv, wr[rr]));
+          for (int k = 0; k < 4; ++k) {
+            const float2 x = xr[rr][k];
+            const float2 nv = WBN ? mul2(mul2(x, g8[k]), inv2) : mul2(mul2(x, inv2), g8[k]);
+            acc[k] = add2(acc[k], mul_each(nv, wr[rr]));  // each product rounded alone
           }
         }
       }
     }
     if (valid) {
-      uint4 r;
-      r.x = pack_bf16x2_pz(acc[0], acc[1]);
-      r.y = pack_bf16x2_pz(acc[2], acc[3]);
-      r.z = pack_bf16x2_pz(acc[4], acc[5]);
-      r.w = pack_bf16x2_pz(acc[6], acc[7]);
+      const uint4 r = pack8p_pz(acc);
       if (a.inputs_before_wait) grid_dependency_wait();  // the preceding kernel may still read out
       st_v4(a.out + (int64_t)t * a.P + vec * 8, r);
     }

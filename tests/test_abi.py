@@ -45,7 +45,7 @@ def test_header_declares_the_four_calls_and_helpers():
 def test_headers_compile_as_c_and_cxx(tmp_path, lang):
     # a plain C (and C++) consumer of the ABI: both headers, no warnings
     src = tmp_path / "consumer.c"
-    src.write_text('#include "moe_tail.h"\n#include "moe_tail_trace.h"\n'
+    src.write_text('#include "moe_tail.h"\n#include "moe_tail_trace.h"\n#include "moe_tail_floor.h"\n'
                    "int main(void) { return moe_tail_workspace_bytes(0, 1, 8) == 0 ? 1 : 0; }\n")
     inc = os.path.join(ROOT, "include")
     subprocess.run(lang[:2] + ["-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only", "-I", inc] + lang[2:]
@@ -411,3 +411,46 @@ def test_kernel_form_accepts_known_forms_and_refuses_the_rest(lib):
         assert lib.moe_tail_set_kernel_form(call, 0) == OK  # back to the library's choice
     assert lib.moe_tail_set_kernel_form(3, 0) == EINVAL
     assert lib.moe_tail_set_kernel_form(-1, 0) == EINVAL
+
+
+def _floor_lib():
+    cuda_build.build(floor=True)
+    fl = ctypes.CDLL(cuda_build.FLOOR_LIB)
+    P_, i32 = ctypes.c_void_p, ctypes.c_int
+    fl.moe_tail_floor_empty.argtypes = [i32, i32, i32, i32, P_]
+    fl.moe_tail_floor_read.argtypes = [P_, ctypes.c_size_t, i32, i32, i32, i32, P_, P_]
+    fl.moe_tail_floor_gather.argtypes = [P_, i32, P_, ctypes.c_int64, i32, i32, i32, i32, P_, P_]
+    return fl
+
+
+def test_floor_library_exports_exactly_its_header():
+    # the measurement-only library: the three calls of include/moe_tail_floor.h, nothing else
+    _floor_lib()
+    out = subprocess.run(["nm", "-D", "--defined-only", cuda_build.FLOOR_LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.split() and line.split()[-2] in "TtDdBbRr"}
+    exported = {e for e in exported if not e.startswith("_")}
+    header = open(os.path.join(ROOT, "include", "moe_tail_floor.h")).read()
+    assert exported == set(re.findall(r"^int (moe_tail_floor_\w+)\(", header, re.M))
+    assert exported == {"moe_tail_floor_empty", "moe_tail_floor_read", "moe_tail_floor_gather"}
+
+
+@host_only
+def test_floor_calls_refuse_bad_shapes_before_launching():
+    fl = _floor_lib()
+    ok = a()
+    for gx, gy, thr, cl in ((0, 1, 32, 1), (2, 0, 32, 1), (2, 1, 33, 1), (2, 1, 2048, 1), (3, 1, 32, 2),
+                            (16, 1, 32, 16)):
+        assert fl.moe_tail_floor_empty(gx, gy, thr, cl, None) == 1
+        assert fl.moe_tail_floor_read(ok, 4096, gx, gy, thr, cl, ok, None) == 1
+        assert fl.moe_tail_floor_gather(ok, 8, ok, 16, gx, gy, thr, cl, ok, None) == 1
+    # bad sizes and pointers: a size not a multiple of 16, more than one trip's worth, null or misaligned
+    assert fl.moe_tail_floor_read(ok, 4008, 2, 1, 32, 1, ok, None) == 1
+    assert fl.moe_tail_floor_read(ok, 2 * 32 * 16 * 16 + 16, 2, 1, 32, 1, ok, None) == 1
+    assert fl.moe_tail_floor_read(None, 4096, 2, 1, 32, 1, ok, None) == 1
+    assert fl.moe_tail_floor_read(a(8), 4096, 2, 1, 32, 1, ok, None) == 1
+    assert fl.moe_tail_floor_gather(ok, 0, ok, 16, 2, 1, 32, 1, ok, None) == 1
+    assert fl.moe_tail_floor_gather(a(2), 8, ok, 16, 2, 1, 32, 1, ok, None) == 1
+    # valid shapes pass the checks and then fail at the launch without a GPU
+    assert fl.moe_tail_floor_empty(2, 64, 256, 2, None) == 2
+    assert fl.moe_tail_floor_read(ok, 4096, 2, 1, 32, 1, ok, None) == 2
