@@ -6,10 +6,12 @@ expert accumulates into the latent tail's output; and latent_main, where the
 latent tail runs beside the shared expert's gate/up and the down projection
 then accumulates into its output), checked against the oracle on sampled
 tokens:
-EP and expert-TP outputs and the latent norm's y bit for bit; the step's
-output against the oracle's up-projection of the GPU's y with the shared
-expert's BF16 output d as one more shared partial (GEMM bound); and d against
-the oracle's down projection of the GPU's h (GEMM bound)."""
+EP and expert-TP outputs and the latent norm's y bit for bit; in the two
+branch compositions, the step's output against the oracle's up-projection of
+the GPU's y with the shared expert's BF16 output d as one more shared partial
+(GEMM bound), and d against the oracle's down projection of the GPU's h (GEMM
+bound); where d is added into the latent tail's output instead, each term at
+the GEMM bound and the add bit for bit, given the GPU's own terms."""
 import importlib.util
 import os
 
@@ -58,6 +60,18 @@ def step(request):
     assert mt.moe_tail_take_device_error() == 0
     got = {k: w[k].cpu() for k in ("out_ep", "out_tp", "out", "shared9")}
     got["y"] = w["ws_lat"][: bench.B * bench.L * 2].view(torch.bfloat16).view(bench.B, bench.L).cpu()
+    if request.param in ("sequential", "latent_main"):
+        # the two terms of the step's last add, recomputed alone from the same
+        # inputs (both calls are deterministic): the latent tail's own output,
+        # and d = bf16(down(h)) of the step's h
+        B, I = bench.B, bench.I
+        ws = torch.empty_like(w["ws_lat"])
+        tail = torch.full_like(w["out"], float("nan"))
+        mt.moe_tail_latent_up(w["latent"], w["lat_gamma"], w["w_up"], w["shared"], tail, ws, eps=1e-6)
+        d = torch.full_like(w["out"], float("nan"))
+        mt.moe_shared_down(w["ws_sh"][: B * I * 2].view(torch.bfloat16).view(B, I), w["w_down"], d, accumulate=False)
+        torch.cuda.synchronize()
+        got["tail"], got["d"] = tail.cpu(), d.cpu()
     return bench, cpu, got, w["ws_sh"].cpu(), request.param
 
 
@@ -93,14 +107,16 @@ def test_step_latent_tail_and_shared_expert(step):
                                        got["shared9"][:, t:t + 1].contiguous(), TP + 1, 1, L, H)
             close(got["out"][t:t + 1], out_ref, f"out token {t}")
         else:
-            # out = bf16(latent tail + bf16(down(h))): the latent tail's own output is
-            # not kept, so check out against the oracle's tail plus the oracle's down
-            # projection of the GPU's h, within the tail's GEMM bound plus d's rounding
-            tail = oracle.latent_up(got["y"][t:t + 1].contiguous(), lat["w_up"],
-                                    got["shared9"][:TP, t:t + 1].contiguous(), TP, 1, L, H)
+            # out = bf16(latent tail + bf16(down(h))): each term against the oracle
+            # (the tail from the GPU's y, d from the GPU's h) at the GEMM bound ...
+            tail_ref = oracle.latent_up(got["y"][t:t + 1].contiguous(), lat["w_up"],
+                                        got["shared9"][:TP, t:t + 1].contiguous(), TP, 1, L, H)
+            close(got["tail"][t:t + 1], tail_ref, f"latent tail token {t}")
             d_ref = oracle.shared_down(h_gpu[t:t + 1].contiguous(), sh["w_down"], 1, H, I, accumulate=False)
-            ref = (tail.float() + d_ref.float()).to(torch.bfloat16)
-            g, r = got["out"][t:t + 1].float(), ref.float()
-            ulp = lambda v: torch.exp2(torch.floor(torch.log2(v.abs().clamp_min(2.0 ** -126))) - 7)
-            bound = 2 * ulp(r) + 2 * ulp(tail.float()) + 2 * ulp(d_ref.float()) + 2e-3
-            assert not bool(((g - r).abs() > bound).any()), f"sequential out token {t}"
+            close(got["d"][t:t + 1], d_ref, f"d token {t}")
+    if not mode.startswith("two_branch"):
+        # ... and the add itself bit for bit, every token: pz(bf16(f32(tail) + f32(d)))
+        s = got["tail"].float() + got["d"].float()
+        ref = s.to(torch.bfloat16).view(torch.int16)
+        ref = torch.where(ref == -32768, torch.zeros_like(ref), ref)
+        assert torch.equal(got["out"].view(torch.int16), ref), f"{mode}: out != bf16(tail + d)"
