@@ -335,6 +335,22 @@ int moe_tail_take_device_error(unsigned int* bits);
  * launch fails. */
 int moe_tail_selftest_wait_timeout(unsigned int limit_us, void* stream);
 
+/* Failure-detection test hook (no counterpart on the pages): the limit of
+ * the operand-stage waits -- the GEMM kernels' tensor-core issuer waiting for
+ * a stage of weights and tokens, the staged expert-TP finalize kernel's
+ * threads waiting for a stage of route rows -- for calls made after it
+ * returns (process-wide), in nanoseconds (1: give up at the first such
+ * wait, whether or not the stage has landed); 0 restores the default (0.5 s).
+ * Only those waits change.  The waits that guard memory a CTA is about to
+ * release keep their full limit: the copies still in flight when a call
+ * aborts, and the tensor-core work issued before it, so an expired short wait
+ * aborts the call cleanly -- the kernel raises bit 1 of the device error word,
+ * issues nothing more, waits for what it started, frees its tensor memory and
+ * returns; that call's outputs are then undefined.  A limit shorter than a
+ * memory trip makes calls fail: it exists for tests of the abort path.
+ * Returns MOE_TAIL_EINVAL for a limit above 1 s. */
+int moe_tail_set_stage_wait_limit(unsigned long long limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

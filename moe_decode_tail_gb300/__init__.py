@@ -21,7 +21,7 @@ __all__ = [
     "moe_tail_latent_norm", "moe_tail_up_project", "WEIGHTS_STATIC", "INPUTS_READY",
     "moe_shared_gate_up", "moe_shared_down", "moe_tail_latent_up_flags", "moe_tail_ep_finalize_flags",
     "moe_tail_tp_finalize_flags", "moe_tail_set_kernel_form", "kernel_form", "FORM_EP", "FORM_TP", "FORM_LATENT",
-    "FORM_LATENT_ONE_KERNEL",
+    "FORM_LATENT_ONE_KERNEL", "moe_tail_set_stage_wait_limit",
 ]
 
 OK, EINVAL, ECUDA, ENOTSUP = 0, 1, 2, 3
@@ -74,11 +74,12 @@ def lib() -> ctypes.CDLL:
         L.moe_tail_status_str.restype = ctypes.c_char_p
         L.moe_tail_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         L.moe_tail_set_kernel_form.argtypes = [i32, i32]
+        L.moe_tail_set_stage_wait_limit.argtypes = [ctypes.c_ulonglong]
         for name in ("moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up", "moe_shared_expert",
                      "moe_tail_take_device_error", "moe_tail_latent_up_noalloc", "moe_tail_selftest_wait_timeout",
                      "moe_tail_latent_norm", "moe_tail_up_project", "moe_shared_gate_up", "moe_shared_down",
                      "moe_tail_latent_up_flags", "moe_tail_ep_finalize_flags", "moe_tail_tp_finalize_flags",
-                     "moe_tail_set_kernel_form"):
+                     "moe_tail_set_kernel_form", "moe_tail_set_stage_wait_limit"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -363,6 +364,13 @@ def moe_tail_set_kernel_form(call: int, form: int) -> None:
     the library's choice, see include/moe_tail.h).  Every form of a call gives
     the same bits; the setting is process-wide."""
     _check("moe_tail_set_kernel_form", lib().moe_tail_set_kernel_form(call, form))
+
+
+def moe_tail_set_stage_wait_limit(limit_ns: int) -> None:
+    """Failure-detection test hook: the operand-stage wait limit (ns) of the
+    GEMM and staged finalize kernels for later calls; 0 restores the default.
+    A limit shorter than a memory trip makes calls abort (device error bit 1)."""
+    _check("moe_tail_set_stage_wait_limit", lib().moe_tail_set_stage_wait_limit(limit_ns))
 
 
 class kernel_form:

@@ -75,13 +75,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase of the given parity to complete; false if the time limit ran out.
+// Wait for the phase of the given parity to complete; false if the time limit
+// ran out, or (given abort_flag) once another thread of the CTA has aborted.
+// A limit of 1 ns (the failure-detection tests' setting) gives up at once,
+// whether or not the phase has completed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          unsigned long long limit_ns = kWaitLimitNs) {
+                                          unsigned long long limit_ns = kWaitLimitNs,
+                                          volatile uint32_t* abort_flag = nullptr) {
+  if (limit_ns <= 1) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
-  while (!mbar_try_wait(bar, parity))
+  while (!mbar_try_wait(bar, parity)) {
+    if (abort_flag && *abort_flag) return false;
     if (global_ns() - t0 > limit_ns) return false;
+  }
   return true;
 }
 
@@ -501,8 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = pre; i < nk; ++i) {
         const int s = i % stages;
         const uint32_t round = (uint32_t)(i / stages);
-        if (!mbar_wait(L.empty + 8 * s, (round - 1u) & 1u)) {
-          raise_error(kErrWaitEmpty);
+        if (!mbar_wait(L.empty + 8 * s, (round - 1u) & 1u, kWaitLimitNs, abort_ptr)) {
+          if (!*abort_ptr) raise_error(kErrWaitEmpty);  // (else the MMA issuer aborted: stop issuing)
           *abort_ptr = 1;
           ok = false;
           break;
@@ -533,9 +540,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
       }
+      // the operand-stage wait (its limit can be shortened for failure-detection tests)
+      const unsigned long long stage_limit = a.stage_wait_ns ? a.stage_wait_ns : kWaitLimitNs;
       for (int i = 0; ok && i < nk; ++i) {
         const int s = i % stages;
-        if (!mbar_wait(L.full + 8 * s, (uint32_t)(i / stages) & 1u)) {
+        if (!mbar_wait(L.full + 8 * s, (uint32_t)(i / stages) & 1u, stage_limit)) {
           raise_error(kErrWaitFull);
           *abort_ptr = 1;
           break;
@@ -849,7 +858,9 @@ static cudaError_t launch_mode(const GemmPlan& p, const CUtensorMap& w0, const C
 }
 
 cudaError_t launch_decode_gemm(int mode, const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1,
-                               const CUtensorMap& x, const GemmArgs& a, bool pdl, cudaStream_t stream) {
+                               const CUtensorMap& x, const GemmArgs& args, bool pdl, cudaStream_t stream) {
+  GemmArgs a = args;
+  a.stage_wait_ns = stage_wait_limit_ns();
   switch (mode) {
     case kGemmUpShared: return launch_mode<kGemmUpShared>(p, w0, w1, x, a, pdl, stream);
     case kGemmGateUpSilu: return launch_mode<kGemmGateUpSilu>(p, w0, w1, x, a, pdl, stream);

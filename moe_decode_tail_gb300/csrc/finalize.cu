@@ -395,7 +395,9 @@ __global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const Fin
 // tracked by mbarriers.  Consumer thread v owns 16-byte vector v of the band.
 // A CTA finalizes tokens blockIdx.y, + gridDim.y, ... so the ring keeps
 // streaming across tokens.  Every wait is bounded; once a wait gives up, all
-// later waits return at once, so the kernel ends without skipping a barrier.
+// later waits return at once, so the kernel ends without skipping a barrier,
+// and the copies still in flight are waited for (with the full limit) before
+// the CTA's shared memory goes away.
 
 constexpr int kStagedMaxStages = 16;
 
@@ -427,12 +429,17 @@ __device__ __forceinline__ bool sb_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool sb_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
-  if (sb_try(bar, parity)) return true;
+// Wait for the phase of the given parity; false once the limit has passed --
+// the first wait to give up raises the abort flag and the error bit -- or at
+// once when the flag is already up.  A limit of 1 ns (the failure-detection
+// tests' setting) gives up at once, whether or not the phase has completed.
+__device__ __forceinline__ bool sb_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                        unsigned long long limit_ns = kWaitLimitNs) {
+  if (limit_ns > 1 && sb_try(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
-  while (!sb_try(bar, parity)) {
+  while (limit_ns <= 1 || !sb_try(bar, parity)) {
     if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (limit_ns <= 1 || global_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(&g_finalize_error, 1u);
       return false;
@@ -505,19 +512,22 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
   // consumers' order) into stage n % S.  Stage reuse waits until every warp
   // has released the stage; the issuer's own warp releases it first, and no
   // warp waits on the issuer before releasing, so this cannot deadlock.
+  // Once any wait has given up (the abort flag), nothing more is issued: the
+  // consumers' waits return at once from then on, and a consumer that gave up
+  // raised the flag before releasing its stage, so the flag is seen here
+  // after the release and a stage whose copy may still be in flight is never
+  // reissued.  The copies in flight are then exactly the last S issued, which
+  // the issuer waits for before the CTA ends.
   RouteCursor cur = {(int)blockIdx.y, 0};
   uint32_t issued = 0;
   auto issue_next = [&]() {
     int64_t j;
-    if (!next_route<LATENT>(a, cur, j)) return;
+    if (*abort_flag || !next_route<LATENT>(a, cur, j)) return;
     const int st = (int)(issued % (uint32_t)S);
-    if (issued >= (uint32_t)S) sb_wait(smem_addr(&sm.empty[st]), ((issued / S) - 1) & 1, abort_flag);
+    if (issued >= (uint32_t)S && !sb_wait(smem_addr(&sm.empty[st]), ((issued / S) - 1) & 1, abort_flag)) return;
+    if (*abort_flag) return;
     ++issued;
     const uint32_t bar = smem_addr(&sm.full[st]);
-    if (*abort_flag) {  // still complete the stage so that nobody waits for it
-      sb_arrive(bar);
-      return;
-    }
     sb_expect(bar, copy_bytes * (uint32_t)a.tp);
     if (copy_bytes) {
       const uint16_t* src = a.rows + j * a.P + col0;
@@ -543,6 +553,8 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
 
   uint32_t g = 0;  // stages consumed
   int pass = 0;
+  // the consumers' stage wait (its limit can be shortened for failure-detection tests)
+  const unsigned long long stage_limit = a.stage_wait_ns ? a.stage_wait_ns : kWaitLimitNs;
   for (int t = blockIdx.y; t < a.b; t += gridDim.y) {
     float2 acc[4];
 #pragma unroll
@@ -563,7 +575,7 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
         for (int k = 0; k < 4; ++k) xr[rr][k] = splat2(0.0f);
         if (has[rr]) {
           const int st = (int)(g % (uint32_t)S);
-          sb_wait(smem_addr(&sm.full[st]), (g / S) & 1, abort_flag);
+          sb_wait(smem_addr(&sm.full[st]), (g / S) & 1, abort_flag, stage_limit);
           ++g;
           if (g == 1) MOE_TRACE_MARK(0);  // first route's rows landed
           if (g == 4) MOE_TRACE_MARK(1);  // fourth route's rows landed
@@ -716,6 +728,7 @@ static cudaError_t launch_staged_t(const FinalizeArgs& a, int split, int groups,
 // slot) does not fit, so the caller can fall back to finalize_kernel.
 static cudaError_t launch_staged(int mode, const FinalizeArgs& args, bool wbn, int wmode, int sms, cudaStream_t stream) {
   FinalizeArgs a = args;
+  a.stage_wait_ns = stage_wait_limit_ns();
   a.chunks = (a.P + 255) / 256;
   // Bands per token: the fewest that keep a stage (one route's band rows in
   // every slot) within 32 KB, then more while the batch leaves over half of

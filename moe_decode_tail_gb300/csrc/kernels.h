@@ -37,6 +37,7 @@ struct FinalizeArgs {
   // 1: the inputs are complete before the preceding kernel of the stream ends,
   // so they are read before the grid dependency wait (out is written after it)
   int inputs_before_wait = 0;
+  unsigned long long stage_wait_ns = 0;  // the staged kernel's consumer wait limit (0: the default)
 };
 
 enum { kFinalizeEP = 0, kFinalizeTP = 1, kFinalizeLatent = 2 };
@@ -67,6 +68,7 @@ struct GemmArgs {
   float eps = 0.f, rcpK = 0.f;
   int chunks = 0;                    // 256-column chunks of K (at most 32)
   int inputs_before_wait = 0;        // latent and gamma complete before the preceding kernel ends
+  unsigned long long stage_wait_ns = 0;  // the MMA issuer's operand-stage wait limit (0: the default)
 };
 
 struct GemmPlan {
@@ -135,6 +137,10 @@ cudaError_t ensure_smem_limit(const void* kernel, int bytes);
 
 // Multiprocessors of the current device (cached per device).
 int device_sms();
+
+// The operand-stage wait limit set by moe_tail_set_stage_wait_limit (0: the
+// kernels' default), copied into each call's arguments.
+unsigned long long stage_wait_limit_ns();
 #ifdef MOE_TAIL_TRACE
 cudaError_t trace_attach_gemm(void* buf, unsigned cap);
 unsigned trace_count_gemm();

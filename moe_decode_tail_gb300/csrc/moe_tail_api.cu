@@ -24,6 +24,7 @@ namespace moetail {
 
 namespace {
 std::atomic<int> g_forms[kFormCalls];  // zero-initialised: the library's choice
+std::atomic<unsigned long long> g_stage_wait_ns{0};  // 0: the kernels' default limit
 
 int env_int(const char* name) {
   const char* v = getenv(name);
@@ -48,6 +49,8 @@ void env_plan(const char* name, int (&plan)[3]) {
 }  // namespace
 
 int kernel_form(int call) { return call >= 0 && call < kFormCalls ? g_forms[call].load(std::memory_order_relaxed) : 0; }
+
+unsigned long long stage_wait_limit_ns() { return g_stage_wait_ns.load(std::memory_order_relaxed); }
 
 const Tuning& tuning() {
   static const Tuning t = [] {
@@ -94,6 +97,12 @@ int device_sms() {
 }
 
 }  // namespace moetail
+
+MOE_API int moe_tail_set_stage_wait_limit(unsigned long long limit_ns) {
+  if (limit_ns > 1000000000ull) return MOE_TAIL_EINVAL;
+  moetail::g_stage_wait_ns.store(limit_ns, std::memory_order_relaxed);
+  return MOE_TAIL_OK;
+}
 
 MOE_API int moe_tail_set_kernel_form(int call, int form) {
   static const int kForms[moetail::kFormCalls] = {3, 3, 3};  // forms 0..2 of each call

@@ -1,7 +1,11 @@
 """Failure detection without a GPU fault: a kernel wait that expires is
 reported through the device error word and the context stays usable.  The
-expiry is produced by a barrier that nothing arrives at, with a 20 ms limit;
-nothing traps and nothing hangs."""
+expiry is produced two ways, and nothing traps and nothing hangs: a barrier
+that nothing arrives at, with a 20 ms limit (the self-test kernel); and the
+product kernels' own operand-stage waits cut to 1 ns, so that a GEMM and the
+staged expert-TP finalize take their abort paths (stop issuing, wait for
+their copies and tensor-core work in flight with the full limit, free tensor
+memory, return) -- after which the next normal call must be bit-exact."""
 import pytest
 import torch
 
@@ -50,4 +54,72 @@ def test_expired_wait_is_reported_and_the_device_stays_usable(mt):
                             gain_center=d["gain_center"], eps=d["eps"], weight_before_norm=d["weight_before_norm"])
     torch.cuda.synchronize()
     assert torch.equal(out.cpu().view(torch.int16), ref.view(torch.int16))
+    assert mt.moe_tail_take_device_error() == 0
+
+
+def test_stage_wait_limit_above_a_second_is_refused(mt):
+    # host-side checks only: nothing is launched
+    assert mt.lib().moe_tail_set_stage_wait_limit(1_000_000_001) == mt.EINVAL
+    assert mt.lib().moe_tail_set_stage_wait_limit(0) == mt.OK
+
+
+def _short_stage_wait_then_normal(mt, call):
+    """Run call() once with a 1 ns operand-stage wait (no stage of weights or
+    rows can land that fast, so the kernels abort), then with the default
+    limit; returns (error bits after the first run, the second run's output)."""
+    assert mt.moe_tail_take_device_error() == 0
+    mt.moe_tail_set_stage_wait_limit(1)
+    try:
+        call()
+        torch.cuda.synchronize()
+    finally:
+        mt.moe_tail_set_stage_wait_limit(0)
+    bits = mt.moe_tail_take_device_error()
+    out = call()
+    torch.cuda.synchronize()
+    return bits, out
+
+
+@pytest.mark.gpu
+def test_gemm_abort_path_raises_and_the_next_call_is_exact(mt):
+    # the up-projection GEMM (clusters of 8 CTAs splitting K): the tensor-core
+    # issuer's stage wait runs out, the CTA stops issuing, waits for its copies
+    # in flight and its issued work, frees its tensor memory and returns
+    b, L, H = 8, 1024, 1024
+    d = synth.latent_up_inputs(0xAB0, b=b, tp=2, tp_s=2, L=L, H=H)
+    y = d["latent"][0].contiguous().cuda()
+    w, sh = d["w_up"].cuda(), d["shared"].cuda()
+
+    def call():
+        out = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+        mt.moe_tail_up_project(y, w, sh, out)
+        return out
+
+    ref = call()
+    torch.cuda.synchronize()
+    bits, out = _short_stage_wait_then_normal(mt, call)
+    assert bits & 1, bits
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert mt.moe_tail_take_device_error() == 0
+
+
+@pytest.mark.gpu
+def test_staged_finalize_abort_path_raises_and_the_next_call_is_exact(mt, pin):
+    # the staged expert-TP finalize: its threads' stage wait runs out, nothing
+    # more is copied, and the copies in flight land before the CTA ends
+    pin(mt.FORM_TP, 1)
+    d = synth.config(3, b=64)
+    args = [d[k].cuda() for k in ("partials", "idx", "w", "gamma")]
+
+    def call():
+        out = torch.full((d["b"], d["P"]), float("nan"), dtype=torch.bfloat16, device="cuda")
+        mt.moe_tail_tp_finalize(*args, out, gain_center=d["gain_center"], eps=d["eps"],
+                                weight_before_norm=d["weight_before_norm"])
+        return out
+
+    ref = call()
+    torch.cuda.synchronize()
+    bits, out = _short_stage_wait_then_normal(mt, call)
+    assert bits & 1, bits
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert mt.moe_tail_take_device_error() == 0
