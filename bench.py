@@ -9,6 +9,10 @@ hot path, each call on its decode shape:
                         + shared partials [8, 64, 7168] -> out [64, 7168]
   4. shared expert      x [64, 7168]; W_gate, W_up [6144, 7168]; W_down [7168, 6144];
                         added into the latent tail's output
+By default (--composition two_branch_fused) 3 and 4 run on a side stream as
+the shared expert's gate/up, the latent norm, then one kernel streaming the
+down projection and the up-projection (moe_tail_up_project_shared_down); 1
+and 2 run beside them on a high-priority stream.
 Inputs are seeded and synthetic (random-init weights); every input is resident
 in device memory before timing.  A step touches about 390 MB, three times the
 L2, so every input is read cold without flushing.  Steps are replayed from a
@@ -42,7 +46,6 @@ NOMINAL_HBM_GBS = 8000.0  # the metric's nominal peak; fractions are also given 
 B = 64                    # decode tokens per step
 TP, P, K_ROUTES, E = 8, 4096, 8, 128
 L, H, I = 3584, 7168, 6144
-LAUNCHES_PER_STEP = 6     # b = 64: EP 1, TP 1, latent 2 (norm, up GEMM), shared 2 (gate/up, down)
 
 # Algorithmic bytes per call (reads + writes the method needs; intermediates
 # such as y and h that a fused kernel would keep on chip are not counted).
@@ -65,7 +68,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload isolated timings")
-    ap.add_argument("--composition", default="two_branch", choices=["two_branch", "two_branch_one_call", "latent_main"],
+    ap.add_argument("--composition", default="two_branch_fused",
+                    choices=["two_branch_fused", "two_branch", "two_branch_one_call", "latent_main"],
                     help="how the step orders the weight-streaming calls (see run_step)")
     ap.add_argument("--only-config", type=int, choices=[1, 2, 3, 4, 5], default=None,
                     help="run one workload's call alone --calls times and exit (for profiling the call)")
@@ -289,7 +293,7 @@ def run_step(mt, w, stream, events=None, side=None):
         rec(7, stream)
         shared_expert(stream, w["out"], True)
         return
-    comp = w.get("composition", "two_branch")
+    comp = w.get("composition", "two_branch_fused")
     if comp == "latent_main":
         # the latent tail on the finalize stream after EP and TP, beside the
         # shared expert's gate/up; the down projection then adds d into the
@@ -315,6 +319,30 @@ def run_step(mt, w, stream, events=None, side=None):
         rec(10, stream)
         mt.moe_shared_down(ws_h, w["w_down"], w["out"], accumulate=True, weights_static=True, stream=stream)
         rec(11, stream)
+        return
+    if comp == "two_branch_fused":
+        # the shared expert's gate/up, the latent norm, then the down projection
+        # and the up-projection in one kernel (d added after the shared partials)
+        bx = w["x"].shape[0]
+        ws_h = w["ws_sh"][: bx * I * 2].view(torch.bfloat16).view(bx, I)
+        w["fork"].record(stream)
+        side.wait_event(w["fork"])
+        rec(8, side)
+        mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], ws_h, weights_static=True, stream=side)
+        rec(9, side)
+        rec(4, side)
+        mt.moe_tail_latent_norm(w["latent"], w["lat_gamma"], w["y"], eps=1e-6, inputs_ready=True, stream=side)
+        rec(5, side)
+        rec(6, side)
+        mt.moe_tail_up_project_shared_down(w["y"], w["w_up"], w["shared"], ws_h, w["w_down"], w["out"],
+                                           weights_static=True, stream=side)
+        rec(7, side)
+        rec(10, side)
+        rec(11, side)
+        w["join"].record(side)
+        ep(stream)
+        tp(stream)
+        stream.wait_event(w["join"])
         return
     w["fork"].record(stream)
     side.wait_event(w["fork"])
@@ -343,22 +371,56 @@ def run_step(mt, w, stream, events=None, side=None):
 
 CALLS = ["ep_finalize", "tp_finalize", "latent_up", "shared_expert"]
 
+# The step's algorithmic bytes whatever its composition: every input read once
+# (EP rows, expert-TP partials, latent partials, W_up, shared partials, the
+# shared expert's weights and x, indices, weights, gains) and the three outputs
+# written once; no intermediate (y, h, d) counted.
+STEP_BYTES = (BYTES["ep_finalize"] + BYTES["tp_finalize"] + BYTES["latent_up"] + 3 * I * H * 2 + B * H * 2)
 
-def traffic_record():
-    """ncu DRAM bytes per launch of the shared-expert call, if the committed
-    profile was taken on the current kernel sources (else None)."""
+
+def step_calls(composition: str, side) -> dict:
+    """The calls of one step as the composition makes them: for each, the
+    (start, end) event pairs around it in an instrumented step, the bytes the
+    call itself moves (its inputs read once, its outputs written once,
+    intermediates it reads or writes included), its FLOPs and its launches."""
+    fin = {"ep_finalize": dict(pairs=[(0, 1)], bytes=BYTES["ep_finalize"], launches=1),
+           "tp_finalize": dict(pairs=[(2, 3)], bytes=BYTES["tp_finalize"], launches=1)}
+    if side is not None and composition == "two_branch_fused":
+        return dict(fin, **{
+            "shared_gate_up": dict(pairs=[(8, 9)], bytes=2 * I * H * 2 + B * H * 2 + B * I * 2,
+                                   flops=2 * B * 2 * I * H, launches=1),
+            "latent_norm": dict(pairs=[(4, 5)], bytes=TP * B * L * 2 + L * 2 + B * L * 2, launches=1),
+            "up_project_shared_down": dict(pairs=[(6, 7)],
+                                           bytes=H * I * 2 + H * L * 2 + B * I * 2 + B * L * 2 + TP * B * H * 2
+                                           + B * H * 2, flops=2 * B * H * (I + L), launches=1)})
+    d_slot = side is not None and composition in ("two_branch", "two_branch_one_call")  # d: a shared slot
+    return dict(fin, **{
+        "latent_up": dict(pairs=[(4, 5), (6, 7)], bytes=BYTES["latent_up"] + (B * H * 2 if d_slot else 0),
+                          flops=FLOPS["latent_up"], launches=2),
+        "shared_expert": dict(pairs=[(8, 9), (10, 11)],
+                              bytes=(3 * I * H * 2 + B * H * 2 + B * H * 2) if d_slot else BYTES["shared_expert"],
+                              flops=FLOPS["shared_expert"], launches=2)})
+
+
+def traffic_record(call: str):
+    """ncu DRAM bytes (read + write) of one call of the step, summed over its
+    launches, if the committed profile holds it and was taken on the current
+    kernel sources (else None).  File lines: 'sources_sha256 <hash>' and
+    'traffic <call> <bytes>'."""
     path = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
     if not os.path.exists(path):
         return None
-    rec = {}
+    sha, rec = None, {}
     for line in open(path):
         parts = line.split()
-        if len(parts) == 2:
-            rec[parts[0]] = parts[1]
-    if rec.get("sources_sha256") != kernel_sources_hash():
+        if len(parts) == 2 and parts[0] == "sources_sha256":
+            sha = parts[1]
+        elif len(parts) == 3 and parts[0] == "traffic":
+            rec[parts[1]] = parts[2]
+    if sha != kernel_sources_hash():
         return None
     try:
-        return int(rec["traffic_bytes_per_call"])
+        return int(rec[call])
     except (KeyError, ValueError):
         return None
 
@@ -619,40 +681,35 @@ def cuda_arm(args, world, rank, local):
     torch.cuda.synchronize()
 
     # per-call durations over the instrumented steps of that replay
-    per_call = {c: [] for c in CALLS}
-    pairs = {"ep_finalize": [(0, 1)], "tp_finalize": [(2, 3)], "latent_up": [(4, 5), (6, 7)],
-             "shared_expert": [(8, 9), (10, 11)]}
+    table = step_calls(args.composition, side)
+    per_call = {c: [] for c in table}
     for evs in inst_ev:
-        for c in CALLS:
-            per_call[c].append(sum(evs[i].elapsed_time(evs[j]) for i, j in pairs[c]) * 1e3)  # us
+        for c, t in table.items():
+            per_call[c].append(sum(evs[i].elapsed_time(evs[j]) for i, j in t["pairs"]) * 1e3)  # us
     calls = {}
     hbm, bf16_tf, peak_kind = peaks()
-    nbytes = dict(BYTES)
-    if side is not None and args.composition in ("two_branch", "two_branch_one_call"):  # d: a slot
-        nbytes["shared_expert"] = 3 * I * H * 2 + B * H * 2 + B * H * 2
-        nbytes["latent_up"] = BYTES["latent_up"] + B * H * 2
-    for c in CALLS:
+    for c, t in table.items():
         us = statistics.mean(per_call[c])
-        gbs = nbytes[c] / (us * 1e-6) / 1e9
-        calls[c] = {"us": round(us, 3), "tokens_per_s": B / (us * 1e-6), "algorithmic_bytes": nbytes[c],
+        gbs = t["bytes"] / (us * 1e-6) / 1e9
+        calls[c] = {"us": round(us, 3), "tokens_per_s": B / (us * 1e-6), "algorithmic_bytes": t["bytes"],
                     "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
-                    "hbm_frac_nominal": round(gbs / NOMINAL_HBM_GBS, 4)}
-        if c in FLOPS:
-            calls[c]["tflops"] = round(FLOPS[c] / (us * 1e-6) / 1e12, 2)
+                    "hbm_frac_nominal": round(gbs / NOMINAL_HBM_GBS, 4), "launches": t["launches"]}
+        if "flops" in t:
+            calls[c]["tflops"] = round(t["flops"] / (us * 1e-6) / 1e12, 2)
 
     # end to end through the public API from pinned host buffers
     e2e = e2e_leg(mt, w, stream, min(args.e2e_steps, K), dist, dev, side)
 
     if rank != 0:
         return 0
-    dom = max(CALLS, key=lambda c: calls[c]["us"])
-    traffic = traffic_record() if dom == "shared_expert" else None
+    dom = max(table, key=lambda c: calls[c]["us"])
     roof = {
-        "bound": "hbm", "kernel": f"moe_{dom}" if dom == "shared_expert" else f"moe_tail_{dom}",
-        "launches": 2 if dom in ("shared_expert", "latent_up") else 1,
+        "bound": "hbm", "kernel": f"moe_{dom}" if dom.startswith("shared") else f"moe_tail_{dom}",
+        "launches": table[dom]["launches"],
         "achieved": calls[dom]["achieved_gbs"], "peak": hbm, "unit": "GB/s",
-        "frac": round(calls[dom]["achieved_gbs"] / hbm, 4), "traffic": traffic,
-        "algorithmic_bytes_per_call": nbytes[dom], "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+        "frac": round(calls[dom]["achieved_gbs"] / hbm, 4), "traffic": traffic_record(dom),
+        "algorithmic_bytes_per_call": table[dom]["bytes"],
+        "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
         "note": "per-call CUDA events on the launch stream, recorded as graph nodes in every tenth step of a "
                 "replay made after the timed region (those steps lose the overlap between calls, so the per-call "
                 "figures are conservative; the timed replays carry no events)",
@@ -670,18 +727,24 @@ def cuda_arm(args, world, rank, local):
             if args.composition == "two_branch" else
             "two branches as two_branch, with the shared expert as one moe_shared_expert call"
             if args.composition == "two_branch_one_call" else
+            "two branches: on a side stream the shared expert's gate/up, the latent norm, then one kernel that "
+            "streams the down projection and the latent up-projection into two accumulators and adds bf16(d) "
+            "after the shared partials (moe_tail_up_project_shared_down); EP and TP on a high-priority stream "
+            "beside them"
+            if args.composition == "two_branch_fused" else
             "two branches: the shared expert's gate/up on a side stream; EP, TP and the latent tail on a "
             "high-priority stream beside it; then the down projection adds d into the latent tail's output")),
         "roofline": roof, "calls": calls, "e2e": e2e,
         "step_roofline": {
-            "algorithmic_bytes": sum(nbytes.values()),
-            "achieved_gbs": round(sum(nbytes.values()) / (max_s / K) / 1e9, 1),
+            "algorithmic_bytes": STEP_BYTES,
+            "achieved_gbs": round(STEP_BYTES / (max_s / K) / 1e9, 1),
             "peak": hbm, "unit": "GB/s",
-            "frac": round(sum(nbytes.values()) / (max_s / K) / 1e9 / hbm, 4),
-            "frac_nominal": round(sum(nbytes.values()) / (max_s / K) / 1e9 / NOMINAL_HBM_GBS, 4),
-            "note": "every call's algorithmic bytes per step over the step time: the whole step is an HBM stream",
+            "frac": round(STEP_BYTES / (max_s / K) / 1e9 / hbm, 4),
+            "frac_nominal": round(STEP_BYTES / (max_s / K) / 1e9 / NOMINAL_HBM_GBS, 4),
+            "note": "the step's algorithmic bytes (every input read once, the outputs written once, no "
+                    "intermediate) over the step time: the whole step is an HBM stream",
         },
-        "gpu_launches": LAUNCHES_PER_STEP * K, "clocks": clocks,
+        "gpu_launches": sum(t["launches"] for t in table.values()) * K, "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cpu)
@@ -983,7 +1046,7 @@ def step_by_batch(mt, w, dev, stream, side, sizes=(1, 8, 32, 128)) -> dict:
     res = {}
     for b in sizes:
         _, wb = make_workload(dev, b, weights=w)
-        wb["composition"] = w.get("composition", "two_branch")
+        wb["composition"] = w.get("composition", "two_branch_fused")
         with torch.cuda.stream(stream):
             for _ in range(3):
                 run_step(mt, wb, stream, side=side)

@@ -254,6 +254,35 @@ int moe_shared_down(const void* h, const void* w_down, int b, int H, int I, void
                     int flags, void* stream);
 
 /*
+ * The latent tail's up-projection with the shared expert's down projection
+ * in one kernel ([KT] module docstring: the shared expert's output joins the
+ * tail's shared partials before the up-projection's epilogue; [KS]
+ * SharedBase.push: the down projection is pushed as BF16, -0 made +0):
+ *   d   = h . w_down^T                     (FP32 accumulate)
+ *   u   = y . w_up^T                       (FP32 accumulate)
+ *   out = bf16( u + ( sum_s fp32(shared[s]) + fp32(bf16(d)) ) )
+ * with the shared partials added in slot order from +0 and bf16(d) last --
+ * the result of moe_shared_down (accumulate = 0) writing bf16(d) into one
+ * more shared slot, then moe_tail_up_project over tp_s + 1 slots, up to the
+ * K split of d (its FP32 sum may round differently).  Both weight streams go
+ * through one ring into two tensor-memory accumulators and share one
+ * epilogue, so the pair costs one kernel's ramp and tail instead of two.
+ *   y       BF16 [b][L] (moe_tail_latent_norm's output)
+ *   w_up    BF16 [H][L];  shared BF16 [tp_s][b][H] or NULL (tp_s = 0)
+ *   h       BF16 [b][I] (moe_shared_gate_up's output);  w_down BF16 [H][I]
+ *   out     BF16 [b][H] (written)
+ *   d_out   BF16 [b][H] receiving bf16(d), or NULL
+ *   flags   0, or MOE_TAIL_WEIGHTS_STATIC (w_up and w_down, as for
+ *           moe_tail_up_project: weight tiles requested before the kernel
+ *           waits for the stream's preceding kernel)
+ * Neither out nor d_out may overlap an input or each other.  Limits: those of
+ * moe_tail_up_project, plus 8 <= I <= 16777216, I % 8 == 0.
+ */
+int moe_tail_up_project_shared_down(const void* y, const void* w_up, const void* shared, int tp_s,
+                                    const void* h, const void* w_down, int b, int L, int I, int H,
+                                    void* out, void* d_out, int flags, void* stream);
+
+/*
  * Latent tail without a workspace (no counterpart on the pages: an addition
  * of this library).  Same computation and arguments as moe_tail_latent_up,
  * minus the workspace: for callers that cannot allocate device memory -- a

@@ -10,7 +10,8 @@
  *   ids = kernel id << 48 | SM id << 32 | linear CTA index
  *   kernel ids: 10 + mode route-parallel finalize (0 EP, 1 expert-TP, 2 latent norm),
  *               20 staged expert-TP finalize, 40 EP finalize (routes in registers),
- *               30 + mode decode GEMM (0 up-projection, 1 gate/up, 2 down)
+ *               30 + mode decode GEMM (0 up-projection, 1 gate/up, 2 down,
+ *               3 latent tail in one kernel, 4 down projection with the up-projection)
  *   GEMM marks: 0 accumulator complete, 1 partial tile staged, 2 first cluster
  *               barrier passed, 3 reduction and epilogue stores done (0 when the
  *               K range is not split); finalize kernels leave the marks at 0.

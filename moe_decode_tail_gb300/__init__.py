@@ -21,7 +21,7 @@ __all__ = [
     "moe_tail_latent_norm", "moe_tail_up_project", "WEIGHTS_STATIC", "INPUTS_READY",
     "moe_shared_gate_up", "moe_shared_down", "moe_tail_latent_up_flags", "moe_tail_ep_finalize_flags",
     "moe_tail_tp_finalize_flags", "moe_tail_set_kernel_form", "kernel_form", "FORM_EP", "FORM_TP", "FORM_LATENT",
-    "FORM_LATENT_ONE_KERNEL", "moe_tail_set_stage_wait_limit",
+    "FORM_LATENT_ONE_KERNEL", "moe_tail_set_stage_wait_limit", "moe_tail_up_project_shared_down",
 ]
 
 OK, EINVAL, ECUDA, ENOTSUP = 0, 1, 2, 3
@@ -75,11 +75,13 @@ def lib() -> ctypes.CDLL:
         L.moe_tail_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         L.moe_tail_set_kernel_form.argtypes = [i32, i32]
         L.moe_tail_set_stage_wait_limit.argtypes = [ctypes.c_ulonglong]
+        L.moe_tail_up_project_shared_down.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, P, P, i32, P]
         for name in ("moe_tail_ep_finalize", "moe_tail_tp_finalize", "moe_tail_latent_up", "moe_shared_expert",
                      "moe_tail_take_device_error", "moe_tail_latent_up_noalloc", "moe_tail_selftest_wait_timeout",
                      "moe_tail_latent_norm", "moe_tail_up_project", "moe_shared_gate_up", "moe_shared_down",
                      "moe_tail_latent_up_flags", "moe_tail_ep_finalize_flags", "moe_tail_tp_finalize_flags",
-                     "moe_tail_set_kernel_form", "moe_tail_set_stage_wait_limit"):
+                     "moe_tail_set_kernel_form", "moe_tail_set_stage_wait_limit",
+                     "moe_tail_up_project_shared_down"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -280,6 +282,32 @@ def moe_tail_up_project(y, w_up, shared, out, *, weights_static=False, stream=No
     _check("moe_tail_up_project", lib().moe_tail_up_project(
         _p(y), _p(w_up), _p(shared), tp_s, b, L, H, _p(out), WEIGHTS_STATIC if weights_static else 0,
         _stream(stream)))
+    return out
+
+
+def moe_tail_up_project_shared_down(y, w_up, shared, h, w_down, out, d_out=None, *, weights_static=False,
+                                    stream=None) -> torch.Tensor:
+    """The up-projection of y (BF16 [b, L]) with w_up (BF16 [H, L]) plus the
+    shared partials (BF16 [tp_s, b, H] or None) plus bf16(d), d the down
+    projection of h (BF16 [b, I]) with w_down (BF16 [H, I]), in one kernel,
+    into out (BF16 [b, H]); d_out (BF16 [b, H], optional) receives bf16(d)."""
+    b, L = _dims("y", y, 2)
+    H, _ = _dims("w_up", w_up, 2)
+    _, I = _dims("h", h, 2)
+    tp_s = 0 if shared is None else _dims("shared", shared, 3)[0]
+    _like("y", y, torch.bfloat16, (b, L))
+    _like("w_up", w_up, torch.bfloat16, (H, L))
+    if shared is not None:
+        _like("shared", shared, torch.bfloat16, (tp_s, b, H))
+    _like("h", h, torch.bfloat16, (b, I))
+    _like("w_down", w_down, torch.bfloat16, (H, I))
+    _like("out", out, torch.bfloat16, (b, H))
+    if d_out is not None:
+        _like("d_out", d_out, torch.bfloat16, (b, H))
+    _cuda(y, w_up, shared, h, w_down, out, d_out)
+    _check("moe_tail_up_project_shared_down", lib().moe_tail_up_project_shared_down(
+        _p(y), _p(w_up), _p(shared), tp_s, _p(h), _p(w_down), b, L, I, H, _p(out), _p(d_out),
+        WEIGHTS_STATIC if weights_static else 0, _stream(stream)))
     return out
 
 

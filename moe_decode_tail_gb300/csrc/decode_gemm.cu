@@ -242,17 +242,20 @@ __device__ __forceinline__ uint32_t kblock_owner(int kb, int kb_per, int kb_rem)
 template <int MODE, int N, int TM>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
-                       const __grid_constant__ CUtensorMap map_x, const GemmArgs a, const int stages) {
+                       const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_x1,
+                       const GemmArgs a, const int stages) {
   MOE_TRACE_SCOPE(30 + MODE);
   extern __shared__ uint8_t smem_raw[];
   constexpr bool kFused = MODE == kGemmLatentUp;
-  constexpr bool kUp = MODE == kGemmUpShared || kFused;  // out = bf16(acc + slot sum of shared)
+  constexpr bool kDU = MODE == kGemmDownUp;  // d and u into two accumulators, one epilogue
+  constexpr bool kUp = MODE == kGemmUpShared || kFused || kDU;  // out = bf16(acc + slot sum of shared)
   constexpr int kATile = TM * kBlockK * 2;
   constexpr int kBTileBytes = N * kBlockK * 2;
   constexpr int kStageBytes = kFused ? kATile : kATile + kBTileBytes;
   constexpr int kMmaM = TM == 64 ? 64 : 128;
   constexpr int kNumAcc = TM / kMmaM;
-  constexpr uint32_t kTmemCols = N * kNumAcc < 32 ? 32 : N * kNumAcc;
+  constexpr int kAccCols = N * kNumAcc;  // one accumulator's TMEM columns (the up-projection's at kAccCols)
+  constexpr uint32_t kTmemCols = (kDU ? 2 : 1) * kAccCols < 32 ? 32 : (kDU ? 2 : 1) * kAccCols;
   constexpr uint32_t kIdesc = idesc_bf16(kMmaM, N);
   constexpr int kOutRows = (MODE == kGemmGateUpSilu) ? TM / 2 : TM;  // output features per tile
 
@@ -261,10 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_tile = blockIdx.y;
   const int tok0 = blockIdx.z * N;
 
-  // K blocks of this CTA: an even split of the tile's K range over the cluster.
+  // K blocks of this CTA: an even split of the tile's K range over the cluster
+  // (down + up: each projection's K range split alike; the CTA streams its
+  // down blocks, then its up blocks, nk_all stages in all).
   const int kb_per = a.kblocks / (int)ksplit, kb_rem = a.kblocks % (int)ksplit;
   const int kb0 = (int)rank * kb_per + min((int)rank, kb_rem);
   const int nk = kb_per + ((int)rank < kb_rem ? 1 : 0);
+  const int kb2_per = kDU ? a.kblocks2 / (int)ksplit : 0, kb2_rem = kDU ? a.kblocks2 % (int)ksplit : 0;
+  const int kb02 = (int)rank * kb2_per + min((int)rank, kb2_rem);
+  const int nk2 = kDU ? kb2_per + ((int)rank < kb2_rem ? 1 : 0) : 0;
+  const int nk_all = nk + nk2;
 
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -305,8 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_ptr = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_w0);
-    if (MODE == kGemmGateUpSilu) prefetch_map(&map_w1);
+    if (MODE == kGemmGateUpSilu || kDU) prefetch_map(&map_w1);
     if (!kFused) prefetch_map(&map_x);
+    if (kDU) prefetch_map(&map_x1);
   }
   if (warp == 5) tmem_alloc(L.tmem_slot, kTmemCols);
   tc_fence_before();
@@ -330,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // depend on the accumulator, so the four epilogue warps gather it while the
   // K loop runs when each holds at most kPre items.
   constexpr int kPre = 4;
-  const bool has_addend = kUp ? a.shared != nullptr : (MODE == kGemmDown && a.accumulate != 0);
+  const bool has_addend = kDU || (kUp ? a.shared != nullptr : (MODE == kGemmDown && a.accumulate != 0));
   const bool pre = has_addend && n_items <= 128 * kPre;
   float4 pre_add[kPre];
   auto addend = [&](int item) -> float4 {
@@ -351,15 +361,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     return v;
   };
 
-  // Weight box of K block kb into stage st (two half-height boxes for gate/up).
-  auto load_weights = [&](uint32_t st, uint32_t bar, int kb, uint64_t policy) {
-    const int kx = kb * kBlockK;
+  // Weight box of the CTA's i-th K block into stage st (two half-height boxes
+  // for gate/up; down + up: the down projection's blocks, then the up-projection's).
+  auto load_weights = [&](uint32_t st, uint32_t bar, int i, uint64_t policy) {
     if (MODE == kGemmGateUpSilu) {
+      const int kx = (kb0 + i) * kBlockK;
       tma_load_2d(st, &map_w0, bar, kx, m_tile * (TM / 2), policy);
       tma_load_2d(st + kATile / 2, &map_w1, bar, kx, m_tile * (TM / 2), policy);
+    } else if (kDU && i >= nk) {
+      tma_load_2d(st, &map_w1, bar, (kb02 + i - nk) * kBlockK, m_tile * TM, policy);
     } else {
-      tma_load_2d(st, &map_w0, bar, kx, m_tile * TM, policy);
+      tma_load_2d(st, &map_w0, bar, (kb0 + i) * kBlockK, m_tile * TM, policy);
     }
+  };
+  // Token box of the CTA's i-th K block (h, then y for down + up).
+  auto load_tokens = [&](uint32_t st, uint32_t bar, int i, uint64_t policy) {
+    if (kDU && i >= nk) tma_load_2d(st + kATile, &map_x1, bar, (kb02 + i - nk) * kBlockK, tok0, policy);
+    else tma_load_2d(st + kATile, &map_x, bar, (kb0 + i) * kBlockK, tok0, policy);
   };
 
   // Fused mode, the four epilogue warps: y of the tile's tokens over this
@@ -489,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Inside the library's own kernel chains the weights never depend on the
       // preceding kernel, so the first ring's worth is requested before waiting
       // for it; the first kernel of a call waits first.
-      const int pre = min(nk, stages);
+      const int pre = min(nk_all, stages);
       if (!a.weights_before_wait) grid_dependency_wait();
       if (kFused && !mbar_wait(L.latbar, 0)) {  // the ring holds the latent rows until y's inputs are read
         raise_error(kErrWaitFull);
@@ -497,15 +515,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int i = 0; i < pre; ++i) {
         mbar_expect_tx(L.full + 8 * i, kStageBytes);
-        load_weights(L.ring + i * kStageBytes, L.full + 8 * i, kb0 + i, stream);
+        load_weights(L.ring + i * kStageBytes, L.full + 8 * i, i, stream);
       }
       if (!kFused) {  // the token tiles are the preceding kernel's output
         if (a.weights_before_wait) grid_dependency_wait();
-        for (int i = 0; i < pre; ++i)
-          tma_load_2d(L.ring + i * kStageBytes + kATile, &map_x, L.full + 8 * i, (kb0 + i) * kBlockK, tok0, keep);
+        for (int i = 0; i < pre; ++i) load_tokens(L.ring + i * kStageBytes, L.full + 8 * i, i, keep);
       }
       issued = pre;
-      for (int i = pre; i < nk; ++i) {
+      for (int i = pre; i < nk_all; ++i) {
         const int s = i % stages;
         const uint32_t round = (uint32_t)(i / stages);
         if (!mbar_wait(L.empty + 8 * s, (round - 1u) & 1u, kWaitLimitNs, abort_ptr)) {
@@ -517,8 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = L.ring + s * kStageBytes;
         const uint32_t bar = L.full + 8 * s;
         mbar_expect_tx(bar, kStageBytes);
-        load_weights(st, bar, kb0 + i, stream);
-        if (!kFused) tma_load_2d(st + kATile, &map_x, bar, (kb0 + i) * kBlockK, tok0, keep);
+        load_weights(st, bar, i, stream);
+        if (!kFused) load_tokens(st, bar, i, keep);
         ++issued;
       }
       if (!ok) {  // let the copies already in flight land before the CTA's memory goes away
@@ -542,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // the operand-stage wait (its limit can be shortened for failure-detection tests)
       const unsigned long long stage_limit = a.stage_wait_ns ? a.stage_wait_ns : kWaitLimitNs;
-      for (int i = 0; ok && i < nk; ++i) {
+      for (int i = 0; ok && i < nk_all; ++i) {
         const int s = i % stages;
         if (!mbar_wait(L.full + 8 * s, (uint32_t)(i / stages) & 1u, stage_limit)) {
           raise_error(kErrWaitFull);
@@ -553,12 +570,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = L.ring + s * kStageBytes;
         const uint64_t adesc = smem_desc_sw128(st);
         const uint64_t bdesc = smem_desc_sw128(kFused ? L.yop + (uint32_t)(i * kBTileBytes) : st + kATile);
+        // down + up: the up-projection's blocks accumulate into the second accumulator
+        const bool second = kDU && i >= nk;
+        const uint32_t dcol = second ? (uint32_t)kAccCols : 0u;
+        const int first_i = second ? nk : 0;
 #pragma unroll
         for (int kk = 0; kk < kBlockK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
 #pragma unroll
           for (int acc = 0; acc < kNumAcc; ++acc)  // accumulator acc: weight rows acc*128 .. +127
-            mma_bf16(tmem + (uint32_t)(acc * N), adesc + (uint64_t)(acc * (kMmaM * 128 >> 4)) + 2 * kk,
-                     bdesc + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16(tmem + dcol + (uint32_t)(acc * N), adesc + (uint64_t)(acc * (kMmaM * 128 >> 4)) + 2 * kk,
+                     bdesc + 2 * kk, kIdesc, (i > first_i || kk > 0) ? 1u : 0u);
         mma_commit(L.empty + 8 * s);
       }
       mma_commit(L.accum);  // also on abort: completes once the issued MMAs are done
@@ -596,23 +617,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_ptr = 1;
     }
     tc_fence_after();
-    float* stage = reinterpret_cast<float*>(base_ptr);
     const bool holds_row = kMmaM == 128 || lane < 16;
     const int row = kMmaM == 128 ? warp * 32 + lane : warp * 16 + lane;
-    for (int acc = 0; acc < kNumAcc; ++acc) {
-      const int r = acc * kMmaM + row;
-      if (got && nk > 0) {
+    // down + up: the second accumulator (u) is staged after the first (d)
+    for (int which = 0; which < (kDU ? 2 : 1); ++which) {
+      float* stage = reinterpret_cast<float*>(base_ptr) + which * N * TM;
+      const bool any = which == 0 ? nk > 0 : nk2 > 0;
+      for (int acc = 0; acc < kNumAcc; ++acc) {
+        const int r = acc * kMmaM + row;
+        if (got && any) {
 #pragma unroll 1
-        for (int c = 0; c < N; c += 16) {
-          float v[16];
-          tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * N + c), v);
-          if (holds_row) {
+          for (int c = 0; c < N; c += 16) {
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(which * kAccCols + acc * N + c), v);
+            if (holds_row) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) stage[(c + i) * TM + r] = v[i];
+              for (int i = 0; i < 16; ++i) stage[(c + i) * TM + r] = v[i];
+            }
           }
+        } else if (got && holds_row) {  // an empty K range contributes zeros
+          for (int c = 0; c < N; ++c) stage[c * TM + r] = 0.0f;
         }
-      } else if (got && holds_row) {  // an empty K range contributes zeros
-        for (int c = 0; c < N; ++c) stage[c * TM + r] = 0.0f;
       }
     }
     tc_fence_before();
@@ -636,8 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4 v = ld_cluster_v4(map_to_rank(off, p));
       acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
       acc.z = __fadd_rn(acc.z, v.z); acc.w = __fadd_rn(acc.w, v.w);
-      if (MODE == kGemmGateUpSilu) {
-        const float4 u = ld_cluster_v4(map_to_rank(off + (TM / 2) * 4, p));
+      if (MODE == kGemmGateUpSilu || kDU) {  // the up rows of the tile / the second partial tile
+        const float4 u = ld_cluster_v4(map_to_rank(off + (kDU ? N * TM * 4 : (TM / 2) * 4), p));
         acc2.x = __fadd_rn(acc2.x, u.x); acc2.y = __fadd_rn(acc2.y, u.y);
         acc2.z = __fadd_rn(acc2.z, u.z); acc2.w = __fadd_rn(acc2.w, u.w);
       }
@@ -656,7 +681,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = m_tile * kOutRows + 4 * q;
       if (n >= a.M) return;
       const float ad[4] = {add.x, add.y, add.z, add.w};
-      if (kUp) {  // out = bf16(acc + slot sum of the shared partials)
+      if (kDU) {  // d = acc rounded to BF16 joins the shared partials as their last slot; u = acc2
+        uint32_t db[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) db[e] = bf16_bits_pz(r[e]);
+        if (a.d_out != nullptr)
+          *reinterpret_cast<uint2*>(a.d_out + (int64_t)tg * a.M + n) =
+              make_uint2(db[0] | (db[1] << 16), db[2] | (db[3] << 16));
+        const float u[4] = {acc2.x, acc2.y, acc2.z, acc2.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) r[e] = __fadd_rn(u[e], __fadd_rn(ad[e], __uint_as_float(db[e] << 16)));
+      } else if (kUp) {  // out = bf16(acc + slot sum of the shared partials)
         if (has_addend) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) r[e] = __fadd_rn(r[e], ad[e]);
@@ -721,8 +756,9 @@ static int stage_bytes(int tm, int n_tile) { return tm * kBlockK * 2 + n_tile * 
 
 // Plan override for tuning (tm, ksplit, stages; read once from the environment).
 static bool plan_override(int mode, GemmPlan& p) {
-  if (mode < 0 || mode > 2) return false;
-  const int* v = tuning().gemm_plan[mode];
+  const int slot = mode == kGemmDownUp ? 3 : mode;
+  if (slot < 0 || slot > 3) return false;
+  const int* v = tuning().gemm_plan[slot];
   if (v[0] == 0) return false;
   p.tm = v[0];
   p.ksplit = v[1];
@@ -730,14 +766,16 @@ static bool plan_override(int mode, GemmPlan& p) {
   return true;
 }
 
-GemmPlan plan_gemm(int mode, int M, int K, int b, int sms) {
+GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
   GemmPlan p;
   p.n_tile = b <= 16 ? 16 : b <= 32 ? 32 : b <= 64 ? 64 : 128;
   const int tok_tiles = (b + p.n_tile - 1) / p.n_tile;
   const int kblocks = (K + kBlockK - 1) / kBlockK;
+  const int kblocks2 = (K2 + kBlockK - 1) / kBlockK;  // down + up: the up-projection's K blocks
   p.tm = 128;
   p.stages = 0;
   const bool forced = plan_override(mode, p);
+  if (mode == kGemmDownUp) p.tm = 128;  // the only tile height this mode is built for
   const int rows_per_tile = mode == kGemmGateUpSilu ? p.tm / 2 : p.tm;
   p.m_tiles = (M + rows_per_tile - 1) / rows_per_tile;
   if (!forced) {  // K split over a cluster: about two CTAs per SM
@@ -750,6 +788,7 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms) {
     p.ksplit = std::max(1, std::min(ks, 8));
   }
   p.ksplit = std::min(p.ksplit, kblocks);
+  if (mode == kGemmDownUp && kblocks2 > 0) p.ksplit = std::min(p.ksplit, kblocks2);
   const int sb = stage_bytes(p.tm, p.n_tile);
   // Ring budget 72 KB at TM <= 128 (3 stages at b = 64): two GEMM CTAs then
   // leave room on their SM for one finalize CTA of a concurrent stream (up to
@@ -758,12 +797,17 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms) {
   // The up-projection ends the step, after the finalize kernels, and takes a
   // 96 KB ring (4 stages at b = 64: 71.4 -> 70.3 us per step with the down
   // projection's split above).
+  // The down + up kernel takes 72 KB as well: in a decode step it runs while
+  // the expert-TP finalize still holds SMs, and two of its CTAs beside one
+  // finalize CTA fit an SM only at this size (b = 64: 63.3 vs 66.9 us per
+  // step with 96 KB, whose second CTA waits for the finalize to end).
   const int budget = p.tm == 256 ? 200 * 1024 : (mode == kGemmUpShared ? 96 * 1024 : 72 * 1024);
   if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, budget / sb));
-  const int per_cta = (kblocks + p.ksplit - 1) / p.ksplit;
+  const int per_cta = (kblocks + p.ksplit - 1) / p.ksplit + (kblocks2 + p.ksplit - 1) / p.ksplit;
   p.stages = std::min(p.stages, std::max(2, per_cta));
-  // the FP32 staging tile reuses the ring
-  while (p.stages * sb < p.n_tile * p.tm * 4) ++p.stages;
+  // the FP32 staging tile (down + up: two of them) reuses the ring
+  const int tiles = mode == kGemmDownUp ? 2 : 1;
+  while (p.stages * sb < tiles * p.n_tile * p.tm * 4) ++p.stages;
   return p;
 }
 
@@ -789,7 +833,7 @@ constexpr size_t kFusedSmemCap = 112 * 1024;
 bool plan_latent_fused(int H, int L, int b, int tp, int sms, GemmPlan* plan) {
   const int chunks = (L + 255) / 256;
   if (b < 1 || b > 32 || chunks > 32 || tp < 1) return false;
-  GemmPlan p = plan_gemm(kGemmUpShared, H, L, b, sms);  // the two-kernel tiles and K split
+  GemmPlan p = plan_gemm(kGemmUpShared, H, L, b, sms, 0);  // the two-kernel tiles and K split
   if (p.tm != 128 || p.n_tile > 32) return false;
   const int kblocks = (L + kBlockK - 1) / kBlockK;
   const size_t fixed = fused_fixed_bytes(p.n_tile, kblocks, p.ksplit, chunks);
@@ -807,7 +851,7 @@ bool plan_latent_fused(int H, int L, int b, int tp, int sms, GemmPlan* plan) {
 
 template <int MODE, int N, int TM>
 static cudaError_t launch_t(const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& x,
-                            const GemmArgs& a, bool pdl, cudaStream_t stream) {
+                            const CUtensorMap& x1, const GemmArgs& a, bool pdl, cudaStream_t stream) {
   auto kernel = decode_gemm_kernel<MODE, N, TM>;
   const size_t smem = smem_bytes(p, MODE, a);
   // Raise the kernel's shared-memory limit once per device (not per call, so
@@ -834,17 +878,18 @@ static cudaError_t launch_t(const GemmPlan& p, const CUtensorMap& w0, const CUte
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kernel, w0, w1, x, a, p.stages);
+  return cudaLaunchKernelEx(&cfg, kernel, w0, w1, x, x1, a, p.stages);
 }
 
 template <int MODE, int TM>
 static cudaError_t launch_n(const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1,
-                            const CUtensorMap& x, const GemmArgs& a, bool pdl, cudaStream_t stream) {
+                            const CUtensorMap& x, const CUtensorMap& x1, const GemmArgs& a, bool pdl,
+                            cudaStream_t stream) {
   switch (p.n_tile) {
-    case 16: return launch_t<MODE, 16, TM>(p, w0, w1, x, a, pdl, stream);
-    case 32: return launch_t<MODE, 32, TM>(p, w0, w1, x, a, pdl, stream);
-    case 64: return launch_t<MODE, 64, TM>(p, w0, w1, x, a, pdl, stream);
-    case 128: return launch_t<MODE, 128, TM>(p, w0, w1, x, a, pdl, stream);
+    case 16: return launch_t<MODE, 16, TM>(p, w0, w1, x, x1, a, pdl, stream);
+    case 32: return launch_t<MODE, 32, TM>(p, w0, w1, x, x1, a, pdl, stream);
+    case 64: return launch_t<MODE, 64, TM>(p, w0, w1, x, x1, a, pdl, stream);
+    case 128: return launch_t<MODE, 128, TM>(p, w0, w1, x, x1, a, pdl, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -852,13 +897,14 @@ static cudaError_t launch_n(const GemmPlan& p, const CUtensorMap& w0, const CUte
 template <int MODE>
 static cudaError_t launch_mode(const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1,
                                const CUtensorMap& x, const GemmArgs& a, bool pdl, cudaStream_t stream) {
-  if (p.tm == 256) return launch_n<MODE, 256>(p, w0, w1, x, a, pdl, stream);
-  return p.tm == 128 ? launch_n<MODE, 128>(p, w0, w1, x, a, pdl, stream)
-                     : launch_n<MODE, 64>(p, w0, w1, x, a, pdl, stream);
+  if (p.tm == 256) return launch_n<MODE, 256>(p, w0, w1, x, x, a, pdl, stream);
+  return p.tm == 128 ? launch_n<MODE, 128>(p, w0, w1, x, x, a, pdl, stream)
+                     : launch_n<MODE, 64>(p, w0, w1, x, x, a, pdl, stream);
 }
 
 cudaError_t launch_decode_gemm(int mode, const GemmPlan& p, const CUtensorMap& w0, const CUtensorMap& w1,
-                               const CUtensorMap& x, const GemmArgs& args, bool pdl, cudaStream_t stream) {
+                               const CUtensorMap& x, const GemmArgs& args, bool pdl, cudaStream_t stream,
+                               const CUtensorMap* x1) {
   GemmArgs a = args;
   a.stage_wait_ns = stage_wait_limit_ns();
   switch (mode) {
@@ -867,9 +913,12 @@ cudaError_t launch_decode_gemm(int mode, const GemmPlan& p, const CUtensorMap& w
     case kGemmDown: return launch_mode<kGemmDown>(p, w0, w1, x, a, pdl, stream);
     case kGemmLatentUp:  // built for the small batches plan_latent_fused admits
       if (p.tm != 128 || a.chunks < 1 || a.chunks > 32) return cudaErrorInvalidValue;
-      if (p.n_tile == 16) return launch_t<kGemmLatentUp, 16, 128>(p, w0, w1, x, a, pdl, stream);
-      if (p.n_tile == 32) return launch_t<kGemmLatentUp, 32, 128>(p, w0, w1, x, a, pdl, stream);
+      if (p.n_tile == 16) return launch_t<kGemmLatentUp, 16, 128>(p, w0, w1, x, x, a, pdl, stream);
+      if (p.n_tile == 32) return launch_t<kGemmLatentUp, 32, 128>(p, w0, w1, x, x, a, pdl, stream);
       return cudaErrorInvalidValue;
+    case kGemmDownUp:  // tm = 128 only; x1 is the up-projection's token map (y)
+      if (p.tm != 128 || x1 == nullptr || a.kblocks2 < 1) return cudaErrorInvalidValue;
+      return launch_n<kGemmDownUp, 128>(p, w0, w1, x, *x1, a, pdl, stream);
     default: return cudaErrorInvalidValue;
   }
 }

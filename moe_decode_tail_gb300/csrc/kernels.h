@@ -48,7 +48,7 @@ cudaError_t take_finalize_error(unsigned* bits);
 
 // ---- decode GEMM (tcgen05) ---------------------------------------------------
 
-enum GemmMode { kGemmUpShared = 0, kGemmGateUpSilu = 1, kGemmDown = 2, kGemmLatentUp = 3 };
+enum GemmMode { kGemmUpShared = 0, kGemmGateUpSilu = 1, kGemmDown = 2, kGemmLatentUp = 3, kGemmDownUp = 4 };
 
 struct GemmArgs {
   int M;             // output features of one weight (rows of W; gate/up: I)
@@ -69,6 +69,13 @@ struct GemmArgs {
   int chunks = 0;                    // 256-column chunks of K (at most 32)
   int inputs_before_wait = 0;        // latent and gamma complete before the preceding kernel ends
   unsigned long long stage_wait_ns = 0;  // the MMA issuer's operand-stage wait limit (0: the default)
+  // mode 4 (the shared expert's down projection and the up-projection in one
+  // kernel): M, K, kblocks, map_w0 and map_x describe the down projection
+  // (W_down [M][K], h [n_tok][K]); K2, kblocks2, map_w1 and map_x1 the
+  // up-projection (W_up [M][K2], y [n_tok][K2]); out = bf16(u + (sum_s shared[s]
+  // + bf16(d))), and d_out (BF16 [n_tok][M], or null) receives bf16(d)
+  int K2 = 0, kblocks2 = 0;
+  uint16_t* d_out = nullptr;
 };
 
 struct GemmPlan {
@@ -79,7 +86,8 @@ struct GemmPlan {
   int m_tiles;  // CTAs clusters along M
 };
 
-GemmPlan plan_gemm(int mode, int M, int K, int b, int sms);
+// K2: the up-projection's reduction length in mode kGemmDownUp (0 otherwise).
+GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2 = 0);
 // The one-kernel latent tail's plan at b tokens and tp slots: the
 // up-projection's tiles and K split (so the product is bit for bit the
 // two-kernel one) and a ring that fits beside the CTA's y operand and can
@@ -88,7 +96,8 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms);
 // override with other tiles, too little shared memory).
 bool plan_latent_fused(int H, int L, int b, int tp, int sms, GemmPlan* plan);
 cudaError_t launch_decode_gemm(int mode, const GemmPlan& plan, const CUtensorMap& w0, const CUtensorMap& w1,
-                               const CUtensorMap& x, const GemmArgs& a, bool pdl, cudaStream_t stream);
+                               const CUtensorMap& x, const GemmArgs& a, bool pdl, cudaStream_t stream,
+                               const CUtensorMap* x1 = nullptr);
 
 // The latent tail's two steps, shared by its entry points (arguments already
 // checked; enqueue_up_project returns a moe_tail status).
@@ -127,7 +136,7 @@ struct Tuning {
   int fin_ring_kb;       // MOE_TAIL_FIN_RING_KB: staged finalize ring budget (KB)
   int fin_groups;        // MOE_TAIL_FIN_GROUPS: staged finalize CTAs along the tokens
   int fin_routes;        // MOE_TAIL_FIN_ROUTES: route-parallel finalize routes per pass
-  int gemm_plan[3][3];   // MOE_TAIL_GEMM_PLAN_<UP|GATEUP|DOWN> = "tm,ksplit,stages"
+  int gemm_plan[4][3];   // MOE_TAIL_GEMM_PLAN_<UP|GATEUP|DOWN|DOWNUP> = "tm,ksplit,stages"
 };
 const Tuning& tuning();
 

@@ -64,6 +64,7 @@ const Tuning& tuning() {
     env_plan("MOE_TAIL_GEMM_PLAN_UP", r.gemm_plan[0]);
     env_plan("MOE_TAIL_GEMM_PLAN_GATEUP", r.gemm_plan[1]);
     env_plan("MOE_TAIL_GEMM_PLAN_DOWN", r.gemm_plan[2]);
+    env_plan("MOE_TAIL_GEMM_PLAN_DOWNUP", r.gemm_plan[3]);
     return r;
   }();
   return t;
@@ -455,6 +456,48 @@ MOE_API int moe_tail_up_project(const void* y, const void* w_up, const void* sha
     return MOE_TAIL_EINVAL;
   return enqueue_up_project(y, w_up, shared, tp_s, b, L, H, out, (flags & MOE_TAIL_WEIGHTS_STATIC) != 0,
                             static_cast<cudaStream_t>(stream));
+}
+
+MOE_API int moe_tail_up_project_shared_down(const void* y, const void* w_up, const void* shared, int tp_s,
+                                            const void* h, const void* w_down, int b, int L, int I, int H,
+                                            void* out, void* d_out, int flags, void* stream) {
+  if (!up_sizes_ok(b, tp_s, L, H) || I < 8 || I % 8 || I > kMaxWidth || (flags & ~MOE_TAIL_WEIGHTS_STATIC))
+    return MOE_TAIL_EINVAL;
+  if (b == 0) return MOE_TAIL_OK;
+  if (!y || !w_up || !h || !w_down || !out) return MOE_TAIL_EINVAL;
+  if ((tp_s > 0) != (shared != nullptr)) return MOE_TAIL_EINVAL;
+  if (!aligned(y, 16) || !aligned(w_up, 16) || !aligned(h, 16) || !aligned(w_down, 16) || !aligned(out, 16) ||
+      (shared && !aligned(shared, 16)) || (d_out && !aligned(d_out, 16)))
+    return MOE_TAIL_EINVAL;
+  const Range o = span(out, (size_t)b * H * 2), dr = span(d_out, (size_t)b * H * 2);
+  const Range ins[5] = {span(y, (size_t)b * L * 2), span(w_up, (size_t)H * L * 2),
+                        span(shared, (size_t)tp_s * b * H * 2), span(h, (size_t)b * I * 2),
+                        span(w_down, (size_t)H * I * 2)};
+  if (overlaps(o, dr)) return MOE_TAIL_EINVAL;
+  for (const Range& r : ins)
+    if (overlaps(o, r) || overlaps(dr, r)) return MOE_TAIL_EINVAL;
+  const GemmPlan plan = moetail::plan_gemm(moetail::kGemmDownUp, H, I, b, device_sms(), L);
+  CUtensorMap md, mh, mu, my;
+  if (!encode_bf16_2d(&md, w_down, H, I, plan.tm, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&mh, h, b, I, plan.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
+      !encode_bf16_2d(&mu, w_up, H, L, plan.tm, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&my, y, b, L, plan.n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+    return MOE_TAIL_ECUDA;
+  GemmArgs g;
+  g.M = H;
+  g.K = I;
+  g.n_tok = b;
+  g.kblocks = (I + 63) / 64;
+  g.K2 = L;
+  g.kblocks2 = (L + 63) / 64;
+  g.shared = static_cast<const uint16_t*>(shared);
+  g.tp_s = tp_s;
+  g.out = static_cast<uint16_t*>(out);
+  g.d_out = static_cast<uint16_t*>(d_out);
+  g.accumulate = 0;
+  g.weights_before_wait = (flags & MOE_TAIL_WEIGHTS_STATIC) ? 1 : 0;
+  return finish(moetail::launch_decode_gemm(moetail::kGemmDownUp, plan, md, mu, mh, g, true,
+                                            static_cast<cudaStream_t>(stream), &my));
 }
 
 // ============================================================================ shared expert

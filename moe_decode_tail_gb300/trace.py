@@ -20,7 +20,7 @@ import torch
 
 KERNELS = {10: "ep_finalize (route-parallel)", 11: "tp_finalize (route-parallel)", 12: "latent_norm",
            20: "tp_finalize (staged)", 21: "latent_norm (staged)", 30: "up-projection GEMM", 31: "gate/up GEMM",
-           32: "down GEMM", 33: "latent tail (one kernel)", 40: "ep_finalize"}
+           32: "down GEMM", 33: "latent tail (one kernel)", 34: "down + up-projection GEMM", 40: "ep_finalize"}
 
 
 class Tracer:
@@ -80,7 +80,7 @@ def describe(group: list[tuple[int, int, list]]) -> list[str]:
         elif kid in (20, 21) and all(r[4][2] and r[4][3] for r in rs):  # staged finalize, first pass
             line += (f"  first rows p50 {p50(lambda r: r[4][0] - r[3]):5.1f}  pass consumed "
                      f"{p50(lambda r: r[4][2] - r[3]):5.1f}  after cluster barrier {p50(lambda r: r[4][3] - r[3]):5.1f}")
-        elif kid in (30, 31, 32) and all(r[4][0] for r in rs):
+        elif kid in (30, 31, 32, 34) and all(r[4][0] for r in rs):
             line += f"  K loop p50 {p50(lambda r: r[4][0] - r[3]):5.1f}"
             if all(r[4][3] for r in rs):
                 line += (f"  epilogue: stage {p50(lambda r: r[4][1] - r[4][0]):.1f}"

@@ -454,3 +454,36 @@ def test_floor_calls_refuse_bad_shapes_before_launching():
     # valid shapes pass the checks and then fail at the launch without a GPU
     assert fl.moe_tail_floor_empty(2, 64, 256, 2, None) == 2
     assert fl.moe_tail_floor_read(ok, 4096, 2, 1, 32, 1, ok, None) == 2
+
+
+def up_sd(lib, **kw):
+    args = dict(y=a(), w=a(1 << 28), sh=a(2 << 28), tp_s=8, h=a(3 << 28), wd=a(4 << 28), b=64, L=3584, I=6144,
+                H=7168, out=a(5 << 28), d=a(6 << 28), flags=1, stream=None)
+    args.update(kw)
+    lib.moe_tail_up_project_shared_down.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] + [ctypes.c_void_p] * 2 + \
+        [ctypes.c_int] * 4 + [ctypes.c_void_p] * 2 + [ctypes.c_int, ctypes.c_void_p]
+    return lib.moe_tail_up_project_shared_down(args["y"], args["w"], args["sh"], args["tp_s"], args["h"], args["wd"],
+                                               args["b"], args["L"], args["I"], args["H"], args["out"], args["d"],
+                                               args["flags"], args["stream"])
+
+
+@host_only
+@pytest.mark.parametrize("bad", [
+    dict(tp_s=-1), dict(tp_s=33), dict(L=3583), dict(I=6140), dict(I=4), dict(I=(1 << 24) + 8), dict(H=7170),
+    dict(H=4), dict(b=-2), dict(b=65536), dict(sh=None), dict(tp_s=0), dict(y=None), dict(w=None), dict(h=None),
+    dict(wd=None), dict(out=None), dict(flags=2), dict(flags=-1), dict(out=a(8)), dict(d=a(8)), dict(h=a(4)),
+    dict(out=a(2 << 28)), dict(out=a(16)), dict(out=a(3 << 28)), dict(out=a(4 << 28)),  # out over shared, y, h, w_down
+    dict(d=a(1 << 28)), dict(d=a(3 << 28)), dict(d=a(5 << 28)),  # d over w_up, h, out
+])
+def test_up_project_shared_down_refuses_bad_arguments(lib, bad):
+    assert up_sd(lib, **bad) == EINVAL
+
+
+@host_only
+def test_up_project_shared_down_accepts_its_defaults_and_b_zero(lib):
+    # the defaults pass every check (then fail at the first CUDA call without a
+    # GPU); b = 0 succeeds with null pointers; no shared partials and no d_out
+    # are both allowed
+    assert up_sd(lib) in (2, 3)
+    assert up_sd(lib, sh=None, tp_s=0, d=None) in (2, 3)
+    assert up_sd(lib, b=0, y=None, w=None, sh=None, tp_s=0, h=None, wd=None, out=None, d=None) == OK

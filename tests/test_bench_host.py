@@ -26,7 +26,7 @@ def test_defaults_keep_the_timing_contract(bench, monkeypatch):
     monkeypatch.setattr(sys, "argv", ["bench.py"])
     a = bench.parse_args()
     assert a.gpus == 1 and a.impl == "cuda" and a.warmup >= 3 and a.steps >= 1000
-    assert a.composition == "two_branch" and not a.sequential
+    assert a.composition == "two_branch_fused" and not a.sequential
 
 
 def test_packed_layout_of_the_step_inputs(bench):
@@ -90,14 +90,34 @@ def test_cuda_arm_refuses_to_run_without_a_device():
 def test_traffic_is_reported_only_for_the_sources_it_was_measured_on(bench, monkeypatch, tmp_path):
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "roofline_traffic.txt").write_text(
-        "# comment lines are skipped\nsources_sha256 abc123\ntraffic_bytes_per_call 270426112\n")
+        "# comment lines are skipped\nsources_sha256 abc123\ntraffic shared_expert 270426112\n"
+        "traffic shared_gate_up 181474560\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "kernel_sources_hash", lambda: "abc123")
-    assert bench.traffic_record() == 270426112
+    assert bench.traffic_record("shared_expert") == 270426112
+    assert bench.traffic_record("shared_gate_up") == 181474560
+    assert bench.traffic_record("latent_up") is None  # not profiled
     monkeypatch.setattr(bench, "kernel_sources_hash", lambda: "changed")
-    assert bench.traffic_record() is None
+    assert bench.traffic_record("shared_expert") is None
     (tmp_path / "profiles" / "roofline_traffic.txt").unlink()
-    assert bench.traffic_record() is None
+    assert bench.traffic_record("shared_expert") is None
+
+
+def test_step_call_tables_cover_each_composition(bench):
+    # every composition's calls: event pairs inside the 12 per-step events, positive
+    # bytes, and launches adding up to the step's kernel count
+    side = object()
+    for comp, launches in (("two_branch", 6), ("two_branch_one_call", 6), ("latent_main", 6),
+                           ("two_branch_fused", 5)):
+        t = bench.step_calls(comp, side)
+        assert all(0 <= i < j < bench.EVENTS_PER_STEP for c in t.values() for i, j in c["pairs"])
+        assert all(c["bytes"] > 0 for c in t.values())
+        assert sum(c["launches"] for c in t.values()) == launches, comp
+    assert sum(c["launches"] for c in bench.step_calls("two_branch", None).values()) == 6  # sequential
+    # the step's algorithmic bytes: the sequential step's per-call figures minus
+    # the shared expert's read and second write of out (367,309,824 at b = 64)
+    seq = bench.step_calls("two_branch", None)
+    assert bench.STEP_BYTES == sum(c["bytes"] for c in seq.values()) - 2 * bench.B * bench.H * 2 == 367_309_824
 
 
 def test_kernel_sources_hash_covers_the_gemm_sources(bench):

@@ -4,7 +4,8 @@ compute-sanitizer is closed on this machine, so out-of-range writes are caught
 with canaries: each output and workspace is carved out of a larger buffer
 whose 4 KB before and after hold a sentinel byte, the call runs at ragged
 sizes (widths not multiples of a tile, odd token counts, more than one K
-split, both finalize kernels, both latent-tail forms), and the sentinel bytes
+split, both finalize kernels, both latent-tail forms, the up-projection with
+the shared down projection), and the sentinel bytes
 must be unchanged afterwards.  The values themselves are checked by the
 parity tests."""
 import math
@@ -126,4 +127,18 @@ def test_shared_expert_calls(mt, kw):
     mt.moe_shared_gate_up(x, wg, wu, h.t, weights_static=True)
     mt.moe_shared_down(h.t, wd, out2.t, accumulate=False, weights_static=True)
     assert all(g.intact() for g in (out, ws, h, out2))
+    assert mt.moe_tail_take_device_error() == 0
+
+
+@pytest.mark.parametrize("kw", [dict(b=37, L=264, I=200, H=136, tp_s=3), dict(b=5, L=1000, I=520, H=392, tp_s=0)])
+def test_up_project_shared_down(mt, kw):
+    b, L, I, H, tp_s = kw["b"], kw["L"], kw["I"], kw["H"], kw["tp_s"]
+    g = lambda *shape: (0.5 * torch.randn(*shape, device=DEV)).to(torch.bfloat16)
+    y, w_up, h, w_down = g(b, L), g(H, L), g(b, I), g(H, I)
+    shared = g(tp_s, b, H) if tp_s else None
+    out, d = Guarded((b, H)), Guarded((b, H))
+    mt.moe_tail_up_project_shared_down(y, w_up, shared, h, w_down, out.t, d.t, weights_static=True)
+    out2 = Guarded((b, H))
+    mt.moe_tail_up_project_shared_down(y, w_up, shared, h, w_down, out2.t)
+    assert out.intact() and d.intact() and out2.intact()
     assert mt.moe_tail_take_device_error() == 0

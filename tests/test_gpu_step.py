@@ -1,6 +1,8 @@
 """The composed decode step exactly as bench.py times it (two branches: the
 shared expert -- as its two calls, or as one -- then the latent tail on a
-side stream, EP and expert-TP finalize beside them; and the sequential
+side stream, EP and expert-TP finalize beside them, or on the side stream
+the shared expert's gate/up, the latent norm and then the down projection
+with the up-projection in one kernel; and the sequential
 composition, where the shared
 expert accumulates into the latent tail's output; and latent_main, where the
 latent tail runs beside the shared expert's gate/up and the down projection
@@ -32,7 +34,8 @@ def close(got, ref, what):
     assert not bool(bad.any()), f"{what}: {int(bad.sum())} of {bad.numel()} out of tolerance"
 
 
-@pytest.fixture(scope="module", params=["two_branch", "two_branch_one_call", "sequential", "latent_main"])
+@pytest.fixture(scope="module", params=["two_branch", "two_branch_one_call", "sequential", "latent_main",
+                                        "two_branch_fused"])
 def step(request):
     from moe_decode_tail_gb300 import build as cuda_build
 
@@ -72,6 +75,16 @@ def step(request):
         mt.moe_shared_down(w["ws_sh"][: B * I * 2].view(torch.bfloat16).view(B, I), w["w_down"], d, accumulate=False)
         torch.cuda.synchronize()
         got["tail"], got["d"] = tail.cpu(), d.cpu()
+    if request.param == "two_branch_fused":
+        # the fused call again, with its optional d output: the same out, and d
+        B, I = bench.B, bench.I
+        again = torch.full_like(w["out"], float("nan"))
+        d = torch.full_like(w["out"], float("nan"))
+        mt.moe_tail_up_project_shared_down(w["y"], w["w_up"], w["shared"],
+                                           w["ws_sh"][: B * I * 2].view(torch.bfloat16).view(B, I), w["w_down"],
+                                           again, d)
+        torch.cuda.synchronize()
+        got["out_again"], got["d"] = again.cpu(), d.cpu()
     return bench, cpu, got, w["ws_sh"].cpu(), request.param
 
 
@@ -97,7 +110,15 @@ def test_step_latent_tail_and_shared_expert(step):
     for t in TOKENS:
         y_ref = oracle.latent_norm(lat["latent"][:, t:t + 1].contiguous(), lat["gamma"], 1e-6, 1, TP, L)
         assert torch.equal(got["y"][t:t + 1].view(torch.int16), y_ref.view(torch.int16)), f"y token {t}"
-        if mode.startswith("two_branch"):
+        if mode == "two_branch_fused":
+            # d: a valid down projection of the GPU's h; out: the up-projection of y
+            # plus the eight shared partials and d, d last
+            d_ref = oracle.shared_down(h_gpu[t:t + 1].contiguous(), sh["w_down"], 1, H, I, accumulate=False)
+            close(got["d"][t:t + 1], d_ref, f"d token {t}")
+            sh9 = torch.cat([got["shared9"][:TP, t:t + 1], got["d"][None, t:t + 1]]).contiguous()
+            close(got["out"][t:t + 1], oracle.latent_up(got["y"][t:t + 1].contiguous(), lat["w_up"], sh9, TP + 1, 1,
+                                                        L, H), f"out token {t}")
+        elif mode.startswith("two_branch"):
             # d: a valid down projection of the GPU's h; out: the up-projection of y
             # plus all nine partials (d included)
             d_gpu = got["shared9"][TP]
@@ -114,6 +135,8 @@ def test_step_latent_tail_and_shared_expert(step):
             close(got["tail"][t:t + 1], tail_ref, f"latent tail token {t}")
             d_ref = oracle.shared_down(h_gpu[t:t + 1].contiguous(), sh["w_down"], 1, H, I, accumulate=False)
             close(got["d"][t:t + 1], d_ref, f"d token {t}")
+    if mode == "two_branch_fused":
+        assert torch.equal(got["out_again"].view(torch.int16), got["out"].view(torch.int16)), "fused call repeats"
     if not mode.startswith("two_branch"):
         # ... and the add itself bit for bit, every token: pz(bf16(f32(tail) + f32(d)))
         s = got["tail"].float() + got["d"].float()
