@@ -71,8 +71,10 @@ def parse_args():
     ap.add_argument("--composition", default="two_branch_fused",
                     choices=["two_branch_fused", "two_branch", "two_branch_one_call", "latent_main"],
                     help="how the step orders the weight-streaming calls (see run_step)")
-    ap.add_argument("--only-config", type=int, choices=[1, 2, 3, 4, 5], default=None,
-                    help="run one workload's call alone --calls times and exit (for profiling the call)")
+    ap.add_argument("--only-config", type=int, choices=[1, 2, 3, 4, 5, 6], default=None,
+                    help="run one workload's call alone --calls times and exit (for profiling the call); 6: the "
+                         "default step's side-stream calls at b = 64 (gate/up, latent norm, up-projection with the "
+                         "down projection)")
     ap.add_argument("--calls", type=int, default=4)
     ap.add_argument("--trace", choices=["step", "latent"], default=None,
                     help="per-CTA timeline from the trace build: ten decode steps as one graph (step), or the latent "
@@ -1197,14 +1199,14 @@ def only_config(args) -> int:
     """One workload's call, eagerly, --calls times on cuda:0 (for ncu): configs
     1-2 EP finalize, 3 expert-TP finalize, 4 the latent tail (moe_tail_latent_up
     and then moe_tail_latent_up_flags with both promises), 5 the shared expert
-    added into out."""
+    added into out, 6 the default step's side-stream calls at b = 64."""
     import moe_decode_tail_gb300 as mt
     from moe_decode_tail_gb300 import synth
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     n = args.only_config
-    d = synth.config(n)
+    d = synth.config(n) if n <= 5 else None
     g = lambda t: t.to(dev)
     if n in (1, 2):
         rows, idx, wt, gam = g(d["rows"]), g(d["idx"]), g(d["w"]), g(d["gamma"])
@@ -1224,11 +1226,21 @@ def only_config(args) -> int:
         calls = [lambda: mt.moe_tail_latent_up(lat, gam, wu, sh, out, ws, eps=d["eps"]),
                  lambda: mt.moe_tail_latent_up_flags(lat, gam, wu, sh, out, y, eps=d["eps"], inputs_ready=True,
                                                      weights_static=True)]
-    else:
+    elif n == 5:
         x, wg, wu, wd = g(d["x"]), g(d["w_gate"]), g(d["w_up"]), g(d["w_down"])
         out = torch.zeros((d["b"], d["H"]), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(mt.moe_tail_workspace_bytes(1, d["b"], d["I"]), dtype=torch.uint8, device=dev)
         calls = [lambda: mt.moe_shared_expert(x, wg, wu, wd, out, ws, accumulate=True)]
+    else:  # the default step's side stream at b = 64
+        _, w = make_workload(dev)
+        h = torch.empty((B, I), dtype=torch.bfloat16, device=dev)
+
+        def side_calls():
+            mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], h, weights_static=True)
+            mt.moe_tail_latent_norm(w["latent"], w["lat_gamma"], w["y"], eps=1e-6, inputs_ready=True)
+            mt.moe_tail_up_project_shared_down(w["y"], w["w_up"], w["shared"], h, w["w_down"], w["out"],
+                                               weights_static=True)
+        calls = [side_calls]
     for call in calls:
         for _ in range(args.calls):
             call()
