@@ -16,7 +16,9 @@ and 2 run beside them on a high-priority stream.
 Inputs are seeded and synthetic (random-init weights); every input is resident
 in device memory before timing.  A step touches about 390 MB, three times the
 L2, so every input is read cold without flushing.  Steps are replayed from a
-CUDA graph; per-call CUDA events inside the graph give each call's duration.
+CUDA graph whose timed replays carry no events; one more replay after the
+timed region carries per-call CUDA events (in every tenth step) for each
+call's duration.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference]
 

@@ -45,7 +45,7 @@ _lib = None
 def lib() -> ctypes.CDLL:
     """The loaded CUDA library (raises if it has not been built).  The
     MOE_TAIL_LIBRARY environment variable selects another build of it (the
-    trace build, see moe_decode_tail_gb300.trace) before the first call."""
+    trace build, whose records moe_decode_tail_gb300.trace reads) before the first call."""
     global _lib
     if _lib is None:
         path = os.environ.get("MOE_TAIL_LIBRARY", LIB)

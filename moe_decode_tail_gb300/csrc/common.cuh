@@ -58,10 +58,11 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 // mul.rn.f32x2 do two binary32 operations in one instruction, each component
 // rounded to nearest even as add.rn.f32 / mul.rn.f32 round it, so the paired
 // loops give the bits of the scalar ones -- with one rule: a paired product
-// never feeds a paired add.  Measured on GB300, such a pair is fused into one
-// multiply-add (a single rounding) despite the explicit rounding modes and
-// with contraction switched off; a product that goes into a sum is formed by
-// mul_each (two __fmul_rn, which are never merged) instead.
+// never feeds a paired add.  Measured on GB300, such a pair gave sums as if
+// the product had not been rounded (one ulp off in rare elements), despite
+// the explicit rounding modes and with contraction switched off; a product
+// that goes into a sum is formed by mul_each (two __fmul_rn, which are never
+// merged) instead.
 __device__ __forceinline__ void unpack8p(const uint4& v, float2 (&f)[4]) {
   f[0] = make_float2(bf16_lo(v.x), bf16_hi(v.x));
   f[1] = make_float2(bf16_lo(v.y), bf16_hi(v.y));
