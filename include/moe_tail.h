@@ -264,9 +264,11 @@ int moe_shared_down(const void* h, const void* w_down, int b, int H, int I, void
  * with the shared partials added in slot order from +0 and bf16(d) last --
  * the result of moe_shared_down (accumulate = 0) writing bf16(d) into one
  * more shared slot, then moe_tail_up_project over tp_s + 1 slots, up to the
- * K split of d (its FP32 sum may round differently).  Both weight streams go
- * through one ring into two tensor-memory accumulators and share one
- * epilogue, so the pair costs one kernel's ramp and tail instead of two.
+ * order of the FP32 sums of d and u (each K range is split differently, so
+ * a few elements may round differently).  One kernel streams both weights:
+ * some CTAs of each cluster take slices of W_down's K range, the others of
+ * W_up's, and one epilogue adds each projection's partials, so the pair
+ * costs one kernel's ramp and tail instead of two.
  *   y       BF16 [b][L] (moe_tail_latent_norm's output)
  *   w_up    BF16 [H][L];  shared BF16 [tp_s][b][H] or NULL (tp_s = 0)
  *   h       BF16 [b][I] (moe_shared_gate_up's output);  w_down BF16 [H][I]

@@ -26,6 +26,12 @@
 //                   pushed as BF16, -0 made +0, added into the tail's output)
 //   kGemmLatentUp   kGemmUpShared with y formed on chip from the latent partials
 //                   (the latent tail in one kernel; taken only on request)
+//   kGemmDownUp     the shared expert's down projection d and the up-projection
+//                   u in one kernel: out = bf16(u + (sum_s shared[s] + bf16(d)))
+//                   (Kimi-K3 tail runtime page, module docstring: the shared
+//                   expert's output is one more shared partial).  The cluster's
+//                   first ranks split W_down's K range, the others W_up's; one
+//                   epilogue adds each projection's partials in rank order.
 //
 // Every wait is bounded in time; on expiry the kernel raises a bit in the
 // device error word, drains what it started, frees its tensor memory and
@@ -247,15 +253,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   MOE_TRACE_SCOPE(30 + MODE);
   extern __shared__ uint8_t smem_raw[];
   constexpr bool kFused = MODE == kGemmLatentUp;
-  constexpr bool kDU = MODE == kGemmDownUp;  // d and u into two accumulators, one epilogue
+  constexpr bool kDU = MODE == kGemmDownUp;  // d on some ranks of the cluster, u on the rest, one epilogue
   constexpr bool kUp = MODE == kGemmUpShared || kFused || kDU;  // out = bf16(acc + slot sum of shared)
   constexpr int kATile = TM * kBlockK * 2;
   constexpr int kBTileBytes = N * kBlockK * 2;
   constexpr int kStageBytes = kFused ? kATile : kATile + kBTileBytes;
   constexpr int kMmaM = TM == 64 ? 64 : 128;
   constexpr int kNumAcc = TM / kMmaM;
-  constexpr int kAccCols = N * kNumAcc;  // one accumulator's TMEM columns (the up-projection's at kAccCols)
-  constexpr uint32_t kTmemCols = (kDU ? 2 : 1) * kAccCols < 32 ? 32 : (kDU ? 2 : 1) * kAccCols;
+  constexpr int kAccCols = N * kNumAcc;  // the accumulator's TMEM columns
+  constexpr uint32_t kTmemCols = kAccCols < 32 ? 32 : kAccCols;
   constexpr uint32_t kIdesc = idesc_bf16(kMmaM, N);
   constexpr int kOutRows = (MODE == kGemmGateUpSilu) ? TM / 2 : TM;  // output features per tile
 
@@ -265,15 +271,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tok0 = blockIdx.z * N;
 
   // K blocks of this CTA: an even split of the tile's K range over the cluster
-  // (down + up: each projection's K range split alike; the CTA streams its
-  // down blocks, then its up blocks, nk_all stages in all).
-  const int kb_per = a.kblocks / (int)ksplit, kb_rem = a.kblocks % (int)ksplit;
-  const int kb0 = (int)rank * kb_per + min((int)rank, kb_rem);
-  const int nk = kb_per + ((int)rank < kb_rem ? 1 : 0);
-  const int kb2_per = kDU ? a.kblocks2 / (int)ksplit : 0, kb2_rem = kDU ? a.kblocks2 % (int)ksplit : 0;
-  const int kb02 = (int)rank * kb2_per + min((int)rank, kb2_rem);
-  const int nk2 = kDU ? kb2_per + ((int)rank < kb2_rem ? 1 : 0) : 0;
-  const int nk_all = nk + nk2;
+  // (down + up: the first n_down ranks split the down projection's K range,
+  // the others the up-projection's; a rank streams one weight into one
+  // accumulator).
+  const int n_down = kDU ? downup_down_ranks((int)ksplit, a.kblocks, a.kblocks2) : 0;
+  const bool up_rank = kDU && (int)rank >= n_down;  // down + up: this CTA streams W_up against y
+  const int g_rank = up_rank ? (int)rank - n_down : (int)rank;
+  const int g_size = kDU ? (up_rank ? (int)ksplit - n_down : n_down) : (int)ksplit;
+  const int g_blocks = up_rank ? a.kblocks2 : a.kblocks;
+  const int kb_per = g_blocks / g_size, kb_rem = g_blocks % g_size;
+  const int kb0 = g_rank * kb_per + min(g_rank, kb_rem);
+  const int nk = kb_per + (g_rank < kb_rem ? 1 : 0);
+  const int nk_all = nk;
 
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -362,22 +371,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // Weight box of the CTA's i-th K block into stage st (two half-height boxes
-  // for gate/up; down + up: the down projection's blocks, then the up-projection's).
+  // for gate/up; down + up: W_down, or W_up on the up-projection's ranks).
   auto load_weights = [&](uint32_t st, uint32_t bar, int i, uint64_t policy) {
     if (MODE == kGemmGateUpSilu) {
       const int kx = (kb0 + i) * kBlockK;
       tma_load_2d(st, &map_w0, bar, kx, m_tile * (TM / 2), policy);
       tma_load_2d(st + kATile / 2, &map_w1, bar, kx, m_tile * (TM / 2), policy);
-    } else if (kDU && i >= nk) {
-      tma_load_2d(st, &map_w1, bar, (kb02 + i - nk) * kBlockK, m_tile * TM, policy);
     } else {
-      tma_load_2d(st, &map_w0, bar, (kb0 + i) * kBlockK, m_tile * TM, policy);
+      tma_load_2d(st, up_rank ? &map_w1 : &map_w0, bar, (kb0 + i) * kBlockK, m_tile * TM, policy);
     }
   };
-  // Token box of the CTA's i-th K block (h, then y for down + up).
+  // Token box of the CTA's i-th K block (down + up: h, or y on the up-projection's ranks).
   auto load_tokens = [&](uint32_t st, uint32_t bar, int i, uint64_t policy) {
-    if (kDU && i >= nk) tma_load_2d(st + kATile, &map_x1, bar, (kb02 + i - nk) * kBlockK, tok0, policy);
-    else tma_load_2d(st + kATile, &map_x, bar, (kb0 + i) * kBlockK, tok0, policy);
+    tma_load_2d(st + kATile, up_rank ? &map_x1 : &map_x, bar, (kb0 + i) * kBlockK, tok0, policy);
   };
 
   // Fused mode, the four epilogue warps: y of the tile's tokens over this
@@ -570,19 +576,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = L.ring + s * kStageBytes;
         const uint64_t adesc = smem_desc_sw128(st);
         const uint64_t bdesc = smem_desc_sw128(kFused ? L.yop + (uint32_t)(i * kBTileBytes) : st + kATile);
-        // down + up: the up-projection's blocks accumulate into the second accumulator
-        const bool second = kDU && i >= nk;
-        const uint32_t dcol = second ? (uint32_t)kAccCols : 0u;
-        const int first_i = second ? nk : 0;
 #pragma unroll
         for (int kk = 0; kk < kBlockK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
 #pragma unroll
           for (int acc = 0; acc < kNumAcc; ++acc)  // accumulator acc: weight rows acc*128 .. +127
-            mma_bf16(tmem + dcol + (uint32_t)(acc * N), adesc + (uint64_t)(acc * (kMmaM * 128 >> 4)) + 2 * kk,
-                     bdesc + 2 * kk, kIdesc, (i > first_i || kk > 0) ? 1u : 0u);
+            mma_bf16(tmem + (uint32_t)(acc * N), adesc + (uint64_t)(acc * (kMmaM * 128 >> 4)) + 2 * kk,
+                     bdesc + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(L.empty + 8 * s);
       }
-      mma_commit(L.accum);  // also on abort: completes once the issued MMAs are done
+      if (nk_all > 0) mma_commit(L.accum);  // also on abort: completes once the issued MMAs are done
+      else mbar_arrive(L.accum);             // an empty K range (the epilogue stages zeros)
     }
     __syncwarp();
   } else {
@@ -619,25 +622,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const bool holds_row = kMmaM == 128 || lane < 16;
     const int row = kMmaM == 128 ? warp * 32 + lane : warp * 16 + lane;
-    // down + up: the second accumulator (u) is staged after the first (d)
-    for (int which = 0; which < (kDU ? 2 : 1); ++which) {
-      float* stage = reinterpret_cast<float*>(base_ptr) + which * N * TM;
-      const bool any = which == 0 ? nk > 0 : nk2 > 0;
-      for (int acc = 0; acc < kNumAcc; ++acc) {
-        const int r = acc * kMmaM + row;
-        if (got && any) {
+    float* stage = reinterpret_cast<float*>(base_ptr);
+    for (int acc = 0; acc < kNumAcc; ++acc) {
+      const int r = acc * kMmaM + row;
+      if (got && nk > 0) {
 #pragma unroll 1
-          for (int c = 0; c < N; c += 16) {
-            float v[16];
-            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(which * kAccCols + acc * N + c), v);
-            if (holds_row) {
+        for (int c = 0; c < N; c += 16) {
+          float v[16];
+          tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * N + c), v);
+          if (holds_row) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) stage[(c + i) * TM + r] = v[i];
-            }
+            for (int i = 0; i < 16; ++i) stage[(c + i) * TM + r] = v[i];
           }
-        } else if (got && holds_row) {  // an empty K range contributes zeros
-          for (int c = 0; c < N; ++c) stage[c * TM + r] = 0.0f;
         }
+      } else if (got && holds_row) {  // an empty K range contributes zeros
+        for (int c = 0; c < N; ++c) stage[c * TM + r] = 0.0f;
       }
     }
     tc_fence_before();
@@ -657,12 +656,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 acc2 = make_float4(0.f, 0.f, 0.f, 0.f);
     const uint32_t off = base + (uint32_t)((t * TM + 4 * q) * 4);
+    // down + up: d is the sum over the down projection's ranks, u over the
+    // up-projection's, each in rank order
     for (uint32_t p = 0; p < ksplit; ++p) {
       const float4 v = ld_cluster_v4(map_to_rank(off, p));
-      acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
-      acc.z = __fadd_rn(acc.z, v.z); acc.w = __fadd_rn(acc.w, v.w);
-      if (MODE == kGemmGateUpSilu || kDU) {  // the up rows of the tile / the second partial tile
-        const float4 u = ld_cluster_v4(map_to_rank(off + (kDU ? N * TM * 4 : (TM / 2) * 4), p));
+      if (kDU && (int)p >= n_down) {
+        acc2.x = __fadd_rn(acc2.x, v.x); acc2.y = __fadd_rn(acc2.y, v.y);
+        acc2.z = __fadd_rn(acc2.z, v.z); acc2.w = __fadd_rn(acc2.w, v.w);
+      } else {
+        acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
+        acc.z = __fadd_rn(acc.z, v.z); acc.w = __fadd_rn(acc.w, v.w);
+      }
+      if (MODE == kGemmGateUpSilu) {  // the up rows of the tile
+        const float4 u = ld_cluster_v4(map_to_rank(off + (TM / 2) * 4, p));
         acc2.x = __fadd_rn(acc2.x, u.x); acc2.y = __fadd_rn(acc2.y, u.y);
         acc2.z = __fadd_rn(acc2.z, u.z); acc2.w = __fadd_rn(acc2.w, u.w);
       }
@@ -787,8 +793,14 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
     int ks = slots / std::max(1, p.m_tiles * tok_tiles);
     p.ksplit = std::max(1, std::min(ks, 8));
   }
-  p.ksplit = std::min(p.ksplit, kblocks);
-  if (mode == kGemmDownUp && kblocks2 > 0) p.ksplit = std::min(p.ksplit, kblocks2);
+  if (mode == kGemmDownUp) {  // at least one rank for each projection, and a K block for every rank
+    p.ksplit = std::max(2, std::min(p.ksplit, 8));
+    for (int n; p.ksplit > 2 && ((n = downup_down_ranks(p.ksplit, kblocks, kblocks2)) > kblocks ||
+                                 p.ksplit - n > kblocks2);)
+      --p.ksplit;
+  } else {
+    p.ksplit = std::min(p.ksplit, kblocks);
+  }
   const int sb = stage_bytes(p.tm, p.n_tile);
   // Ring budget 72 KB at TM <= 128 (3 stages at b = 64): two GEMM CTAs then
   // leave room on their SM for one finalize CTA of a concurrent stream (up to
@@ -803,11 +815,14 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
   // step with 96 KB, whose second CTA waits for the finalize to end).
   const int budget = p.tm == 256 ? 200 * 1024 : (mode == kGemmUpShared ? 96 * 1024 : 72 * 1024);
   if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, budget / sb));
-  const int per_cta = (kblocks + p.ksplit - 1) / p.ksplit + (kblocks2 + p.ksplit - 1) / p.ksplit;
+  int per_cta = (kblocks + p.ksplit - 1) / p.ksplit;  // the longest K range of a CTA
+  if (mode == kGemmDownUp) {
+    const int n = downup_down_ranks(p.ksplit, kblocks, kblocks2);
+    per_cta = std::max((kblocks + n - 1) / n, (kblocks2 + p.ksplit - n - 1) / (p.ksplit - n));
+  }
   p.stages = std::min(p.stages, std::max(2, per_cta));
-  // the FP32 staging tile (down + up: two of them) reuses the ring
-  const int tiles = mode == kGemmDownUp ? 2 : 1;
-  while (p.stages * sb < tiles * p.n_tile * p.tm * 4) ++p.stages;
+  // the FP32 staging tile reuses the ring
+  while (p.stages * sb < p.n_tile * p.tm * 4) ++p.stages;
   return p;
 }
 
@@ -916,8 +931,9 @@ cudaError_t launch_decode_gemm(int mode, const GemmPlan& p, const CUtensorMap& w
       if (p.n_tile == 16) return launch_t<kGemmLatentUp, 16, 128>(p, w0, w1, x, x, a, pdl, stream);
       if (p.n_tile == 32) return launch_t<kGemmLatentUp, 32, 128>(p, w0, w1, x, x, a, pdl, stream);
       return cudaErrorInvalidValue;
-    case kGemmDownUp:  // tm = 128 only; x1 is the up-projection's token map (y)
-      if (p.tm != 128 || x1 == nullptr || a.kblocks2 < 1) return cudaErrorInvalidValue;
+    case kGemmDownUp:  // tm = 128 only, a rank for each projection; x1 is the up-projection's token map (y)
+      if (p.tm != 128 || p.ksplit < 2 || p.ksplit > 8 || x1 == nullptr || a.kblocks < 1 || a.kblocks2 < 1)
+        return cudaErrorInvalidValue;
       return launch_n<kGemmDownUp, 128>(p, w0, w1, x, *x1, a, pdl, stream);
     default: return cudaErrorInvalidValue;
   }

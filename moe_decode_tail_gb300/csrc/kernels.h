@@ -78,6 +78,23 @@ struct GemmArgs {
   uint16_t* d_out = nullptr;
 };
 
+// Mode 4's cluster of ksplit >= 2 CTAs: ranks 0 .. n-1 stream the down
+// projection's K range, ranks n .. ksplit-1 the up-projection's, each range
+// split evenly over its ranks.  n minimises the longest per-CTA range (the
+// smallest such n).
+__host__ __device__ inline int downup_down_ranks(int ksplit, int kblocks, int kblocks2) {
+  int best = 1, best_len = 1 << 30;
+  for (int n = 1; n < ksplit; ++n) {
+    const int d = (kblocks + n - 1) / n, u = (kblocks2 + ksplit - n - 1) / (ksplit - n);
+    const int len = d > u ? d : u;
+    if (len < best_len) {
+      best = n;
+      best_len = len;
+    }
+  }
+  return best;
+}
+
 struct GemmPlan {
   int tm;       // MMA M: weight rows per CTA (64 or 128)
   int n_tile;   // MMA N (tokens, padded)
