@@ -12,7 +12,9 @@ hot path, each call on its decode shape:
 By default (--composition two_branch_fused) 3 and 4 run on a side stream as
 the shared expert's gate/up, the latent norm, then one kernel streaming the
 down projection and the up-projection (moe_tail_up_project_shared_down); 1
-and 2 run beside them on a high-priority stream.
+and 2 run beside them on a high-priority stream.  Gate/up and the norm take
+the inputs-ready promise (their inputs are the step's own), the GEMMs the
+static-weights promise.
 Inputs are seeded and synthetic (random-init weights); every input is resident
 in device memory before timing.  A step touches about 390 MB, three times the
 L2, so every input is read cold without flushing.  Steps are replayed from a
@@ -240,7 +242,11 @@ def run_step(mt, w, stream, events=None, side=None):
 
     With a side stream the weight-streaming calls run beside the routed
     finalize calls, as the Kimi-K3 tail runs its shared expert (its output is
-    pushed into the tail's reduce-scatter partials): on the side stream the
+    pushed into the tail's reduce-scatter partials).  The default,
+    "two_branch_fused": on the side stream moe_shared_gate_up (static
+    weights, inputs ready), moe_tail_latent_norm (inputs ready), then
+    moe_tail_up_project_shared_down (static weights), which adds bf16(d)
+    after the shared partials.  "two_branch": on the side stream the
     shared expert's two calls, moe_shared_gate_up and moe_shared_down, with
     static weights (each requests its first weight tiles before waiting for
     the preceding kernel), write d = bf16(down(h)) into the last of the
@@ -326,13 +332,17 @@ def run_step(mt, w, stream, events=None, side=None):
         return
     if comp == "two_branch_fused":
         # the shared expert's gate/up, the latent norm, then the down projection
-        # and the up-projection in one kernel (d added after the shared partials)
+        # and the up-projection in one kernel (d added after the shared partials).
+        # Gate/up takes both promises: its weights are static and x, the step's
+        # input, is complete before the previous step's last kernel ends, so its
+        # whole K loop may run while that kernel drains (h is written after it).
         bx = w["x"].shape[0]
         ws_h = w["ws_sh"][: bx * I * 2].view(torch.bfloat16).view(bx, I)
         w["fork"].record(stream)
         side.wait_event(w["fork"])
         rec(8, side)
-        mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], ws_h, weights_static=True, stream=side)
+        mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], ws_h, weights_static=True, inputs_ready=True,
+                              stream=side)
         rec(9, side)
         rec(4, side)
         mt.moe_tail_latent_norm(w["latent"], w["lat_gamma"], w["y"], eps=1e-6, inputs_ready=True, stream=side)
@@ -731,10 +741,10 @@ def cuda_arm(args, world, rank, local):
             if args.composition == "two_branch" else
             "two branches as two_branch, with the shared expert as one moe_shared_expert call"
             if args.composition == "two_branch_one_call" else
-            "two branches: on a side stream the shared expert's gate/up, the latent norm, then one kernel that "
-            "streams the down projection and the latent up-projection into two accumulators and adds bf16(d) "
-            "after the shared partials (moe_tail_up_project_shared_down); EP and TP on a high-priority stream "
-            "beside them"
+            "two branches: on a side stream the shared expert's gate/up (static weights, inputs ready), the "
+            "latent norm (inputs ready), then one kernel whose cluster ranks stream the down projection or the "
+            "latent up-projection and which adds bf16(d) after the shared partials "
+            "(moe_tail_up_project_shared_down, static weights); EP and TP on a high-priority stream beside them"
             if args.composition == "two_branch_fused" else
             "two branches: the shared expert's gate/up on a side stream; EP, TP and the latent tail on a "
             "high-priority stream beside it; then the down projection adds d into the latent tail's output")),
@@ -1238,7 +1248,7 @@ def only_config(args) -> int:
         h = torch.empty((B, I), dtype=torch.bfloat16, device=dev)
 
         def side_calls():
-            mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], h, weights_static=True)
+            mt.moe_shared_gate_up(w["x"], w["w_gate"], w["w_up_s"], h, weights_static=True, inputs_ready=True)
             mt.moe_tail_latent_norm(w["latent"], w["lat_gamma"], w["y"], eps=1e-6, inputs_ready=True)
             mt.moe_tail_up_project_shared_down(w["y"], w["w_up"], w["shared"], h, w["w_down"], w["out"],
                                                weights_static=True)

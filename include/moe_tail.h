@@ -244,7 +244,12 @@ int moe_shared_expert(const void* x, const void* w_gate, const void* w_up, const
  *   accumulate != 0; must not overlap an input).
  *   flags (both calls): 0, or MOE_TAIL_WEIGHTS_STATIC (as for
  *   moe_tail_up_project: the first weight tiles are requested before the
- *   kernel waits for the stream's preceding kernel).
+ *   kernel waits for the stream's preceding kernel).  moe_shared_gate_up
+ *   also takes MOE_TAIL_INPUTS_READY: a promise that x is not being written
+ *   by work still in flight on the stream.  The kernel then reads x and runs
+ *   its whole K loop while the preceding kernel drains, and waits for that
+ *   kernel only before it writes h (which the preceding kernel may still be
+ *   reading).  The flags change only when memory is read, never the result.
  *   Limits: 8 <= H <= 16777216, 8 <= I <= 16777216, H % 8 == 0, I % 8 == 0,
  *   b <= 65535.
  */

@@ -311,9 +311,11 @@ def moe_tail_up_project_shared_down(y, w_up, shared, h, w_down, out, d_out=None,
     return out
 
 
-def moe_shared_gate_up(x, w_gate, w_up, h, *, weights_static=False, stream=None) -> torch.Tensor:
+def moe_shared_gate_up(x, w_gate, w_up, h, *, weights_static=False, inputs_ready=False, stream=None) -> torch.Tensor:
     """The shared expert's gate/up projection and SiLU into h (BF16 [b, I]):
-    x BF16 [b, H], w_gate and w_up BF16 [I, H]."""
+    x BF16 [b, H], w_gate and w_up BF16 [I, H].  inputs_ready promises that x
+    is not being written by work in flight on the stream (h is written only
+    after that work ends)."""
     b, H = _dims("x", x, 2)
     I, _ = _dims("w_gate", w_gate, 2)
     _like("x", x, torch.bfloat16, (b, H))
@@ -322,7 +324,8 @@ def moe_shared_gate_up(x, w_gate, w_up, h, *, weights_static=False, stream=None)
     _like("h", h, torch.bfloat16, (b, I))
     _cuda(x, w_gate, w_up, h)
     _check("moe_shared_gate_up", lib().moe_shared_gate_up(
-        _p(x), _p(w_gate), _p(w_up), b, H, I, _p(h), WEIGHTS_STATIC if weights_static else 0, _stream(stream)))
+        _p(x), _p(w_gate), _p(w_up), b, H, I, _p(h),
+        (WEIGHTS_STATIC if weights_static else 0) | (INPUTS_READY if inputs_ready else 0), _stream(stream)))
     return h
 
 

@@ -512,8 +512,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       // Inside the library's own kernel chains the weights never depend on the
       // preceding kernel, so the first ring's worth is requested before waiting
-      // for it; the first kernel of a call waits first.
+      // for it; the first kernel of a call waits first.  With the inputs-ready
+      // promise (gate/up: x complete before the preceding kernel ends) the
+      // token tiles are read without waiting as well, and only the epilogue
+      // waits, before it writes.
       const int pre = min(nk_all, stages);
+      const bool tokens_ready = !kFused && a.inputs_before_wait;
       if (!a.weights_before_wait) grid_dependency_wait();
       if (kFused && !mbar_wait(L.latbar, 0)) {  // the ring holds the latent rows until y's inputs are read
         raise_error(kErrWaitFull);
@@ -523,8 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(L.full + 8 * i, kStageBytes);
         load_weights(L.ring + i * kStageBytes, L.full + 8 * i, i, stream);
       }
-      if (!kFused) {  // the token tiles are the preceding kernel's output
-        if (a.weights_before_wait) grid_dependency_wait();
+      if (!kFused) {  // the token tiles are the preceding kernel's output, unless promised ready
+        if (a.weights_before_wait && !tokens_ready) grid_dependency_wait();
         for (int i = 0; i < pre; ++i) load_tokens(L.ring + i * kStageBytes, L.full + 8 * i, i, keep);
       }
       issued = pre;
@@ -552,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
-    if (!kFused) grid_dependency_wait();  // fused: reads shared memory only
+    if (!kFused && !a.inputs_before_wait) grid_dependency_wait();  // fused: reads shared memory only
     if (lane == 0) {
       bool ok = true;
       if (kFused) {  // y is in shared memory (and visible to the tensor cores)

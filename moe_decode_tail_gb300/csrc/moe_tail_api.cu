@@ -511,7 +511,7 @@ bool shared_sizes_ok(int b, int H, int I) {
 
 // h = bf16(silu(bf16(x . w_gate^T)) * bf16(x . w_up^T)).  Arguments already checked.
 int launch_gate_up(const void* x, const void* w_gate, const void* w_up, int b, int H, int I, void* h,
-                   bool weights_before_wait, cudaStream_t st) {
+                   bool weights_before_wait, cudaStream_t st, bool inputs_before_wait = false) {
   const GemmPlan p1 = moetail::plan_gemm(moetail::kGemmGateUpSilu, I, H, b, device_sms());
   CUtensorMap mg, mu, mx;
   if (!encode_bf16_2d(&mg, w_gate, I, H, p1.tm / 2, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
@@ -528,6 +528,7 @@ int launch_gate_up(const void* x, const void* w_gate, const void* w_up, int b, i
   g.out = static_cast<uint16_t*>(h);
   g.accumulate = 0;
   g.weights_before_wait = weights_before_wait ? 1 : 0;
+  g.inputs_before_wait = inputs_before_wait ? 1 : 0;
   return finish(moetail::launch_decode_gemm(moetail::kGemmGateUpSilu, p1, mg, mu, mx, g, true, st));
 }
 
@@ -581,7 +582,7 @@ MOE_API int moe_shared_expert(const void* x, const void* w_gate, const void* w_u
 
 MOE_API int moe_shared_gate_up(const void* x, const void* w_gate, const void* w_up, int b, int H, int I, void* h,
                                int flags, void* stream) {
-  if (!shared_sizes_ok(b, H, I) || (flags & ~MOE_TAIL_WEIGHTS_STATIC)) return MOE_TAIL_EINVAL;
+  if (!shared_sizes_ok(b, H, I) || (flags & ~(MOE_TAIL_WEIGHTS_STATIC | MOE_TAIL_INPUTS_READY))) return MOE_TAIL_EINVAL;
   if (b == 0) return MOE_TAIL_OK;
   if (!x || !w_gate || !w_up || !h) return MOE_TAIL_EINVAL;
   if (!aligned(x, 16) || !aligned(w_gate, 16) || !aligned(w_up, 16) || !aligned(h, 16)) return MOE_TAIL_EINVAL;
@@ -590,7 +591,7 @@ MOE_API int moe_shared_gate_up(const void* x, const void* w_gate, const void* w_
       overlaps(rh, span(w_up, (size_t)I * H * 2)))
     return MOE_TAIL_EINVAL;
   return launch_gate_up(x, w_gate, w_up, b, H, I, h, (flags & MOE_TAIL_WEIGHTS_STATIC) != 0,
-                        static_cast<cudaStream_t>(stream));
+                        static_cast<cudaStream_t>(stream), (flags & MOE_TAIL_INPUTS_READY) != 0);
 }
 
 MOE_API int moe_shared_down(const void* h, const void* w_down, int b, int H, int I, void* out, int accumulate,

@@ -314,7 +314,7 @@ def down(lib, **kw):
 @host_only
 @pytest.mark.parametrize("bad", [
     dict(H=7169), dict(I=6142), dict(b=-1), dict(x=None), dict(wu=None), dict(h=None), dict(h=a(8)),
-    dict(h=a(16)), dict(flags=2), dict(wg=a(4)),  # h over x
+    dict(h=a(16)), dict(flags=4), dict(flags=7), dict(wg=a(4)),  # h over x
 ])
 def test_shared_gate_up_refuses_bad_arguments(lib, bad):
     assert gate_up(lib, **bad) == EINVAL
@@ -332,6 +332,7 @@ def test_shared_down_refuses_bad_arguments(lib, bad):
 @host_only
 def test_shared_steps_b_zero(lib):
     assert gate_up(lib, b=0, x=None, h=None) == OK
+    assert gate_up(lib, b=0, x=None, h=None, flags=3) == OK  # both promises are valid flags
     assert down(lib, b=0, h=None, out=None, flags=1) == OK
 
 

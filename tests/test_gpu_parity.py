@@ -750,10 +750,11 @@ def test_shared_expert_down_stage_full_size_exact_h(mt):
 
 
 @pytest.mark.parametrize("kw", [dict(b=64, H=7168, I=6144), dict(b=5, H=264, I=200), dict(b=130, H=256, I=128)])
-@pytest.mark.parametrize("static", [False, True])
-def test_shared_expert_as_two_calls(mt, kw, static):
-    # moe_shared_gate_up then moe_shared_down on two streams joined by an event,
-    # with the latent-tail-like addend in out: bit-identical to the one call
+@pytest.mark.parametrize("static,ready", [(False, False), (True, False), (True, True), (False, True)])
+def test_shared_expert_as_two_calls(mt, kw, static, ready):
+    # moe_shared_gate_up (with or without the promises) then moe_shared_down on
+    # two streams joined by an event, with the latent-tail-like addend in out:
+    # bit-identical to the one call
     s = synth.shared_expert_inputs(0x2C + kw["b"], **kw)
     b, H, I = s["b"], s["H"], s["I"]
     out_in = synth.bf16(synth.normal(0x2C, 5, b * H), (b, H))
@@ -763,10 +764,10 @@ def test_shared_expert_as_two_calls(mt, kw, static):
     out = out_in.to(DEV).clone()
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
     torch.cuda.synchronize()
-    ready = torch.cuda.Event()
-    mt.moe_shared_gate_up(x, wg, wu, h, weights_static=static, stream=s1)
-    ready.record(s1)
-    s2.wait_event(ready)
+    mt.moe_shared_gate_up(x, wg, wu, h, weights_static=static, inputs_ready=ready, stream=s1)
+    joined = torch.cuda.Event()
+    joined.record(s1)
+    s2.wait_event(joined)
     mt.moe_shared_down(h, wd, out, accumulate=True, weights_static=static, stream=s2)
     torch.cuda.synchronize()
     assert_bitexact(h, h1, f"h {kw}")
@@ -777,6 +778,37 @@ def test_shared_expert_as_two_calls(mt, kw, static):
     t = min(3, b - 1)
     assert_gemm_close(d[t:t + 1], oracle.shared_down(h[t:t + 1].cpu(), s["w_down"], 1, H, I, accumulate=False),
                       f"d token {t} {kw}")
+    assert mt.moe_tail_take_device_error() == 0
+
+
+def test_gate_up_inputs_ready_waits_before_writing_h(mt):
+    # on one stream: gate/up(x1) -> h; the down projection reading h -> d1;
+    # gate/up(x2) with both promises -> h.  The last call may run its K loop
+    # while the down projection still reads h, so it writes h only after that
+    # call ends: d1 is the down projection of h(x1), h is h(x2) -- each bit for
+    # bit the result of the same call made alone
+    s1 = synth.shared_expert_inputs(0x6A1, b=64, H=7168, I=6144)
+    s2 = synth.shared_expert_inputs(0x6A2, b=64, H=7168, I=6144)
+    b, H, I = 64, 7168, 6144
+    x1, x2 = s1["x"].to(DEV), s2["x"].to(DEV)
+    wg, wu, wd = (s1[k].to(DEV) for k in ("w_gate", "w_up", "w_down"))
+    h_a = torch.empty((b, I), dtype=torch.bfloat16, device=DEV)
+    h_b = torch.empty((b, I), dtype=torch.bfloat16, device=DEV)
+    d_ref = torch.empty((b, H), dtype=torch.bfloat16, device=DEV)
+    mt.moe_shared_gate_up(x1, wg, wu, h_a)
+    mt.moe_shared_gate_up(x2, wg, wu, h_b)
+    mt.moe_shared_down(h_a, wd, d_ref, accumulate=False)
+    torch.cuda.synchronize()
+    h = torch.empty((b, I), dtype=torch.bfloat16, device=DEV)
+    d1 = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    mt.moe_shared_gate_up(x1, wg, wu, h, stream=st)
+    mt.moe_shared_down(h, wd, d1, accumulate=False, weights_static=True, stream=st)
+    mt.moe_shared_gate_up(x2, wg, wu, h, weights_static=True, inputs_ready=True, stream=st)
+    torch.cuda.synchronize()
+    assert_bitexact(d1, d_ref, "the down projection saw the first h")
+    assert_bitexact(h, h_b, "h is the last call's output")
     assert mt.moe_tail_take_device_error() == 0
 
 
