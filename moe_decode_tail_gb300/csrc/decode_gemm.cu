@@ -788,12 +788,17 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
   if (mode == kGemmDownUp) p.tm = 128;  // the only tile height this mode is built for
   const int rows_per_tile = mode == kGemmGateUpSilu ? p.tm / 2 : p.tm;
   p.m_tiles = (M + rows_per_tile - 1) / rows_per_tile;
+  // The up-projection of at most 16 tokens (18 KB stages) runs three CTAs per
+  // SM with 3-stage rings: the latent tail alone at b = 16 with both promises
+  // 11.9 -> 11.3 us, at b = 1 10.7 -> 10.2, b = 8 11.5 -> 10.9; without them
+  // the same at b = 16, faster at b = 1 and 8.
+  const bool small_up = mode == kGemmUpShared && p.n_tile <= 16;
   if (!forced) {  // K split over a cluster: about two CTAs per SM
     // Above 32 tokens the down projection takes about 1.5 per SM: in a decode
     // step it runs beside the expert-TP finalize, which then finds SMs sooner
     // (b = 64: K split 4 instead of 5, 72.7 -> 71.4 us per step).  Small
     // batches keep two (b = 1 alone: 45.9 vs 48.5 us for the shared expert).
-    const int slots = (mode == kGemmDown && b > 32) ? 3 * sms / 2 : 2 * sms;
+    const int slots = (mode == kGemmDown && b > 32) ? 3 * sms / 2 : small_up ? 3 * sms : 2 * sms;
     int ks = slots / std::max(1, p.m_tiles * tok_tiles);
     p.ksplit = std::max(1, std::min(ks, 8));
   }
@@ -817,7 +822,7 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
   // the expert-TP finalize still holds SMs, and two of its CTAs beside one
   // finalize CTA fit an SM only at this size (b = 64: 63.3 vs 66.9 us per
   // step with 96 KB, whose second CTA waits for the finalize to end).
-  const int budget = p.tm == 256 ? 200 * 1024 : (mode == kGemmUpShared ? 96 * 1024 : 72 * 1024);
+  const int budget = p.tm == 256 ? 200 * 1024 : small_up ? 3 * sb : (mode == kGemmUpShared ? 96 * 1024 : 72 * 1024);
   if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, budget / sb));
   int per_cta = (kblocks + p.ksplit - 1) / p.ksplit;  // the longest K range of a CTA
   if (mode == kGemmDownUp) {
