@@ -978,16 +978,19 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
     us = timed(shared_static, n)
     report("5_shared_expert_b64_static", us, nb, n, ">= 0.60 of the weight-stream roofline")
 
-    # the composed layer of configs 4 and 5 at b = 64: the shared expert writes d into
-    # the latent tail's extra partial slot, then the latent tail's two calls follow
+    # the composed layer of configs 4 and 5 at b = 64, as the default step's side
+    # stream runs it: gate/up, the latent norm, then the down projection and the
+    # up-projection in one kernel (algorithmic bytes: no intermediate counted)
     wl = [w["w_up"], w["w_up"].clone()]
 
     def layer(i):
-        mt.moe_shared_expert(w["x"], *ws_[i], w["d_slot"], w["ws_sh"], accumulate=False, stream=stream)
+        mt.moe_shared_gate_up(w["x"], ws_[i][0], ws_[i][1], h_, weights_static=True, inputs_ready=True,
+                              stream=stream)
         mt.moe_tail_latent_norm(w["latent"], w["lat_gamma"], w["y"], eps=1e-6, inputs_ready=True, stream=stream)
-        mt.moe_tail_up_project(w["y"], wl[i], w["shared9"], w["out"], weights_static=True, stream=stream)
+        mt.moe_tail_up_project_shared_down(w["y"], wl[i], w["shared"], h_, ws_[i][2], w["out"], weights_static=True,
+                                           stream=stream)
 
-    nb_layer = (3 * H * I * 2 + B * H * 2 + 2 * B * I * 2 + B * H * 2) + BYTES["latent_up"] + B * H * 2
+    nb_layer = 3 * H * I * 2 + B * H * 2 + BYTES["latent_up"]
     us = timed(layer, 2)
     report("4+5_latent_tail_and_shared_expert_b64", us, nb_layer, 2, "composed layer (report)")
     del ws_, wl
