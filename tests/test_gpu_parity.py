@@ -542,7 +542,7 @@ def test_latent_norm_inputs_ready_waits_before_writing_y(mt):
 
 
 @pytest.mark.parametrize("kw", [
-    dict(b=1, tp=8, tp_s=9, L=3584, H=7168),     # the decode step's latent tail: K split over 5-CTA clusters
+    dict(b=1, tp=8, tp_s=9, L=3584, H=7168),     # the decode shape: K split over 8-CTA clusters, 3 CTAs per SM
     dict(b=16, tp=8, tp_s=8, L=3584, H=7168),
     dict(b=5, tp=3, tp_s=0, L=1000, H=520),      # split 8, ragged last chunk, M tail
     dict(b=17, tp=2, tp_s=1, L=8192, H=264),     # N tile 32, 32 chunks, two ring stages
