@@ -793,12 +793,18 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
   // 11.9 -> 11.3 us, at b = 1 10.7 -> 10.2, b = 8 11.5 -> 10.9; without them
   // the same at b = 16, faster at b = 1 and 8.
   const bool small_up = mode == kGemmUpShared && p.n_tile <= 16;
+  // The gate/up projection of at most 32 tokens takes a 4-way K split with
+  // 3-stage rings (384 CTAs, about 2.5 per SM), measured in the decode step:
+  // b = 32 59.0 -> 55.1 us, b = 8 52.3 -> 51.5, b = 1 50.9 -> 50.5; at b = 64
+  // and 128 the 3-way split stays (58.0 vs 58.4, 84.7 vs 87.5).
+  const bool small_gateup = mode == kGemmGateUpSilu && p.n_tile <= 32;
   if (!forced) {  // K split over a cluster: about two CTAs per SM
     // Above 32 tokens the down projection takes about 1.5 per SM: in a decode
     // step it runs beside the expert-TP finalize, which then finds SMs sooner
     // (b = 64: K split 4 instead of 5, 72.7 -> 71.4 us per step).  Small
     // batches keep two (b = 1 alone: 45.9 vs 48.5 us for the shared expert).
-    const int slots = (mode == kGemmDown && b > 32) ? 3 * sms / 2 : small_up ? 3 * sms : 2 * sms;
+    const int slots = (mode == kGemmDown && b > 32) ? 3 * sms / 2 : small_up ? 3 * sms
+                      : small_gateup ? 8 * sms / 3 : 2 * sms;
     int ks = slots / std::max(1, p.m_tiles * tok_tiles);
     p.ksplit = std::max(1, std::min(ks, 8));
   }
@@ -822,7 +828,8 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
   // the expert-TP finalize still holds SMs, and two of its CTAs beside one
   // finalize CTA fit an SM only at this size (b = 64: 63.3 vs 66.9 us per
   // step with 96 KB, whose second CTA waits for the finalize to end).
-  const int budget = p.tm == 256 ? 200 * 1024 : small_up ? 3 * sb : (mode == kGemmUpShared ? 96 * 1024 : 72 * 1024);
+  const int budget = p.tm == 256 ? 200 * 1024 : (small_up || small_gateup) ? 3 * sb
+                     : (mode == kGemmUpShared ? 96 * 1024 : 72 * 1024);
   if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, budget / sb));
   int per_cta = (kblocks + p.ksplit - 1) / p.ksplit;  // the longest K range of a CTA
   if (mode == kGemmDownUp) {
