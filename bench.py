@@ -978,6 +978,19 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
     us = timed(shared_static, n)
     report("5_shared_expert_b64_static", us, nb, n, ">= 0.60 of the weight-stream roofline")
 
+    # the shared expert's down projection alone (d written, not accumulated): the
+    # split-K GEMM against the page's persistent form on 56, 28 and 14 CTAs (each
+    # walking 1, 2 or 4 output tiles with two alternating TMEM accumulators)
+    wds = [ws_[0][2], ws_[1][2]] + [ws_[0][2].clone() for _ in range(2)]
+    nb_down = H * I * 2 + B * I * 2 + B * H * 2
+    us = timed(lambda i: mt.moe_shared_down(h_, wds[i], out, accumulate=False, stream=stream), len(wds))
+    report("5_down_b64", us, nb_down, len(wds), "report (the persistent form's comparison)")
+    for ctas in (56, 28, 14):
+        us = timed(lambda i: mt.moe_shared_down_persistent(h_, wds[i], out, accumulate=False, ctas=ctas,
+                                                           stream=stream), len(wds))
+        report(f"5_down_persistent_b64_{ctas}ctas", us, nb_down, len(wds), "report (the page's SharedDown form)")
+    del wds
+
     # the composed layer of configs 4 and 5 at b = 64, as the default step's side
     # stream runs it: gate/up, the latent norm, then the down projection and the
     # up-projection in one kernel (algorithmic bytes: no intermediate counted)

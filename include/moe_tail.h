@@ -259,6 +259,23 @@ int moe_shared_down(const void* h, const void* w_down, int b, int H, int I, void
                     int flags, void* stream);
 
 /*
+ * The down projection as the Kimi-K3 shared expert page's persistent kernel
+ * ([KS] SharedDown): the same out as moe_shared_down, up to the order of d's
+ * FP32 sum (here no K split: a few elements may round differently).  ctas
+ * CTAs (one per SM; 0: one per output tile, at most the GPU's SM count) walk
+ * the output tiles of 128 rows x the token tile (16, 32, 64 or 128 tokens),
+ * tile c, c + ctas, ..., each over the whole K range, with two tensor-memory
+ * accumulators that alternate between a CTA's consecutive tiles, so each
+ * tile's epilogue overlaps the next tile's weight stream.  A caller that runs
+ * other work beside it gives it the SMs that work leaves free.
+ *   h, w_down, out, accumulate, flags: as moe_shared_down.
+ *   ctas: 0 .. 65535.
+ * Limits and refusals: those of moe_shared_down, plus ctas out of range.
+ */
+int moe_shared_down_persistent(const void* h, const void* w_down, int b, int H, int I, void* out, int accumulate,
+                               int ctas, int flags, void* stream);
+
+/*
  * The latent tail's up-projection with the shared expert's down projection
  * in one kernel ([KT] module docstring: the shared expert's output joins the
  * tail's shared partials before the up-projection's epilogue; [KS]

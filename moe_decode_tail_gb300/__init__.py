@@ -22,6 +22,7 @@ __all__ = [
     "moe_shared_gate_up", "moe_shared_down", "moe_tail_latent_up_flags", "moe_tail_ep_finalize_flags",
     "moe_tail_tp_finalize_flags", "moe_tail_set_kernel_form", "kernel_form", "FORM_EP", "FORM_TP", "FORM_LATENT",
     "FORM_LATENT_ONE_KERNEL", "moe_tail_set_stage_wait_limit", "moe_tail_up_project_shared_down",
+    "moe_shared_down_persistent",
 ]
 
 OK, EINVAL, ECUDA, ENOTSUP = 0, 1, 2, 3
@@ -68,6 +69,7 @@ def lib() -> ctypes.CDLL:
         L.moe_tail_latent_up_flags.argtypes = [P, P, f32, P, P, i32, i32, i32, i32, i32, P, P, i32, P]
         L.moe_shared_gate_up.argtypes = [P, P, P, i32, i32, i32, P, i32, P]
         L.moe_shared_down.argtypes = [P, P, i32, i32, i32, P, i32, i32, P]
+        L.moe_shared_down_persistent.argtypes = [P, P, i32, i32, i32, P, i32, i32, i32, P]
         L.moe_tail_workspace_bytes.argtypes = [i32, i32, i32]
         L.moe_tail_workspace_bytes.restype = sz
         L.moe_tail_status_str.argtypes = [i32]
@@ -81,7 +83,7 @@ def lib() -> ctypes.CDLL:
                      "moe_tail_latent_norm", "moe_tail_up_project", "moe_shared_gate_up", "moe_shared_down",
                      "moe_tail_latent_up_flags", "moe_tail_ep_finalize_flags", "moe_tail_tp_finalize_flags",
                      "moe_tail_set_kernel_form", "moe_tail_set_stage_wait_limit",
-                     "moe_tail_up_project_shared_down"):
+                     "moe_tail_up_project_shared_down", "moe_shared_down_persistent"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -341,6 +343,24 @@ def moe_shared_down(h, w_down, out, *, accumulate=True, weights_static=False, st
     _check("moe_shared_down", lib().moe_shared_down(
         _p(h), _p(w_down), b, H, I, _p(out), int(bool(accumulate)), WEIGHTS_STATIC if weights_static else 0,
         _stream(stream)))
+    return out
+
+
+def moe_shared_down_persistent(h, w_down, out, *, accumulate=True, ctas=0, weights_static=False,
+                               stream=None) -> torch.Tensor:
+    """The down projection as a persistent kernel: ctas CTAs (0: one per output
+    tile, at most one per SM) walk the output tiles over the whole K range with
+    two alternating tensor-memory accumulators.  Same arguments and result as
+    moe_shared_down, up to the order of d's FP32 sum."""
+    b, I = _dims("h", h, 2)
+    H, _ = _dims("w_down", w_down, 2)
+    _like("h", h, torch.bfloat16, (b, I))
+    _like("w_down", w_down, torch.bfloat16, (H, I))
+    _like("out", out, torch.bfloat16, (b, H))
+    _cuda(h, w_down, out)
+    _check("moe_shared_down_persistent", lib().moe_shared_down_persistent(
+        _p(h), _p(w_down), b, H, I, _p(out), int(bool(accumulate)), int(ctas),
+        WEIGHTS_STATIC if weights_static else 0, _stream(stream)))
     return out
 
 

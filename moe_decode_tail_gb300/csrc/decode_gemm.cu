@@ -737,6 +737,209 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---- persistent down projection ----------------------------------------------------
+//
+//   out[t, n] = accumulate ? bf16(out[t, n] + bf16(d)) : bf16(d),   d = sum_k W[n, k] * h[t, k]
+//
+// The Kimi-K3 shared expert page's down projection (SharedDown): a persistent
+// grid whose CTAs walk output tiles of 128 weight rows x N tokens, tile
+// blockIdx.x, + gridDim.x, ..., each over the whole K range (no K split, no
+// cluster), with two tensor-memory accumulators that alternate between a
+// CTA's consecutive tiles: the MMA issuer fills one while the epilogue warps
+// drain the other, so a tile's epilogue overlaps the next tile's weight
+// stream.  Warp 4 streams the weight and token tiles of all the CTA's tiles
+// through one ring, warp 5 issues the MMAs, warps 0-3 read an accumulator (one
+// TMEM lane = one weight row per thread) and write out directly: per token a
+// warp's 32 rows are 64 contiguous bytes.  Waits are bounded as in
+// decode_gemm_kernel; after an abort no copy or MMA is issued, the epilogue
+// skips its stores, and the CTA waits for what it started before freeing its
+// tensor memory.
+template <int N>
+__global__ void __launch_bounds__(kThreads, 1)
+    persistent_down_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
+                           const GemmArgs a, const int stages) {
+  extern __shared__ uint8_t smem_raw[];
+  constexpr int kATile = 128 * kBlockK * 2;
+  constexpr int kStageBytes = kATile + N * kBlockK * 2;
+  constexpr uint32_t kTmemCols = 2 * N < 32 ? 32 : 2 * N;  // two accumulators of N columns
+  constexpr uint32_t kIdesc = idesc_bf16(128, N);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tiles = (a.M + 127) / 128;
+  const int n_items = m_tiles * ((a.n_tok + N - 1) / N);
+  const int my_items =
+      (int)blockIdx.x < n_items ? (n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  const int total = my_items * a.kblocks;  // ring stages this CTA streams
+
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t ring = base;
+  const uint32_t full = ring + (uint32_t)(stages * kStageBytes);  // [stages]
+  const uint32_t empty = full + 8u * stages;                       // [stages]
+  const uint32_t acc_full = empty + 8u * stages;                   // [2]: accumulator holds a finished tile
+  const uint32_t acc_empty = acc_full + 16;                        // [2]: the epilogue has read it
+  const uint32_t mma_done = acc_empty + 16;                        // the issuer's MMAs have all completed
+  const uint32_t tmem_slot = mma_done + 8;
+  const uint32_t abort_off = tmem_slot + 4;
+  volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+  volatile uint32_t* abort_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (abort_off - base));
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full + 8 * s, 1);
+      mbar_init(empty + 8 * s, 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(acc_full + 8 * k, 1);
+      mbar_init(acc_empty + 8 * k, 4);  // one arrival per epilogue warp
+    }
+    mbar_init(mma_done, 1);
+    *abort_ptr = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_map(&map_w);
+    prefetch_map(&map_h);
+  }
+  if (warp == 5) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot_ptr;
+  launch_dependents();
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();     // token tiles: re-read by every weight tile
+      const uint64_t stream = policy_evict_first();  // weights: read once
+      // stage g of the CTA: its tile g / kblocks, K block g % kblocks
+      auto load = [&](int g, bool weights, bool tokens) {
+        const int j = g / a.kblocks, kb = g - j * a.kblocks;
+        const int item = (int)blockIdx.x + j * (int)gridDim.x;
+        const uint32_t st = ring + (uint32_t)((g % stages) * kStageBytes), bar = full + 8u * (g % stages);
+        if (weights) tma_load_2d(st, &map_w, bar, kb * kBlockK, (item % m_tiles) * 128, stream);
+        if (tokens) tma_load_2d(st + kATile, &map_h, bar, kb * kBlockK, (item / m_tiles) * N, keep);
+      };
+      const int pre = min(total, stages);
+      if (!a.weights_before_wait) grid_dependency_wait();
+      for (int g = 0; g < pre; ++g) {
+        mbar_expect_tx(full + 8u * g, kStageBytes);
+        load(g, true, false);
+      }
+      if (a.weights_before_wait) grid_dependency_wait();  // h is the preceding kernel's output
+      for (int g = 0; g < pre; ++g) load(g, false, true);
+      int issued = pre;
+      bool ok = true;
+      for (int g = pre; g < total; ++g) {
+        const int s = g % stages;
+        if (!mbar_wait(empty + 8u * s, (uint32_t)(g / stages - 1) & 1u, kWaitLimitNs, abort_ptr)) {
+          if (!*abort_ptr) raise_error(kErrWaitEmpty);  // (else the MMA issuer aborted: stop issuing)
+          *abort_ptr = 1;
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(full + 8u * s, kStageBytes);
+        load(g, true, true);
+        ++issued;
+      }
+      if (!ok) {  // let the copies already in flight land before the CTA's memory goes away
+        for (int g = max(0, issued - stages); g < issued; ++g)
+          if (!mbar_wait(full + 8u * (g % stages), (uint32_t)(g / stages) & 1u)) raise_error(kErrWaitDrain);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---------------- MMA issuer: accumulator j % 2 for the CTA's tile j ----------------
+    if (lane == 0) {
+      const unsigned long long stage_limit = a.stage_wait_ns ? a.stage_wait_ns : kWaitLimitNs;
+      bool ok = true;
+      int g = 0;
+      for (int j = 0; ok && j < my_items; ++j) {
+        const uint32_t acc = (uint32_t)(j & 1);
+        // the epilogue has read this accumulator's previous tile (j - 2)
+        if (j >= 2 && !mbar_wait(acc_empty + 8u * acc, (uint32_t)(j / 2 - 1) & 1u, kWaitLimitNs, abort_ptr)) {
+          if (!*abort_ptr) raise_error(kErrWaitAccum);
+          *abort_ptr = 1;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < a.kblocks; ++kb, ++g) {
+          const int s = g % stages;
+          if (!mbar_wait(full + 8u * s, (uint32_t)(g / stages) & 1u, stage_limit)) {
+            raise_error(kErrWaitFull);
+            *abort_ptr = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = ring + (uint32_t)(s * kStageBytes);
+          const uint64_t adesc = smem_desc_sw128(st), bdesc = smem_desc_sw128(st + kATile);
+#pragma unroll
+          for (int kk = 0; kk < kBlockK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
+            mma_bf16(tmem + acc * (uint32_t)N, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(empty + 8u * s);
+        }
+        mma_commit(acc_full + 8u * acc);  // also on abort: the epilogue then skips the tile
+      }
+      mma_commit(mma_done);  // completes once every MMA issued above has
+      if (!mbar_wait(mma_done, 0)) raise_error(kErrWaitAccum);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps ----------------
+    grid_dependency_wait();  // out may still be read (or, accumulating, written) by the preceding kernel
+    const int row = warp * 32 + lane;
+    for (int j = 0; j < my_items; ++j) {
+      const uint32_t acc = (uint32_t)(j & 1);
+      const int item = (int)blockIdx.x + j * (int)gridDim.x;
+      const int n = (item % m_tiles) * 128 + row;
+      const int tok0 = (item / m_tiles) * N;
+      // lane 0 waits and the warp follows its outcome, so the warp stays converged
+      // for the tcgen05.ld below (an abort seen by some lanes only would split it)
+      bool got = true;
+      if (lane == 0) {
+        got = mbar_wait(acc_full + 8u * acc, (uint32_t)(j / 2) & 1u, kWaitLimitNs, abort_ptr);
+        if (!got) {
+          if (!*abort_ptr) raise_error(kErrWaitAccum);
+          *abort_ptr = 1;
+        }
+      }
+      got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+      if (!got) break;
+      __syncwarp();
+      tc_fence_after();
+      const bool skip = __shfl_sync(0xffffffffu, *abort_ptr != 0 ? 1 : 0, 0) != 0;
+      if (!skip) {
+#pragma unroll 1
+        for (int c = 0; c < N; c += 16) {
+          float v[16];
+          tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + acc * (uint32_t)N + (uint32_t)c, v);
+          if (n < a.M) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int t = tok0 + c + i;
+              if (t < a.n_tok) {
+                uint16_t* o = a.out + (int64_t)t * a.M + n;
+                const uint32_t db = bf16_bits_pz(v[i]);  // d pushed as BF16, -0 made +0
+                *o = (uint16_t)(a.accumulate ? bf16_bits_pz(__fadd_rn(__uint_as_float((uint32_t)*o << 16),
+                                                                      __uint_as_float(db << 16)))
+                                             : db);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty + 8u * acc);
+    }
+  }
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // Failure-detection self-test: one thread waits, with the kernels' bounded
 // wait, on an mbarrier that nothing arrives at; after limit_ns it gives up,
 // raises kErrWaitFull and returns, so the host sees the error and the context
@@ -951,6 +1154,48 @@ cudaError_t launch_decode_gemm(int mode, const GemmPlan& p, const CUtensorMap& w
       if (p.tm != 128 || p.ksplit < 2 || p.ksplit > 8 || x1 == nullptr || a.kblocks < 1 || a.kblocks2 < 1)
         return cudaErrorInvalidValue;
       return launch_n<kGemmDownUp, 128>(p, w0, w1, x, *x1, a, pdl, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Ring of the persistent down projection: one CTA per SM with a deep ring
+// (about 192 KB, as the page's SharedDown budget), at most kMaxStages stages.
+static int persistent_stages(int n_tile) {
+  return std::max(2, std::min(kMaxStages, (192 * 1024) / stage_bytes(128, n_tile)));
+}
+
+template <int N>
+static cudaError_t launch_persistent_t(const CUtensorMap& w, const CUtensorMap& h, const GemmArgs& a, int ctas,
+                                       bool pdl, cudaStream_t stream) {
+  auto kernel = persistent_down_kernel<N>;
+  const int stages = persistent_stages(N);
+  const size_t smem = 1024 + (size_t)stages * stage_bytes(128, N) + 16 * (size_t)stages + 16 + 16 + 8 + 8 + 64;
+  const cudaError_t e = ensure_smem_limit((const void*)kernel, 220 * 1024);
+  if (e != cudaSuccess) return e;
+  if (smem > 220 * 1024) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, w, h, a, stages);
+}
+
+cudaError_t launch_persistent_down(const CUtensorMap& w, const CUtensorMap& h, const GemmArgs& args, int n_tile,
+                                   int ctas, bool pdl, cudaStream_t stream) {
+  GemmArgs a = args;
+  a.stage_wait_ns = stage_wait_limit_ns();
+  if (ctas < 1 || a.kblocks < 1) return cudaErrorInvalidValue;
+  switch (n_tile) {
+    case 16: return launch_persistent_t<16>(w, h, a, ctas, pdl, stream);
+    case 32: return launch_persistent_t<32>(w, h, a, ctas, pdl, stream);
+    case 64: return launch_persistent_t<64>(w, h, a, ctas, pdl, stream);
+    case 128: return launch_persistent_t<128>(w, h, a, ctas, pdl, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -105,6 +105,13 @@ struct GemmPlan {
 
 // K2: the up-projection's reduction length in mode kGemmDownUp (0 otherwise).
 GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2 = 0);
+// The persistent down projection (out = [accumulate ? out + ] bf16(h . w^T)):
+// ctas CTAs walk the output tiles of 128 rows x n_tile tokens over the whole
+// K range with two alternating TMEM accumulators.  Uses M, K, kblocks, n_tok,
+// out, accumulate and weights_before_wait of a; w: [M][K] (box 128 rows),
+// h: [n_tok][K] (box n_tile rows).
+cudaError_t launch_persistent_down(const CUtensorMap& w, const CUtensorMap& h, const GemmArgs& a, int n_tile,
+                                   int ctas, bool pdl, cudaStream_t stream);
 // The one-kernel latent tail's plan at b tokens and tp slots: the
 // up-projection's tiles and K split (so the product is bit for bit the
 // two-kernel one) and a ring that fits beside the CTA's y operand and can

@@ -8,6 +8,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <set>
@@ -605,6 +606,36 @@ MOE_API int moe_shared_down(const void* h, const void* w_down, int b, int H, int
     return MOE_TAIL_EINVAL;
   return launch_down(h, w_down, b, H, I, out, accumulate != 0, (flags & MOE_TAIL_WEIGHTS_STATIC) != 0,
                      static_cast<cudaStream_t>(stream));
+}
+
+MOE_API int moe_shared_down_persistent(const void* h, const void* w_down, int b, int H, int I, void* out,
+                                       int accumulate, int ctas, int flags, void* stream) {
+  if (!shared_sizes_ok(b, H, I) || ctas < 0 || ctas > 65535 || (flags & ~MOE_TAIL_WEIGHTS_STATIC))
+    return MOE_TAIL_EINVAL;
+  if (b == 0) return MOE_TAIL_OK;
+  if (!h || !w_down || !out) return MOE_TAIL_EINVAL;
+  if (!aligned(h, 16) || !aligned(w_down, 16) || !aligned(out, 16)) return MOE_TAIL_EINVAL;
+  const Range o = span(out, (size_t)b * H * 2);
+  if (overlaps(o, span(h, (size_t)b * I * 2)) || overlaps(o, span(w_down, (size_t)H * I * 2)))
+    return MOE_TAIL_EINVAL;
+  const int n_tile = b <= 16 ? 16 : b <= 32 ? 32 : b <= 64 ? 64 : 128;
+  const int64_t tiles = (int64_t)((H + 127) / 128) * ((b + n_tile - 1) / n_tile);
+  const int grid = (int)std::min<int64_t>(tiles, ctas > 0 ? ctas : device_sms());
+  CUtensorMap md, mh;
+  if (!encode_bf16_2d(&md, w_down, H, I, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !encode_bf16_2d(&mh, h, b, I, n_tile, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+    return MOE_TAIL_ECUDA;
+  GemmArgs d;
+  d.M = H;
+  d.K = I;
+  d.n_tok = b;
+  d.kblocks = (I + 63) / 64;
+  d.shared = nullptr;
+  d.tp_s = 0;
+  d.out = static_cast<uint16_t*>(out);
+  d.accumulate = accumulate != 0 ? 1 : 0;
+  d.weights_before_wait = (flags & MOE_TAIL_WEIGHTS_STATIC) ? 1 : 0;
+  return finish(moetail::launch_persistent_down(md, mh, d, n_tile, grid, true, static_cast<cudaStream_t>(stream)));
 }
 
 // ============================================================================ misc

@@ -329,6 +329,27 @@ def test_shared_down_refuses_bad_arguments(lib, bad):
     assert down(lib, **bad) == EINVAL
 
 
+def down_persistent(lib, **kw):
+    args = dict(h=a(), wd=a(1 << 28), b=64, H=7168, I=6144, out=a(2 << 28), acc=1, ctas=0, flags=0, stream=None)
+    args.update(kw)
+    return lib.moe_shared_down_persistent(args["h"], args["wd"], args["b"], args["H"], args["I"], args["out"],
+                                          args["acc"], args["ctas"], args["flags"], args["stream"])
+
+
+@host_only
+@pytest.mark.parametrize("bad", [
+    dict(H=4), dict(I=6150), dict(b=65536), dict(h=None), dict(wd=None), dict(out=None), dict(out=a(8)),
+    dict(out=a(16)), dict(flags=2), dict(h=a(2)), dict(ctas=-1), dict(ctas=65536),  # out over h
+])
+def test_shared_down_persistent_refuses_bad_arguments(lib, bad):
+    assert down_persistent(lib, **bad) == EINVAL
+
+
+@host_only
+def test_shared_down_persistent_b_zero(lib):
+    assert down_persistent(lib, b=0, h=None, out=None, flags=1, ctas=65535) == OK
+
+
 @host_only
 def test_shared_steps_b_zero(lib):
     assert gate_up(lib, b=0, x=None, h=None) == OK

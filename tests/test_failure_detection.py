@@ -104,6 +104,48 @@ def test_gemm_abort_path_raises_and_the_next_call_is_exact(mt):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("mode", ["gate_up", "down", "down_up", "persistent_down", "latent_one_kernel"])
+def test_every_gemm_mode_aborts_cleanly_and_the_next_call_is_exact(mt, pin, mode):
+    # each other decode-GEMM kernel the same way: its operand-stage wait runs
+    # out, it raises bit 1, drains what it started and returns; the next call
+    # with the default limit gives the bits of a call made before
+    b, H, I, L = 8, 1024, 768, 512
+    s = synth.shared_expert_inputs(0xAB1, b=b, H=H, I=I)
+    x, wg, wu, wd = (s[k].cuda() for k in ("x", "w_gate", "w_up", "w_down"))
+    h = synth.bf16(synth.normal(0xAB2, 1, b * I, std=0.5), (b, I)).cuda()
+    d = synth.latent_up_inputs(0xAB3, b=b, tp=2, tp_s=2, L=L, H=H)
+    lat, gam, wl, sh = d["latent"].cuda(), d["gamma"].cuda(), d["w_up"].cuda(), d["shared"].cuda()
+    y = d["latent"][0].contiguous().cuda()
+    if mode == "latent_one_kernel":
+        pin(mt.FORM_LATENT, mt.FORM_LATENT_ONE_KERNEL)
+
+    def call():
+        if mode == "gate_up":
+            out = torch.full((b, I), float("nan"), dtype=torch.bfloat16, device="cuda")
+            mt.moe_shared_gate_up(x, wg, wu, out)
+        elif mode == "latent_one_kernel":
+            out = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+            yy = torch.empty((b, L), dtype=torch.bfloat16, device="cuda")
+            mt.moe_tail_latent_up_flags(lat, gam, wl, sh, out, yy, eps=d["eps"])
+        else:
+            out = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+            if mode == "down":
+                mt.moe_shared_down(h, wd, out, accumulate=False)
+            elif mode == "persistent_down":
+                mt.moe_shared_down_persistent(h, wd, out, accumulate=False, ctas=3)
+            else:
+                mt.moe_tail_up_project_shared_down(y, wl, sh, h, wd, out)
+        return out
+
+    ref = call()
+    torch.cuda.synchronize()
+    bits, out = _short_stage_wait_then_normal(mt, call)
+    assert bits & 1, bits
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert mt.moe_tail_take_device_error() == 0
+
+
+@pytest.mark.gpu
 def test_staged_finalize_abort_path_raises_and_the_next_call_is_exact(mt, pin):
     # the staged expert-TP finalize: its threads' stage wait runs out, nothing
     # more is copied, and the copies in flight land before the CTA ends

@@ -5,7 +5,7 @@ with canaries: each output and workspace is carved out of a larger buffer
 whose 4 KB before and after hold a sentinel byte, the call runs at ragged
 sizes (widths not multiples of a tile, odd token counts, more than one K
 split, both finalize kernels, both latent-tail forms, the up-projection with
-the shared down projection), and the sentinel bytes
+the shared down projection, the persistent down projection), and the sentinel bytes
 must be unchanged afterwards.  The values themselves are checked by the
 parity tests."""
 import math
@@ -126,7 +126,11 @@ def test_shared_expert_calls(mt, kw):
     h, out2 = Guarded((b, I)), Guarded((b, H))
     mt.moe_shared_gate_up(x, wg, wu, h.t, weights_static=True)
     mt.moe_shared_down(h.t, wd, out2.t, accumulate=False, weights_static=True)
-    assert all(g.intact() for g in (out, ws, h, out2))
+    out3, out4 = Guarded((b, H)), Guarded((b, H))
+    out4.t.zero_()
+    mt.moe_shared_down_persistent(h.t, wd, out3.t, accumulate=False, ctas=3)
+    mt.moe_shared_down_persistent(h.t, wd, out4.t, accumulate=True)
+    assert all(g.intact() for g in (out, ws, h, out2, out3, out4))
     assert mt.moe_tail_take_device_error() == 0
 
 

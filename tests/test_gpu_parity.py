@@ -824,6 +824,44 @@ def test_no_device_error_raised(mt):
     assert mt.moe_tail_take_device_error() == 0
 
 
+# ------------------------------------------ the persistent down projection
+
+@pytest.mark.parametrize("kw", [
+    dict(b=64, H=7168, I=6144, ctas=0), dict(b=64, H=7168, I=6144, ctas=28),   # 56 tiles: 1 or 2 per CTA
+    dict(b=1, H=7168, I=6144, ctas=14), dict(b=16, H=1024, I=768, ctas=3),      # 4 tiles per CTA
+    dict(b=130, H=264, I=200, ctas=2),   # two token tiles, ragged M and K
+    dict(b=37, H=136, I=136, ctas=1),    # one CTA walks every tile
+    dict(b=5, H=520, I=1000, ctas=200),  # more CTAs asked for than there are tiles
+])
+def test_persistent_down(mt, kw):
+    # d against the oracle's down projection of h (GEMM bound) on sampled tokens,
+    # against moe_shared_down (K split over a cluster) on every element (the same
+    # bits almost everywhere, within the GEMM bound), and the accumulating call
+    # bit for bit bf16(out_in + d) given the GPU's d
+    b, H, I, ctas = kw["b"], kw["H"], kw["I"], kw["ctas"]
+    seed = 0xE0 + b + H
+    h = synth.bf16(synth.normal(seed, 1, b * I, std=0.5), (b, I))
+    wd = synth.bf16(synth.normal(seed, 2, H * I, std=0.02), (H, I))
+    out_in = synth.bf16(synth.normal(seed, 3, b * H), (b, H))
+    hg, wg = h.to(DEV), wd.to(DEV)
+    d = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mt.moe_shared_down_persistent(hg, wg, d, accumulate=False, ctas=ctas)
+    d2 = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mt.moe_shared_down(hg, wg, d2, accumulate=False)
+    out = out_in.to(DEV)
+    mt.moe_shared_down_persistent(hg, wg, out, accumulate=True, ctas=ctas, weights_static=True)
+    torch.cuda.synchronize()
+    assert mt.moe_tail_take_device_error() == 0
+    d_c = d.cpu()
+    for t in sorted({0, b // 2, b - 1}):
+        sl = slice(t, t + 1)
+        assert_gemm_close(d_c[sl], oracle.shared_down(h[sl], wd, 1, H, I, accumulate=False), f"d token {t} {kw}")
+    same = bits(d) == bits(d2)
+    assert same.mean() > 0.99, f"d differs from the split-K call in {1 - same.mean():.4f} of elements {kw}"
+    assert_gemm_close(d_c, d2.cpu(), f"d vs the split-K call, every element {kw}")
+    assert_accumulated_exact(out, out_in, d_c, f"accumulated out, every token {kw}")
+
+
 # ------------------------------------------ up-projection + shared down projection in one kernel
 
 @pytest.mark.parametrize("kw", [
