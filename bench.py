@@ -846,6 +846,34 @@ def ep_floor(d, dev, timed, copies_for, ep_us) -> dict:
     return out
 
 
+def tp_floor(d, dev, timed, parts, tp_us) -> dict:
+    """Memory floor of the expert-TP call at config 3 on its own grid (two
+    column bands of 256 threads per token, clusters of two, b = 128 tokens):
+    a kernel that only gathers the call's rows -- each token's K routes in all
+    tp slots, 16 rows in flight per thread, the depth of the call's 2-stage
+    ring -- timed as the call is."""
+    import ctypes
+
+    fl = floor_lib()
+    gx, gy, thr, cl = 2, d["b"], 256, 2
+    sptr = lambda: ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    sink = torch.zeros(gx * gy, dtype=torch.int32, device=dev)
+    tp, K, R = d["tp"], d["K"], d["num_rows"]
+    idx = d["idx"].numpy()
+    gidx = torch.tensor([[s * R + int(idx[t, k]) for k in range(K) for s in range(tp)] for t in range(d["b"])],
+                        dtype=torch.int32, device=dev)
+
+    def call(i):
+        rc = fl.moe_tail_floor_gather(ctypes.c_void_p(gidx.data_ptr()), K * tp, ctypes.c_void_p(parts[i].data_ptr()),
+                                      tp * R, gx, gy, thr, cl, ctypes.c_void_p(sink.data_ptr()), sptr())
+        assert rc == 0, rc
+
+    out = {"grid": f"{gx} x {gy} CTAs of {thr} threads, clusters of {cl}"}
+    out["gather_us"] = round(timed(call, len(parts)), 3)
+    out["tp_over_gather"] = round(tp_us / out["gather_us"], 3)
+    return out
+
+
 def isolated_configs(mt, cpu, w, dev, stream) -> dict:
     """Each workload timed alone: one call per graph node, CUDA events around
     replays of a graph of max(20, copies) calls that cycles over copies of the
@@ -924,6 +952,7 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
                                                  eps=d["eps"], weight_before_norm=d["weight_before_norm"],
                                                  stream=stream), n)
     report("3_tp_b128_P4096", us, nb, n, ">= 0.70 of HBM")
+    res["3_tp_b128_P4096"]["floor"] = tp_floor(d, dev, timed, parts, us)
     # ... with the inputs-ready promise (moe_tail_tp_finalize_flags): each call reads its
     # partials while the previous call drains
     us = timed(lambda i: mt.moe_tail_tp_finalize_flags(parts[i], idx, wt, gam, out, gain_center=d["gain_center"],
