@@ -11,14 +11,16 @@
  * cannot go:
  *   - moe_tail_floor_empty: the launch and the dependency wait alone;
  *   - moe_tail_floor_read:  one trip to memory for `bytes` bytes, every thread
- *     loading its share (16-byte loads, all issued before any is used);
+ *     loading its share (16-byte asynchronous copies into shared memory, up
+ *     to 16 per thread, all issued before any is waited for);
  *   - moe_tail_floor_gather: two dependent trips -- a token's nk route indices,
- *     then the indexed rows of the CTA's column band -- the access pattern of
- *     EP finalize without its arithmetic or cluster exchange.
+ *     then the indexed rows of the CTA's column band, 16 rows in flight per
+ *     thread (asynchronous copies as above) -- the access pattern of EP and
+ *     expert-TP finalize without their arithmetic or cluster exchange.
  * Each writes one 32-bit word per CTA into sink (grid_x * grid_y words), so
  * that no load is dead.  Pointers are device pointers, 16-byte aligned (idx:
  * 4-byte); stream is a cudaStream_t.  Returns 0, 1 for refused arguments
- * (non-positive sizes, threads not a multiple of 32 or above 1024, cluster
+ * (non-positive sizes, threads not a multiple of 32 or above 768, cluster
  * not dividing grid_x or above 8, a null or misaligned pointer), 2 for a CUDA
  * launch error.
  */

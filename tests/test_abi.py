@@ -461,8 +461,8 @@ def test_floor_library_exports_exactly_its_header():
 def test_floor_calls_refuse_bad_shapes_before_launching():
     fl = _floor_lib()
     ok = a()
-    for gx, gy, thr, cl in ((0, 1, 32, 1), (2, 0, 32, 1), (2, 1, 33, 1), (2, 1, 2048, 1), (3, 1, 32, 2),
-                            (16, 1, 32, 16)):
+    for gx, gy, thr, cl in ((0, 1, 32, 1), (2, 0, 32, 1), (2, 1, 33, 1), (2, 1, 2048, 1), (2, 1, 800, 1),
+                            (3, 1, 32, 2), (16, 1, 32, 16)):
         assert fl.moe_tail_floor_empty(gx, gy, thr, cl, None) == 1
         assert fl.moe_tail_floor_read(ok, 4096, gx, gy, thr, cl, ok, None) == 1
         assert fl.moe_tail_floor_gather(ok, 8, ok, 16, gx, gy, thr, cl, ok, None) == 1
