@@ -75,10 +75,11 @@ def parse_args():
     ap.add_argument("--composition", default="two_branch_fused",
                     choices=["two_branch_fused", "two_branch", "two_branch_one_call", "latent_main"],
                     help="how the step orders the weight-streaming calls (see run_step)")
-    ap.add_argument("--only-config", type=int, choices=[1, 2, 3, 4, 5, 6], default=None,
+    ap.add_argument("--only-config", type=int, choices=[1, 2, 3, 4, 5, 6, 7], default=None,
                     help="run one workload's call alone --calls times and exit (for profiling the call); 6: the "
                          "default step's side-stream calls at b = 64 (gate/up, latent norm, up-projection with the "
-                         "down projection)")
+                         "down projection); 7: config 5's down projection as the K-split GEMM and as the "
+                         "persistent kernel on 56 CTAs")
     ap.add_argument("--calls", type=int, default=4)
     ap.add_argument("--trace", choices=["step", "latent"], default=None,
                     help="per-CTA timeline from the trace build: ten decode steps as one graph (step), or the latent "
@@ -1256,7 +1257,8 @@ def only_config(args) -> int:
     """One workload's call, eagerly, --calls times on cuda:0 (for ncu): configs
     1-2 EP finalize, 3 expert-TP finalize, 4 the latent tail (moe_tail_latent_up
     and then moe_tail_latent_up_flags with both promises), 5 the shared expert
-    added into out, 6 the default step's side-stream calls at b = 64."""
+    added into out, 6 the default step's side-stream calls at b = 64, 7 config 5's
+    down projection, K-split and persistent."""
     import moe_decode_tail_gb300 as mt
     from moe_decode_tail_gb300 import synth
 
@@ -1288,6 +1290,12 @@ def only_config(args) -> int:
         out = torch.zeros((d["b"], d["H"]), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(mt.moe_tail_workspace_bytes(1, d["b"], d["I"]), dtype=torch.uint8, device=dev)
         calls = [lambda: mt.moe_shared_expert(x, wg, wu, wd, out, ws, accumulate=True)]
+    elif n == 7:  # config 5's down projection: the K-split GEMM, then the persistent form on 56 CTAs
+        s = synth.shared_expert_inputs(0x5EED0007, b=B, H=H, I=I)
+        hh, wd = g(s["x"][:, :I].contiguous()), g(s["w_down"])
+        out = torch.zeros((B, H), dtype=torch.bfloat16, device=dev)
+        calls = [lambda: mt.moe_shared_down(hh, wd, out, accumulate=False),
+                 lambda: mt.moe_shared_down_persistent(hh, wd, out, accumulate=False, ctas=56)]
     else:  # the default step's side stream at b = 64
         _, w = make_workload(dev)
         h = torch.empty((B, I), dtype=torch.bfloat16, device=dev)
