@@ -67,7 +67,8 @@ struct GemmArgs {
   int tp = 0;
   float eps = 0.f, rcpK = 0.f;
   int chunks = 0;                    // 256-column chunks of K (at most 32)
-  int inputs_before_wait = 0;        // latent and gamma complete before the preceding kernel ends
+  int inputs_before_wait = 0;        // mode 3: latent and gamma, mode 1: x, complete before the
+                                     // preceding kernel ends (read before its grid dependency wait)
   unsigned long long stage_wait_ns = 0;  // the MMA issuer's operand-stage wait limit (0: the default)
   // mode 4 (the shared expert's down projection and the up-projection in one
   // kernel): M, K, kblocks, map_w0 and map_x describe the down projection
