@@ -445,11 +445,24 @@ def traffic_record(call: str):
 GEMM_SOURCES = ("common.cuh", "decode_gemm.cu", "kernels.h", "moe_tail_api.cu")
 
 
+def code_only(text: str) -> str:
+    """C/CUDA source without its comments, trailing blanks and empty lines:
+    what a comment edit leaves unchanged (the sources hold no "//" or "/*"
+    inside string literals)."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_sources_hash() -> str:
+    """SHA-256 of the code (comments aside) of the files that define the
+    measured GEMM kernels and their launch."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_decode_tail_gb300", "csrc")
     for f in GEMM_SOURCES:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(code_only(open(os.path.join(csrc, f), encoding="utf-8").read()).encode())
     return h.hexdigest()
 
 

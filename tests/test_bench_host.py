@@ -120,6 +120,14 @@ def test_step_call_tables_cover_each_composition(bench):
     assert bench.STEP_BYTES == sum(c["bytes"] for c in seq.values()) - 2 * bench.B * bench.H * 2 == 367_309_824
 
 
+def test_code_only_drops_comments_but_not_code(bench):
+    src = "int a; // one\n/* two\n   lines */\nint b;   \n\n  x = y / z;  /* tail */\n"
+    assert bench.code_only(src) == "int a;\nint b;\n  x = y / z;"
+    # a comment edit leaves the hash's input unchanged, a code edit does not
+    assert bench.code_only(src.replace("one", "uno")) == bench.code_only(src)
+    assert bench.code_only(src.replace("y / z", "y * z")) != bench.code_only(src)
+
+
 def test_kernel_sources_hash_covers_the_gemm_sources(bench):
     # the hash is of the files that define the measured kernels and their launch
     csrc = os.path.join(ROOT, "moe_decode_tail_gb300", "csrc")
