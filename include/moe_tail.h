@@ -50,7 +50,7 @@ typedef enum {
   MOE_TAIL_OK = 0,
   MOE_TAIL_EINVAL = 1,  /* arguments refused before any launch */
   MOE_TAIL_ECUDA = 2,   /* a CUDA call failed */
-  MOE_TAIL_ENOTSUP = 3  /* valid arguments this build does not support */
+  MOE_TAIL_ENOTSUP = 3  /* valid arguments the library does not support */
 } moe_tail_status;
 
 enum { MOE_TAIL_W_FP32 = 0, MOE_TAIL_W_BF16 = 1 };
