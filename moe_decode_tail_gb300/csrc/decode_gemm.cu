@@ -1006,8 +1006,11 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
     // step it runs beside the expert-TP finalize, which then finds SMs sooner
     // (b = 64: K split 4 instead of 5, 72.7 -> 71.4 us per step).  Small
     // batches keep two (b = 1 alone: 45.9 vs 48.5 us for the shared expert).
+    // The down + up kernel above 64 tokens (128-token tiles, 2-stage rings) takes
+    // a 6-way split (about 2.2 CTAs per SM): the decode step at b = 128 84.4 ->
+    // 81.7 us (5-way; 7-way 83.1, 8-way 88.8, 3-stage rings 91-93).
     const int slots = (mode == kGemmDown && b > 32) ? 3 * sms / 2 : small_up ? 3 * sms
-                      : small_gateup ? 8 * sms / 3 : 2 * sms;
+                      : small_gateup ? 8 * sms / 3 : (mode == kGemmDownUp && b > 64) ? 9 * sms / 4 : 2 * sms;
     int ks = slots / std::max(1, p.m_tiles * tok_tiles);
     p.ksplit = std::max(1, std::min(ks, 8));
   }
