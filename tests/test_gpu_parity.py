@@ -661,6 +661,39 @@ def test_maximum_sizes(mt, case):
     assert mt.moe_tail_take_device_error() == 0
 
 
+@pytest.mark.parametrize("ctas", [2, 0])
+def test_down_projections_at_the_token_limit(mt, ctas):
+    # b = 65535 (512 token tiles of 128): the persistent down projection walks
+    # 512 tiles over 2 CTAs (each accumulator reused 128 times) or over one CTA
+    # per SM, and the down + up kernel runs 512 token tiles of its clusters;
+    # d against the oracle on sampled tokens and against moe_shared_down on
+    # every element, out against the oracle with the GPU's d as a shared slot
+    b, H, I, L = 65535, 8, 64, 64
+    h = synth.bf16(synth.normal(0x3B0, 1, b * I, std=0.5), (b, I))
+    wd = synth.bf16(synth.normal(0x3B0, 2, H * I, std=0.05), (H, I))
+    y = synth.bf16(synth.normal(0x3B0, 3, b * L, std=0.5), (b, L))
+    wu = synth.bf16(synth.normal(0x3B0, 4, H * L, std=0.05), (H, L))
+    hg, wdg = h.to(DEV), wd.to(DEV)
+    d = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mt.moe_shared_down_persistent(hg, wdg, d, accumulate=False, ctas=ctas)
+    d2 = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mt.moe_shared_down(hg, wdg, d2, accumulate=False)
+    out = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    d3 = torch.full((b, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mt.moe_tail_up_project_shared_down(y.to(DEV), wu.to(DEV), None, hg, wdg, out, d3)
+    torch.cuda.synchronize()
+    assert mt.moe_tail_take_device_error() == 0
+    d_c, d3_c, out_c = d.cpu(), d3.cpu(), out.cpu()
+    for t in (0, 127, 128, 40000, b - 1):
+        sl = slice(t, t + 1)
+        d_ref = oracle.shared_down(h[sl], wd, 1, H, I, accumulate=False)
+        assert_gemm_close(d_c[sl], d_ref, f"persistent d token {t}")
+        assert_gemm_close(d3_c[sl], d_ref, f"down + up d token {t}")
+        assert_gemm_close(out_c[sl], oracle.latent_up(y[sl], wu, d3_c[None, sl].contiguous(), 1, 1, L, H),
+                          f"down + up out token {t}")
+    assert_gemm_close(d_c, d2.cpu(), "persistent d vs the split-K call, every element")
+
+
 # ------------------------------------------------------------------ shared expert
 #
 # gate and up are FP32 sums whose order the pages leave open, so bf16(gate),
