@@ -310,6 +310,7 @@ __global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const Fin
 
   const uint4 gv = valid ? ld_v4(a.gamma + col) : make_uint4(0, 0, 0, 0);
   const int count = load_route_list<kModeEP, WMODE>(a, sm, t);
+  MOE_TRACE_MARK(0);  // the token's route list resolved
   float2 g[4];
   unpack8p(gv, g);
 #pragma unroll
@@ -351,7 +352,9 @@ __global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const Fin
           st_cluster_f32(map_to_rank(smem_addr(&ssp[q * kMaxChunks + chunk]), (uint32_t)lane), acc);
       }
     }
+    if (pass == 0) MOE_TRACE_MARK(1);  // rows landed, chunk sums published
     cluster_sync_all();
+    if (pass == 0) MOE_TRACE_MARK(2);  // cluster barrier passed
     // lane q of every warp forms route q's 1/rms; the warp shares them
     const float my_inv = inv_rms_of_route(ssp + (lane & (kEpRoutes - 1)) * kMaxChunks, a);
 #pragma unroll
@@ -386,6 +389,7 @@ __global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const Fin
 #pragma unroll
     for (int k = 0; k < 4; ++k) o[k] = add2(o[k], bf16_round2(part[k]));
   }
+  MOE_TRACE_MARK(3);  // products summed
   if (valid) {
     const uint4 r = pack8p_pz(o);
     if (a.inputs_before_wait) grid_dependency_wait();

@@ -80,6 +80,10 @@ def describe(group: list[tuple[int, int, list]]) -> list[str]:
         elif kid in (20, 21) and all(r[4][2] and r[4][3] for r in rs):  # staged finalize, first pass
             line += (f"  first rows p50 {p50(lambda r: r[4][0] - r[3]):5.1f}  pass consumed "
                      f"{p50(lambda r: r[4][2] - r[3]):5.1f}  after cluster barrier {p50(lambda r: r[4][3] - r[3]):5.1f}")
+        elif kid == 40 and all(r[4][0] and r[4][1] and r[4][2] and r[4][3] for r in rs):  # EP finalize
+            line += (f"  route list p50 {p50(lambda r: r[4][0] - r[3]):5.1f}  rows summed {p50(lambda r: r[4][1] - r[3]):5.1f}"
+                     f"  after cluster barrier {p50(lambda r: r[4][2] - r[3]):5.1f}"
+                     f"  products {p50(lambda r: r[4][3] - r[3]):5.1f}")
         elif kid in (30, 31, 32, 34) and all(r[4][0] for r in rs):
             line += f"  K loop p50 {p50(lambda r: r[4][0] - r[3]):5.1f}"
             if all(r[4][3] for r in rs):

@@ -99,3 +99,13 @@ def test_describe_reads_gemm_and_one_kernel_marks():
     assert "stage 0.4 peers 1.0 reduce 2.0 barrier+exit 1.4" in gemm_line
     assert "x formed p50   2.0  y ready   6.5  accumulator  11.0" in fused_line
     assert "CTAs    3" in gemm_line and "CTA p50  13.8" in gemm_line
+
+
+def test_describe_reads_ep_finalize_marks():
+    # EP finalize: marks 0 (route list), 1 (rows summed), 2 (cluster barrier), 3 (products)
+    from moe_decode_tail_gb300.trace import describe
+
+    ep = [_rec(40, c, c, 100 * c, [100 * c + 900, 100 * c + 2500, 100 * c + 3100, 100 * c + 3600], 100 * c + 4000)
+          for c in range(3)]
+    line = describe([(40, 0, ep)])[0]
+    assert "route list p50   0.9  rows summed   2.5  after cluster barrier   3.1  products   3.6" in line
