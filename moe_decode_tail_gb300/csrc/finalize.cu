@@ -40,6 +40,9 @@ enum { kModeEP = kFinalizeEP, kModeTP = kFinalizeTP, kModeLatent = kFinalizeLate
 
 constexpr int kMaxRoutesPerPass = 8;
 constexpr int kMaxChunks = 128;  // P <= 32768
+// A route's chunk sums sit kChunkStride floats apart: the lanes that form
+// different routes' 1/rms at once then read different shared-memory banks.
+constexpr int kChunkStride = kMaxChunks + 1;
 constexpr int kMaxList = 1024;   // tp * K <= 32 * 32
 // At most 512 threads of at most 64 registers (half an SM's register file), so
 // that a finalize CTA fits on an SM beside the GEMM CTAs of a concurrent
@@ -47,7 +50,7 @@ constexpr int kMaxList = 1024;   // tp * K <= 32 * 32
 constexpr int kMaxThreads = 512;
 
 struct __align__(16) FinalizeSmem {
-  float ss[2][kMaxRoutesPerPass][kMaxChunks];  // chunk sums of squares, per pass parity
+  float ss[2][kMaxRoutesPerPass][kChunkStride];  // chunk sums of squares, per pass parity
   int32_t list_row[kMaxList];                  // the token's routes: row within the slot
   int16_t list_slot[kMaxList];                 // EP: the slot holding it
   int16_t list_route[kMaxList];                // route index k (for its weight)
@@ -223,9 +226,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
     }
     cluster_sync_all();
     if (active) {
-      float ss = 0.0f;
-      for (int c = 0; c < a.chunks; ++c) ss = __fadd_rn(ss, ssp[c]);
-      const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, a.rcpP), a.eps)));
+      const float inv = inv_rms_of_route(ssp, a);
       const float w = MODE == kModeLatent ? 1.0f : sm.w[sm.list_route[e]];
       const float2 inv2 = splat2(inv);
       float4* dst = reinterpret_cast<float4*>(prod + ((size_t)r_local * VB + vb) * 8);
@@ -349,14 +350,14 @@ __global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const Fin
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
         if (chunk < a.chunks && lane < (int)split)
-          st_cluster_f32(map_to_rank(smem_addr(&ssp[q * kMaxChunks + chunk]), (uint32_t)lane), acc);
+          st_cluster_f32(map_to_rank(smem_addr(&ssp[q * kChunkStride + chunk]), (uint32_t)lane), acc);
       }
     }
     if (pass == 0) MOE_TRACE_MARK(1);  // rows landed, chunk sums published
     cluster_sync_all();
     if (pass == 0) MOE_TRACE_MARK(2);  // cluster barrier passed
     // lane q of every warp forms route q's 1/rms; the warp shares them
-    const float my_inv = inv_rms_of_route(ssp + (lane & (kEpRoutes - 1)) * kMaxChunks, a);
+    const float my_inv = inv_rms_of_route(ssp + (lane & (kEpRoutes - 1)) * kChunkStride, a);
 #pragma unroll
     for (int q = 0; q < kEpRoutes; ++q) {
       const float inv = __shfl_sync(0xffffffffu, my_inv, q);
@@ -420,7 +421,7 @@ constexpr int kStagedMaxStages = 16;
 __device__ unsigned int g_finalize_error = 0;
 
 struct __align__(16) StagedSmem {
-  float ss[2][kMaxRoutesPerPass][kMaxChunks];
+  float ss[2][kMaxRoutesPerPass][kChunkStride];
   unsigned long long full[kStagedMaxStages];
   uint32_t released[kStagedMaxStages];  // warps done with the stage's current route
   uint32_t issued;                      // routes issued (a prefix of the CTA's route numbers)
@@ -604,7 +605,7 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
 #pragma unroll
           for (int off = 1; off < 32; off <<= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, off));
           if (chunk < a.chunks && lane < (int)split)
-            st_cluster_f32(map_to_rank(smem_addr(&ss[rr * kMaxChunks + chunk]), (uint32_t)lane), sq);
+            st_cluster_f32(map_to_rank(smem_addr(&ss[rr * kChunkStride + chunk]), (uint32_t)lane), sq);
         }
       }
       if (m <= (uint32_t)kMaxRoutesPerPass) MOE_TRACE_MARK(2);  // first pass: all its routes consumed
@@ -612,7 +613,7 @@ __global__ void __launch_bounds__(512) staged_finalize_kernel(const FinalizeArgs
       if (m <= (uint32_t)kMaxRoutesPerPass) MOE_TRACE_MARK(3);
       // lane r of every warp folds route r's chunk sums in chunk order and forms
       // its 1/rms (one square root and division per thread); the warp shares them
-      const float my_inv = inv_rms_of_route(ss + (lane & (kMaxRoutesPerPass - 1)) * kMaxChunks, a);
+      const float my_inv = inv_rms_of_route(ss + (lane & (kMaxRoutesPerPass - 1)) * kChunkStride, a);
 #pragma unroll
       for (int rr = 0; rr < kMaxRoutesPerPass; ++rr) {
         const float inv = __shfl_sync(0xffffffffu, my_inv, rr);
