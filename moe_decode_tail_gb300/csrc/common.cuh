@@ -89,7 +89,13 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
 // following add (the form to use for a product that is summed).
 __device__ __forceinline__ float2 mul_each(float2 v, float s) { return make_float2(__fmul_rn(v.x, s), __fmul_rn(v.y, s)); }
 __device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
-__device__ __forceinline__ float2 bf16_round2(float2 v) { return make_float2(bf16_round(v.x), bf16_round(v.y)); }
+// Both components rounded to BF16 as bf16_round rounds each, by one paired
+// conversion (cvt.rn.bf16x2.f32 puts its first source in the upper half).
+__device__ __forceinline__ float2 bf16_round2(float2 v) {
+  uint32_t b;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(v.y), "f"(v.x));
+  return make_float2(bf16_lo(b), bf16_hi(b));
+}
 __device__ __forceinline__ uint4 pack8p_pz(const float2 (&o)[4]) {
   return make_uint4(pack_bf16x2_pz(o[0].x, o[0].y), pack_bf16x2_pz(o[1].x, o[1].y), pack_bf16x2_pz(o[2].x, o[2].y),
                     pack_bf16x2_pz(o[3].x, o[3].y));

@@ -334,6 +334,15 @@ __global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const Fin
         raw[q] = ld_stream_v4(a.rows + (int64_t)sm.list_slot[e] * a.slot_stride + (int64_t)sm.list_row[e] * a.P + col);
       }
     }
+    // the routes' weights and slots, read while the rows are in flight
+    float wq[kEpRoutes];
+    int sq[kEpRoutes];
+#pragma unroll
+    for (int q = 0; q < kEpRoutes; ++q) {
+      const int e = min(base + q, count - 1);
+      wq[q] = sm.w[sm.list_route[e]];
+      sq[q] = sm.list_slot[e];
+    }
     float* ssp = &sm.ss[pass & 1][0][0];  // [route of the pass][chunk]
 #pragma unroll
     for (int q = 0; q < kEpRoutes; ++q) {
@@ -358,13 +367,14 @@ __global__ void __launch_bounds__(kEpMaxThreads, 1) ep_finalize_kernel(const Fin
     if (pass == 0) MOE_TRACE_MARK(2);  // cluster barrier passed
     // lane q of every warp forms route q's 1/rms; the warp shares them
     const float my_inv = inv_rms_of_route(ssp + (lane & (kEpRoutes - 1)) * kChunkStride, a);
+    float invq[kEpRoutes];
+#pragma unroll
+    for (int q = 0; q < kEpRoutes; ++q) invq[q] = __shfl_sync(0xffffffffu, my_inv, q);
 #pragma unroll
     for (int q = 0; q < kEpRoutes; ++q) {
-      const float inv = __shfl_sync(0xffffffffu, my_inv, q);
       if (q < n_pass) {
-        const int e = base + q;
-        const float w = sm.w[sm.list_route[e]];
-        const int s = sm.list_slot[e];
+        const float inv = invq[q], w = wq[q];
+        const int s = sq[q];
         if (s != cur_slot) {  // slot boundary: its BF16 partial joins the slot sum
           if (cur_slot >= 0) {
 #pragma unroll
