@@ -1002,10 +1002,11 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
   // and 128 the 3-way split stays (58.0 vs 58.4, 84.7 vs 87.5).
   const bool small_gateup = mode == kGemmGateUpSilu && p.n_tile <= 32;
   if (!forced) {  // K split over a cluster: about two CTAs per SM
-    // Above 32 tokens the down projection takes about 1.5 per SM: in a decode
-    // step it runs beside the expert-TP finalize, which then finds SMs sooner
-    // (b = 64: K split 4 instead of 5, 72.7 -> 71.4 us per step).  Small
-    // batches keep two (b = 1 alone: 45.9 vs 48.5 us for the shared expert).
+    // Above 32 tokens the down projection takes about 1.5 per SM (K split 4
+    // at H = 7168; with its 96 KB rings the shared expert alone at b = 64
+    // measured 49.4 us against 51.0 / 52.6 with a 5- / 3-way split, at b = 128
+    // 59.3 against 63.8 / 63.4).  Small batches keep two (b = 1 alone: 45.9
+    // vs 48.5 us for the shared expert).
     // The down + up kernel above 64 tokens (128-token tiles, 2-stage rings) takes
     // a 6-way split (about 2.2 CTAs per SM): the decode step at b = 128 84.4 ->
     // 81.7 us (5-way; 7-way 83.1, 8-way 88.8, 3-stage rings 91-93).
@@ -1033,9 +1034,13 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
   // The down + up kernel takes 72 KB as well: in a decode step it runs while
   // the expert-TP finalize still holds SMs, and two of its CTAs beside one
   // finalize CTA fit an SM only at this size (b = 64: 63.3 vs 66.9 us per
-  // step with 96 KB, whose second CTA waits for the finalize to end).
+  // step with 96 KB, whose second CTA waits for the finalize to end).  The
+  // down projection on its own (moe_shared_down, moe_shared_expert; the
+  // decode step streams it in the down + up kernel) takes 96 KB: the shared
+  // expert alone at b = 64 52.9 -> 49.4 us, b = 128 65.8 -> 59.3, b = 1..32
+  // 2-3 % faster.
   const int budget = p.tm == 256 ? 200 * 1024 : (small_up || small_gateup) ? 3 * sb
-                     : (mode == kGemmUpShared ? 96 * 1024 : 72 * 1024);
+                     : ((mode == kGemmUpShared || mode == kGemmDown) ? 96 * 1024 : 72 * 1024);
   if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, budget / sb));
   int per_cta = (kblocks + p.ksplit - 1) / p.ksplit;  // the longest K range of a CTA
   if (mode == kGemmDownUp) {
