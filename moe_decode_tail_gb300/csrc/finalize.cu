@@ -154,10 +154,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
   if (!a.inputs_before_wait) grid_dependency_wait();
   // A kernel chained behind this one may start its own prologue.  The latent
   // norm that waited first, from 8 tokens on, lets it start only once this
-  // thread's latent rows are summed (below): the up-projection behind it
+  // thread's latent row loads are issued (below): the up-projection behind it
   // requests its weights at once, and that flood would otherwise queue ahead
-  // of the norm's own loads (one call at b = 16: 15.1 -> 14.4 us; b = 8:
-  // 14.8 -> 14.1).  At b = 1 the early start is worth more (12.3 vs 13.2 us).
+  // of the norm's own loads (one call at b = 16: 15.1 -> 14.4 us with the
+  // start held back until the rows were summed, 13.9 -> 13.5 us once it
+  // followed their issue; b = 8: 14.8 -> 14.1 -> 13.0).  At b = 1 the early
+  // start is worth more (12.3 vs 13.2 us).
   const bool late_trigger = MODE == kModeLatent && !a.inputs_before_wait && a.b >= 8;
   if (!late_trigger) launch_dependents();
 
@@ -194,6 +196,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             v[q] = s0 + q < a.tp ? ld_stream_v4(src + (int64_t)(s0 + q) * a.slot_stride) : make_uint4(0, 0, 0, 0);
+          if (late_trigger && pass == 0 && s0 == 0) launch_dependents();  // the first slots' loads are out
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             if (s0 + q < a.tp) {  // slot order, FP32 from +0
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) finalize_kernel(const Finalize
         for (int k = 0; k < 4; ++k) x[k] = bf16_round2(x[k]);
       }
     }
-    if (late_trigger && pass == 0) launch_dependents();  // issued after the loads' data is summed
+    if (late_trigger && pass == 0) launch_dependents();  // threads without a row (a repeat is harmless)
     // this warp's chunk sum of squares, published to every CTA of the cluster
     float* ssp = sm.ss[pass & 1][r_local];
     {
