@@ -778,6 +778,9 @@ def cuda_arm(args, world, rank, local):
         line["cpu_baseline"] = cpu_baseline(cpu)
     if not args.no_configs:
         line["configs_isolated"] = isolated_configs(mt, cpu, w, dev, stream)
+        alone = line["configs_isolated"]["results"].get("5_gate_up_b64")
+        if alone and dom == "shared_gate_up":  # the same kernel timed alone, for comparison
+            roof["alone"] = {"configs_isolated": "5_gate_up_b64", "us": alone["us"], "frac": alone["hbm_frac"]}
         line["step_by_batch"] = dict(step_by_batch(mt, w, dev, stream, side),
                                      b64={"us_per_step": round(ms * 1e3, 2), "tokens_per_s": round(units / max_s, 1)})
     print(json.dumps(line), flush=True)
@@ -1020,6 +1023,11 @@ def isolated_configs(mt, cpu, w, dev, stream) -> dict:
 
     us = timed(shared_static, n)
     report("5_shared_expert_b64_static", us, nb, n, ">= 0.60 of the weight-stream roofline")
+    # its gate/up alone: the decode step's longest call without the step's
+    # concurrent finalize calls and down + up stream
+    nb_gu = 2 * I * H * 2 + B * H * 2 + B * I * 2
+    us = timed(lambda i: mt.moe_shared_gate_up(w["x"], ws_[i][0], ws_[i][1], h_, stream=stream), n)
+    report("5_gate_up_b64", us, nb_gu, n, "report (the decode step's longest call, alone)")
 
     # the shared expert's down projection alone (d written, not accumulated): the
     # split-K GEMM against the page's persistent form on 56, 28 and 14 CTAs (each
