@@ -808,6 +808,12 @@ cudaError_t launch_finalize(int mode, const FinalizeArgs& args, bool wbn, int wm
     // us; b = 4: 13.5 vs 14.6).  From b = 8 the wide bands are far slower
     // there (~20 us), and the composed step is the same either way.
     if (mode == kModeLatent && a.b <= 4) split = std::min(split, 2);
+    // An EP CTA of 512 threads holds a whole SM's registers (about 114 each),
+    // so none of a concurrent weight stream's CTAs fits beside it: at most 8
+    // warps per band where the row allows (the decode step at b = 128: 87.8 ->
+    // 82.0 us per step with 2 bands instead of 1; b = 32 and 96 unchanged).
+    if (mode == kModeEP)
+      while (split < 8 && split < a.chunks && (a.chunks + split - 1) / split > 8) split *= 2;
   }
   while (split < 8 && (a.chunks + split - 1) / split > kMaxThreads / 32) split *= 2;
   a.band_vectors = 32 * ((a.chunks + split - 1) / split);
