@@ -996,11 +996,13 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
   // 11.9 -> 11.3 us, at b = 1 10.7 -> 10.2, b = 8 11.5 -> 10.9; without them
   // the same at b = 16, faster at b = 1 and 8.
   const bool small_up = mode == kGemmUpShared && p.n_tile <= 16;
-  // The gate/up projection of at most 32 tokens takes a 4-way K split with
-  // 3-stage rings (384 CTAs, about 2.5 per SM), measured in the decode step:
-  // b = 32 59.0 -> 55.1 us, b = 8 52.3 -> 51.5, b = 1 50.9 -> 50.5; at b = 64
-  // and 128 the 3-way split stays (58.0 vs 58.4, 84.7 vs 87.5).
-  const bool small_gateup = mode == kGemmGateUpSilu && p.n_tile <= 32;
+  // The gate/up projection of at most 64 tokens takes a 4-way K split with
+  // 3-stage rings (384 CTAs, about 2.5 per SM).  Alone it is 1.2-1.6 us
+  // faster than the 3-way split at b = 40 ... 64 (b = 64: 32.5 -> 31.2 us);
+  // in the decode step b = 64 59.8 -> 56.7 us, b = 40 63.6 -> 60.5, b = 32
+  // 59.0 -> 55.1, b = 8 52.3 -> 51.5, b = 1 50.9 -> 50.5 (b = 48 and 56 +1.7
+  // and +1.4).  At 128 tokens the 3-way split stays (step 80.5 vs 84.7 us).
+  const bool small_gateup = mode == kGemmGateUpSilu && p.n_tile <= 64;
   if (!forced) {  // K split over a cluster: about two CTAs per SM
     // Above 32 tokens the down projection takes about 1.5 per SM (K split 4
     // at H = 7168; with its 96 KB rings the shared expert alone at b = 64
