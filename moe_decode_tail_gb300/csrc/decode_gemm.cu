@@ -996,13 +996,14 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
   // 11.9 -> 11.3 us, at b = 1 10.7 -> 10.2, b = 8 11.5 -> 10.9; without them
   // the same at b = 16, faster at b = 1 and 8.
   const bool small_up = mode == kGemmUpShared && p.n_tile <= 16;
-  // The gate/up projection of at most 64 tokens takes a 4-way K split with
-  // 3-stage rings (384 CTAs, about 2.5 per SM).  Alone it is 1.2-1.6 us
-  // faster than the 3-way split at b = 40 ... 64 (b = 64: 32.5 -> 31.2 us);
-  // in the decode step b = 64 59.8 -> 56.7 us, b = 40 63.6 -> 60.5, b = 32
-  // 59.0 -> 55.1, b = 8 52.3 -> 51.5, b = 1 50.9 -> 50.5 (b = 48 and 56 +1.7
-  // and +1.4).  At 128 tokens the 3-way split stays (step 80.5 vs 84.7 us).
-  const bool small_gateup = mode == kGemmGateUpSilu && p.n_tile <= 64;
+  // The gate/up projection takes a 4-way K split (384 CTAs at I = 6144, about
+  // 2.5 per SM) with rings of up to 3 stages and 72 KB.  Alone it is 4-6 %
+  // faster than the 3-way split at b = 40 ... 128 (b = 64: 32.5 -> 31.2 us,
+  // b = 128: 38.5 -> 36.1); in the decode step b = 64 59.8 -> 56.7 us, b = 40
+  // 63.6 -> 60.5, b = 96 71.6 -> 69.2, b = 128 80.2 -> 79.2, b = 32 59.0 ->
+  // 55.1, b = 8 52.3 -> 51.5, b = 1 50.9 -> 50.5 (b = 48 and 56 +1.7 and +1.4;
+  // at b = 128 a 3-stage, 96 KB ring leaves too few CTAs per SM: 84.7 us).
+  const bool small_gateup = mode == kGemmGateUpSilu;
   if (!forced) {  // K split over a cluster: about two CTAs per SM
     // Above 32 tokens the down projection takes about 1.5 per SM (K split 4
     // at H = 7168; with its 96 KB rings the shared expert alone at b = 64
@@ -1041,7 +1042,7 @@ GemmPlan plan_gemm(int mode, int M, int K, int b, int sms, int K2) {
   // decode step streams it in the down + up kernel) takes 96 KB: the shared
   // expert alone at b = 64 52.9 -> 49.4 us, b = 128 65.8 -> 59.3, b = 1..32
   // 2-3 % faster.
-  const int budget = p.tm == 256 ? 200 * 1024 : (small_up || small_gateup) ? 3 * sb
+  const int budget = p.tm == 256 ? 200 * 1024 : small_up ? 3 * sb : small_gateup ? std::min(3 * sb, 72 * 1024)
                      : ((mode == kGemmUpShared || mode == kGemmDown) ? 96 * 1024 : 72 * 1024);
   if (p.stages == 0) p.stages = std::max(2, std::min(kMaxStages, budget / sb));
   int per_cta = (kblocks + p.ksplit - 1) / p.ksplit;  // the longest K range of a CTA
