@@ -737,6 +737,16 @@ def test_shared_expert_shapes(mt, kw):
     check_shared(mt, s, out_in, what=str(kw))
 
 
+def test_shared_expert_full_size_b128_sampled_tokens(mt):
+    # H = 7168, I = 6144 at b = 128: 128-token tiles, gate/up's 4-way K split
+    # with 2-stage rings and the down projection's 3-stage rings; the oracle
+    # recomputes 4 tokens (both ends of the tile and its middle), and every
+    # token's accumulated output is checked bit for bit against the GPU's d
+    s = synth.shared_expert_inputs(0x5EED0128, b=128, H=7168, I=6144)
+    out_in = synth.bf16(synth.normal(0x5E, 128, 128 * 7168), (128, 7168))
+    check_shared(mt, s, out_in, tokens=(0, 63, 64, 127), what="b=128 H=7168 I=6144")
+
+
 def test_shared_expert_full_size_sampled_tokens(mt):
     # the full decode layer: latent tail at b = 64, then the shared expert
     # added into its output; the oracle recomputes 6 sampled tokens
